@@ -1,0 +1,207 @@
+/*
+ * ce.h -- C ABI of the GB300 (sm_103a) softmax cross-entropy library (libce.so).
+ *
+ * The operation: for a [n_rows, vocab] logits matrix X (row stride ld
+ * elements), targets t, optional class weights w, label smoothing eps and a
+ * reduction, compute the cross-entropy loss and its gradient with respect to
+ * X, writing the gradient over X. Per valid row i (t_i != ignore_index and
+ * 0 <= t_i < vocab):
+ *
+ *   loss_i = (1-eps) * w_{t_i} * (LSE_i - x_{i,t_i})
+ *          + (eps/V) * sum_c w_c * (LSE_i - x_ic),   LSE_i = log sum_c exp(x_ic)
+ *   dX_ic  = s_i * [ (1-eps) * w_{t_i} * (p_ic - [c == t_i])
+ *                    + (eps/V) * (p_ic * W_all - w_c) ],  p = softmax(x_i)
+ *
+ * with W_all = sum_c w_c, W_y = sum over valid rows of w_{t_i} (the
+ * non-ignored count when unweighted), s_i = g / W_y for mean, g for sum and
+ * g_i for none. Rows that are not valid contribute loss 0 and gradient 0.
+ * Unweighted this is (softmax - (1-eps) onehot - eps/V) * g / N.
+ *
+ * Sources: Liger-Kernel PR "perf(ce): single-shot dx_y gradient correction
+ * - #1268" (review diff: the eps/V term and the weighted true-class term;
+ * the #1329 commit message quoted there: dx_y recomputed once in fp32 and
+ * stored once, the logits buffer holding the gradient; the #1290 commit
+ * message: gradient scaled in place, peak memory one logits tensor);
+ * Liger-Kernel PR "perf(flce): drop host syncs that do not feed the
+ * computation - #1622" (Summary: normalisers, reductions, device-side
+ * grad_output == 1 skip, no host syncs); TransformerEngine PR #2325 "change
+ * fused cross entropy backward grad to fp32 and reduce one read/write"
+ * (forward saves per-row m, d, X_y and the smoothing sum; backward forms the
+ * gradient in fp32 from them).
+ *
+ * Conventions for every entry point:
+ *  - Pointers marked "device" are CUDA device (or managed) memory owned by
+ *    the caller. The library allocates nothing and keeps no pointer after a
+ *    call returns.
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream). Every call
+ *    only enqueues work on it and returns; nothing waits for the GPU, except
+ *    ce_get_status, which synchronises `stream` explicitly.
+ *  - The return code reports host-side argument checks and launch errors.
+ *    On an error nothing has been enqueued (argument errors) or the CUDA
+ *    error of the failed launch is reported (CE_ERR_CUDA, see
+ *    ce_last_cuda_error). Data errors found on the device (a target outside
+ *    [0, vocab) that is not ignore_index) set bits in the workspace status
+ *    word; such rows are treated as ignored.
+ *  - The workspace is scratch owned by the caller, at least
+ *    ce_workspace_size() bytes, 256-byte aligned. Calls that share a
+ *    workspace must be ordered on one stream (or otherwise serialised).
+ *    Its contents need no initialisation.
+ */
+#ifndef CE_H
+#define CE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    CE_OK = 0,
+    CE_ERR_INVALID_ARG = 1,   /* a pointer, size, stride or enum is invalid */
+    CE_ERR_UNSUPPORTED = 2,   /* valid but not supported (e.g. misaligned for the asked variant) */
+    CE_ERR_CUDA = 3,          /* a CUDA runtime call or launch failed */
+    CE_ERR_WORKSPACE = 4      /* workspace missing, too small or misaligned */
+} ce_status;
+
+typedef enum { CE_RED_NONE = 0, CE_RED_MEAN = 1, CE_RED_SUM = 2 } ce_reduction;
+
+/* storage type of the logits / gradient buffer */
+typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
+
+/* bits of the device status word (ce_get_status) */
+#define CE_FLAG_TARGET_OUT_OF_RANGE 0x1u /* some target was neither ignore_index nor in [0, vocab) */
+#define CE_FLAG_NO_VALID_ROWS 0x2u       /* mean over zero valid rows: loss and gradient set to 0 */
+#define CE_FLAG_WAIT_TIMEOUT 0x4u        /* a device-side wait gave up (results invalid) */
+
+/* ce_params.variant: which kernels ce_fwd_bwd uses */
+#define CE_VARIANT_AUTO 0   /* fused single-read kernel when the rows allow it, else split */
+#define CE_VARIANT_SPLIT 1  /* ce_forward then ce_backward kernels (row read twice) */
+#define CE_VARIANT_FUSED 2  /* fused kernel; CE_ERR_UNSUPPORTED if the rows do not allow it */
+/* bits 8..15 of variant: fused-kernel cluster size override (0 = automatic) */
+#define CE_VARIANT_CLUSTER_SHIFT 8
+/* the workspace already holds this batch's normalisers from ce_prepare (same
+ * target, weights, n_rows and reduction): ce_forward / ce_backward /
+ * ce_fwd_bwd skip their own normaliser kernel */
+#define CE_VARIANT_PREPARED 0x10000
+
+typedef struct ce_params {
+    int64_t n_rows;             /* BT >= 0 */
+    int64_t vocab;              /* V >= 1 */
+    int64_t ld;                 /* row stride of logits in elements, >= vocab */
+    int64_t ignore_index;       /* targets equal to this are ignored (torch default -100) */
+    const float *class_weight;  /* device [vocab] fp32, or NULL for all ones */
+    float label_smoothing;      /* eps in [0, 1] */
+    int32_t dtype;              /* ce_dtype of the logits buffer */
+    int32_t reduction;          /* ce_reduction */
+    int32_t target_is_int32;    /* 0: int64 targets, 1: int32 targets */
+    int32_t variant;            /* CE_VARIANT_* (ce_fwd_bwd only) */
+    int32_t reserved;           /* must be 0 */
+} ce_params; /* 64 bytes */
+
+/* Library version string, e.g. "ce-gb300 1.0". */
+const char *ce_version(void);
+
+/* Human-readable name of a status code. */
+const char *ce_status_string(ce_status status);
+
+/* Text of the last CUDA error seen by this thread's calls ("" if none). */
+const char *ce_last_cuda_error(void);
+
+/*
+ * Bytes of workspace the calls below need for these parameters: O(n_rows),
+ * independent of vocab (20 bytes per row plus at most 512 bytes).
+ */
+ce_status ce_workspace_size(const ce_params *p, size_t *bytes);
+
+/*
+ * Batch normalisers into the workspace: the number of valid rows, W_y (the
+ * target-weight sum, the mean's divisor), W_all (the class-weight sum, used
+ * with label smoothing), and the target check (CE_FLAG_TARGET_OUT_OF_RANGE).
+ * Every other call runs this itself unless p->variant has
+ * CE_VARIANT_PREPARED. One single-block kernel; no host synchronisation
+ * (Liger-Kernel #1622: the count and weight sums stay on the device).
+ *   target device [n_rows] int64 / int32.
+ */
+ce_status ce_prepare(const ce_params *p, const void *target, void *workspace,
+                     size_t workspace_bytes, void *stream);
+
+/*
+ * Forward: one online-softmax pass over each row (TransformerEngine #2325's
+ * forward; the row statistics it saves are the pages' m_d_X_y).
+ *   logits    device [n_rows, ld] of p->dtype, read only.
+ *   target    device [n_rows] int64 (or int32 with target_is_int32).
+ *   loss      device fp32: [1] for mean/sum, [n_rows] for none (written).
+ *   stats     device fp32 [n_rows][4] or NULL. Row i gets
+ *             {m_i, s_i, x_{i,t_i}, r_i}: m_i = max_c x_ic;
+ *             s_i = sum_{c != t_i} exp(x_ic - m_i) (all c on invalid rows),
+ *             so that d_i = s_i + exp(x_{i,t_i} - m_i); x_{i,t_i} (0 on invalid
+ *             rows); r_i = sum_c w_c (x_ic - m_i). The target term is kept out
+ *             of s_i so that the backward forms 1 - p_y = s/d without
+ *             cancellation.
+ */
+ce_status ce_forward(const ce_params *p, const void *logits, const void *target, float *loss,
+                     float *stats, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * Backward from saved statistics: reads each row once more and writes the
+ * fp32 gradient, rounded once to p->dtype, over it (TransformerEngine
+ * #2325's backward; dx_y recomputed once in fp32 and stored once, as in
+ * Liger-Kernel #1329).
+ *   logits_inout device [n_rows, ld]: logits in, gradient out (columns >= vocab untouched).
+ *   stats        device fp32 [n_rows][4] from ce_forward on the same logits.
+ *   grad_output  device fp32 [1] for mean/sum, [n_rows] for none, or NULL for 1.0.
+ * The logits are consumed: call it once per forward.
+ */
+ce_status ce_backward(const ce_params *p, void *logits_inout, const void *target,
+                      const float *stats, const float *grad_output, void *workspace,
+                      size_t workspace_bytes, void *stream);
+
+/*
+ * Forward and backward in one call: loss as ce_forward, gradient as
+ * ce_backward, written over the logits. With the fused variant each row is
+ * read from HBM once and written once (the row is held in the shared memory
+ * of a thread-block cluster); the split variant reads it twice. Peak memory
+ * is the logits buffer plus the workspace.
+ *   grad_output device fp32 ([1] or [n_rows] for none) or NULL for 1.0. It is
+ *               applied inside the gradient pass (single rounding).
+ */
+ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target, float *loss,
+                     const float *grad_output, void *workspace, size_t workspace_bytes,
+                     void *stream);
+
+/*
+ * Scale a gradient already written with grad_output = 1 (ce_fwd_bwd with
+ * grad_output NULL) by the grad_output that arrives later: row i is
+ * multiplied by g ([1]) or g_i ([n_rows], reduction none). With a [1]
+ * grad_output equal to 1.0 every block returns after reading it (the
+ * device-side skip of Liger-Kernel #1622). The product is rounded again to
+ * the buffer dtype; callers that know grad_output before the gradient pass
+ * should pass it to ce_fwd_bwd / ce_backward instead (one rounding).
+ *   grad_inout device [n_rows, ld] of p->dtype (columns < vocab are scaled).
+ */
+ce_status ce_scale_grad(const ce_params *p, void *grad_inout, const float *grad_output,
+                        void *stream);
+
+/*
+ * The fused-kernel launch the library picks for these parameters (host
+ * query, no GPU work): cluster size, CTAs per cluster row slice, clusters
+ * in the grid and slice bytes per CTA. Returns CE_ERR_UNSUPPORTED when the
+ * fused kernel cannot take these rows (ce_fwd_bwd then runs split).
+ */
+ce_status ce_fused_plan(const ce_params *p, int32_t *cluster_size, int32_t *n_clusters,
+                        int32_t *ctas_per_sm, int64_t *slice_bytes);
+
+/*
+ * Synchronises `stream`, then copies the workspace status word (CE_FLAG_*
+ * bits of the most recent call that used this workspace) to *flags. The
+ * only call that waits for the GPU.
+ */
+ce_status ce_get_status(const void *workspace, uint32_t *flags, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CE_H */

@@ -1,0 +1,293 @@
+"""GB300 (sm_103a) fused softmax cross-entropy: Python binding of libce.so.
+
+Thin ctypes layer over the C ABI in include/ce.h. It only marshals
+arguments: device pointers from torch tensors, the current CUDA stream, and
+workspace memory allocated through torch. Every step of the computation
+runs in the library's CUDA kernels; there is no CPU or PyTorch fallback,
+and importing this package fails if the library has not been built
+(``python -c "import __graft_entry__ as g; g.build()"``).
+
+Entry points (same names as the C ABI):
+  ce_forward(logits, target, ...)            -> (loss, stats)
+  ce_backward(logits, target, stats, ...)    gradient written over logits
+  ce_fwd_bwd(logits, target, ...)            -> loss; gradient over logits
+  ce_scale_grad(grad, grad_output, ...)      in-place grad_output scaling
+  ce_workspace_size / ce_fused_plan / ce_get_status
+and ``CrossEntropyFunction`` / ``cross_entropy``: a torch.autograd wrapper
+that computes the gradient in the forward (in place) and scales it by
+grad_output in the backward, with a device-side skip when grad_output is 1.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "_lib", "libce.so")
+
+CE_OK, CE_ERR_INVALID_ARG, CE_ERR_UNSUPPORTED, CE_ERR_CUDA, CE_ERR_WORKSPACE = 0, 1, 2, 3, 4
+CE_RED = {"none": 0, "mean": 1, "sum": 2}
+CE_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
+CE_FLAG_TARGET_OUT_OF_RANGE, CE_FLAG_NO_VALID_ROWS, CE_FLAG_WAIT_TIMEOUT = 1, 2, 4
+VARIANTS = {"auto": 0, "split": 1, "fused": 2}
+CE_VARIANT_PREPARED = 0x10000
+
+
+class CEError(RuntimeError):
+    pass
+
+
+class ce_params(ctypes.Structure):
+    _fields_ = [("n_rows", ctypes.c_int64), ("vocab", ctypes.c_int64), ("ld", ctypes.c_int64),
+                ("ignore_index", ctypes.c_int64), ("class_weight", ctypes.c_void_p),
+                ("label_smoothing", ctypes.c_float), ("dtype", ctypes.c_int32),
+                ("reduction", ctypes.c_int32), ("target_is_int32", ctypes.c_int32),
+                ("variant", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
+assert ctypes.sizeof(ce_params) == 64
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libce.so is not built ({LIB_PATH}); run softmax_cross_entropy_pass_gb300._build.build()")
+    lib = ctypes.CDLL(LIB_PATH)
+    P = ctypes.POINTER(ce_params)
+    vp, sz, st = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    sigs = {
+        "ce_version": (ctypes.c_char_p, []),
+        "ce_status_string": (ctypes.c_char_p, [st]),
+        "ce_last_cuda_error": (ctypes.c_char_p, []),
+        "ce_workspace_size": (st, [P, ctypes.POINTER(sz)]),
+        "ce_prepare": (st, [P, vp, vp, sz, vp]),
+        "ce_forward": (st, [P, vp, vp, vp, vp, vp, sz, vp]),
+        "ce_backward": (st, [P, vp, vp, vp, vp, vp, sz, vp]),
+        "ce_fwd_bwd": (st, [P, vp, vp, vp, vp, vp, sz, vp]),
+        "ce_scale_grad": (st, [P, vp, vp, vp]),
+        "ce_fused_plan": (st, [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
+                               ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]),
+        "ce_get_status": (st, [vp, ctypes.POINTER(ctypes.c_uint32), vp]),
+    }
+    for name, (res, args) in sigs.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+_lib = _load()
+
+
+def version() -> str:
+    return _lib.ce_version().decode()
+
+
+def _check(status: int, what: str):
+    if status != CE_OK:
+        msg = _lib.ce_status_string(status).decode()
+        if status == CE_ERR_CUDA:
+            msg += " (" + _lib.ce_last_cuda_error().decode() + ")"
+        raise CEError(f"{what}: {msg}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def make_params(logits: torch.Tensor, target: torch.Tensor, *, weight=None, ignore_index: int = -100,
+                label_smoothing: float = 0.0, reduction: str = "mean", variant="auto",
+                cluster: int = 0) -> ce_params:
+    if logits.dim() != 2 or logits.stride(1) != 1:
+        raise ValueError("logits must be a 2-D tensor with unit column stride")
+    if logits.dtype not in CE_DT:
+        raise TypeError(f"unsupported logits dtype {logits.dtype}")
+    if target.dtype not in (torch.int64, torch.int32):
+        raise TypeError("target must be int64 or int32")
+    n, v = logits.shape
+    if target.numel() != n:
+        raise ValueError("target must have one entry per row")
+    if weight is not None and (weight.dtype != torch.float32 or weight.numel() != v or not weight.is_contiguous()):
+        raise ValueError("weight must be a contiguous fp32 tensor of vocab entries")
+    p = ce_params()
+    p.n_rows, p.vocab = n, v
+    p.ld = logits.stride(0) if n > 1 else v
+    p.ignore_index = ignore_index
+    p.class_weight = weight.data_ptr() if weight is not None else None
+    p.label_smoothing = float(label_smoothing)
+    p.dtype = CE_DT[logits.dtype]
+    p.reduction = CE_RED[reduction]
+    p.target_is_int32 = 1 if target.dtype == torch.int32 else 0
+    p.variant = (VARIANTS[variant] if isinstance(variant, str) else int(variant)) | (int(cluster) << 8)
+    p.reserved = 0
+    return p
+
+
+def ce_workspace_size(n_rows: int) -> int:
+    p = ce_params()
+    p.n_rows, p.vocab, p.ld = n_rows, 1, 1
+    out = ctypes.c_size_t()
+    _check(_lib.ce_workspace_size(ctypes.byref(p), ctypes.byref(out)), "ce_workspace_size")
+    return out.value
+
+
+def workspace(n_rows: int, device=None) -> torch.Tensor:
+    """Workspace tensor for n_rows (device memory from torch's allocator)."""
+    nbytes = ce_workspace_size(n_rows)
+    return torch.empty(nbytes, dtype=torch.uint8, device=device or "cuda")
+
+
+def _ws(ws, n_rows, device):
+    if ws is None:
+        ws = workspace(n_rows, device)
+    return ws, ws.numel() * ws.element_size()
+
+
+def _check_dev(*ts):
+    for t in ts:
+        if t is not None and not t.is_cuda:
+            raise ValueError("all tensors must live on the GPU")
+
+
+def ce_prepare(logits, target, *, weight=None, ignore_index=-100, label_smoothing=0.0,
+               reduction="mean", ws=None, stream=None):
+    """Batch normalisers into a workspace; later calls on it may pass prepared=True."""
+    _check_dev(logits, target, weight)
+    p = make_params(logits, target, weight=weight, ignore_index=ignore_index,
+                    label_smoothing=label_smoothing, reduction=reduction)
+    ws, wsb = _ws(ws, logits.shape[0], logits.device)
+    _check(_lib.ce_prepare(ctypes.byref(p), _ptr(target), _ptr(ws), wsb, _stream(stream)), "ce_prepare")
+    return ws
+
+
+def ce_forward(logits, target, *, weight=None, ignore_index=-100, label_smoothing=0.0,
+               reduction="mean", stats=None, loss=None, ws=None, stream=None):
+    """Loss and per-row statistics [n_rows, 4] (m, off-target exp-sum, x_y, smoothing sum)."""
+    _check_dev(logits, target, weight)
+    p = make_params(logits, target, weight=weight, ignore_index=ignore_index,
+                    label_smoothing=label_smoothing, reduction=reduction)
+    n = logits.shape[0]
+    if loss is None:
+        loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=logits.device)
+    if stats is None:
+        stats = torch.empty(n, 4, dtype=torch.float32, device=logits.device)
+    ws, wsb = _ws(ws, n, logits.device)
+    _check(_lib.ce_forward(ctypes.byref(p), _ptr(logits), _ptr(target), _ptr(loss), _ptr(stats),
+                           _ptr(ws), wsb, _stream(stream)), "ce_forward")
+    return loss, stats
+
+
+def ce_backward(logits, target, stats, *, grad_output=None, weight=None, ignore_index=-100,
+                label_smoothing=0.0, reduction="mean", ws=None, stream=None):
+    """Writes the gradient over ``logits`` (in place) and returns it."""
+    _check_dev(logits, target, stats, grad_output, weight)
+    p = make_params(logits, target, weight=weight, ignore_index=ignore_index,
+                    label_smoothing=label_smoothing, reduction=reduction)
+    ws, wsb = _ws(ws, logits.shape[0], logits.device)
+    _check(_lib.ce_backward(ctypes.byref(p), _ptr(logits), _ptr(target), _ptr(stats),
+                            _ptr(grad_output), _ptr(ws), wsb, _stream(stream)), "ce_backward")
+    return logits
+
+
+def ce_fwd_bwd(logits, target, *, grad_output=None, weight=None, ignore_index=-100,
+               label_smoothing=0.0, reduction="mean", variant="auto", cluster=0, loss=None,
+               ws=None, stream=None, prepared=False):
+    """Loss; the gradient (times grad_output, or 1) is written over ``logits``.
+    ``prepared``: ``ws`` already holds this batch's normalisers (ce_prepare)."""
+    _check_dev(logits, target, grad_output, weight)
+    p = make_params(logits, target, weight=weight, ignore_index=ignore_index,
+                    label_smoothing=label_smoothing, reduction=reduction, variant=variant,
+                    cluster=cluster)
+    if prepared:
+        if ws is None:
+            raise ValueError("prepared=True needs the prepared workspace")
+        p.variant |= CE_VARIANT_PREPARED
+    n = logits.shape[0]
+    if loss is None:
+        loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=logits.device)
+    ws, wsb = _ws(ws, n, logits.device)
+    _check(_lib.ce_fwd_bwd(ctypes.byref(p), _ptr(logits), _ptr(target), _ptr(loss),
+                           _ptr(grad_output), _ptr(ws), wsb, _stream(stream)), "ce_fwd_bwd")
+    return loss
+
+
+def ce_scale_grad(grad, grad_output, *, reduction="mean", vocab=None, stream=None):
+    """grad[i, :vocab] *= grad_output ([1]) or grad_output[i] (reduction none);
+    skipped on the device when a [1] grad_output equals 1."""
+    _check_dev(grad, grad_output)
+    n, v = grad.shape
+    p = ce_params()
+    p.n_rows, p.vocab = n, v if vocab is None else vocab
+    p.ld = grad.stride(0) if n > 1 else v
+    p.dtype = CE_DT[grad.dtype]
+    p.reduction = CE_RED[reduction]
+    _check(_lib.ce_scale_grad(ctypes.byref(p), _ptr(grad), _ptr(grad_output), _stream(stream)),
+           "ce_scale_grad")
+    return grad
+
+
+def ce_fused_plan(n_rows: int, vocab: int, dtype=torch.bfloat16, *, weighted=False,
+                  label_smoothing=0.0, cluster=0):
+    """(cluster_size, n_clusters, ctas_per_sm, slice_bytes) of the fused kernel, or None."""
+    p = ce_params()
+    p.n_rows, p.vocab, p.ld = n_rows, vocab, vocab
+    p.dtype = CE_DT[dtype]
+    p.label_smoothing = label_smoothing
+    p.reduction = 1
+    p.variant = int(cluster) << 8
+    dummy = None
+    if weighted:
+        dummy = torch.empty(vocab, dtype=torch.float32, device="cuda")
+        p.class_weight = dummy.data_ptr()
+    c, ncl, per_sm = ctypes.c_int32(), ctypes.c_int32(), ctypes.c_int32()
+    sb = ctypes.c_int64()
+    st = _lib.ce_fused_plan(ctypes.byref(p), ctypes.byref(c), ctypes.byref(ncl), ctypes.byref(per_sm),
+                            ctypes.byref(sb))
+    if st == CE_ERR_UNSUPPORTED:
+        return None
+    _check(st, "ce_fused_plan")
+    return c.value, ncl.value, per_sm.value, sb.value
+
+
+def ce_get_status(ws, stream=None) -> int:
+    """Synchronises the stream and returns the CE_FLAG_* bits of the last call on ``ws``."""
+    out = ctypes.c_uint32()
+    _check(_lib.ce_get_status(_ptr(ws), ctypes.byref(out), _stream(stream)), "ce_get_status")
+    return out.value
+
+
+class CrossEntropyFunction(torch.autograd.Function):
+    """loss = CE(logits, target); the forward runs the fused pass with
+    grad_output = 1 and leaves the gradient in the logits buffer (one
+    logits tensor of peak memory); the backward scales it by grad_output in
+    place (device-side skip when grad_output == 1). The logits tensor is
+    consumed: its contents after the forward are the gradient."""
+
+    @staticmethod
+    def forward(ctx, logits, target, weight, ignore_index, label_smoothing, reduction):
+        loss = ce_fwd_bwd(logits.detach(), target, weight=weight, ignore_index=ignore_index,
+                          label_smoothing=label_smoothing, reduction=reduction)
+        ctx.save_for_backward(logits.detach())
+        ctx.reduction = reduction
+        out = loss if reduction == "none" else loss.reshape(())
+        return out
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        (grad,) = ctx.saved_tensors
+        g = grad_out.detach().to(torch.float32).reshape(-1).contiguous()
+        ce_scale_grad(grad, g, reduction=ctx.reduction)
+        return grad, None, None, None, None, None
+
+
+def cross_entropy(logits, target, weight=None, ignore_index=-100, label_smoothing=0.0, reduction="mean"):
+    """torch.nn.functional.cross_entropy-like entry; ``logits`` is overwritten by its gradient."""
+    return CrossEntropyFunction.apply(logits, target, weight, ignore_index, label_smoothing, reduction)

@@ -1,0 +1,419 @@
+// ce_device.cuh -- device-side building blocks shared by the cross-entropy
+// kernels: element formats, vector loads/stores with cache hints, the
+// online (max, sum) state and its merge, the per-row scalars of the
+// gradient, and thin inline-PTX wrappers for mbarriers, bulk async copies
+// and cluster shared memory (sm_103a).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ce.h"
+
+namespace ce {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+
+// ------------------------------------------------------------------ workspace
+// Control block at the start of the workspace (the rest holds per-row loss).
+struct WsCtl {
+    unsigned int status;      // CE_FLAG_* bits of the current call
+    unsigned int done;        // blocks finished (last-block reduction)
+    unsigned int pad0[2];
+    float n_valid;            // number of valid rows
+    float w_y;                // sum of w_{t_i} over valid rows (n_valid when unweighted)
+    float w_all;              // sum_c w_c (vocab when unweighted)
+    float pad1;
+};
+constexpr size_t kWsCtlBytes = 256;
+
+// Workspace layout: [control block 256 B][row loss: n_rows fp32, padded to
+// 256 B][row statistics: n_rows x 4 fp32 (split ce_fwd_bwd only)].
+__host__ __device__ inline size_t ws_row_loss_bytes(int64_t n_rows) {
+    return (static_cast<size_t>(n_rows) * sizeof(float) + 255) & ~static_cast<size_t>(255);
+}
+__host__ __device__ inline size_t ws_bytes(int64_t n_rows) {
+    return kWsCtlBytes + ws_row_loss_bytes(n_rows) + static_cast<size_t>(n_rows) * 4 * sizeof(float);
+}
+__host__ __device__ inline float *ws_row_loss(void *ws) {
+    return reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + kWsCtlBytes);
+}
+__host__ __device__ inline float *ws_stats(void *ws, int64_t n_rows) {
+    return reinterpret_cast<float *>(reinterpret_cast<char *>(ws) + kWsCtlBytes + ws_row_loss_bytes(n_rows));
+}
+
+// ------------------------------------------------------------------ element formats
+// 16-byte vectors: 4 fp32 or 8 bf16 / f16 elements.
+template <int DT> struct Fmt;
+template <> struct Fmt<CE_DT_F32> {
+    static constexpr int kVec = 4;
+    static constexpr int kBytes = 4;
+    __device__ static inline void unpack(const uint4 &v, float *x) {
+        x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
+        x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
+    }
+    __device__ static inline uint4 pack(const float *g) {
+        return make_uint4(__float_as_uint(g[0]), __float_as_uint(g[1]),
+                          __float_as_uint(g[2]), __float_as_uint(g[3]));
+    }
+    __device__ static inline float load1(const void *p, int64_t i) {
+        return reinterpret_cast<const float *>(p)[i];
+    }
+    __device__ static inline void store1(void *p, int64_t i, float g) {
+        reinterpret_cast<float *>(p)[i] = g;
+    }
+    // max of a vector (no packed max for fp32)
+    __device__ static inline float vmax(const uint4 &v) {
+        return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
+                     fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
+    }
+};
+template <> struct Fmt<CE_DT_BF16> {
+    static constexpr int kVec = 8;
+    static constexpr int kBytes = 2;
+    __device__ static inline void unpack2(uint32_t u, float &lo, float &hi) {
+        lo = __uint_as_float(u << 16);
+        hi = __uint_as_float(u & 0xffff0000u);
+    }
+    __device__ static inline void unpack(const uint4 &v, float *x) {
+        unpack2(v.x, x[0], x[1]); unpack2(v.y, x[2], x[3]);
+        unpack2(v.z, x[4], x[5]); unpack2(v.w, x[6], x[7]);
+    }
+    __device__ static inline uint32_t pack2(float lo, float hi) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // one RNE rounding each
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ static inline uint4 pack(const float *g) {
+        return make_uint4(pack2(g[0], g[1]), pack2(g[2], g[3]), pack2(g[4], g[5]), pack2(g[6], g[7]));
+    }
+    __device__ static inline float load1(const void *p, int64_t i) {
+        uint16_t b = reinterpret_cast<const uint16_t *>(p)[i];
+        return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    }
+    __device__ static inline void store1(void *p, int64_t i, float g) {
+        reinterpret_cast<__nv_bfloat16 *>(p)[i] = __float2bfloat16_rn(g);
+    }
+    __device__ static inline uint32_t hmax2(uint32_t a, uint32_t b) {
+        __nv_bfloat162 r = __hmax2(*reinterpret_cast<__nv_bfloat162 *>(&a),
+                                   *reinterpret_cast<__nv_bfloat162 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+    // max of 8 elements via packed bf16x2 max, then one unpack
+    __device__ static inline float vmax(const uint4 &v) {
+        uint32_t m = hmax2(hmax2(v.x, v.y), hmax2(v.z, v.w));
+        float lo, hi;
+        unpack2(m, lo, hi);
+        return fmaxf(lo, hi);
+    }
+};
+template <> struct Fmt<CE_DT_F16> {
+    static constexpr int kVec = 8;
+    static constexpr int kBytes = 2;
+    __device__ static inline void unpack2(uint32_t u, float &lo, float &hi) {
+        float2 f = __half22float2(*reinterpret_cast<__half2 *>(&u));
+        lo = f.x; hi = f.y;
+    }
+    __device__ static inline void unpack(const uint4 &v, float *x) {
+        unpack2(v.x, x[0], x[1]); unpack2(v.y, x[2], x[3]);
+        unpack2(v.z, x[4], x[5]); unpack2(v.w, x[6], x[7]);
+    }
+    __device__ static inline uint32_t pack2(float lo, float hi) {
+        __half2 h = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t *>(&h);
+    }
+    __device__ static inline uint4 pack(const float *g) {
+        return make_uint4(pack2(g[0], g[1]), pack2(g[2], g[3]), pack2(g[4], g[5]), pack2(g[6], g[7]));
+    }
+    __device__ static inline float load1(const void *p, int64_t i) {
+        return __half2float(reinterpret_cast<const __half *>(p)[i]);
+    }
+    __device__ static inline void store1(void *p, int64_t i, float g) {
+        reinterpret_cast<__half *>(p)[i] = __float2half_rn(g);
+    }
+    __device__ static inline uint32_t hmax2(uint32_t a, uint32_t b) {
+        __half2 r = __hmax2(*reinterpret_cast<__half2 *>(&a), *reinterpret_cast<__half2 *>(&b));
+        return *reinterpret_cast<uint32_t *>(&r);
+    }
+    __device__ static inline float vmax(const uint4 &v) {
+        uint32_t m = hmax2(hmax2(v.x, v.y), hmax2(v.z, v.w));
+        float lo, hi;
+        unpack2(m, lo, hi);
+        return fmaxf(lo, hi);
+    }
+};
+
+// ------------------------------------------------------------------ memory ops
+__device__ inline uint4 ld_stream_ro(const void *p) {  // read-only, no L1 allocation
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ inline uint4 ld_stream(const void *p) {     // coherent, no L1 allocation
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p));
+    return v;
+}
+__device__ inline void st_stream(void *p, const uint4 &v) {  // streaming store (evict first)
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+__device__ inline uint4 ld_shared_v4(uint32_t addr) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ inline uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------------ targets
+__device__ inline int64_t load_target(const void *target, int is32, int64_t i) {
+    return is32 ? static_cast<int64_t>(reinterpret_cast<const int32_t *>(target)[i])
+                : reinterpret_cast<const int64_t *>(target)[i];
+}
+__device__ inline bool target_valid(int64_t t, int64_t ignore_index, int64_t vocab) {
+    return t != ignore_index && t >= 0 && t < vocab;
+}
+
+// ------------------------------------------------------------------ online softmax state
+// One thread's (or block's) running statistics over a set of columns:
+//   m = max x, s = sum exp(x - m) over non-target columns,
+//   r = sum w_c (x_c - m) (smoothing sum relative to m), n = sum w_c.
+struct RowState {
+    float m, s, r, n;
+};
+__device__ inline RowState row_state_empty() { return RowState{-INFINITY, 0.f, 0.f, 0.f}; }
+
+// Merge two states onto the larger max. Terms n*(m_old - M) are <= 0 and
+// empty states (n == 0) contribute nothing, so no inf*0 appears.
+__device__ inline RowState row_state_merge(const RowState &a, const RowState &b) {
+    float M = fmaxf(a.m, b.m);
+    if (M == -INFINITY) return RowState{-INFINITY, a.s + b.s, a.r + b.r, a.n + b.n};
+    float fa = (a.m == -INFINITY) ? 0.f : exp2f((a.m - M) * kLog2e);
+    float fb = (b.m == -INFINITY) ? 0.f : exp2f((b.m - M) * kLog2e);
+    RowState o;
+    o.m = M;
+    o.s = a.s * fa + b.s * fb;
+    o.r = a.r + b.r + (a.n > 0.f ? a.n * (a.m - M) : 0.f) + (b.n > 0.f ? b.n * (b.m - M) : 0.f);
+    o.n = a.n + b.n;
+    return o;
+}
+
+__device__ inline RowState warp_merge(RowState st) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        RowState o;
+        o.m = __shfl_xor_sync(0xffffffffu, st.m, off);
+        o.s = __shfl_xor_sync(0xffffffffu, st.s, off);
+        o.r = __shfl_xor_sync(0xffffffffu, st.r, off);
+        o.n = __shfl_xor_sync(0xffffffffu, st.n, off);
+        st = row_state_merge(st, o);
+    }
+    return st;
+}
+
+// Fold the values of one vector into the state. `skip` (-1 for none) is the
+// lane holding the target column, left out of s but kept in m, r and n.
+// `SMOOTH` accumulates r and n (label smoothing); `w` is the class weight of
+// each lane (nullptr for all ones).
+template <int VEC, bool SMOOTH>
+__device__ inline void row_state_add(RowState &st, const float *x, float vmax, int skip,
+                                     const float *w) {
+    if (vmax > st.m) {
+        float f = (st.m == -INFINITY) ? 0.f : exp2f((st.m - vmax) * kLog2e);
+        if (SMOOTH && st.n > 0.f) st.r += st.n * (st.m - vmax);
+        st.s *= f;
+        st.m = vmax;
+    }
+    if (st.m == -INFINITY) return;  // every value seen so far is -inf: nothing to add
+    float acc = 0.f;
+    if (skip < 0) {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc += exp2f((x[j] - st.m) * kLog2e);
+    } else {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) acc += (j == skip) ? 0.f : exp2f((x[j] - st.m) * kLog2e);
+    }
+    st.s += acc;
+    if (SMOOTH) {
+        float racc = 0.f, nacc = 0.f;
+        if (w) {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) { racc = fmaf(w[j], x[j] - st.m, racc); nacc += w[j]; }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) racc += x[j] - st.m;
+            nacc = static_cast<float>(VEC);
+        }
+        st.r += racc;
+        st.n += nacc;
+    }
+}
+
+// ------------------------------------------------------------------ per-row scalars
+// Everything the gradient and the loss of one row need, formed once in fp32
+// from the row statistics (m, s, x_y, r) and the batch normalisers.
+struct RowScalars {
+    float neg_log2d;  // -log2(d): p = exp2((x - m) * log2e - log2 d)
+    float m;
+    float a;          // scale * ((1-eps) w_y + (eps/V) W_all): coefficient of p
+    float b;          // scale * eps / V: coefficient of -w_c
+    float dxy;        // the gradient at the target column, formed once
+    float loss;       // loss_i (0 on invalid rows)
+    int64_t y;        // target column (-1 on invalid rows)
+};
+
+__device__ inline float softplus_f(float t) {
+    return t > 0.f ? t + log1pf(expf(-t)) : log1pf(expf(t));
+}
+
+// m, s (off-target exp-sum), xy, r as in the stats layout; wy = w_{t_i};
+// scale = s_i of the gradient; valid = row has a usable target.
+__device__ inline RowScalars make_row_scalars(float m, float s, float xy, float r, bool valid,
+                                              int64_t y, float wy, float w_all, float eps,
+                                              float inv_v, float scale) {
+    RowScalars o;
+    o.m = m;
+    if (!valid) {
+        o.neg_log2d = 0.f; o.a = 0.f; o.b = 0.f; o.dxy = 0.f; o.loss = 0.f; o.y = -1;
+        return o;
+    }
+    const float e_y = expf(xy - m);     // <= 1
+    const float d = s + e_y;            // >= 1
+    const float log_d = logf(d);
+    o.neg_log2d = -log_d * kLog2e;
+    const float eps_v = eps * inv_v;
+    o.a = scale * ((1.f - eps) * wy + eps_v * w_all);
+    o.b = scale * eps_v;
+    const float p_y = e_y / d;
+    const float one_minus_py = s / d;   // no cancellation: s excludes the target
+    o.dxy = scale * (-(1.f - eps) * wy * one_minus_py + eps_v * (p_y * w_all - wy));
+    // LSE - x_y = log1p(s * exp(m - x_y)) = softplus(log s + m - x_y)
+    const float nll = (s > 0.f) ? softplus_f(logf(s) + (m - xy)) : 0.f;
+    o.loss = (1.f - eps) * wy * nll + eps_v * (w_all * log_d - r);
+    o.y = y;
+    return o;
+}
+
+// gradient of one off-target element
+__device__ inline float grad_elem(const RowScalars &rs, float x, float wc) {
+    float p = exp2f(fmaf(x - rs.m, kLog2e, rs.neg_log2d));
+    return fmaf(p, rs.a, -rs.b * wc);
+}
+
+// ------------------------------------------------------------------ mbarrier / bulk copy / cluster
+__device__ inline void mbar_init(uint32_t bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" :: "r"(bar), "r"(count) : "memory");
+}
+__device__ inline void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;"
+                 :: "r"(bar), "r"(bytes) : "memory");
+}
+__device__ inline void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
+}
+// arrive on an mbarrier of another CTA of the cluster (address from mapa),
+// releasing this thread's earlier shared::cluster stores at cluster scope
+__device__ inline void mbar_arrive_remote(uint32_t cluster_bar) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];"
+                 :: "r"(cluster_bar) : "memory");
+}
+__device__ inline bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ inline bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
+    return ok != 0;
+}
+__device__ inline uint64_t globaltimer_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait: gives up after ~`limit_ns` and returns false. A wait that
+// gives up marks `*abort` so that later waits of the CTA return at once.
+template <bool CLUSTER_SCOPE>
+__device__ inline bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
+                                         uint64_t limit_ns = 2000000000ull) {
+    if (CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    uint64_t t0 = globaltimer_ns();
+    for (uint32_t it = 0;; ++it) {
+        if (CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 255u) == 255u) {
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) { *abort = 1; return false; }
+        }
+    }
+}
+
+// 1-D bulk async copy global -> this CTA's shared memory, completing on `bar`.
+// dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ inline void bulk_g2s(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar,
+                                uint64_t policy) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(policy) : "memory");
+}
+__device__ inline uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ inline uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ inline uint32_t cluster_nctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %cluster_nctarank;" : "=r"(r));
+    return r;
+}
+__device__ inline uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ inline uint32_t nclusters_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %nclusterid.x;" : "=r"(r));
+    return r;
+}
+// address of the same shared-memory variable in CTA `rank` of the cluster
+__device__ inline uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+__device__ inline void st_cluster_v4(uint32_t addr, float a, float b, float c, float d) {
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1,%2,%3,%4};"
+                 :: "r"(addr), "f"(a), "f"(b), "f"(c), "f"(d) : "memory");
+}
+__device__ inline void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+__device__ inline void fence_mbar_init_cluster() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+}  // namespace ce

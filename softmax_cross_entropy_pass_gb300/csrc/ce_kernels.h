@@ -1,0 +1,99 @@
+// ce_kernels.h -- host-visible kernel argument blocks and launchers of the
+// cross-entropy library (shared by the C-ABI layer and the kernel files).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "ce.h"
+
+namespace ce {
+
+struct WsCtl;
+
+constexpr int kPrepThreads = 1024;
+constexpr int kRowThreads = 256;
+
+struct PrepArgs {
+    const void *target;
+    int tgt32;
+    int reduction;
+    int64_t n_rows, vocab, ignore_index;
+    const float *weight;
+    int need_w_all;
+    WsCtl *ctl;
+};
+
+// arguments of the split-path row kernels (stats, grad)
+struct RowArgs {
+    const void *logits;        // stats kernel input
+    void *grad;                // grad kernel in/out (in place)
+    int64_t n_rows, vocab, ld;
+    const void *target;
+    int tgt32;
+    int reduction;
+    int64_t ignore_index;
+    const float *weight;
+    float eps;
+    const float *grad_output;  // NULL = 1.0
+    float *loss;               // [1] or [n_rows]
+    float *stats;              // [n_rows][4] (stats: out, grad: in)
+    float *row_loss;           // workspace per-row loss (mean / sum)
+    WsCtl *ctl;
+};
+
+struct ScaleArgs {
+    void *grad;
+    int64_t n_rows, vocab, ld;
+    const float *grad_output;
+    int per_row;
+};
+
+// fused single-read forward + backward (thread-block cluster per row)
+struct FusedArgs {
+    void *x;                   // logits in, gradient out
+    int64_t n_rows, vocab, ld;
+    const void *target;
+    int tgt32;
+    int reduction;
+    int64_t ignore_index;
+    const float *weight;
+    float eps;
+    const float *grad_output;
+    float *loss;
+    float *row_loss;
+    WsCtl *ctl;
+    int64_t slice_elems;       // columns per CTA of a cluster (multiple of 8)
+    int32_t chunk_bytes;       // bulk-copy chunk (multiple of 16)
+    int32_t n_chunks;          // chunks per slice (<= kMaxChunks)
+};
+
+constexpr int kFusedConsumerWarps = 8;
+constexpr int kFusedThreads = (kFusedConsumerWarps + 1) * 32;  // + one producer warp
+constexpr int kMaxChunks = 32;
+constexpr int kMaxCluster = 16;
+
+// smem bytes of the fused kernel besides the row slice
+constexpr int kFusedSmemFixed = 2048;
+
+cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s);
+cudaError_t launch_stats(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s);
+cudaError_t launch_grad(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s);
+cudaError_t launch_scale(const ScaleArgs &a, int dtype, int grid, cudaStream_t s);
+
+// Fused kernel plan / launch. `mode`: 0 no smoothing, 1 smoothing, 2 weighted smoothing.
+struct FusedPlan {
+    int cluster;
+    int n_clusters;
+    int ctas_per_sm;
+    int64_t slice_elems;
+    int chunk_bytes;
+    int n_chunks;
+    size_t smem_bytes;
+};
+cudaError_t fused_plan(int dtype, int mode, int64_t n_rows, int64_t vocab, int cluster_override,
+                       FusedPlan *plan, bool *supported);
+cudaError_t launch_fused(const FusedArgs &a, const FusedPlan &plan, int dtype, int mode,
+                         cudaStream_t s);
+
+}  // namespace ce

@@ -1,0 +1,357 @@
+// ce_split.cu -- the forward/backward split of softmax cross-entropy:
+//   ce_prep_kernel    normalisers (valid count, target-weight sum, class-weight
+//                     sum) and target validation, on the device, no host sync
+//                     (Liger-Kernel #1622, Summary);
+//   ce_stats_kernel   one online-softmax pass per row writing the row
+//                     statistics and the row loss (TransformerEngine #2325's
+//                     forward), with a last-block deterministic reduction;
+//   ce_grad_kernel    rereads each row once and writes the fp32 gradient,
+//                     rounded once, over it; dx_y formed once per row and
+//                     stored once (Liger-Kernel #1329 quoted on #1268);
+//   ce_scale_kernel   grad_output scaling in place with the device-side
+//                     skip when grad_output == 1 (Liger-Kernel #1622).
+// Rows may start at any element alignment: each row is walked as a scalar
+// head up to the first 16-byte boundary, 16-byte vectors, and a scalar tail.
+#include "ce_device.cuh"
+#include "ce_kernels.h"
+
+namespace ce {
+
+// ------------------------------------------------------------------ prep
+__global__ void __launch_bounds__(kPrepThreads) ce_prep_kernel(PrepArgs a) {
+    __shared__ double sh[3][kPrepThreads / 32];
+    __shared__ unsigned sh_bad;
+    if (threadIdx.x == 0) sh_bad = 0;
+    __syncthreads();
+    double cnt = 0.0, wy = 0.0, wall = 0.0;
+    unsigned bad = 0;
+    for (int64_t i = threadIdx.x; i < a.n_rows; i += blockDim.x) {
+        int64_t t = load_target(a.target, a.tgt32, i);
+        if (target_valid(t, a.ignore_index, a.vocab)) {
+            cnt += 1.0;
+            wy += a.weight ? static_cast<double>(__ldg(a.weight + t)) : 1.0;
+        } else if (t != a.ignore_index) {
+            bad = 1;
+        }
+    }
+    if (a.weight && a.need_w_all)
+        for (int64_t c = threadIdx.x; c < a.vocab; c += blockDim.x) wall += __ldg(a.weight + c);
+    // fixed-order block reduction (deterministic)
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        cnt += __shfl_xor_sync(0xffffffffu, cnt, off);
+        wy += __shfl_xor_sync(0xffffffffu, wy, off);
+        wall += __shfl_xor_sync(0xffffffffu, wall, off);
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) { sh[0][warp] = cnt; sh[1][warp] = wy; sh[2][warp] = wall; }
+    if (bad) atomicOr(&sh_bad, 1u);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double c = 0.0, y = 0.0, w = 0.0;
+        for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) { c += sh[0][k]; y += sh[1][k]; w += sh[2][k]; }
+        WsCtl *ctl = a.ctl;
+        unsigned status = sh_bad ? CE_FLAG_TARGET_OUT_OF_RANGE : 0u;
+        if (a.reduction == CE_RED_MEAN && y == 0.0) status |= CE_FLAG_NO_VALID_ROWS;
+        ctl->status = status;
+        ctl->done = 0u;
+        ctl->n_valid = static_cast<float>(c);
+        ctl->w_y = static_cast<float>(y);
+        ctl->w_all = a.weight ? static_cast<float>(w) : static_cast<float>(a.vocab);
+    }
+}
+
+// ------------------------------------------------------------------ shared helpers
+// Column handled by thread `tid` among the scalar columns of a row: the head
+// [0, head) (at most 7 elements) then the tail [tail0, V) (at most 7); -1
+// when the thread has none. Threads 0..head-1 take the head, the next ones
+// the tail.
+__device__ inline int64_t scalar_col(unsigned tid, int64_t head, int64_t tail0, int64_t V) {
+    const int64_t t = static_cast<int64_t>(tid);
+    if (t < head) return t;
+    const int64_t k = t - head;
+    return (k < V - tail0) ? tail0 + k : -1;
+}
+
+__device__ inline float grad_scale(const RowArgs &a, const WsCtl *ctl, int64_t row) {
+    float g = a.grad_output ? __ldg(a.grad_output + (a.reduction == CE_RED_NONE ? row : 0)) : 1.f;
+    if (a.reduction == CE_RED_MEAN) {
+        float wy = ctl->w_y;
+        return wy != 0.f ? g / wy : 0.f;
+    }
+    return g;
+}
+
+// Last block to finish reduces the per-row losses in a fixed order (double
+// accumulation) and resets the counter. Thread 0 of each block must have
+// written its rows' losses before calling.
+__device__ inline void finish_loss(const RowArgs &a, WsCtl *ctl, unsigned n_blocks) {
+    __shared__ unsigned sh_last;
+    __shared__ double sh_sum[32];
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        unsigned prev = atomicAdd(&ctl->done, 1u);
+        sh_last = (prev == n_blocks - 1) ? 1u : 0u;
+    }
+    __syncthreads();
+    if (!sh_last) return;
+    __threadfence();
+    const float *rl = a.row_loss;
+    double s = 0.0;
+    for (int64_t i = threadIdx.x; i < a.n_rows; i += blockDim.x) s += static_cast<double>(__ldcg(rl + i));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if ((threadIdx.x & 31) == 0) sh_sum[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = 0.0;
+        for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) tot += sh_sum[k];
+        if (a.reduction == CE_RED_MEAN) {
+            float wy = ctl->w_y;
+            tot = wy != 0.f ? tot / static_cast<double>(wy) : 0.0;
+        }
+        a.loss[0] = static_cast<float>(tot);
+        ctl->done = 0u;
+    }
+}
+
+// Block-wide merge of per-thread states; the result is valid in thread 0.
+__device__ inline RowState block_merge(RowState st, RowState *sh /*[32]*/) {
+    st = warp_merge(st);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) sh[warp] = st;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        st = lane < nw ? sh[lane] : row_state_empty();
+        st = warp_merge(st);
+    }
+    return st;
+}
+
+// ------------------------------------------------------------------ forward: row statistics
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
+    using F = Fmt<DT>;
+    constexpr int VEC = F::kVec;
+    constexpr bool SMOOTH = MODE != 0;
+    constexpr int UNROLL = 4;
+    __shared__ RowState sh[32];
+    WsCtl *ctl = a.ctl;
+    const float inv_v = 1.f / static_cast<float>(a.vocab);
+
+    for (int64_t row = blockIdx.x; row < a.n_rows; row += gridDim.x) {
+        const char *rowp = reinterpret_cast<const char *>(a.logits) + row * a.ld * F::kBytes;
+        const int64_t t = load_target(a.target, a.tgt32, row);
+        const bool valid = target_valid(t, a.ignore_index, a.vocab);
+        const int64_t y = valid ? t : -1;
+        const int64_t V = a.vocab;
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
+        int64_t head = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) / F::kBytes);
+        if (head > V) head = V;
+        const int64_t nvec = (V - head) / VEC;
+        const int64_t tail0 = head + nvec * VEC;
+
+        RowState st = row_state_empty();
+        // scalar head (< 16 bytes before the first aligned vector) and tail
+        if (const int64_t c = scalar_col(threadIdx.x, head, tail0, V); c >= 0) {
+            float x = F::load1(rowp, c);
+            float w = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
+            row_state_add<1, SMOOTH>(st, &x, x, (c == y) ? 0 : -1, MODE == 2 ? &w : nullptr);
+        }
+        // 16-byte vectors
+        const uint4 *vp = reinterpret_cast<const uint4 *>(rowp + head * F::kBytes);
+        for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += static_cast<int64_t>(blockDim.x) * UNROLL) {
+            uint4 raw[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                int64_t v = v0 + static_cast<int64_t>(u) * blockDim.x;
+                if (v < nvec) raw[u] = ld_stream_ro(vp + v);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                int64_t v = v0 + static_cast<int64_t>(u) * blockDim.x;
+                if (v >= nvec) break;
+                float x[VEC];
+                F::unpack(raw[u], x);
+                const int64_t base = head + v * VEC;
+                const int skip = (static_cast<uint64_t>(y - base) < static_cast<uint64_t>(VEC)) ? static_cast<int>(y - base) : -1;
+                float w[VEC];
+                if (MODE == 2) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) w[j] = __ldg(a.weight + base + j);
+                }
+                row_state_add<VEC, SMOOTH>(st, x, F::vmax(raw[u]), skip, MODE == 2 ? w : nullptr);
+            }
+        }
+        st = block_merge(st, sh);
+        if (threadIdx.x == 0) {
+            const float xy = valid ? F::load1(rowp, y) : 0.f;
+            const float wy = valid ? (a.weight ? __ldg(a.weight + y) : 1.f) : 0.f;
+            // the loss needs no gradient scale
+            RowScalars rs = make_row_scalars(st.m, st.s, xy, st.r, valid, y, wy, ctl->w_all,
+                                             a.eps, inv_v, 1.f);
+            if (a.stats) {
+                float4 s4 = make_float4(st.m, st.s, xy, SMOOTH ? st.r : 0.f);
+                reinterpret_cast<float4 *>(a.stats)[row] = s4;
+            }
+            if (a.reduction == CE_RED_NONE) a.loss[row] = rs.loss;
+            else a.row_loss[row] = rs.loss;
+        }
+        __syncthreads();
+    }
+    if (a.reduction != CE_RED_NONE) finish_loss(a, ctl, gridDim.x);
+}
+
+// ------------------------------------------------------------------ backward: gradient in place
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kRowThreads, 3) ce_grad_kernel(RowArgs a) {
+    using F = Fmt<DT>;
+    constexpr int VEC = F::kVec;
+    constexpr int UNROLL = 4;
+    const WsCtl *ctl = a.ctl;
+    const float inv_v = 1.f / static_cast<float>(a.vocab);
+    const float w_all = ctl->w_all;
+
+    for (int64_t row = blockIdx.x; row < a.n_rows; row += gridDim.x) {
+        char *rowp = reinterpret_cast<char *>(a.grad) + row * a.ld * F::kBytes;
+        const int64_t t = load_target(a.target, a.tgt32, row);
+        const bool valid = target_valid(t, a.ignore_index, a.vocab);
+        const int64_t y = valid ? t : -1;
+        const float4 s4 = __ldg(reinterpret_cast<const float4 *>(a.stats) + row);
+        const float wy = valid ? (a.weight ? __ldg(a.weight + y) : 1.f) : 0.f;
+        const RowScalars rs = make_row_scalars(s4.x, s4.y, s4.z, s4.w, valid, y, wy, w_all, a.eps,
+                                               inv_v, grad_scale(a, ctl, row));
+        const int64_t V = a.vocab;
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
+        int64_t head = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) / F::kBytes);
+        if (head > V) head = V;
+        const int64_t nvec = (V - head) / VEC;
+        const int64_t tail0 = head + nvec * VEC;
+
+        if (const int64_t c = scalar_col(threadIdx.x, head, tail0, V); c >= 0) {
+            float g = 0.f;
+            if (valid) {
+                float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
+                g = (c == y) ? rs.dxy : grad_elem(rs, F::load1(rowp, c), wc);
+            }
+            F::store1(rowp, c, g);
+        }
+        uint4 *vp = reinterpret_cast<uint4 *>(rowp + head * F::kBytes);
+        if (!valid) {
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) st_stream(vp + v, z);
+            continue;
+        }
+        for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += static_cast<int64_t>(blockDim.x) * UNROLL) {
+            uint4 raw[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                int64_t v = v0 + static_cast<int64_t>(u) * blockDim.x;
+                if (v < nvec) raw[u] = ld_stream(vp + v);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                int64_t v = v0 + static_cast<int64_t>(u) * blockDim.x;
+                if (v >= nvec) break;
+                float x[VEC], g[VEC];
+                F::unpack(raw[u], x);
+                const int64_t base = head + v * VEC;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    float wc = (MODE == 2) ? __ldg(a.weight + base + j) : 1.f;
+                    g[j] = grad_elem(rs, x[j], wc);
+                }
+                if (static_cast<uint64_t>(y - base) < static_cast<uint64_t>(VEC)) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) g[e] = (base + e == y) ? rs.dxy : g[e];
+                }
+                st_stream(vp + v, F::pack(g));
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ grad_output scaling in place
+template <int DT>
+__global__ void __launch_bounds__(kRowThreads) ce_scale_kernel(ScaleArgs a) {
+    using F = Fmt<DT>;
+    constexpr int VEC = F::kVec;
+    if (!a.per_row) {
+        const float g = __ldg(a.grad_output);
+        if (g == 1.f) return;  // device-side skip: nothing to scale
+    }
+    for (int64_t row = blockIdx.x; row < a.n_rows; row += gridDim.x) {
+        const float g = __ldg(a.grad_output + (a.per_row ? row : 0));
+        char *rowp = reinterpret_cast<char *>(a.grad) + row * a.ld * F::kBytes;
+        const int64_t V = a.vocab;
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
+        int64_t head = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) / F::kBytes);
+        if (head > V) head = V;
+        const int64_t nvec = (V - head) / VEC;
+        const int64_t tail0 = head + nvec * VEC;
+        if (const int64_t c = scalar_col(threadIdx.x, head, tail0, V); c >= 0)
+            F::store1(rowp, c, F::load1(rowp, c) * g);
+        uint4 *vp = reinterpret_cast<uint4 *>(rowp + head * F::kBytes);
+        for (int64_t v = threadIdx.x; v < nvec; v += blockDim.x) {
+            float x[VEC];
+            F::unpack(ld_stream(vp + v), x);
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) x[j] *= g;
+            st_stream(vp + v, F::pack(x));
+        }
+    }
+}
+
+// ------------------------------------------------------------------ launchers
+template <int DT>
+static cudaError_t launch_stats_dt(const RowArgs &a, int mode, int grid, cudaStream_t s) {
+    switch (mode) {
+    case 0: ce_stats_kernel<DT, 0><<<grid, kRowThreads, 0, s>>>(a); break;
+    case 1: ce_stats_kernel<DT, 1><<<grid, kRowThreads, 0, s>>>(a); break;
+    default: ce_stats_kernel<DT, 2><<<grid, kRowThreads, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+template <int DT>
+static cudaError_t launch_grad_dt(const RowArgs &a, int mode, int grid, cudaStream_t s) {
+    switch (mode) {
+    case 0: ce_grad_kernel<DT, 0><<<grid, kRowThreads, 0, s>>>(a); break;
+    case 1: ce_grad_kernel<DT, 1><<<grid, kRowThreads, 0, s>>>(a); break;
+    default: ce_grad_kernel<DT, 2><<<grid, kRowThreads, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s) {
+    ce_prep_kernel<<<1, kPrepThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_stats(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s) {
+    switch (dtype) {
+    case CE_DT_F32: return launch_stats_dt<CE_DT_F32>(a, mode, grid, s);
+    case CE_DT_BF16: return launch_stats_dt<CE_DT_BF16>(a, mode, grid, s);
+    default: return launch_stats_dt<CE_DT_F16>(a, mode, grid, s);
+    }
+}
+
+cudaError_t launch_grad(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s) {
+    switch (dtype) {
+    case CE_DT_F32: return launch_grad_dt<CE_DT_F32>(a, mode, grid, s);
+    case CE_DT_BF16: return launch_grad_dt<CE_DT_BF16>(a, mode, grid, s);
+    default: return launch_grad_dt<CE_DT_F16>(a, mode, grid, s);
+    }
+}
+
+cudaError_t launch_scale(const ScaleArgs &a, int dtype, int grid, cudaStream_t s) {
+    switch (dtype) {
+    case CE_DT_F32: ce_scale_kernel<CE_DT_F32><<<grid, kRowThreads, 0, s>>>(a); break;
+    case CE_DT_BF16: ce_scale_kernel<CE_DT_BF16><<<grid, kRowThreads, 0, s>>>(a); break;
+    default: ce_scale_kernel<CE_DT_F16><<<grid, kRowThreads, 0, s>>>(a); break;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace ce

@@ -1,0 +1,101 @@
+"""Comparison helpers for the parity tests (CUDA path vs the fp64 oracle).
+
+Tolerances (derived from the arithmetic; the reasoning is in the design
+notes):
+  * loss per row: 1e-5 relative (the floor 1e-6 absolute covers rows whose
+    loss is ~0); reduced loss: 1e-6 relative.
+  * bf16 / f16 gradient: |got - RNE(oracle)| <= max(1 ulp of RNE(oracle),
+    2^-18 * T_ic * |s_i|), T_ic the sum of the magnitudes of the gradient's
+    terms before they cancel: (1-eps) w_y p_ic + (1-eps) w_y [c = y]
+    + (eps/V) p_ic W_all + (eps/V) w_c. fp32 gradient: 2^-18 * T_ic * |s_i|
+    plus 2 fp32 ulps of the value.
+  * dx_y: relative error <= 0.4%.
+"""
+from __future__ import annotations
+
+import torch
+
+LOSS_ROW_RTOL = 1e-5
+LOSS_ROW_ATOL = 1e-6
+LOSS_RED_RTOL = 1e-6
+FLOOR = 2.0 ** -18
+DXY_RTOL = 4e-3
+
+
+def ulp_of(v: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:
+    """Spacing of the representable values of ``dtype`` at |v| (v already
+    representable in dtype), as float64."""
+    a = v.abs().to(dtype)
+    if dtype == torch.float32:
+        up = torch.nextafter(a, torch.full_like(a, float("inf")))
+    else:
+        bits = a.view(torch.int16).to(torch.int32) + 1
+        up = bits.to(torch.int16).view(dtype)
+    return (up.double() - a.double()).abs()
+
+
+def rne(v64: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:
+    return v64.to(torch.float32).to(dtype)
+
+
+def magnitude_T(x: torch.Tensor, target: torch.Tensor, stats64: torch.Tensor, weight, eps: float,
+                w_all: float, scale: torch.Tensor) -> torch.Tensor:
+    """|s_i| * T_ic for every element, in fp64 (rows not valid: 0)."""
+    xd = x.double()
+    R, V = xd.shape
+    m, s, xy = stats64[:, 0:1], stats64[:, 1:2], stats64[:, 2:3]
+    lse = m + torch.log(s + torch.exp(xy - m))
+    p = torch.exp(xd - lse)
+    valid = (target >= 0) & (target < V)
+    tt = target.clamp(0, V - 1)
+    w = weight.double() if weight is not None else torch.ones(V, dtype=torch.float64)
+    wy = w[tt][:, None]
+    onehot = torch.zeros(R, V, dtype=torch.float64)
+    onehot[torch.arange(R), tt] = 1.0
+    T = (1 - eps) * wy * (p + onehot) + (eps / V) * (p * w_all + w[None, :])
+    T = T * scale.abs().reshape(-1, 1).double()
+    T[~valid] = 0.0
+    return T
+
+
+def grad_mismatch(got: torch.Tensor, want64: torch.Tensor, T: torch.Tensor):
+    """(n_bad, n_floor, max_err_over_ulp) for a gradient block on the CPU."""
+    dtype = got.dtype
+    g = got.double()
+    if dtype == torch.float32:
+        tol = FLOOR * T + 2.0 * ulp_of(want64.to(torch.float32), torch.float32)
+        err = (g - want64).abs()
+        bad = err > tol
+        return int(bad.sum()), 0, float((err / tol.clamp_min(1e-300)).max()) if g.numel() else 0.0
+    ref = rne(want64, dtype)
+    u = ulp_of(ref, dtype)
+    err = (g - ref.double()).abs()
+    floor = FLOOR * T
+    ok_ulp = err <= u
+    ok_floor = err <= floor
+    bad = ~(ok_ulp | ok_floor)
+    n_floor = int((~ok_ulp & ok_floor).sum())
+    return int(bad.sum()), n_floor, float((err / u).max()) if g.numel() else 0.0
+
+
+def check_loss_rows(got: torch.Tensor, want64: torch.Tensor):
+    err = (got.double() - want64).abs()
+    tol = LOSS_ROW_RTOL * want64.abs() + LOSS_ROW_ATOL
+    bad = err > tol
+    assert not bad.any(), f"{int(bad.sum())} row losses off; worst rel {float((err / want64.abs().clamp_min(1e-30)).max()):.3e}"
+
+
+def check_loss_reduced(got: float, want: float):
+    assert abs(got - want) <= LOSS_RED_RTOL * abs(want) + 1e-30, f"reduced loss {got!r} vs oracle {want!r}"
+
+
+def row_scale(reduction: str, grad_output, n_rows: int, norm_wy: float) -> torch.Tensor:
+    """s_i of the gradient for every row (fp64)."""
+    if grad_output is None:
+        g = torch.ones(1, dtype=torch.float64)
+    else:
+        g = grad_output.detach().double().cpu().reshape(-1)
+    if reduction == "none":
+        return g.expand(n_rows).clone() if g.numel() == 1 else g
+    s = g[0] / norm_wy if reduction == "mean" and norm_wy != 0 else (g[0] if reduction != "mean" else 0.0)
+    return torch.full((n_rows,), float(s), dtype=torch.float64)

@@ -1,0 +1,98 @@
+"""Host-side checks of the C ABI, runnable without a GPU: the library loads,
+exports every entry point declared in include/*.h, its parameter block has
+the declared layout, argument errors are reported before any CUDA call, and
+the workspace stays O(rows) (the pages' one-logits-tensor memory rule)."""
+import ctypes
+import glob
+import json
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", "", text)
+        for m in re.finditer(r"\b([a-z_][a-z0-9_]*)\s*\(", text):
+            name = m.group(1)
+            # declarations only: return type precedes the name on the same statement
+            before = text[:m.start()].rstrip()
+            if before.endswith(("*", "ce_status", "void", "char", "int", "size_t")) or re.search(
+                    r"(ce_status|const char \*|void|int32_t|size_t)\s*\**\s*$", before):
+                names.add(name)
+    return sorted(n for n in names if n not in {"sizeof"})
+
+
+@pytest.fixture(scope="module")
+def lib():
+    import softmax_cross_entropy_pass_gb300 as ce
+    return ce
+
+
+def test_header_declares_entry_points():
+    names = _declared_functions()
+    for n in ("ce_forward", "ce_backward", "ce_fwd_bwd", "ce_scale_grad", "ce_workspace_size",
+              "ce_get_status", "ce_fused_plan", "ce_version", "ce_status_string"):
+        assert n in names, n
+
+
+def test_library_exports_every_declared_symbol(lib):
+    so = ctypes.CDLL(lib.LIB_PATH)
+    missing = [n for n in _declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    assert "sm_103a" in lib.version()
+    assert lib._lib.ce_status_string(1) == b"CE_ERR_INVALID_ARG"
+
+
+def test_params_layout(lib):
+    P = lib.ce_params
+    assert ctypes.sizeof(P) == 64
+    assert P.class_weight.offset == 32 and P.label_smoothing.offset == 40 and P.reserved.offset == 60
+
+
+def _params(lib, **kw):
+    p = lib.ce_params()
+    p.n_rows, p.vocab, p.ld = kw.get("n_rows", 4), kw.get("vocab", 10), kw.get("ld", 10)
+    p.label_smoothing = kw.get("eps", 0.0)
+    p.dtype, p.reduction = kw.get("dtype", 1), kw.get("reduction", 1)
+    p.variant, p.reserved = kw.get("variant", 0), kw.get("reserved", 0)
+    return p
+
+
+@pytest.mark.parametrize("bad", [dict(vocab=0), dict(ld=5), dict(n_rows=-1), dict(eps=1.5),
+                                 dict(eps=float("nan")), dict(dtype=7), dict(reduction=9),
+                                 dict(reserved=1)])
+def test_invalid_params_rejected_on_host(lib, bad):
+    p = _params(lib, **bad)
+    fake = ctypes.c_void_p(0x1000)
+    st = lib._lib.ce_fwd_bwd(ctypes.byref(p), fake, fake, fake, None, ctypes.c_void_p(0x100000), 1 << 20, None)
+    assert st == lib.CE_ERR_INVALID_ARG
+
+
+def test_workspace_errors_rejected_on_host(lib):
+    p = _params(lib)
+    fake = ctypes.c_void_p(0x1000)
+    # NULL, misaligned and too small workspaces
+    for ws, nb in ((None, 1 << 20), (ctypes.c_void_p(0x100010), 1 << 20), (ctypes.c_void_p(0x100000), 16)):
+        st = lib._lib.ce_fwd_bwd(ctypes.byref(p), fake, fake, fake, None, ws, nb, None)
+        assert st == lib.CE_ERR_WORKSPACE
+
+
+def test_workspace_is_o_rows_and_far_below_one_logits_tensor(lib):
+    """The pages' peak memory for BT=8192, V=128256 bf16 is the logits tensor
+    alone (2004 MB); the library's scratch must be a rounding error on it."""
+    gold = json.load(open(os.path.join(ROOT, "tests", "golden", "peak_memory_mb.json")))
+    mb = gold["bf16_vocab_sweep_bt8192"]["128256"]
+    ws = lib.ce_workspace_size(8192)
+    assert ws <= 20 * 8192 + 512
+    assert ws / 2 ** 20 < 0.001 * mb
+    assert lib.ce_workspace_size(16384) - lib.ce_workspace_size(8192) == 20 * 8192
