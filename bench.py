@@ -199,6 +199,38 @@ def run_reference(args):
     return 0
 
 
+def measure_e2e(ce, pristine, target, work, flush, loss, kw, stream, steps):
+    """ms per step through the public Python API with host inputs: H2D of the
+    logits and targets (pinned), ce_fwd_bwd, D2H of the loss."""
+    import torch
+    host_x = pristine.cpu().pin_memory()
+    host_t = target.cpu().pin_memory()
+    host_loss = torch.empty(1, dtype=torch.float32).pin_memory()
+    dev_t = torch.empty_like(target)
+    e2e_steps = max(3, min(steps, 10))
+    for _ in range(2):
+        work.copy_(host_x, non_blocking=True)
+        dev_t.copy_(host_t, non_blocking=True)
+        ce.ce_fwd_bwd(work, dev_t, **kw)
+        host_loss.copy_(loss, non_blocking=True)
+    torch.cuda.synchronize()
+    e2e_ev = []
+    for _ in range(e2e_steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        work.copy_(host_x, non_blocking=True)
+        dev_t.copy_(host_t, non_blocking=True)
+        ce.ce_fwd_bwd(work, dev_t, **kw)
+        host_loss.copy_(loss, non_blocking=True)
+        b.record(stream)
+        e2e_ev.append((a, b))
+    torch.cuda.synchronize()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps
+
+    return e2e_ms
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_ours(args):
     import torch
@@ -212,6 +244,9 @@ def run_ours(args):
     import softmax_cross_entropy_pass_gb300 as ce
     from workloads import CONFIGS, make_ce_inputs
     cfg = CONFIGS[WORKLOAD]
+    if args.rows:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, n_rows=args.rows)
     R, V = cfg.n_rows, cfg.vocab
     inp = make_ce_inputs(cfg, device=device)
     pristine, target, g = inp["logits"], inp["target"], inp["grad_output"]
@@ -280,30 +315,9 @@ def run_ours(args):
 
     # end to end through the public API with host buffers: H2D of the logits
     # and targets from pinned memory, the call, D2H of the loss
-    host_x = pristine.cpu().pin_memory()
-    host_t = target.cpu().pin_memory()
-    host_loss = torch.empty(1, dtype=torch.float32).pin_memory()
-    dev_t = torch.empty_like(target)
-    e2e_steps = max(3, min(args.steps, 10))
-    for _ in range(2):
-        work.copy_(host_x, non_blocking=True)
-        dev_t.copy_(host_t, non_blocking=True)
-        ce.ce_fwd_bwd(work, dev_t, **kw)
-        host_loss.copy_(loss, non_blocking=True)
-    torch.cuda.synchronize()
-    e2e_ev = []
-    for _ in range(e2e_steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        work.copy_(host_x, non_blocking=True)
-        dev_t.copy_(host_t, non_blocking=True)
-        ce.ce_fwd_bwd(work, dev_t, **kw)
-        host_loss.copy_(loss, non_blocking=True)
-        b.record(stream)
-        e2e_ev.append((a, b))
-    torch.cuda.synchronize()
-    e2e_ms = sum(a.elapsed_time(b) for a, b in e2e_ev) / e2e_steps
+    e2e_ms = float("nan")
+    if not args.no_e2e:
+        e2e_ms = measure_e2e(ce, pristine, target, work, flush, loss, kw, stream, args.steps)
 
     total_ms = reduce_max(total_ms, world, device)
     e2e_ms = reduce_max(e2e_ms, world, device)
@@ -345,7 +359,7 @@ def run_ours(args):
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "ce_fused_kernel<bf16, smoothing>", "kernel_ms": kernel_avg_s * 1e3,
                      "algorithmic_bytes": algo_bytes, "peak_source": peak_kind},
-        "e2e": {"value": R * world / (e2e_ms / 1e3), "unit": "tokens/s",
+        "e2e": None if args.no_e2e else {"value": R * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": pristine.numel() * esz + R * 8, "d2h_bytes_per_step": 4,
                 "ms_per_step": e2e_ms},
         "gpu_launches": 2 * args.steps,
@@ -371,6 +385,8 @@ def main():
     ap.add_argument("--cpu-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--rows", type=int, default=0, help="rows of a smaller case of the workload (profiling)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

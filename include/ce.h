@@ -200,6 +200,66 @@ ce_status ce_fused_plan(const ce_params *p, int32_t *cluster_size, int32_t *n_cl
  */
 ce_status ce_get_status(const void *workspace, uint32_t *flags, void *stream);
 
+/* ------------------------------------------------------------------------
+ * Fused-linear cross-entropy (Liger-Kernel PR "perf(flce): drop host syncs
+ * that do not feed the computation - #1622": logits = hidden x weight^T
+ * formed chunk by chunk, cross-entropy forward and backward on each chunk,
+ * then the gradient GEMMs; the full logits are never materialised and the
+ * host never waits).
+ * ------------------------------------------------------------------------ */
+
+/* CE_GEMM_* output modes of ce_gemm_bf16 */
+#define CE_GEMM_F32_STORE 0   /* D = A B (+ bias[n]) in fp32 */
+#define CE_GEMM_F32_ACCUM 1   /* D += A B in fp32 */
+#define CE_GEMM_BF16_STORE 2  /* D = A B rounded once to bf16 */
+
+/*
+ * D[M,N] = A[M,K] x B[K,N] on the tcgen05 tensor cores: bf16 operands,
+ * fp32 accumulation in tensor memory, 128 x 256 tiles fed by TMA. The GEMM
+ * the fused-linear path is built from, exposed for direct use and testing.
+ *   A  device bf16. a_mn_major = 0: stored [M, K] row-major (row stride
+ *      lda >= K); 1: stored [K, M] (lda >= M).
+ *   B  device bf16. b_mn_major = 0: stored [N, K] (ldb >= K); 1: stored
+ *      [K, N] (ldb >= N).
+ *   D  device fp32 or bf16 (out_kind) [M, N], row stride ldd elements.
+ *   bias device fp32 [N] added in CE_GEMM_F32_STORE mode, or NULL.
+ * Base pointers 16-byte aligned and lda/ldb multiples of 8 (TMA rules),
+ * else CE_ERR_INVALID_ARG.
+ */
+ce_status ce_gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int32_t a_mn_major,
+                       const void *B, int64_t ldb, int32_t b_mn_major, int32_t out_kind, void *D,
+                       int64_t ldd, const float *bias, void *stream);
+
+/* Workspace bytes of flce_fwd_bwd for these sizes (the fp32 logits chunk,
+ * the bf16 logits-gradient chunk and the cross-entropy workspace). */
+ce_status flce_workspace_size(const ce_params *p, int64_t hidden_dim, int64_t chunk_rows, size_t *bytes);
+
+/*
+ * Fused-linear cross-entropy forward and backward.
+ *   p            n_rows = BT, vocab = V, dtype = CE_DT_BF16 (hidden and
+ *                weight), ignore_index, class_weight, label_smoothing,
+ *                reduction; ld and variant are ignored.
+ *   hidden       device bf16 [BT, H] row-major.
+ *   weight       device bf16 [V, H] row-major (the lm head).
+ *   bias         device fp32 [V] or NULL.
+ *   target       device [BT] int64 / int32.
+ *   loss         device fp32 [1] (mean/sum) or [BT] (none).
+ *   grad_output  device fp32 [1] / [BT] or NULL for 1.0, applied to dZ.
+ *   grad_hidden  device bf16 [BT, H] (written).
+ *   grad_weight  device fp32 [V, H] (written: the sum over all chunks).
+ *   grad_bias    device fp32 [V] or NULL (written when bias is given).
+ *   chunk_rows   rows per chunk (> 0); the logits of one chunk,
+ *                chunk_rows x V fp32, are the largest intermediate.
+ * Per chunk: Z = hidden_c W^T (+ b) in fp32; the fused cross-entropy kernel
+ * turns Z into dZ (bf16, one rounding) with the batch's normalisers;
+ * grad_hidden_c = dZ W; grad_weight (+)= dZ^T hidden_c. H and V multiples
+ * of 8.
+ */
+ce_status flce_fwd_bwd(const ce_params *p, int64_t hidden_dim, const void *hidden, const void *weight,
+                       const float *bias, const void *target, float *loss, const float *grad_output,
+                       void *grad_hidden, float *grad_weight, float *grad_bias, int64_t chunk_rows,
+                       void *workspace, size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -70,6 +70,10 @@ def _load():
         "ce_fused_plan": (st, [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]),
         "ce_get_status": (st, [vp, ctypes.POINTER(ctypes.c_uint32), vp]),
+        "ce_gemm_bf16": (st, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int64, ctypes.c_int32,
+                              vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int64, vp, vp]),
+        "flce_workspace_size": (st, [P, ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(sz)]),
+        "flce_fwd_bwd": (st, [P, ctypes.c_int64, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int64, vp, sz, vp]),
     }
     for name, (res, args) in sigs.items():
         fn = getattr(lib, name)
@@ -291,3 +295,72 @@ class CrossEntropyFunction(torch.autograd.Function):
 def cross_entropy(logits, target, weight=None, ignore_index=-100, label_smoothing=0.0, reduction="mean"):
     """torch.nn.functional.cross_entropy-like entry; ``logits`` is overwritten by its gradient."""
     return CrossEntropyFunction.apply(logits, target, weight, ignore_index, label_smoothing, reduction)
+
+
+# ---------------------------------------------------------------------- fused linear
+CE_GEMM_F32_STORE, CE_GEMM_F32_ACCUM, CE_GEMM_BF16_STORE = 0, 1, 2
+
+
+def ce_gemm_bf16(A, B, *, a_mn_major=False, b_mn_major=False, out=None, out_kind=CE_GEMM_F32_STORE,
+                 bias=None, stream=None):
+    """D = A_op @ B_op on the tensor cores. A is [M, K] (or [K, M] when
+    a_mn_major); B is [N, K] (or [K, N] when b_mn_major). Returns D [M, N]."""
+    _check_dev(A, B, out, bias)
+    if A.dtype != torch.bfloat16 or B.dtype != torch.bfloat16:
+        raise TypeError("A and B must be bf16")
+    if A.stride(1) != 1 or B.stride(1) != 1:
+        raise ValueError("A and B must have unit column stride")
+    M = A.shape[1] if a_mn_major else A.shape[0]
+    K = A.shape[0] if a_mn_major else A.shape[1]
+    N = B.shape[1] if b_mn_major else B.shape[0]
+    if (B.shape[0] if b_mn_major else B.shape[1]) != K:
+        raise ValueError("inner dimensions differ")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16 if out_kind == CE_GEMM_BF16_STORE else torch.float32,
+                          device=A.device)
+    _check(_lib.ce_gemm_bf16(M, N, K, _ptr(A), A.stride(0), int(a_mn_major), _ptr(B), B.stride(0),
+                             int(b_mn_major), out_kind, _ptr(out), out.stride(0), _ptr(bias), _stream(stream)),
+           "ce_gemm_bf16")
+    return out
+
+
+def flce_workspace_size(n_rows: int, hidden: int, vocab: int, chunk_rows: int) -> int:
+    p = ce_params()
+    p.n_rows, p.vocab, p.ld, p.dtype = n_rows, vocab, vocab, CE_DT[torch.bfloat16]
+    out = ctypes.c_size_t()
+    _check(_lib.flce_workspace_size(ctypes.byref(p), hidden, chunk_rows, ctypes.byref(out)), "flce_workspace_size")
+    return out.value
+
+
+def flce_fwd_bwd(hidden, weight, target, *, bias=None, class_weight=None, ignore_index=-100,
+                 label_smoothing=0.0, reduction="mean", grad_output=None, chunk_rows=2048, loss=None,
+                 grad_hidden=None, grad_weight=None, grad_bias=None, ws=None, stream=None):
+    """Fused-linear cross-entropy: returns (loss, grad_hidden [BT, H] bf16,
+    grad_weight [V, H] fp32, grad_bias [V] fp32 or None)."""
+    _check_dev(hidden, weight, target, bias, class_weight, grad_output)
+    BT, H = hidden.shape
+    V = weight.shape[0]
+    p = ce_params()
+    p.n_rows, p.vocab, p.ld = BT, V, V
+    p.ignore_index = ignore_index
+    p.class_weight = class_weight.data_ptr() if class_weight is not None else None
+    p.label_smoothing = float(label_smoothing)
+    p.dtype = CE_DT[torch.bfloat16]
+    p.reduction = CE_RED[reduction]
+    p.target_is_int32 = 1 if target.dtype == torch.int32 else 0
+    dev = hidden.device
+    if loss is None:
+        loss = torch.empty(BT if reduction == "none" else 1, dtype=torch.float32, device=dev)
+    if grad_hidden is None:
+        grad_hidden = torch.empty(BT, H, dtype=torch.bfloat16, device=dev)
+    if grad_weight is None:
+        grad_weight = torch.empty(V, H, dtype=torch.float32, device=dev)
+    if bias is not None and grad_bias is None:
+        grad_bias = torch.empty(V, dtype=torch.float32, device=dev)
+    if ws is None:
+        ws = torch.empty(flce_workspace_size(BT, H, V, chunk_rows), dtype=torch.uint8, device=dev)
+    _check(_lib.flce_fwd_bwd(ctypes.byref(p), H, _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(target), _ptr(loss),
+                             _ptr(grad_output), _ptr(grad_hidden), _ptr(grad_weight), _ptr(grad_bias), chunk_rows,
+                             _ptr(ws), ws.numel(), _stream(stream)), "flce_fwd_bwd")
+    return loss, grad_hidden, grad_weight, grad_bias
+

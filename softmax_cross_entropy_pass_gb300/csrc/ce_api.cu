@@ -133,7 +133,8 @@ cudaError_t get_plan(const ce_params *p, FusedPlan *plan, bool *ok) {
 // the rows allow the fused kernel: 16-byte aligned row starts and weights
 bool fused_layout_ok(const ce_params *p, const void *x) {
     const int64_t esz = elem_bytes(p->dtype);
-    if (!aligned(x, 16) || ((p->ld * esz) & 15) != 0) return false;
+    if (!aligned(x, 16)) return false;
+    if (p->n_rows > 1 && ((p->ld * esz) & 15) != 0) return false;
     if (p->class_weight && !aligned(p->class_weight, 16)) return false;
     return true;
 }
@@ -281,6 +282,9 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
     a.loss = loss;
     a.row_loss = ws_row_loss(ws);
     a.ctl = reinterpret_cast<WsCtl *>(ws);
+    a.out = logits_inout;
+    a.ld_out = p->ld;
+    a.finalize = 1;
     e = launch_fused(a, plan, p->dtype, smoothing_mode(p), s);
     return e == cudaSuccess ? CE_OK : cuda_fail(e);
 }

@@ -162,6 +162,9 @@ __device__ inline void st_stream(void *p, const uint4 &v) {  // streaming store 
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};"
                  :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
 }
+__device__ inline void st_stream_v2(void *p, uint32_t a, uint32_t b) {
+    asm volatile("st.global.cs.v2.u32 [%0], {%1,%2};" :: "l"(p), "r"(a), "r"(b) : "memory");
+}
 __device__ inline uint4 ld_shared_v4(uint32_t addr) {
     uint4 v;
     asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];"
@@ -182,6 +185,16 @@ __device__ inline bool target_valid(int64_t t, int64_t ignore_index, int64_t voc
     return t != ignore_index && t >= 0 && t < vocab;
 }
 
+// ------------------------------------------------------------------ exponentials
+// 2^x on the hardware exponential unit (MUFU ex2, approximate, flushing
+// subnormal inputs and results to zero): every exponential of the kernels
+// has x <= 0 and a result in (0, 1]; results under 2^-126 become 0.
+__device__ inline float ex2_hw(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // ------------------------------------------------------------------ online softmax state
 // One thread's (or block's) running statistics over a set of columns:
 //   m = max x, s = sum exp(x - m) over non-target columns,
@@ -196,8 +209,8 @@ __device__ inline RowState row_state_empty() { return RowState{-INFINITY, 0.f, 0
 __device__ inline RowState row_state_merge(const RowState &a, const RowState &b) {
     float M = fmaxf(a.m, b.m);
     if (M == -INFINITY) return RowState{-INFINITY, a.s + b.s, a.r + b.r, a.n + b.n};
-    float fa = (a.m == -INFINITY) ? 0.f : exp2f((a.m - M) * kLog2e);
-    float fb = (b.m == -INFINITY) ? 0.f : exp2f((b.m - M) * kLog2e);
+    float fa = (a.m == -INFINITY) ? 0.f : ex2_hw((a.m - M) * kLog2e);
+    float fb = (b.m == -INFINITY) ? 0.f : ex2_hw((b.m - M) * kLog2e);
     RowState o;
     o.m = M;
     o.s = a.s * fa + b.s * fb;
@@ -227,7 +240,7 @@ template <int VEC, bool SMOOTH>
 __device__ inline void row_state_add(RowState &st, const float *x, float vmax, int skip,
                                      const float *w) {
     if (vmax > st.m) {
-        float f = (st.m == -INFINITY) ? 0.f : exp2f((st.m - vmax) * kLog2e);
+        float f = (st.m == -INFINITY) ? 0.f : ex2_hw((st.m - vmax) * kLog2e);
         if (SMOOTH && st.n > 0.f) st.r += st.n * (st.m - vmax);
         st.s *= f;
         st.m = vmax;
@@ -236,10 +249,10 @@ __device__ inline void row_state_add(RowState &st, const float *x, float vmax, i
     float acc = 0.f;
     if (skip < 0) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) acc += exp2f((x[j] - st.m) * kLog2e);
+        for (int j = 0; j < VEC; ++j) acc += ex2_hw((x[j] - st.m) * kLog2e);
     } else {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) acc += (j == skip) ? 0.f : exp2f((x[j] - st.m) * kLog2e);
+        for (int j = 0; j < VEC; ++j) acc += (j == skip) ? 0.f : ex2_hw((x[j] - st.m) * kLog2e);
     }
     st.s += acc;
     if (SMOOTH) {
@@ -304,7 +317,7 @@ __device__ inline RowScalars make_row_scalars(float m, float s, float xy, float 
 
 // gradient of one off-target element
 __device__ inline float grad_elem(const RowScalars &rs, float x, float wc) {
-    float p = exp2f(fmaf(x - rs.m, kLog2e, rs.neg_log2d));
+    float p = ex2_hw(fmaf(x - rs.m, kLog2e, rs.neg_log2d));
     return fmaf(p, rs.a, -rs.b * wc);
 }
 

@@ -49,9 +49,25 @@ __device__ inline void consumer_sync() {
     asm volatile("bar.sync 1, %0;" :: "n"(kFusedConsumerWarps * 32) : "memory");
 }
 
-template <int DT, int MODE>
+// Writes one vector of gradients (VEC values of the input format) to the
+// output row: 16 bytes when the output has the input's type, 8 bytes for
+// fp32 -> bf16.
+template <int DT, int ODT>
+__device__ inline void store_grad_vec(char *outp, int base, const float *gr) {
+    using F = Fmt<DT>;
+    if constexpr (DT == ODT) {
+        st_stream(outp + static_cast<uint32_t>(base) * F::kBytes, F::pack(gr));
+    } else {
+        static_assert(DT == CE_DT_F32 && ODT == CE_DT_BF16, "fp32 -> bf16 only");
+        st_stream_v2(outp + static_cast<uint32_t>(base) * 2u, Fmt<CE_DT_BF16>::pack2(gr[0], gr[1]),
+                     Fmt<CE_DT_BF16>::pack2(gr[2], gr[3]));
+    }
+}
+
+template <int DT, int MODE, int ODT>
 __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a) {
     using F = Fmt<DT>;
+    using FO = Fmt<ODT>;
     constexpr int VEC = F::kVec;
     constexpr bool SMOOTH = MODE != 0;
     constexpr int NCT = kFusedConsumerWarps * 32;
@@ -94,6 +110,8 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
     volatile int *abort = &S.abort;
     const size_t row_bytes = static_cast<size_t>(a.ld) * F::kBytes;
     char *const xbase = reinterpret_cast<char *>(a.x);
+    const size_t out_row_bytes = static_cast<size_t>(a.ld_out) * FO::kBytes;
+    char *const obase = reinterpret_cast<char *>(a.out);
 
     if (warp == kFusedConsumerWarps) {
         // ---------------------------------------------------------------- producer
@@ -130,12 +148,13 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
             const int64_t t = load_target(a.target, a.tgt32, row);
             const bool valid = target_valid(t, a.ignore_index, V);
             char *rowp = xbase + row * row_bytes;
+            char *outp = obase + row * out_row_bytes;
             if (!valid) {
                 // ignored row: no read, zero gradient, zero loss
-                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-                uint4 *vp = reinterpret_cast<uint4 *>(rowp + lo * F::kBytes);
-                for (int v = tid; v < nvec; v += NCT) st_stream(vp + v, z);
-                if (tid < ntail) F::store1(rowp, tail0 + tid, 0.f);
+                const float zero[VEC] = {};
+                char *const out_slice = outp + lo * FO::kBytes;
+                for (int v = tid; v < nvec; v += NCT) store_grad_vec<DT, ODT>(out_slice, v * VEC, zero);
+                if (tid < ntail) FO::store1(outp, tail0 + tid, 0.f);
                 if (rank == 0 && tid == 0) {
                     if (a.reduction == CE_RED_NONE) a.loss[row] = 0.f;
                     else a.row_loss[row] = 0.f;
@@ -143,6 +162,8 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
                 continue;
             }
             const int64_t y = t;
+            // target column relative to this CTA's slice (outside: a value no vector matches)
+            const int y_rel = (y >= lo && y < hi) ? static_cast<int>(y - lo) : -(1 << 30);
             // ------------------------------------------------ statistics pass over the slice
             RowState st = row_state_empty();
             for (int k = 0; k < nch; ++k) {
@@ -152,11 +173,11 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
                     const uint4 raw = ld_shared_v4(buf + 16u * v);
                     float x[VEC];
                     F::unpack(raw, x);
-                    const int64_t base = lo + static_cast<int64_t>(v) * VEC;
-                    const int skip = (static_cast<uint64_t>(y - base) < static_cast<uint64_t>(VEC)) ? static_cast<int>(y - base) : -1;
+                    const int vb = v * VEC;
+                    const int skip = (static_cast<unsigned>(y_rel - vb) < static_cast<unsigned>(VEC)) ? y_rel - vb : -1;
                     float w[VEC];
                     if (MODE == 2) {
-                        const float4 *wp = reinterpret_cast<const float4 *>(a.weight + base);
+                        const float4 *wp = reinterpret_cast<const float4 *>(a.weight + lo + vb);
 #pragma unroll
                         for (int h = 0; h < VEC / 4; ++h) {
                             float4 w4 = __ldg(wp + h);
@@ -227,15 +248,15 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
                 else a.row_loss[row] = rl.loss;
             }
             // ------------------------------------------------ gradient pass from shared memory
-            uint4 *vp = reinterpret_cast<uint4 *>(rowp + lo * F::kBytes);
+            char *const out_slice = outp + lo * FO::kBytes;
             for (int k = 0; k < nch; ++k) {
                 const int v1 = min(nvec, (k + 1) * vec_per_chunk);
                 for (int v = k * vec_per_chunk + tid; v < v1; v += NCT) {
                     float x[VEC], gr[VEC];
                     F::unpack(ld_shared_v4(buf + 16u * v), x);
-                    const int64_t base = lo + static_cast<int64_t>(v) * VEC;
+                    const int vb = v * VEC;
                     if (MODE == 2) {
-                        const float4 *wp = reinterpret_cast<const float4 *>(a.weight + base);
+                        const float4 *wp = reinterpret_cast<const float4 *>(a.weight + lo + vb);
 #pragma unroll
                         for (int h = 0; h < VEC / 4; ++h) {
                             float4 w4 = __ldg(wp + h);
@@ -248,11 +269,11 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) gr[e] = grad_elem(rs, x[e], 1.f);
                     }
-                    if (static_cast<uint64_t>(y - base) < static_cast<uint64_t>(VEC)) {
+                    if (static_cast<unsigned>(y_rel - vb) < static_cast<unsigned>(VEC)) {
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e) gr[e] = (base + e == y) ? rs.dxy : gr[e];
+                        for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y_rel) ? rs.dxy : gr[e];
                     }
-                    st_stream(vp + v, F::pack(gr));
+                    store_grad_vec<DT, ODT>(out_slice, vb, gr);
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.empty[k]));
@@ -260,12 +281,12 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
             if (tid < ntail) {
                 const int64_t c = tail0 + tid;
                 const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
-                F::store1(rowp, c, (c == y) ? rs.dxy : grad_elem(rs, F::load1(rowp, c), wc));
+                FO::store1(outp, c, (c == y) ? rs.dxy : grad_elem(rs, F::load1(rowp, c), wc));
             }
             ++j;
         }
         // ---------------------------------------------------- batch reduction (last CTA)
-        if (a.reduction != CE_RED_NONE) {
+        if (a.reduction != CE_RED_NONE && a.finalize) {
             __shared__ unsigned sh_last;
             __shared__ double sh_sum[kFusedConsumerWarps];
             consumer_sync();
@@ -300,9 +321,9 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
 }
 
 // ------------------------------------------------------------------ host side: plan and launch
-template <int DT, int MODE>
+template <int DT, int MODE, int ODT = DT>
 static const void *fused_fn() {
-    return reinterpret_cast<const void *>(&ce_fused_kernel<DT, MODE>);
+    return reinterpret_cast<const void *>(&ce_fused_kernel<DT, MODE, ODT>);
 }
 
 static const void *fused_kernel_ptr(int dtype, int mode) {
@@ -319,13 +340,21 @@ static const void *fused_kernel_ptr(int dtype, int mode) {
     }
 }
 
+static const void *fused_f32_to_bf16_ptr(int mode) {
+    switch (mode) {
+    case 0: return fused_fn<CE_DT_F32, 0, CE_DT_BF16>();
+    case 1: return fused_fn<CE_DT_F32, 1, CE_DT_BF16>();
+    default: return fused_fn<CE_DT_F32, 2, CE_DT_BF16>();
+    }
+}
+
 // Largest row slice one CTA holds; three such CTAs share an SM.
 constexpr int64_t kTargetSliceBytes = 64 * 1024;
 constexpr int64_t kMaxSliceBytes = 200 * 1024;
 constexpr int kMinChunkBytes = 8192;
 
-cudaError_t fused_plan(int dtype, int mode, int64_t n_rows, int64_t vocab, int cluster_override,
-                       FusedPlan *plan, bool *supported) {
+static cudaError_t plan_for(const void *fn, int dtype, int64_t n_rows, int64_t vocab,
+                            int cluster_override, FusedPlan *plan, bool *supported) {
     *supported = false;
     const int64_t esz = dtype == CE_DT_F32 ? 4 : 2;
     const int64_t vec = 16 / esz;
@@ -350,8 +379,11 @@ cudaError_t fused_plan(int dtype, int mode, int64_t n_rows, int64_t vocab, int c
     if (chunk < 16) chunk = 16;
     const size_t smem = static_cast<size_t>(((slice_bytes + 127) / 128) * 128) + kFusedSmemFixed;
 
-    const void *fn = fused_kernel_ptr(dtype, mode);
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    // The attribute belongs to the kernel function, not to a launch: set it
+    // to the largest slice any plan may use, so that every cached plan of
+    // this function stays launchable.
+    const size_t smem_cap = static_cast<size_t>(((kMaxSliceBytes + 127) / 128) * 128) + kFusedSmemFixed;
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem_cap));
     if (e != cudaSuccess) return e;
     if (C > 8) {
         e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
@@ -391,13 +423,21 @@ cudaError_t fused_plan(int dtype, int mode, int64_t n_rows, int64_t vocab, int c
     return cudaSuccess;
 }
 
-cudaError_t launch_fused(const FusedArgs &a0, const FusedPlan &plan, int dtype, int mode,
-                         cudaStream_t s) {
+cudaError_t fused_plan(int dtype, int mode, int64_t n_rows, int64_t vocab, int cluster_override,
+                       FusedPlan *plan, bool *supported) {
+    return plan_for(fused_kernel_ptr(dtype, mode), dtype, n_rows, vocab, cluster_override, plan, supported);
+}
+
+cudaError_t fused_plan_f32_to_bf16(int mode, int64_t n_rows, int64_t vocab, FusedPlan *plan,
+                                   bool *supported) {
+    return plan_for(fused_f32_to_bf16_ptr(mode), CE_DT_F32, n_rows, vocab, 0, plan, supported);
+}
+
+static cudaError_t launch_plan(const void *fn, const FusedArgs &a0, const FusedPlan &plan, cudaStream_t s) {
     FusedArgs a = a0;
     a.slice_elems = plan.slice_elems;
     a.chunk_bytes = plan.chunk_bytes;
     a.n_chunks = plan.n_chunks;
-    const void *fn = fused_kernel_ptr(dtype, mode);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(plan.cluster * plan.n_clusters), 1, 1);
     cfg.blockDim = dim3(kFusedThreads, 1, 1);
@@ -412,6 +452,14 @@ cudaError_t launch_fused(const FusedArgs &a0, const FusedPlan &plan, int dtype, 
     cfg.numAttrs = 1;
     void *args[] = {&a};
     return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t launch_fused(const FusedArgs &a, const FusedPlan &plan, int dtype, int mode, cudaStream_t s) {
+    return launch_plan(fused_kernel_ptr(dtype, mode), a, plan, s);
+}
+
+cudaError_t launch_fused_f32_to_bf16(const FusedArgs &a, const FusedPlan &plan, int mode, cudaStream_t s) {
+    return launch_plan(fused_f32_to_bf16_ptr(mode), a, plan, s);
 }
 
 }  // namespace ce

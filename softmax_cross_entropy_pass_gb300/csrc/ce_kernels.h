@@ -66,6 +66,9 @@ struct FusedArgs {
     int64_t slice_elems;       // columns per CTA of a cluster (multiple of 8)
     int32_t chunk_bytes;       // bulk-copy chunk (multiple of 16)
     int32_t n_chunks;          // chunks per slice (<= kMaxChunks)
+    void *out;                 // gradient destination (== x for in place)
+    int64_t ld_out;            // row stride of out in elements of the output dtype
+    int32_t finalize;          // 1: the last CTA reduces the row losses into loss[0]
 };
 
 constexpr int kFusedConsumerWarps = 8;
@@ -95,5 +98,10 @@ cudaError_t fused_plan(int dtype, int mode, int64_t n_rows, int64_t vocab, int c
                        FusedPlan *plan, bool *supported);
 cudaError_t launch_fused(const FusedArgs &a, const FusedPlan &plan, int dtype, int mode,
                          cudaStream_t s);
+// fp32 logits in, bf16 gradient out to a separate buffer (fused-linear chunks)
+cudaError_t launch_fused_f32_to_bf16(const FusedArgs &a, const FusedPlan &plan, int mode,
+                                     cudaStream_t s);
+cudaError_t fused_plan_f32_to_bf16(int mode, int64_t n_rows, int64_t vocab, FusedPlan *plan,
+                                   bool *supported);
 
 }  // namespace ce

@@ -305,53 +305,53 @@ __global__ void __launch_bounds__(kRowThreads) ce_scale_kernel(ScaleArgs a) {
 }
 
 // ------------------------------------------------------------------ launchers
+// cudaLaunchKernel reports the status of this launch itself (a <<<>>> launch
+// followed by cudaGetLastError could return an earlier, unrelated error).
+template <typename Args>
+static cudaError_t launch(const void *fn, int grid, int block, const Args &a, cudaStream_t s) {
+    Args copy = a;
+    void *args[] = {&copy};
+    return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(static_cast<unsigned>(block)), args, 0, s);
+}
+
 template <int DT>
-static cudaError_t launch_stats_dt(const RowArgs &a, int mode, int grid, cudaStream_t s) {
+static const void *stats_fn(int mode) {
     switch (mode) {
-    case 0: ce_stats_kernel<DT, 0><<<grid, kRowThreads, 0, s>>>(a); break;
-    case 1: ce_stats_kernel<DT, 1><<<grid, kRowThreads, 0, s>>>(a); break;
-    default: ce_stats_kernel<DT, 2><<<grid, kRowThreads, 0, s>>>(a); break;
+    case 0: return reinterpret_cast<const void *>(&ce_stats_kernel<DT, 0>);
+    case 1: return reinterpret_cast<const void *>(&ce_stats_kernel<DT, 1>);
+    default: return reinterpret_cast<const void *>(&ce_stats_kernel<DT, 2>);
     }
-    return cudaGetLastError();
 }
 template <int DT>
-static cudaError_t launch_grad_dt(const RowArgs &a, int mode, int grid, cudaStream_t s) {
+static const void *grad_fn(int mode) {
     switch (mode) {
-    case 0: ce_grad_kernel<DT, 0><<<grid, kRowThreads, 0, s>>>(a); break;
-    case 1: ce_grad_kernel<DT, 1><<<grid, kRowThreads, 0, s>>>(a); break;
-    default: ce_grad_kernel<DT, 2><<<grid, kRowThreads, 0, s>>>(a); break;
+    case 0: return reinterpret_cast<const void *>(&ce_grad_kernel<DT, 0>);
+    case 1: return reinterpret_cast<const void *>(&ce_grad_kernel<DT, 1>);
+    default: return reinterpret_cast<const void *>(&ce_grad_kernel<DT, 2>);
     }
-    return cudaGetLastError();
 }
 
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s) {
-    ce_prep_kernel<<<1, kPrepThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return launch(reinterpret_cast<const void *>(&ce_prep_kernel), 1, kPrepThreads, a, s);
 }
 
 cudaError_t launch_stats(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s) {
-    switch (dtype) {
-    case CE_DT_F32: return launch_stats_dt<CE_DT_F32>(a, mode, grid, s);
-    case CE_DT_BF16: return launch_stats_dt<CE_DT_BF16>(a, mode, grid, s);
-    default: return launch_stats_dt<CE_DT_F16>(a, mode, grid, s);
-    }
+    const void *fn = dtype == CE_DT_F32 ? stats_fn<CE_DT_F32>(mode)
+                   : dtype == CE_DT_BF16 ? stats_fn<CE_DT_BF16>(mode) : stats_fn<CE_DT_F16>(mode);
+    return launch(fn, grid, kRowThreads, a, s);
 }
 
 cudaError_t launch_grad(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s) {
-    switch (dtype) {
-    case CE_DT_F32: return launch_grad_dt<CE_DT_F32>(a, mode, grid, s);
-    case CE_DT_BF16: return launch_grad_dt<CE_DT_BF16>(a, mode, grid, s);
-    default: return launch_grad_dt<CE_DT_F16>(a, mode, grid, s);
-    }
+    const void *fn = dtype == CE_DT_F32 ? grad_fn<CE_DT_F32>(mode)
+                   : dtype == CE_DT_BF16 ? grad_fn<CE_DT_BF16>(mode) : grad_fn<CE_DT_F16>(mode);
+    return launch(fn, grid, kRowThreads, a, s);
 }
 
 cudaError_t launch_scale(const ScaleArgs &a, int dtype, int grid, cudaStream_t s) {
-    switch (dtype) {
-    case CE_DT_F32: ce_scale_kernel<CE_DT_F32><<<grid, kRowThreads, 0, s>>>(a); break;
-    case CE_DT_BF16: ce_scale_kernel<CE_DT_BF16><<<grid, kRowThreads, 0, s>>>(a); break;
-    default: ce_scale_kernel<CE_DT_F16><<<grid, kRowThreads, 0, s>>>(a); break;
-    }
-    return cudaGetLastError();
+    const void *fn = dtype == CE_DT_F32 ? reinterpret_cast<const void *>(&ce_scale_kernel<CE_DT_F32>)
+                   : dtype == CE_DT_BF16 ? reinterpret_cast<const void *>(&ce_scale_kernel<CE_DT_BF16>)
+                                         : reinterpret_cast<const void *>(&ce_scale_kernel<CE_DT_F16>);
+    return launch(fn, grid, kRowThreads, a, s);
 }
 
 }  // namespace ce

@@ -1,0 +1,501 @@
+// flce.cu -- fused-linear cross-entropy: the lm-head GEMMs on the 5th
+// generation tensor cores and the chunk loop around the cross-entropy
+// kernel (Liger-Kernel PR #1622's FLCE: logits computed chunk by chunk,
+// never materialised for the whole batch, no host syncs).
+//
+// GEMM kernel: D[M,N] (fp32 in TMEM) = A[M,K] * B[K,N], bf16 operands,
+// 128 x 256 x 64 tiles, persistent CTAs (one per SM), warp-specialised:
+//   warp 0      TMA producer: 2-D tiled bulk tensor loads (128-byte swizzle)
+//               into a 4-stage shared-memory ring;
+//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32
+//               accumulators) and issues tcgen05.mma (one elected thread),
+//               releasing each stage with tcgen05.commit;
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (one row per
+//               thread), optional bias, then fp32 store, fp32 accumulate or
+//               bf16 store; the accumulator is handed back so the next
+//               tile's MMAs overlap this epilogue.
+// Either operand may be K-major or MN-major in memory, so the three FLCE
+// products need no transposed copies:
+//   Z      = h W^T      A = h (K-major), B = W (K-major)
+//   dh     = dZ W       A = dZ (K-major), B = W (MN-major)
+//   dW    += dZ^T h     A = dZ (MN-major), B = h (MN-major)
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include "ce_device.cuh"
+#include "ce_kernels.h"
+#include "flce.h"
+#include "tc_device.cuh"
+
+namespace ce {
+
+constexpr int GB_M = 128, GB_N = 256, GB_K = 64, GB_STAGES = 4;
+constexpr int GB_A_BYTES = GB_M * GB_K * 2;  // 16 KB
+constexpr int GB_B_BYTES = GB_N * GB_K * 2;  // 32 KB
+constexpr int GB_THREADS = 192;
+constexpr int GB_TMEM_COLS = 512;
+constexpr size_t GB_SMEM = 1024 + GB_STAGES * (GB_A_BYTES + GB_B_BYTES) + 256;
+
+enum { OUT_F32_STORE = 0, OUT_F32_ACCUM = 1, OUT_BF16_STORE = 2 };
+
+struct GemmArgs {
+    int M, N, K;
+    int a_mn, b_mn;        // 1: operand is MN-major in memory
+    int out_kind;
+    void *out;
+    int64_t ldo;           // elements
+    const float *bias;     // [N] (fp32 store only) or NULL
+    int tiles_m, tiles_n;
+    int m_fastest;         // tile order: consecutive tiles step along M
+    unsigned int *status;
+};
+
+__device__ inline void tile_coords(const GemmArgs &g, int t, int &tm, int &tn) {
+    if (g.m_fastest) { tm = t % g.tiles_m; tn = t / g.tiles_m; }
+    else { tn = t % g.tiles_n; tm = t / g.tiles_n; }
+}
+
+// One thread's 32 consecutive accumulator columns of one output row.
+__device__ inline void epilogue_store(const GemmArgs &g, int row, int col0, const uint32_t (&v)[32]) {
+    if (row >= g.M) return;
+    const bool full = col0 + 32 <= g.N;
+    if (g.out_kind == OUT_BF16_STORE) {
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(g.out) + static_cast<int64_t>(row) * g.ldo + col0;
+        if (full && (g.ldo % 8) == 0) {
+            uint4 *o4 = reinterpret_cast<uint4 *>(o);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint4 w;
+                w.x = Fmt<CE_DT_BF16>::pack2(__uint_as_float(v[8 * q + 0]), __uint_as_float(v[8 * q + 1]));
+                w.y = Fmt<CE_DT_BF16>::pack2(__uint_as_float(v[8 * q + 2]), __uint_as_float(v[8 * q + 3]));
+                w.z = Fmt<CE_DT_BF16>::pack2(__uint_as_float(v[8 * q + 4]), __uint_as_float(v[8 * q + 5]));
+                w.w = Fmt<CE_DT_BF16>::pack2(__uint_as_float(v[8 * q + 6]), __uint_as_float(v[8 * q + 7]));
+                o4[q] = w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < g.N) o[j] = __float2bfloat16_rn(__uint_as_float(v[j]));
+        }
+        return;
+    }
+    float *o = reinterpret_cast<float *>(g.out) + static_cast<int64_t>(row) * g.ldo + col0;
+    const bool accum = g.out_kind == OUT_F32_ACCUM;
+    if (full && (g.ldo % 4) == 0) {
+        float4 *o4 = reinterpret_cast<float4 *>(o);
+        const float4 *b4 = reinterpret_cast<const float4 *>(g.bias + col0);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            float4 w = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                   __uint_as_float(v[4 * q + 2]), __uint_as_float(v[4 * q + 3]));
+            if (g.bias) {
+                const float4 bb = __ldg(b4 + q);
+                w.x += bb.x; w.y += bb.y; w.z += bb.z; w.w += bb.w;
+            }
+            if (accum) {
+                const float4 old = o4[q];
+                w.x += old.x; w.y += old.y; w.z += old.z; w.w += old.w;
+            }
+            o4[q] = w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (col0 + j < g.N) {
+                float w = __uint_as_float(v[j]) + (g.bias ? __ldg(g.bias + col0 + j) : 0.f);
+                o[j] = accum ? o[j] + w : w;
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(GB_THREADS, 1)
+flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // 128-byte swizzle atoms need 1 KB alignment
+    uint8_t *basep = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + GB_STAGES * GB_A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(basep + GB_STAGES * (GB_A_BYTES + GB_B_BYTES));
+    uint64_t *full = bars, *empty = bars + GB_STAGES, *tfull = bars + 2 * GB_STAGES, *tempty = bars + 2 * GB_STAGES + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * GB_STAGES + 4);
+    int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+    volatile int *abort = abort_flag;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < GB_STAGES; ++s) { mbar_init(smem_u32(&full[s]), 1); mbar_init(smem_u32(&empty[s]), 1); }
+        for (int a = 0; a < 2; ++a) { mbar_init(smem_u32(&tfull[a]), 1); mbar_init(smem_u32(&tempty[a]), 4); }
+        *abort_flag = 0;
+        fence_mbar_init_cluster();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), GB_TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    const int num_tiles = g.tiles_m * g.tiles_n;
+    const int kiters = (g.K + GB_K - 1) / GB_K;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t it = 0;
+            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(g, t, tm, tn);
+                for (int k = 0; k < kiters; ++k, ++it) {
+                    const uint32_t s = it % GB_STAGES, r = it / GB_STAGES;
+                    if (r > 0) mbar_wait_bounded<false>(smem_u32(&empty[s]), (r - 1) & 1u, abort);
+                    const uint32_t fb = smem_u32(&full[s]);
+                    mbar_expect_tx(fb, GB_A_BYTES + GB_B_BYTES);
+                    const uint32_t a_dst = sA + s * GB_A_BYTES, b_dst = sB + s * GB_B_BYTES;
+                    if (!g.a_mn) tma_load_2d(a_dst, &tmA, k * GB_K, tm * GB_M, fb);
+                    else for (int j = 0; j < GB_M / 64; ++j) tma_load_2d(a_dst + j * 8192, &tmA, tm * GB_M + 64 * j, k * GB_K, fb);
+                    if (!g.b_mn) tma_load_2d(b_dst, &tmB, k * GB_K, tn * GB_N, fb);
+                    else for (int j = 0; j < GB_N / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, tn * GB_N + 64 * j, k * GB_K, fb);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            const uint32_t idesc = idesc_bf16_f32(GB_M, GB_N, g.a_mn, g.b_mn);
+            // K-major: the 16-wide K step is 32 bytes inside the swizzle atom, 8-row groups 1 KB apart.
+            // MN-major: the K step is 16 rows of 128 bytes; 64-element MN blocks are 8 KB apart
+            // (one TMA box each), 8-row K groups 1 KB apart.
+            const uint32_t a_kstep = g.a_mn ? 2048u : 32u, b_kstep = g.b_mn ? 2048u : 32u;
+            const uint32_t a_lbo = g.a_mn ? 8192u : 16u, b_lbo = g.b_mn ? 8192u : 16u;
+            uint32_t it = 0, lt = 0;
+            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
+                const uint32_t acc = lt & 1u, u = lt >> 1;
+                if (u > 0) mbar_wait_bounded<false>(smem_u32(&tempty[acc]), (u - 1) & 1u, abort);
+                tc_fence_after();
+                const uint32_t d = tmem + acc * GB_N;
+                for (int k = 0; k < kiters; ++k, ++it) {
+                    const uint32_t s = it % GB_STAGES, r = it / GB_STAGES;
+                    mbar_wait_bounded<false>(smem_u32(&full[s]), r & 1u, abort);
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < GB_K / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(sA + s * GB_A_BYTES + kk * a_kstep, a_lbo, 1024);
+                        const uint64_t bd = smem_desc_sw128(sB + s * GB_B_BYTES + kk * b_kstep, b_lbo, 1024);
+                        mma_bf16(d, ad, bd, idesc, (k | kk) ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&empty[s]));
+                }
+                mma_commit(smem_u32(&tfull[acc]));
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (warps 2..5)
+        const int q = warp & 3;  // TMEM lane quarter this warp may access
+        uint32_t lt = 0;
+        for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
+            int tm, tn;
+            tile_coords(g, t, tm, tn);
+            const uint32_t acc = lt & 1u, u = lt >> 1;
+            mbar_wait_bounded<false>(smem_u32(&tfull[acc]), u & 1u, abort);
+            tc_fence_after();
+            const int row = tm * GB_M + q * 32 + lane;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * GB_N;
+#pragma unroll 1
+            for (int c0 = 0; c0 < GB_N; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + c0, v);
+                tmem_ld_wait();
+                epilogue_store(g, row, tn * GB_N + c0, v);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, GB_TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag && g.status) atomicOr(g.status, CE_FLAG_WAIT_TIMEOUT);
+}
+
+// ------------------------------------------------------------------ small kernels
+// grad_bias[c] (+)= sum over rows of dZ[r, c]
+__global__ void flce_colsum_kernel(const __nv_bfloat16 *dz, int64_t ldd, int rows, int64_t V, float *gb, int accumulate) {
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= V) return;
+    float s = 0.f;
+    for (int r = 0; r < rows; ++r) s += __bfloat162float(dz[static_cast<int64_t>(r) * ldd + c]);
+    gb[c] = accumulate ? gb[c] + s : s;
+}
+
+// loss[0] = sum of the row losses (/ W_y for mean), fixed order, fp64
+__global__ void __launch_bounds__(256) flce_reduce_kernel(const float *row_loss, int64_t n, int reduction,
+                                                          const WsCtl *ctl, float *loss) {
+    __shared__ double sh[8];
+    double s = 0.0;
+    for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += static_cast<double>(row_loss[i]);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
+    if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = s;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        double tot = 0.0;
+        for (int k = 0; k < 8; ++k) tot += sh[k];
+        if (reduction == CE_RED_MEAN) {
+            const float wy = ctl->w_y;
+            tot = wy != 0.f ? tot / static_cast<double>(wy) : 0.0;
+        }
+        loss[0] = static_cast<float>(tot);
+    }
+}
+
+// ------------------------------------------------------------------ host: tensor maps and launch
+static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        cudaDriverEntryPointQueryResult q;
+        void *p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    }
+    return fn;
+}
+
+// 2-D bf16 row-major matrix [rows, cols] with row stride ld (elements), box
+// of box_cols x box_rows, 128-byte swizzle, zero fill out of bounds.
+static cudaError_t make_tmap(CUtensorMap *m, const void *ptr, uint64_t rows, uint64_t cols, uint64_t ld,
+                             uint32_t box_cols, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (!fn) return cudaErrorNotSupported;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {ld * 2};
+    cuuint32_t box[2] = {box_cols, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+static int sm_count() {
+    static int n = 0;
+    if (!n) {
+        int dev = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (n < 1) n = 1;
+    }
+    return n;
+}
+
+// D[M,N] = A[M,K] B[K,N]. A: K-major = memory [M, K] (lda >= K); MN-major =
+// memory [K, M] (lda >= M). B: K-major = memory [N, K]; MN-major = memory [K, N].
+cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B, int64_t ldb,
+                      int b_mn, int out_kind, void *out, int64_t ldo, const float *bias, unsigned int *status,
+                      cudaStream_t s) {
+    if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+    CUtensorMap ta, tb;
+    cudaError_t e;
+    if (!a_mn) e = make_tmap(&ta, A, M, K, lda, GB_K, GB_M);
+    else e = make_tmap(&ta, A, K, M, lda, 64, GB_K);
+    if (e != cudaSuccess) return e;
+    if (!b_mn) e = make_tmap(&tb, B, N, K, ldb, GB_K, GB_N);
+    else e = make_tmap(&tb, B, K, N, ldb, 64, GB_K);
+    if (e != cudaSuccess) return e;
+    GemmArgs g{};
+    g.M = M; g.N = N; g.K = K;
+    g.a_mn = a_mn; g.b_mn = b_mn;
+    g.out_kind = out_kind; g.out = out; g.ldo = ldo; g.bias = bias;
+    g.tiles_m = (M + GB_M - 1) / GB_M;
+    g.tiles_n = (N + GB_N - 1) / GB_N;
+    g.m_fastest = g.tiles_m <= g.tiles_n ? 1 : 0;  // the operand of the short side stays in L2
+    g.status = status;
+    static bool attr_set = false;
+    if (!attr_set) {
+        e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&flce_gemm_kernel),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(GB_SMEM));
+        if (e != cudaSuccess) return e;
+        attr_set = true;
+    }
+    const int tiles = g.tiles_m * g.tiles_n;
+    const int grid = tiles < sm_count() ? tiles : sm_count();
+    void *args[] = {&ta, &tb, &g};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(&flce_gemm_kernel), dim3(grid), dim3(GB_THREADS), args,
+                            GB_SMEM, s);
+}
+
+}  // namespace ce
+
+// ------------------------------------------------------------------ C ABI
+using namespace ce;
+
+namespace {
+
+bool al16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
+
+struct FlceLayout {
+    size_t ce_ws, z_off, dz_off, total;
+    int64_t ldz, ldd;
+};
+
+FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk) {
+    FlceLayout L{};
+    L.ce_ws = round_up(static_cast<int64_t>(ws_bytes(n_rows)), 1024);
+    L.ldz = round_up(vocab, 4);
+    L.ldd = round_up(vocab, 8);
+    L.z_off = L.ce_ws;
+    L.dz_off = L.z_off + round_up(chunk * L.ldz * 4, 1024);
+    L.total = L.dz_off + round_up(chunk * L.ldd * 2, 1024);
+    return L;
+}
+
+ce_status flce_cuda_fail(cudaError_t e) {
+    (void)cudaGetLastError();
+    return e == cudaSuccess ? CE_OK : CE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+ce_status ce_gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int32_t a_mn, const void *B,
+                       int64_t ldb, int32_t b_mn, int32_t out_kind, void *D, int64_t ldd, const float *bias,
+                       void *stream) {
+    if (M < 0 || N < 0 || K < 0 || M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return CE_ERR_INVALID_ARG;
+    if ((a_mn != 0 && a_mn != 1) || (b_mn != 0 && b_mn != 1)) return CE_ERR_INVALID_ARG;
+    if (out_kind < CE_GEMM_F32_STORE || out_kind > CE_GEMM_BF16_STORE) return CE_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return CE_OK;
+    if (!A || !B || !D || !al16(A) || !al16(B)) return CE_ERR_INVALID_ARG;
+    if ((lda % 8) || (ldb % 8) || lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldd < N) return CE_ERR_INVALID_ARG;
+    if (bias && out_kind != CE_GEMM_F32_STORE) return CE_ERR_INVALID_ARG;
+    if (K == 0) return CE_ERR_UNSUPPORTED;
+    cudaError_t e = gemm_bf16(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), A, lda, a_mn, B, ldb,
+                              b_mn, out_kind, D, ldd, bias, nullptr, reinterpret_cast<cudaStream_t>(stream));
+    return flce_cuda_fail(e);
+}
+
+ce_status flce_workspace_size(const ce_params *p, int64_t hidden_dim, int64_t chunk_rows, size_t *bytes) {
+    if (!p || !bytes || p->n_rows < 0 || p->vocab < 1 || hidden_dim < 1 || chunk_rows < 1) return CE_ERR_INVALID_ARG;
+    int64_t chunk = chunk_rows < p->n_rows ? chunk_rows : (p->n_rows > 0 ? p->n_rows : 1);
+    *bytes = flce_layout(p->n_rows, p->vocab, chunk).total;
+    return CE_OK;
+}
+
+ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const void *weight, const float *bias,
+                       const void *target, float *loss, const float *grad_output, void *grad_hidden,
+                       float *grad_weight, float *grad_bias, int64_t chunk_rows, void *ws, size_t ws_bytes,
+                       void *stream) {
+    if (!p || p->n_rows < 0 || p->vocab < 1 || H < 1 || chunk_rows < 1) return CE_ERR_INVALID_ARG;
+    if (p->dtype != CE_DT_BF16 || (H % 8) || (p->vocab % 8)) return CE_ERR_UNSUPPORTED;
+    if (p->reduction != CE_RED_NONE && p->reduction != CE_RED_MEAN && p->reduction != CE_RED_SUM)
+        return CE_ERR_INVALID_ARG;
+    if (!(p->label_smoothing >= 0.f && p->label_smoothing <= 1.f) || p->reserved != 0) return CE_ERR_INVALID_ARG;
+    if (p->target_is_int32 != 0 && p->target_is_int32 != 1) return CE_ERR_INVALID_ARG;
+    if (p->class_weight && (reinterpret_cast<uintptr_t>(p->class_weight) & 15u)) return CE_ERR_INVALID_ARG;
+    if (!loss || !ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CE_ERR_INVALID_ARG;
+    const int64_t BT = p->n_rows, V = p->vocab;
+    if (BT > INT32_MAX || V > INT32_MAX || H > INT32_MAX) return CE_ERR_UNSUPPORTED;
+    const int64_t C = chunk_rows < BT ? chunk_rows : (BT > 0 ? BT : 1);
+    const FlceLayout L = flce_layout(BT, V, C);
+    if (ws_bytes < L.total) return CE_ERR_WORKSPACE;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (BT > 0 && (!hidden || !weight || !target || !grad_hidden || !grad_weight)) return CE_ERR_INVALID_ARG;
+    if (BT > 0 && (!al16(hidden) || !al16(weight) || !al16(grad_hidden) || !al16(grad_weight))) return CE_ERR_INVALID_ARG;
+    if (bias && !grad_bias) return CE_ERR_INVALID_ARG;
+
+    WsCtl *ctl = reinterpret_cast<WsCtl *>(ws);
+    char *wsb = reinterpret_cast<char *>(ws);
+    float *Z = reinterpret_cast<float *>(wsb + L.z_off);
+    __nv_bfloat16 *dZ = reinterpret_cast<__nv_bfloat16 *>(wsb + L.dz_off);
+    float *row_loss = ws_row_loss(ws);
+
+    // batch normalisers over every row (the mean's W_y spans all chunks)
+    PrepArgs pa{};
+    pa.target = target; pa.tgt32 = p->target_is_int32; pa.reduction = p->reduction;
+    pa.n_rows = BT; pa.vocab = V; pa.ignore_index = p->ignore_index; pa.weight = p->class_weight;
+    pa.need_w_all = p->label_smoothing > 0.f ? 1 : 0; pa.ctl = ctl;
+    cudaError_t e = launch_prep(pa, s);
+    if (e != cudaSuccess) return flce_cuda_fail(e);
+    if (BT == 0) {
+        if (p->reduction != CE_RED_NONE && (e = cudaMemsetAsync(loss, 0, sizeof(float), s)) != cudaSuccess)
+            return flce_cuda_fail(e);
+        if ((e = cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * H * 4, s)) != cudaSuccess)
+            return flce_cuda_fail(e);
+        if (grad_bias && (e = cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(V) * 4, s)) != cudaSuccess)
+            return flce_cuda_fail(e);
+        return CE_OK;
+    }
+    const int mode = p->label_smoothing <= 0.f ? 0 : (p->class_weight ? 2 : 1);
+    FusedPlan plan{};
+    bool ok = false;
+    if ((e = fused_plan_f32_to_bf16(mode, C, V, &plan, &ok)) != cudaSuccess) return flce_cuda_fail(e);
+    if (!ok) return CE_ERR_UNSUPPORTED;
+    const int tgt_bytes = p->target_is_int32 ? 4 : 8;
+
+    for (int64_t r0 = 0; r0 < BT; r0 += C) {
+        const int64_t c = (BT - r0) < C ? (BT - r0) : C;
+        const char *h_c = reinterpret_cast<const char *>(hidden) + r0 * H * 2;
+        // Z = h_c W^T (+ b), fp32
+        e = gemm_bf16(static_cast<int>(c), static_cast<int>(V), static_cast<int>(H), h_c, H, 0, weight, H, 0,
+                      0, Z, L.ldz, bias, &ctl->status, s);
+        if (e != cudaSuccess) return flce_cuda_fail(e);
+        // cross-entropy forward + backward on the chunk: dZ (bf16) and row losses
+        FusedArgs a{};
+        a.x = Z; a.n_rows = c; a.vocab = V; a.ld = L.ldz;
+        a.target = reinterpret_cast<const char *>(target) + r0 * tgt_bytes;
+        a.tgt32 = p->target_is_int32; a.reduction = p->reduction; a.ignore_index = p->ignore_index;
+        a.weight = p->class_weight; a.eps = p->label_smoothing;
+        a.grad_output = grad_output ? (p->reduction == CE_RED_NONE ? grad_output + r0 : grad_output) : nullptr;
+        a.loss = p->reduction == CE_RED_NONE ? loss + r0 : loss;
+        a.row_loss = row_loss + r0;
+        a.ctl = ctl;
+        a.out = dZ; a.ld_out = L.ldd; a.finalize = 0;
+        FusedPlan pl = plan;
+        if (pl.n_clusters > c) pl.n_clusters = static_cast<int>(c);
+        if ((e = launch_fused_f32_to_bf16(a, pl, mode, s)) != cudaSuccess) return flce_cuda_fail(e);
+        // grad_hidden_c = dZ W   (A = dZ K-major, B = W stored [V, H] = [K, N]: MN-major)
+        e = gemm_bf16(static_cast<int>(c), static_cast<int>(H), static_cast<int>(V), dZ, L.ldd, 0, weight, H, 1,
+                      2, reinterpret_cast<char *>(grad_hidden) + r0 * H * 2, H, nullptr, &ctl->status, s);
+        if (e != cudaSuccess) return flce_cuda_fail(e);
+        // grad_weight (+)= dZ^T h_c   (A = dZ stored [c, V] = [K, M]: MN-major; B = h_c [K, N]: MN-major)
+        e = gemm_bf16(static_cast<int>(V), static_cast<int>(H), static_cast<int>(c), dZ, L.ldd, 1, h_c, H, 1,
+                      r0 == 0 ? 0 : 1, grad_weight, H, nullptr, &ctl->status, s);
+        if (e != cudaSuccess) return flce_cuda_fail(e);
+        if (grad_bias) {
+            const int threads = 256;
+            const int blocks = static_cast<int>((V + threads - 1) / threads);
+            const __nv_bfloat16 *dzc = dZ;
+            int64_t ldd = L.ldd;
+            int rows = static_cast<int>(c);
+            int64_t vv = V;
+            int accum = r0 == 0 ? 0 : 1;
+            void *args[] = {&dzc, &ldd, &rows, &vv, &grad_bias, &accum};
+            e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_colsum_kernel), dim3(blocks), dim3(threads),
+                                 args, 0, s);
+            if (e != cudaSuccess) return flce_cuda_fail(e);
+        }
+    }
+    if (p->reduction != CE_RED_NONE) {
+        const float *rl = row_loss;
+        int64_t n = BT;
+        int red = p->reduction;
+        const WsCtl *cc = ctl;
+        void *args[] = {&rl, &n, &red, &cc, &loss};
+        e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_reduce_kernel), dim3(1), dim3(256), args, 0, s);
+        if (e != cudaSuccess) return flce_cuda_fail(e);
+    }
+    return CE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,18 @@
+// flce.h -- internal declarations of the tensor-core GEMM used by the
+// fused-linear cross-entropy.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ce {
+
+// D[M,N] (op)= A[M,K] B[K,N] with bf16 operands and fp32 accumulation.
+// a_mn / b_mn: operand stored MN-major (A as [K, M], B as [K, N]) instead of
+// K-major (A as [M, K], B as [N, K]). out_kind: 0 fp32 store (+ bias[N]),
+// 1 fp32 accumulate, 2 bf16 store.
+cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B,
+                      int64_t ldb, int b_mn, int out_kind, void *out, int64_t ldo, const float *bias,
+                      unsigned int *status, cudaStream_t s);
+
+}  // namespace ce

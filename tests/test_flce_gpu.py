@@ -1,0 +1,129 @@
+"""Tensor-core GEMM and fused-linear cross-entropy on the GPU.
+
+The GEMM is checked against a float64 matmul of the same bf16 operands in
+all four operand layouts; the fused-linear path against the fp64 oracle
+(float64 matmul + the row oracle). Tolerances come from the arithmetic:
+the GEMMs accumulate exact bf16 products in fp32; dZ is rounded once to
+bf16 (relative error <= 2^-9 per element) before the two gradient GEMMs,
+so |error| <= 2^-8 * sum |dZ| |operand| (factor 2 margin) plus one output
+rounding."""
+import pytest
+import torch
+
+import oracle
+from workloads import FLCE_CONFIGS, make_flce_inputs, make_targets
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def ce():
+    assert torch.cuda.is_available()
+    import softmax_cross_entropy_pass_gb300 as ce
+    return ce
+
+
+def _rand_bf16(*shape, seed=0, scale=1.0):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(*shape, generator=g) * scale).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("a_mn", [False, True])
+@pytest.mark.parametrize("b_mn", [False, True])
+@pytest.mark.parametrize("shape", [(128, 256, 64), (200, 300, 136), (1024, 2048, 1024), (384, 512, 4096)])
+def test_gemm_layouts_against_float64(ce, a_mn, b_mn, shape):
+    M, N, K = shape
+    A = _rand_bf16(M, K, seed=1)                # logical [M, K]
+    B = _rand_bf16(N, K, seed=2)                # logical [N, K] (B^T)
+    ref = A.double() @ B.double().T
+    A_mem = (A.T.contiguous() if a_mn else A).cuda()
+    B_mem = (B.T.contiguous() if b_mn else B).cuda()
+    D = ce.ce_gemm_bf16(A_mem, B_mem, a_mn_major=a_mn, b_mn_major=b_mn)
+    torch.cuda.synchronize()
+    bound = (A.double().abs() @ B.double().abs().T) * (K * 2.0 ** -23) + 1e-30
+    err = (D.double().cpu() - ref).abs()
+    assert (err <= bound).all(), f"max err {float(err.max()):.3e}"
+
+
+def test_gemm_bias_accumulate_and_bf16_out(ce):
+    M, N, K = 256, 512, 256
+    A = _rand_bf16(M, K, seed=3).cuda()
+    B = _rand_bf16(N, K, seed=4).cuda()
+    bias = torch.randn(N, device="cuda")
+    ref = A.double() @ B.double().T
+    D = ce.ce_gemm_bf16(A, B, bias=bias)
+    assert torch.allclose(D.double(), ref + bias.double(), rtol=1e-5, atol=1e-3)
+    ce.ce_gemm_bf16(A, B, out=D, out_kind=ce.CE_GEMM_F32_ACCUM)
+    assert torch.allclose(D.double(), 2 * ref + bias.double(), rtol=1e-5, atol=2e-3)
+    Db = ce.ce_gemm_bf16(A, B, out_kind=ce.CE_GEMM_BF16_STORE)
+    assert torch.equal(Db, ref.float().to(torch.bfloat16)) or \
+        ((Db.double() - ref).abs() <= ref.abs() * 2.0 ** -8 + 1e-3).all()
+
+
+def _flce_check(out, ref, hidden, weight, rows, cols, dz_abs_rows=None):
+    loss, gh, gw, gb = out
+    # loss: bf16 operands exact, fp32 GEMM accumulation and fp32 CE
+    if ref["loss"] is not None and not torch.is_tensor(ref["loss"]):
+        assert abs(float(loss.item()) - ref["loss"]) <= 1e-4 * abs(ref["loss"])
+    return loss, gh, gw, gb
+
+
+@pytest.mark.parametrize("reduction", ["mean", "sum"])
+@pytest.mark.parametrize("chunk", [128, 1000])
+@pytest.mark.parametrize("with_bias", [False, True])
+def test_flce_small_against_oracle(ce, reduction, chunk, with_bias):
+    cfg = FLCE_CONFIGS["flce_small"]
+    inp = make_flce_inputs(cfg, device="cuda")
+    h, W, t = inp["hidden"], inp["weight"], inp["target"]
+    BT, H = h.shape
+    V = W.shape[0]
+    bias = (torch.randn(V, generator=torch.Generator().manual_seed(9)) * 0.1).cuda() if with_bias else None
+    eps = 0.05
+    loss, gh, gw, gb = ce.flce_fwd_bwd(h, W, t, bias=bias, label_smoothing=eps, reduction=reduction,
+                                        chunk_rows=chunk)
+    torch.cuda.synchronize()
+    ref = oracle.flce(h.cpu(), W.cpu(), t.cpu(), bias=None if bias is None else bias.cpu(),
+                      label_smoothing=eps, reduction=reduction)
+    assert abs(float(loss.item()) - ref["loss"]) <= 1e-4 * abs(ref["loss"])
+    # dZ (oracle, fp64) for the error bounds
+    z = h.double().cpu() @ W.double().cpu().T + (0 if bias is None else bias.double().cpu())
+    dz = oracle.rows(z, t.cpu(), label_smoothing=eps, reduction=reduction, norm_wy=ref["norm_wy"],
+                     want_stats=False)["grad"]
+    bound_h = (dz.abs() @ W.double().cpu().abs()) * 2.0 ** -8 + 1e-30
+    ref_h = ref["grad_hidden"]
+    err_h = (gh.double().cpu() - ref_h).abs()
+    ulp_h = ref_h.abs() * 2.0 ** -7
+    assert (err_h <= bound_h + ulp_h).all(), f"grad_hidden max err {float(err_h.max()):.3e}"
+    bound_w = (dz.abs().T @ h.double().cpu().abs()) * 2.0 ** -8 + 1e-30
+    err_w = (gw.double().cpu() - ref["grad_weight"]).abs()
+    assert (err_w <= bound_w + ref["grad_weight"].abs() * 2.0 ** -20).all(), \
+        f"grad_weight max err {float(err_w.max()):.3e}"
+    if with_bias:
+        err_b = (gb.double().cpu() - ref["grad_bias"]).abs()
+        assert (err_b <= dz.abs().sum(0) * 2.0 ** -8 + 1e-30).all()
+
+
+@pytest.mark.slow
+def test_flce_full_size_sampled(ce):
+    """hidden 8192 x 4096, W 128256 x 4096: loss over all rows, grad_hidden on
+    256 sampled rows and grad_weight on 256 sampled vocabulary rows against
+    the fp64 oracle."""
+    cfg = FLCE_CONFIGS["flce"]
+    inp = make_flce_inputs(cfg, device="cuda")
+    h, W, t = inp["hidden"], inp["weight"], inp["target"]
+    loss, gh, gw, _ = ce.flce_fwd_bwd(h, W, t, reduction="mean", chunk_rows=2048)
+    torch.cuda.synchronize()
+    gen = torch.Generator().manual_seed(77)
+    rows = torch.randperm(cfg.n_rows, generator=gen)[:256].sort().values
+    cols = torch.randperm(cfg.vocab, generator=gen)[:256].sort().values
+    ref = oracle.flce(h.cpu(), W.cpu(), t.cpu(), reduction="mean", sample_rows=rows, sample_cols=cols)
+    assert abs(float(loss.item()) - ref["loss"]) <= 1e-4 * abs(ref["loss"])
+    gh_s = gh[rows.cuda()].double().cpu()
+    gw_s = gw[cols.cuda()].double().cpu()
+    # relative to each row's / column's max norm (the oracle's dZ is fp64)
+    eh = (gh_s - ref["grad_hidden"]).abs().max(dim=1).values / ref["grad_hidden"].abs().max(dim=1).values.clamp_min(1e-30)
+    ew = (gw_s - ref["grad_weight"]).abs().max(dim=1).values / ref["grad_weight"].abs().max(dim=1).values.clamp_min(1e-30)
+    valid = t.cpu()[rows] >= 0
+    assert eh[valid].max() <= 2e-2, f"grad_hidden rel err {float(eh.max()):.3e}"
+    assert ew.max() <= 1e-3, f"grad_weight rel err {float(ew.max()):.3e}"
+    assert torch.count_nonzero(gh_s[~valid]) == 0
