@@ -258,11 +258,7 @@ def run_ours(args):
     kw = dict(label_smoothing=cfg.label_smoothing, reduction=cfg.reduction, grad_output=g, loss=loss,
               ws=ws, stream=stream, variant=args.variant, cluster=args.cluster)
 
-    def step(prepared_split=False):
-        if prepared_split:
-            ce.ce_prepare(work, target, label_smoothing=cfg.label_smoothing, reduction=cfg.reduction,
-                          ws=ws, stream=stream)
-            return ce.ce_fwd_bwd(work, target, prepared=True, **kw)
+    def step():
         return ce.ce_fwd_bwd(work, target, **kw)
 
     for _ in range(args.warmup):
@@ -280,20 +276,20 @@ def run_ours(args):
     sampler = ClockSampler(local)
     if rank == 0:
         sampler.start()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
-           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
     for k in range(args.steps):
         work.copy_(pristine)
         flush.zero_()
         ev[k][0].record(stream)
-        step(prepared_split=True)  # normaliser kernel | fused kernel, one event between
-        ev[k][2].record(stream)
+        step()  # normaliser kernel + cross-entropy kernel(s)
+        ev[k][1].record(stream)
     torch.cuda.synchronize()
     barrier(world)
     clocks = sampler.stop() if rank == 0 else None
-    step_ms = [a.elapsed_time(c) for a, _, c in ev]
+    step_ms = [a.elapsed_time(c) for a, c in ev]
     total_ms = sum(step_ms)
 
     # the fused kernel alone (for the roofline): same steps, events around
@@ -362,7 +358,7 @@ def run_ours(args):
         "e2e": None if args.no_e2e else {"value": R * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": pristine.numel() * esz + R * 8, "d2h_bytes_per_step": 4,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": (3 if args.variant == "split" else 2) * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
@@ -380,7 +376,7 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--variant", choices=["auto", "fused", "split"], default="auto")
+    ap.add_argument("--variant", choices=["auto", "fused", "split", "rowpass"], default="auto")
     ap.add_argument("--cluster", type=int, default=0)
     ap.add_argument("--cpu-rows", type=int, default=2048)
     ap.add_argument("--ref-rows", type=int, default=512)

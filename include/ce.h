@@ -79,7 +79,9 @@ typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
 #define CE_VARIANT_AUTO 0   /* fused single-read kernel when the rows allow it, else split */
 #define CE_VARIANT_SPLIT 1  /* ce_forward then ce_backward kernels (row read twice) */
 #define CE_VARIANT_FUSED 2  /* fused kernel; CE_ERR_UNSUPPORTED if the rows do not allow it */
-/* bits 8..15 of variant: fused-kernel cluster size override (0 = automatic) */
+#define CE_VARIANT_ROWPASS 3 /* one kernel, each row read twice, the second read from L2 */
+/* bits 8..15 of variant: fused-kernel cluster size override, or CTAs per SM
+ * of the row-pass kernel (0 = automatic) */
 #define CE_VARIANT_CLUSTER_SHIFT 8
 /* the workspace already holds this batch's normalisers from ce_prepare (same
  * target, weights, n_rows and reduction): ce_forward / ce_backward /

@@ -32,7 +32,7 @@ CE_OK, CE_ERR_INVALID_ARG, CE_ERR_UNSUPPORTED, CE_ERR_CUDA, CE_ERR_WORKSPACE = 0
 CE_RED = {"none": 0, "mean": 1, "sum": 2}
 CE_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 CE_FLAG_TARGET_OUT_OF_RANGE, CE_FLAG_NO_VALID_ROWS, CE_FLAG_WAIT_TIMEOUT = 1, 2, 4
-VARIANTS = {"auto": 0, "split": 1, "fused": 2}
+VARIANTS = {"auto": 0, "split": 1, "fused": 2, "rowpass": 3}
 CE_VARIANT_PREPARED = 0x10000
 
 

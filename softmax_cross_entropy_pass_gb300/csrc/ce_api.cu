@@ -225,9 +225,26 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
     if (!loss || (p->n_rows > 0 && (!logits_inout || !target))) return CE_ERR_INVALID_ARG;
     const int path = p->variant & 0xff;
     if (p->variant & ~(0xffff | CE_VARIANT_PREPARED)) return CE_ERR_INVALID_ARG;
-    if (path != CE_VARIANT_AUTO && path != CE_VARIANT_SPLIT && path != CE_VARIANT_FUSED)
+    if (path != CE_VARIANT_AUTO && path != CE_VARIANT_SPLIT && path != CE_VARIANT_FUSED &&
+        path != CE_VARIANT_ROWPASS)
         return CE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if (path == CE_VARIANT_ROWPASS) {
+        cudaError_t e = enqueue_prep(p, target, ws, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (p->n_rows == 0) {
+            if (p->reduction != CE_RED_NONE && (e = cudaMemsetAsync(loss, 0, sizeof(float), s)) != cudaSuccess)
+                return cuda_fail(e);
+            return CE_OK;
+        }
+        RowArgs a = row_args(p, target, ws);
+        a.grad = logits_inout;
+        a.loss = loss;
+        a.grad_output = grad_output;
+        e = launch_rowpass(a, p->dtype, smoothing_mode(p), (p->variant >> CE_VARIANT_CLUSTER_SHIFT) & 0xff, s);
+        return e == cudaSuccess ? CE_OK : cuda_fail(e);
+    }
 
     bool use_fused = false;
     FusedPlan plan{};
@@ -285,7 +302,7 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
     a.out = logits_inout;
     a.ld_out = p->ld;
     a.finalize = 1;
-    e = launch_fused(a, plan, p->dtype, smoothing_mode(p), s);
+    e = launch_fused(a, plan, p->dtype, smoothing_mode(p), s, (p->variant & CE_VARIANT_PREPARED) == 0);
     return e == cudaSuccess ? CE_OK : cuda_fail(e);
 }
 

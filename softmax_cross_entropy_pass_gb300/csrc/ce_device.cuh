@@ -198,24 +198,25 @@ __device__ inline float ex2_hw(float x) {
 // ------------------------------------------------------------------ online softmax state
 // One thread's (or block's) running statistics over a set of columns:
 //   m = max x, s = sum exp(x - m) over non-target columns,
-//   r = sum w_c (x_c - m) (smoothing sum relative to m), n = sum w_c.
+//   r = sum w_c x_c (the smoothing sum), n = sum w_c.
+// r is kept as a plain sum; the statistics report r - n*m, the smoothing
+// sum relative to m.
 struct RowState {
     float m, s, r, n;
 };
 __device__ inline RowState row_state_empty() { return RowState{-INFINITY, 0.f, 0.f, 0.f}; }
 
-// Merge two states onto the larger max. Terms n*(m_old - M) are <= 0 and
-// empty states (n == 0) contribute nothing, so no inf*0 appears.
+// Merge two states onto the larger max.
 __device__ inline RowState row_state_merge(const RowState &a, const RowState &b) {
     float M = fmaxf(a.m, b.m);
-    if (M == -INFINITY) return RowState{-INFINITY, a.s + b.s, a.r + b.r, a.n + b.n};
-    float fa = (a.m == -INFINITY) ? 0.f : ex2_hw((a.m - M) * kLog2e);
-    float fb = (b.m == -INFINITY) ? 0.f : ex2_hw((b.m - M) * kLog2e);
     RowState o;
     o.m = M;
-    o.s = a.s * fa + b.s * fb;
-    o.r = a.r + b.r + (a.n > 0.f ? a.n * (a.m - M) : 0.f) + (b.n > 0.f ? b.n * (b.m - M) : 0.f);
+    o.r = a.r + b.r;
     o.n = a.n + b.n;
+    if (M == -INFINITY) { o.s = a.s + b.s; return o; }
+    float fa = (a.m == -INFINITY) ? 0.f : ex2_hw((a.m - M) * kLog2e);
+    float fb = (b.m == -INFINITY) ? 0.f : ex2_hw((b.m - M) * kLog2e);
+    o.s = a.s * fa + b.s * fb;
     return o;
 }
 
@@ -233,41 +234,47 @@ __device__ inline RowState warp_merge(RowState st) {
 }
 
 // Fold the values of one vector into the state. `skip` (-1 for none) is the
-// lane holding the target column, left out of s but kept in m, r and n.
+// lane holding the target column, left out of s but kept in m and r.
 // `SMOOTH` accumulates r and n (label smoothing); `w` is the class weight of
-// each lane (nullptr for all ones).
+// each lane (nullptr for all ones). One FFMA and one MUFU ex2 per element
+// for the exp-sum: exp(x - m) = 2^(x log2e - m log2e).
 template <int VEC, bool SMOOTH>
 __device__ inline void row_state_add(RowState &st, const float *x, float vmax, int skip,
                                      const float *w) {
     if (vmax > st.m) {
-        float f = (st.m == -INFINITY) ? 0.f : ex2_hw((st.m - vmax) * kLog2e);
-        if (SMOOTH && st.n > 0.f) st.r += st.n * (st.m - vmax);
-        st.s *= f;
+        if (st.m != -INFINITY) st.s *= ex2_hw((st.m - vmax) * kLog2e);
         st.m = vmax;
     }
+    if (SMOOTH) {
+        float racc = 0.f;
+        if (w) {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) { racc = fmaf(w[j], x[j], racc); st.n += w[j]; }
+        } else {
+#pragma unroll
+            for (int j = 0; j < VEC; ++j) racc += x[j];
+            st.n += static_cast<float>(VEC);
+        }
+        st.r += racc;
+    }
     if (st.m == -INFINITY) return;  // every value seen so far is -inf: nothing to add
+    const float mL = st.m * kLog2e;
     float acc = 0.f;
     if (skip < 0) {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) acc += ex2_hw((x[j] - st.m) * kLog2e);
+        for (int j = 0; j < VEC; ++j) acc += ex2_hw(fmaf(x[j], kLog2e, -mL));
     } else {
 #pragma unroll
-        for (int j = 0; j < VEC; ++j) acc += (j == skip) ? 0.f : ex2_hw((x[j] - st.m) * kLog2e);
+        for (int j = 0; j < VEC; ++j) acc += (j == skip) ? 0.f : ex2_hw(fmaf(x[j], kLog2e, -mL));
     }
     st.s += acc;
-    if (SMOOTH) {
-        float racc = 0.f, nacc = 0.f;
-        if (w) {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) { racc = fmaf(w[j], x[j] - st.m, racc); nacc += w[j]; }
-        } else {
-#pragma unroll
-            for (int j = 0; j < VEC; ++j) racc += x[j] - st.m;
-            nacc = static_cast<float>(VEC);
-        }
-        st.r += racc;
-        st.n += nacc;
-    }
+}
+
+// the smoothing sum relative to the row max, as reported in the statistics
+// (the product is rounded on its own, not fused into the subtraction, so a
+// row of equal logits gives exactly 0)
+__device__ inline float row_state_rel_sum(const RowState &st) {
+    return st.n > 0.f ? __fsub_rn(st.r, __fmul_rn(st.n, st.m)) : 0.f;
 }
 
 // ------------------------------------------------------------------ per-row scalars
@@ -390,6 +397,13 @@ __device__ inline uint64_t policy_evict_first() {
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
+
+// Programmatic dependent launch: the normaliser kernel lets the next kernel
+// of the stream start at once; that kernel waits for the normalisers (the
+// whole previous grid, with its memory visible) only where it reads them.
+// Both are no-ops when the launch carries no programmatic dependency.
+__device__ inline void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ inline void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 __device__ inline uint32_t cluster_ctarank() {
     uint32_t r;

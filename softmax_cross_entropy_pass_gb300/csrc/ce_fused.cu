@@ -141,8 +141,8 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
         // ---------------------------------------------------------------- consumers
         const float inv_v = 1.f / static_cast<float>(V);
         const float eps = a.eps;
-        const float w_all = a.ctl->w_all;
-        const float w_y_sum = a.ctl->w_y;
+        float w_all = 0.f, w_y_sum = 0.f;   // batch normalisers, read after the normaliser kernel ends
+        bool have_norm = false;
         uint32_t j = 0;
         for (int64_t row = q; row < a.n_rows; row += nq) {
             const int64_t t = load_target(a.target, a.tgt32, row);
@@ -234,15 +234,22 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
             const uint32_t owner = static_cast<uint32_t>(y / a.slice_elems);
             const float xy = S.slot[par][owner].xy;
             // ------------------------------------------------ row scalars and loss
+            if (!have_norm) {
+                pdl_wait();
+                w_all = a.ctl->w_all;
+                w_y_sum = a.ctl->w_y;
+                have_norm = true;
+            }
             const float wy = a.weight ? __ldg(a.weight + y) : 1.f;
             float g = a.grad_output ? __ldg(a.grad_output + (a.reduction == CE_RED_NONE ? row : 0)) : 1.f;
             float scale = g;
             if (a.reduction == CE_RED_MEAN) scale = (w_y_sum != 0.f) ? g / w_y_sum : 0.f;
-            const RowScalars rs = make_row_scalars(tot.m, tot.s, xy, tot.r, true, y, wy, w_all,
+            const float rrel = row_state_rel_sum(tot);
+            const RowScalars rs = make_row_scalars(tot.m, tot.s, xy, rrel, true, y, wy, w_all,
                                                    eps, inv_v, scale);
             if (rank == 0 && tid == 0) {
                 // loss_i without the gradient scale
-                const RowScalars rl = make_row_scalars(tot.m, tot.s, xy, tot.r, true, y, wy, w_all,
+                const RowScalars rl = make_row_scalars(tot.m, tot.s, xy, rrel, true, y, wy, w_all,
                                                        eps, inv_v, 1.f);
                 if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
                 else a.row_loss[row] = rl.loss;
@@ -289,6 +296,10 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
         if (a.reduction != CE_RED_NONE && a.finalize) {
             __shared__ unsigned sh_last;
             __shared__ double sh_sum[kFusedConsumerWarps];
+            if (!have_norm) {
+                pdl_wait();
+                w_y_sum = a.ctl->w_y;
+            }
             consumer_sync();
             if (tid == 0) {
                 __threadfence();
@@ -316,7 +327,10 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
         }
     }
     __syncthreads();
-    if (tid == 0 && S.abort) atomicOr(&a.ctl->status, CE_FLAG_WAIT_TIMEOUT);
+    if (tid == 0 && S.abort) {
+        pdl_wait();  // the status word is rewritten by the normaliser kernel
+        atomicOr(&a.ctl->status, CE_FLAG_WAIT_TIMEOUT);
+    }
     cluster_sync_all();  // no CTA leaves while a peer may still write into it
 }
 
@@ -433,7 +447,13 @@ cudaError_t fused_plan_f32_to_bf16(int mode, int64_t n_rows, int64_t vocab, Fuse
     return plan_for(fused_f32_to_bf16_ptr(mode), CE_DT_F32, n_rows, vocab, 0, plan, supported);
 }
 
-static cudaError_t launch_plan(const void *fn, const FusedArgs &a0, const FusedPlan &plan, cudaStream_t s) {
+// `after_prep`: the previous kernel on the stream is the normaliser kernel,
+// which writes nothing this kernel reads before its griddepcontrol.wait, so
+// the launch may overlap it. Any other predecessor (for instance the GEMM
+// that writes the logits) must complete first: the producer warp reads the
+// logits at once.
+static cudaError_t launch_plan(const void *fn, const FusedArgs &a0, const FusedPlan &plan, cudaStream_t s,
+                               bool after_prep) {
     FusedArgs a = a0;
     a.slice_elems = plan.slice_elems;
     a.chunk_bytes = plan.chunk_bytes;
@@ -443,23 +463,26 @@ static cudaError_t launch_plan(const void *fn, const FusedArgs &a0, const FusedP
     cfg.blockDim = dim3(kFusedThreads, 1, 1);
     cfg.dynamicSmemBytes = plan.smem_bytes;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = plan.cluster;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // overlap the normaliser kernel
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = after_prep ? 2 : 1;
     void *args[] = {&a};
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-cudaError_t launch_fused(const FusedArgs &a, const FusedPlan &plan, int dtype, int mode, cudaStream_t s) {
-    return launch_plan(fused_kernel_ptr(dtype, mode), a, plan, s);
+cudaError_t launch_fused(const FusedArgs &a, const FusedPlan &plan, int dtype, int mode, cudaStream_t s,
+                         bool after_prep) {
+    return launch_plan(fused_kernel_ptr(dtype, mode), a, plan, s, after_prep);
 }
 
 cudaError_t launch_fused_f32_to_bf16(const FusedArgs &a, const FusedPlan &plan, int mode, cudaStream_t s) {
-    return launch_plan(fused_f32_to_bf16_ptr(mode), a, plan, s);
+    return launch_plan(fused_f32_to_bf16_ptr(mode), a, plan, s, false);
 }
 
 }  // namespace ce

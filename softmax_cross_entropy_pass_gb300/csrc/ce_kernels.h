@@ -11,8 +11,9 @@ namespace ce {
 
 struct WsCtl;
 
-constexpr int kPrepThreads = 1024;
+constexpr int kPrepThreads = 256;
 constexpr int kRowThreads = 256;
+constexpr int kRowpassThreads = 512;
 
 struct PrepArgs {
     const void *target;
@@ -83,6 +84,8 @@ cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s);
 cudaError_t launch_stats(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s);
 cudaError_t launch_grad(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s);
 cudaError_t launch_scale(const ScaleArgs &a, int dtype, int grid, cudaStream_t s);
+// one-kernel forward + backward, two passes per row (second from L2)
+cudaError_t launch_rowpass(const RowArgs &a, int dtype, int mode, int ctas_per_sm, cudaStream_t s);
 
 // Fused kernel plan / launch. `mode`: 0 no smoothing, 1 smoothing, 2 weighted smoothing.
 struct FusedPlan {
@@ -97,7 +100,7 @@ struct FusedPlan {
 cudaError_t fused_plan(int dtype, int mode, int64_t n_rows, int64_t vocab, int cluster_override,
                        FusedPlan *plan, bool *supported);
 cudaError_t launch_fused(const FusedArgs &a, const FusedPlan &plan, int dtype, int mode,
-                         cudaStream_t s);
+                         cudaStream_t s, bool after_prep);
 // fp32 logits in, bf16 gradient out to a separate buffer (fused-linear chunks)
 cudaError_t launch_fused_f32_to_bf16(const FusedArgs &a, const FusedPlan &plan, int mode,
                                      cudaStream_t s);

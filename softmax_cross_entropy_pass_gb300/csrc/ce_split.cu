@@ -18,24 +18,50 @@
 namespace ce {
 
 // ------------------------------------------------------------------ prep
+// One small block (it shares an SM with the next kernel's CTAs, which may
+// start before it ends): every thread keeps 8 target loads in flight.
 __global__ void __launch_bounds__(kPrepThreads) ce_prep_kernel(PrepArgs a) {
+    pdl_launch_dependents();
     __shared__ double sh[3][kPrepThreads / 32];
     __shared__ unsigned sh_bad;
+    constexpr int U = 8;
     if (threadIdx.x == 0) sh_bad = 0;
     __syncthreads();
     double cnt = 0.0, wy = 0.0, wall = 0.0;
     unsigned bad = 0;
-    for (int64_t i = threadIdx.x; i < a.n_rows; i += blockDim.x) {
-        int64_t t = load_target(a.target, a.tgt32, i);
-        if (target_valid(t, a.ignore_index, a.vocab)) {
-            cnt += 1.0;
-            wy += a.weight ? static_cast<double>(__ldg(a.weight + t)) : 1.0;
-        } else if (t != a.ignore_index) {
-            bad = 1;
+    for (int64_t i0 = threadIdx.x; i0 < a.n_rows; i0 += static_cast<int64_t>(blockDim.x) * U) {
+        int64_t t[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int64_t i = i0 + static_cast<int64_t>(u) * blockDim.x;
+            t[u] = i < a.n_rows ? load_target(a.target, a.tgt32, i) : a.ignore_index;
         }
+        float w[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const bool ok = target_valid(t[u], a.ignore_index, a.vocab);
+            w[u] = ok ? (a.weight ? __ldg(a.weight + t[u]) : 1.f) : 0.f;
+            cnt += ok ? 1.0 : 0.0;
+            bad |= (!ok && t[u] != a.ignore_index) ? 1u : 0u;
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) wy += static_cast<double>(w[u]);
     }
-    if (a.weight && a.need_w_all)
-        for (int64_t c = threadIdx.x; c < a.vocab; c += blockDim.x) wall += __ldg(a.weight + c);
+    if (a.weight && a.need_w_all) {
+        const int64_t n4 = (reinterpret_cast<uintptr_t>(a.weight) & 15u) ? 0 : a.vocab / 4;
+        const float4 *w4 = reinterpret_cast<const float4 *>(a.weight);
+        for (int64_t c0 = threadIdx.x; c0 < n4; c0 += static_cast<int64_t>(blockDim.x) * U) {
+            float4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t c = c0 + static_cast<int64_t>(u) * blockDim.x;
+                v[u] = c < n4 ? __ldg(w4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) wall += static_cast<double>(v[u].x) + v[u].y + v[u].z + v[u].w;
+        }
+        for (int64_t c = 4 * n4 + threadIdx.x; c < a.vocab; c += blockDim.x) wall += __ldg(a.weight + c);
+    }
     // fixed-order block reduction (deterministic)
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
@@ -140,6 +166,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
     __shared__ RowState sh[32];
     WsCtl *ctl = a.ctl;
     const float inv_v = 1.f / static_cast<float>(a.vocab);
+    pdl_wait();
 
     for (int64_t row = blockIdx.x; row < a.n_rows; row += gridDim.x) {
         const char *rowp = reinterpret_cast<const char *>(a.logits) + row * a.ld * F::kBytes;
@@ -190,10 +217,11 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
             const float xy = valid ? F::load1(rowp, y) : 0.f;
             const float wy = valid ? (a.weight ? __ldg(a.weight + y) : 1.f) : 0.f;
             // the loss needs no gradient scale
-            RowScalars rs = make_row_scalars(st.m, st.s, xy, st.r, valid, y, wy, ctl->w_all,
+            const float rrel = SMOOTH ? row_state_rel_sum(st) : 0.f;
+            RowScalars rs = make_row_scalars(st.m, st.s, xy, rrel, valid, y, wy, ctl->w_all,
                                              a.eps, inv_v, 1.f);
             if (a.stats) {
-                float4 s4 = make_float4(st.m, st.s, xy, SMOOTH ? st.r : 0.f);
+                float4 s4 = make_float4(st.m, st.s, xy, rrel);
                 reinterpret_cast<float4 *>(a.stats)[row] = s4;
             }
             if (a.reduction == CE_RED_NONE) a.loss[row] = rs.loss;
@@ -212,6 +240,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_grad_kernel(RowArgs a) {
     constexpr int UNROLL = 4;
     const WsCtl *ctl = a.ctl;
     const float inv_v = 1.f / static_cast<float>(a.vocab);
+    pdl_wait();
     const float w_all = ctl->w_all;
 
     for (int64_t row = blockIdx.x; row < a.n_rows; row += gridDim.x) {
@@ -273,6 +302,143 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_grad_kernel(RowArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ one kernel, two passes per row
+// Forward + backward in one kernel without cluster shared memory: each CTA
+// owns whole rows; the statistics pass reads the row from HBM marking its
+// lines evict-last in L2, and the gradient pass rereads it (from L2 while
+// the lines survive) marking them evict-first and writes the gradient in
+// place. HBM then sees one read and one write per element, as the fused
+// cluster kernel does, at the price of the L2 holding the rows in flight
+// (a few CTAs per SM x the row size).
+__device__ inline uint4 ld_policy(const void *p, uint64_t pol) {
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "l"(p), "l"(pol));
+    return v;
+}
+__device__ inline uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+template <int DT, int MODE>
+__global__ void __launch_bounds__(kRowpassThreads, 2) ce_rowpass_kernel(RowArgs a) {
+    using F = Fmt<DT>;
+    constexpr int VEC = F::kVec;
+    constexpr bool SMOOTH = MODE != 0;
+    constexpr int UNROLL = 4;
+    __shared__ RowState sh[32];
+    __shared__ RowScalars sh_rs;
+    WsCtl *ctl = a.ctl;
+    const float inv_v = 1.f / static_cast<float>(a.vocab);
+    const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
+    pdl_wait();
+    const float w_all = ctl->w_all;
+
+    for (int64_t row = blockIdx.x; row < a.n_rows; row += gridDim.x) {
+        char *rowp = reinterpret_cast<char *>(a.grad) + row * a.ld * F::kBytes;
+        const int64_t t = load_target(a.target, a.tgt32, row);
+        const bool valid = target_valid(t, a.ignore_index, a.vocab);
+        const int64_t y = valid ? t : -1;
+        const int64_t V = a.vocab;
+        const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
+        int64_t head = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) / F::kBytes);
+        if (head > V) head = V;
+        const int nvec = static_cast<int>((V - head) / VEC);
+        const int64_t tail0 = head + static_cast<int64_t>(nvec) * VEC;
+        uint4 *vp = reinterpret_cast<uint4 *>(rowp + head * F::kBytes);
+        const int y_rel = valid ? static_cast<int>(y - head) : -(1 << 30);
+
+        if (!valid) {
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            for (int v = threadIdx.x; v < nvec; v += blockDim.x) st_stream(vp + v, z);
+            if (const int64_t c = scalar_col(threadIdx.x, head, tail0, V); c >= 0) F::store1(rowp, c, 0.f);
+            if (threadIdx.x == 0) {
+                if (a.reduction == CE_RED_NONE) a.loss[row] = 0.f;
+                else a.row_loss[row] = 0.f;
+            }
+            continue;
+        }
+        // ---------------------------------------------------------------- pass 1: statistics
+        RowState st = row_state_empty();
+        if (const int64_t c = scalar_col(threadIdx.x, head, tail0, V); c >= 0) {
+            float x = F::load1(rowp, c);
+            float w = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
+            row_state_add<1, SMOOTH>(st, &x, x, (c == y) ? 0 : -1, MODE == 2 ? &w : nullptr);
+        }
+        for (int v0 = threadIdx.x; v0 < nvec; v0 += blockDim.x * UNROLL) {
+            uint4 raw[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int v = v0 + u * blockDim.x;
+                if (v < nvec) raw[u] = ld_policy(vp + v, keep);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int v = v0 + u * blockDim.x;
+                if (v >= nvec) break;
+                float x[VEC];
+                F::unpack(raw[u], x);
+                const int vb = v * VEC;
+                const int skip = (static_cast<unsigned>(y_rel - vb) < static_cast<unsigned>(VEC)) ? y_rel - vb : -1;
+                float w[VEC];
+                if (MODE == 2) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) w[j] = __ldg(a.weight + head + vb + j);
+                }
+                row_state_add<VEC, SMOOTH>(st, x, F::vmax(raw[u]), skip, MODE == 2 ? w : nullptr);
+            }
+        }
+        st = block_merge(st, sh);
+        if (threadIdx.x == 0) {
+            const float xy = F::load1(rowp, y);
+            const float wy = a.weight ? __ldg(a.weight + y) : 1.f;
+            const float rrel = SMOOTH ? row_state_rel_sum(st) : 0.f;
+            const RowScalars rl = make_row_scalars(st.m, st.s, xy, rrel, true, y, wy, w_all, a.eps, inv_v, 1.f);
+            if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
+            else a.row_loss[row] = rl.loss;
+            sh_rs = make_row_scalars(st.m, st.s, xy, rrel, true, y, wy, w_all, a.eps, inv_v,
+                                     grad_scale(a, ctl, row));
+        }
+        __syncthreads();
+        const RowScalars rs = sh_rs;
+        // ---------------------------------------------------------------- pass 2: gradient in place
+        if (const int64_t c = scalar_col(threadIdx.x, head, tail0, V); c >= 0) {
+            const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
+            F::store1(rowp, c, (c == y) ? rs.dxy : grad_elem(rs, F::load1(rowp, c), wc));
+        }
+        for (int v0 = threadIdx.x; v0 < nvec; v0 += blockDim.x * UNROLL) {
+            uint4 raw[UNROLL];
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int v = v0 + u * blockDim.x;
+                if (v < nvec) raw[u] = ld_policy(vp + v, drop);
+            }
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                const int v = v0 + u * blockDim.x;
+                if (v >= nvec) break;
+                float x[VEC], g[VEC];
+                F::unpack(raw[u], x);
+                const int vb = v * VEC;
+#pragma unroll
+                for (int j = 0; j < VEC; ++j) {
+                    const float wc = (MODE == 2) ? __ldg(a.weight + head + vb + j) : 1.f;
+                    g[j] = grad_elem(rs, x[j], wc);
+                }
+                if (static_cast<unsigned>(y_rel - vb) < static_cast<unsigned>(VEC)) {
+#pragma unroll
+                    for (int e = 0; e < VEC; ++e) g[e] = (vb + e == y_rel) ? rs.dxy : g[e];
+                }
+                st_stream(vp + v, F::pack(g));
+            }
+        }
+        __syncthreads();  // sh / sh_rs are reused by the next row
+    }
+    if (a.reduction != CE_RED_NONE) finish_loss(a, ctl, gridDim.x);
+}
+
 // ------------------------------------------------------------------ grad_output scaling in place
 template <int DT>
 __global__ void __launch_bounds__(kRowThreads) ce_scale_kernel(ScaleArgs a) {
@@ -307,11 +473,23 @@ __global__ void __launch_bounds__(kRowThreads) ce_scale_kernel(ScaleArgs a) {
 // ------------------------------------------------------------------ launchers
 // cudaLaunchKernel reports the status of this launch itself (a <<<>>> launch
 // followed by cudaGetLastError could return an earlier, unrelated error).
+// Kernels that follow the normaliser kernel are launched with programmatic
+// stream serialisation: they may start while it runs and wait for it inside.
 template <typename Args>
-static cudaError_t launch(const void *fn, int grid, int block, const Args &a, cudaStream_t s) {
+static cudaError_t launch(const void *fn, int grid, int block, const Args &a, cudaStream_t s,
+                          bool after_prep = true) {
     Args copy = a;
     void *args[] = {&copy};
-    return cudaLaunchKernel(fn, dim3(static_cast<unsigned>(grid)), dim3(static_cast<unsigned>(block)), args, 0, s);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(block));
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_prep ? 1 : 0;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 template <int DT>
@@ -332,7 +510,7 @@ static const void *grad_fn(int mode) {
 }
 
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s) {
-    return launch(reinterpret_cast<const void *>(&ce_prep_kernel), 1, kPrepThreads, a, s);
+    return launch(reinterpret_cast<const void *>(&ce_prep_kernel), 1, kPrepThreads, a, s, false);
 }
 
 cudaError_t launch_stats(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s) {
@@ -345,6 +523,28 @@ cudaError_t launch_grad(const RowArgs &a, int dtype, int mode, int grid, cudaStr
     const void *fn = dtype == CE_DT_F32 ? grad_fn<CE_DT_F32>(mode)
                    : dtype == CE_DT_BF16 ? grad_fn<CE_DT_BF16>(mode) : grad_fn<CE_DT_F16>(mode);
     return launch(fn, grid, kRowThreads, a, s);
+}
+
+template <int DT>
+static const void *rowpass_fn(int mode) {
+    switch (mode) {
+    case 0: return reinterpret_cast<const void *>(&ce_rowpass_kernel<DT, 0>);
+    case 1: return reinterpret_cast<const void *>(&ce_rowpass_kernel<DT, 1>);
+    default: return reinterpret_cast<const void *>(&ce_rowpass_kernel<DT, 2>);
+    }
+}
+
+cudaError_t launch_rowpass(const RowArgs &a, int dtype, int mode, int ctas_per_sm, cudaStream_t s) {
+    const void *fn = dtype == CE_DT_F32 ? rowpass_fn<CE_DT_F32>(mode)
+                   : dtype == CE_DT_BF16 ? rowpass_fn<CE_DT_BF16>(mode) : rowpass_fn<CE_DT_F16>(mode);
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int64_t grid = static_cast<int64_t>(sms) * (ctas_per_sm > 0 ? ctas_per_sm : 2);
+    if (grid > a.n_rows) grid = a.n_rows;
+    if (grid < 1) grid = 1;
+    return launch(fn, static_cast<int>(grid), kRowpassThreads, a, s);
 }
 
 cudaError_t launch_scale(const ScaleArgs &a, int dtype, int grid, cudaStream_t s) {

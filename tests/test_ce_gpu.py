@@ -68,7 +68,7 @@ SMALL = [
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: f"{s[0]}x{s[1]}+{s[2]}")
 @pytest.mark.parametrize("opt", ["plain", "smooth", "weighted_smooth"])
 @pytest.mark.parametrize("red", ["mean", "sum", "none"])
-@pytest.mark.parametrize("api", ["fused", "split", "fwd+bwd calls"])
+@pytest.mark.parametrize("api", ["fused", "split", "rowpass", "fwd+bwd calls"])
 def test_parity_small(ce, dtype, shape, opt, red, api):
     R, V, extra = shape
     dev = torch.device("cuda")
@@ -93,7 +93,7 @@ def test_parity_small(ce, dtype, shape, opt, red, api):
         assert torch.equal(st[valid, 2], ref["stats"][valid, 2].float().double())  # x_y is exact
         assert torch.allclose(st[:, 1], ref["stats"][:, 1], rtol=2e-5, atol=0)
     else:
-        variant = "fused" if api == "fused" else "split"
+        variant = api
         ld = x.stride(0) if R > 1 else V
         fusable = x.data_ptr() % 16 == 0 and (R == 1 or (ld * x.element_size()) % 16 == 0)
         if variant == "fused" and not fusable:
@@ -342,7 +342,7 @@ def _full_size_check(ce, cfg, variant, sample_rows=48, check_dxy_thirds=False):
     return out
 
 
-@pytest.mark.parametrize("variant", ["fused", "split"])
+@pytest.mark.parametrize("variant", ["fused", "split", "rowpass"])
 def test_confident_full_size_dxy(ce, variant):
     """4096 x 32000 bf16, softmax(x_y) near 0.9 / 0.99 / 0.999: dx_y within
     0.4% of the oracle in every third (the #1329 accuracy table's workload)."""
@@ -362,7 +362,7 @@ def test_confident_full_size_dxy(ce, variant):
         assert rel[sel].max() <= DXY_RTOL, f"third {k}: dx_y max rel err {float(rel[sel].max()):.4%}"
 
 
-@pytest.mark.parametrize("variant", ["fused", "split"])
+@pytest.mark.parametrize("variant", ["fused", "split", "rowpass"])
 def test_headline_full_size(ce, variant):
     _full_size_check(ce, CONFIGS["headline"], variant)
 
