@@ -58,6 +58,14 @@ def read_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def read_bf16_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"])
+    except Exception:
+        return 1900.0
+
+
 def read_traffic():
     """ncu DRAM bytes per launch of the fused kernel, if captured on the
     current kernel source (else None)."""
@@ -231,6 +239,64 @@ def measure_e2e(ce, pristine, target, work, flush, loss, kw, stream, steps):
     return e2e_ms
 
 
+def measure_flce(ce, device, steps: int, chunk_rows: int):
+    """Fused-linear cross-entropy at hidden 8192 x 4096, W 128256 x 4096 bf16:
+    ms per forward + backward step, and each tcgen05 GEMM timed alone on the
+    step's chunk shapes (TFLOP/s against the measured bf16 peak)."""
+    import torch
+
+    from workloads import FLCE_CONFIGS, make_flce_inputs
+    cfg = FLCE_CONFIGS["flce"]
+    inp = make_flce_inputs(cfg, device=device)
+    h, W, t = inp["hidden"], inp["weight"], inp["target"]
+    BT, H, V = cfg.n_rows, cfg.hidden, cfg.vocab
+    loss = torch.empty(1, device=device)
+    gh = torch.empty(BT, H, dtype=torch.bfloat16, device=device)
+    gw = torch.empty(V, H, dtype=torch.float32, device=device)
+    ws = torch.empty(ce.flce_workspace_size(BT, H, V, chunk_rows), dtype=torch.uint8, device=device)
+    kw = dict(reduction="mean", chunk_rows=chunk_rows, loss=loss, grad_hidden=gh, grad_weight=gw, ws=ws)
+    for _ in range(2):
+        ce.flce_fwd_bwd(h, W, t, **kw)
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for a, b in ev:
+        a.record()
+        ce.flce_fwd_bwd(h, W, t, **kw)
+        b.record()
+    torch.cuda.synchronize()
+    step_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+    flop = 3 * 2.0 * BT * V * H
+    # the three GEMMs of one chunk, each timed alone
+    c = min(chunk_rows, BT)
+    dz = torch.randn(c, V, device=device).to(torch.bfloat16)
+    z = torch.empty(c, V, device=device)
+    ghc = torch.empty(c, H, dtype=torch.bfloat16, device=device)
+    gemms = {
+        "logits  Z = h W^T": (lambda: ce.ce_gemm_bf16(h[:c], W, out=z), 2.0 * c * V * H),
+        "grad_h  dZ W": (lambda: ce.ce_gemm_bf16(dz, W, b_mn_major=True, out=ghc,
+                                                 out_kind=ce.CE_GEMM_BF16_STORE), 2.0 * c * V * H),
+        "grad_W += dZ^T h": (lambda: ce.ce_gemm_bf16(dz, h[:c], a_mn_major=True, b_mn_major=True, out=gw,
+                                                     out_kind=ce.CE_GEMM_F32_ACCUM), 2.0 * c * V * H),
+    }
+    per = {}
+    for name, (fn, fl) in gemms.items():
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(3):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / 3
+        per[name] = {"ms": ms, "tflops": fl / ms / 1e9}
+    del dz, z, ghc
+    return {"workload": f"flce: hidden [{BT}, {H}] bf16 N(0,1), weight [{V}, {H}] bf16 N(0, 0.02^2), "
+                        f"5% ignore_index, mean, chunk_rows={chunk_rows}",
+            "ms_per_step": step_ms, "tokens_per_s": BT / (step_ms / 1e3),
+            "gemm_tflops_whole_step": flop / step_ms / 1e9, "gemm_chunk": per}
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_ours(args):
     import torch
@@ -243,7 +309,7 @@ def run_ours(args):
 
     import softmax_cross_entropy_pass_gb300 as ce
     from workloads import CONFIGS, make_ce_inputs
-    cfg = CONFIGS[WORKLOAD]
+    cfg = CONFIGS[args.workload]
     if args.rows:
         import dataclasses
         cfg = dataclasses.replace(cfg, n_rows=args.rows)
@@ -253,10 +319,11 @@ def run_ours(args):
     work = torch.empty_like(pristine)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
     ws = ce.workspace(R, device)
-    loss = torch.empty(1, dtype=torch.float32, device=device)
+    loss = torch.empty(R if cfg.reduction == "none" else 1, dtype=torch.float32, device=device)
     stream = torch.cuda.current_stream(device)
+    weight = inp["weight"]
     kw = dict(label_smoothing=cfg.label_smoothing, reduction=cfg.reduction, grad_output=g, loss=loss,
-              ws=ws, stream=stream, variant=args.variant, cluster=args.cluster)
+              ws=ws, stream=stream, variant=args.variant, cluster=args.cluster, weight=weight)
 
     def step():
         return ce.ce_fwd_bwd(work, target, **kw)
@@ -266,12 +333,19 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
 
-    plan = ce.ce_fused_plan(R, V, pristine.dtype, label_smoothing=cfg.label_smoothing, cluster=args.cluster)
+    plan = ce.ce_fused_plan(R, V, pristine.dtype, label_smoothing=cfg.label_smoothing, cluster=args.cluster,
+                            weighted=weight is not None)
     n_valid = int((target >= 0).sum().item())
     esz = pristine.element_size()
-    # algorithmic bytes per step: every valid row read once, every row written
-    # once (ignored rows are only zeroed), plus the targets read by both kernels
-    algo_bytes = (n_valid + R) * V * esz + 2 * R * 8
+    path = args.variant if args.variant != "auto" else ce.auto_variant(pristine, target, weight=weight)
+    # algorithmic bytes per step of the chosen path: the one-read paths read
+    # every valid row once and write every row once (ignored rows are only
+    # zeroed); the split path also reads every row in its statistics pass.
+    # Plus the targets, read by the normaliser kernel and the row kernel.
+    reads = n_valid + (R if path == "split" else 0)
+    algo_bytes = (reads + R) * V * esz + 2 * R * 8
+    kernel_name = {"fused": f"ce_fused_kernel<{cfg.dtype}>", "rowpass": f"ce_rowpass_kernel<{cfg.dtype}>",
+                   "split": f"ce_stats_kernel + ce_grad_kernel <{cfg.dtype}>"}[path]
 
     sampler = ClockSampler(local)
     if rank == 0:
@@ -298,7 +372,7 @@ def run_ours(args):
     for k in range(args.steps):
         work.copy_(pristine)
         ce.ce_prepare(work, target, label_smoothing=cfg.label_smoothing, reduction=cfg.reduction,
-                      ws=ws, stream=stream)
+                      ws=ws, stream=stream, weight=weight)
         flush.zero_()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -330,6 +404,16 @@ def run_ours(args):
     achieved = algo_bytes / kernel_avg_s / 1e9
     traffic = read_traffic()
 
+    flce = None
+    if not args.no_flce:
+        del work
+        flce = measure_flce(ce, device, max(3, min(args.steps, 5)), args.flce_chunk)
+        peak_tf = read_bf16_peak()
+        flce["peak_tflops"] = peak_tf
+        flce["frac_whole_step"] = flce["gemm_tflops_whole_step"] / peak_tf
+        for v in flce["gemm_chunk"].values():
+            v["frac"] = v["tflops"] / peak_tf
+
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -344,23 +428,25 @@ def run_ours(args):
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: BT={R}, V={V}, bf16 logits N(0,1), 5% ignore_index=-100 "
-                               f"({R - n_valid} rows), label_smoothing=0.1, mean, grad_output=1, "
-                               "gradient in place",
+        "config": {"workload": f"{cfg.name}: BT={R}, V={V}, {cfg.dtype} logits N(0,{cfg.sigma:g}^2), "
+                               f"{R - n_valid} rows ignore_index=-100, label_smoothing={cfg.label_smoothing:g}, "
+                               f"{cfg.reduction}, grad_output={cfg.grad_output}, "
+                               f"{'class weights, ' if cfg.weighted else ''}gradient in place",
                    "global_batch": R * world, "seq_len": None, "parallelism": f"replicas x{world}",
-                   "variant": args.variant, "fused_plan": plan,
+                   "variant": args.variant, "path": path, "fused_plan": plan,
                    "l2": "inputs 2.1 GB > 129 MB L2; logits restored and a 256 MB buffer written "
                          "before every step, outside the timed region"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
-                     "kernel": "ce_fused_kernel<bf16, smoothing>", "kernel_ms": kernel_avg_s * 1e3,
+                     "kernel": kernel_name, "kernel_ms": kernel_avg_s * 1e3,
                      "algorithmic_bytes": algo_bytes, "peak_source": peak_kind},
         "e2e": None if args.no_e2e else {"value": R * world / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": pristine.numel() * esz + R * 8, "d2h_bytes_per_step": 4,
+                "h2d_bytes_per_step": pristine.numel() * esz + R * 8, "d2h_bytes_per_step": loss.numel() * 4,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": (3 if args.variant == "split" else 2) * args.steps,
+        "gpu_launches": (3 if path == "split" else 2) * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "flce": flce,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
     }
     print(json.dumps(line), flush=True)
@@ -382,7 +468,11 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=512)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-flce", action="store_true", help="skip the fused-linear measurement")
+    ap.add_argument("--flce-chunk", type=int, default=2048)
     ap.add_argument("--rows", type=int, default=0, help="rows of a smaller case of the workload (profiling)")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="CE workload of workloads.CONFIGS (the default is the headline metric's)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

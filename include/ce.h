@@ -76,7 +76,7 @@ typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
 #define CE_FLAG_WAIT_TIMEOUT 0x4u        /* a device-side wait gave up (results invalid) */
 
 /* ce_params.variant: which kernels ce_fwd_bwd uses */
-#define CE_VARIANT_AUTO 0   /* fused single-read kernel when the rows allow it, else split */
+#define CE_VARIANT_AUTO 0   /* the library picks (ce_select_variant): the row-pass kernel */
 #define CE_VARIANT_SPLIT 1  /* ce_forward then ce_backward kernels (row read twice) */
 #define CE_VARIANT_FUSED 2  /* fused kernel; CE_ERR_UNSUPPORTED if the rows do not allow it */
 #define CE_VARIANT_ROWPASS 3 /* one kernel, each row read twice, the second read from L2 */
@@ -194,6 +194,13 @@ ce_status ce_scale_grad(const ce_params *p, void *grad_inout, const float *grad_
  */
 ce_status ce_fused_plan(const ce_params *p, int32_t *cluster_size, int32_t *n_clusters,
                         int32_t *ctas_per_sm, int64_t *slice_bytes);
+
+/*
+ * The kernel path ce_fwd_bwd takes for p->variant == CE_VARIANT_AUTO (host
+ * query, no GPU work): CE_VARIANT_ROWPASS, CE_VARIANT_FUSED or
+ * CE_VARIANT_SPLIT in *variant. `logits` is only inspected for alignment.
+ */
+ce_status ce_select_variant(const ce_params *p, const void *logits, int32_t *variant);
 
 /*
  * Synchronises `stream`, then copies the workspace status word (CE_FLAG_*

@@ -179,13 +179,15 @@ def flce_logits(hidden: torch.Tensor, weight: torch.Tensor, bias=None, row_block
 
 def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
          label_smoothing: float = 0.0, reduction: str = "mean", sample_rows=None,
-         sample_cols=None, n_threads: int | None = None) -> dict:
+         sample_cols=None, abs_sums: bool = False, n_threads: int | None = None) -> dict:
     """Fused-linear cross-entropy reference (fp64).
 
     Returns the reduced loss, the per-row losses, grad_hidden on
     ``sample_rows`` (all rows if None) and grad_weight on ``sample_cols``
     (all vocabulary rows if None): grad_hidden = dZ @ W, grad_weight = dZ^T @ h
-    with dZ the oracle gradient of the loss with respect to z = h W^T + b."""
+    with dZ the oracle gradient of the loss with respect to z = h W^T + b.
+    With ``abs_sums`` it also returns |dZ| @ |W| and |dZ|^T @ |h| on the same
+    samples (the magnitudes that bound rounding errors of dZ in the tests)."""
     BT, H = hidden.shape
     V = weight.shape[0]
     n, wy, wall, bad = normalizers(target, V, ignore_index, None)
@@ -202,6 +204,8 @@ def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
     pos = torch.full((BT,), -1, dtype=torch.int64)
     pos[rows_sel] = torch.arange(len(rows_sel))
     grad_b = torch.zeros(len(cols_sel), dtype=torch.float64) if bias is not None else None
+    abs_h = torch.zeros(len(rows_sel), H, dtype=torch.float64) if abs_sums else None
+    abs_w = torch.zeros(len(cols_sel), H, dtype=torch.float64) if abs_sums else None
     for r0, z in flce_logits(hidden, weight, bias):
         r1 = r0 + z.shape[0]
         res = rows(z, tgt[r0:r1], ignore_index=ignore_index, label_smoothing=label_smoothing,
@@ -210,11 +214,16 @@ def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
         row_loss[r0:r1] = res["row_loss"]
         dz = res["grad"]
         grad_w += dz[:, cols_sel].T @ hd[r0:r1]
+        if abs_w is not None:
+            abs_w += dz[:, cols_sel].abs().T @ hd[r0:r1].abs()
         if grad_b is not None:
             grad_b += dz[:, cols_sel].sum(0)
         sel = row_mask[r0:r1].nonzero().flatten()
         if sel.numel():
             grad_h[pos[r0 + sel]] = dz[sel] @ Wd
+            if abs_h is not None:
+                abs_h[pos[r0 + sel]] = dz[sel].abs() @ Wd.abs()
     return {"loss": reduce(row_loss, reduction, wy), "row_loss": row_loss,
             "grad_hidden": grad_h, "grad_weight": grad_w, "grad_bias": grad_b,
+            "grad_hidden_abs": abs_h, "grad_weight_abs": abs_w,
             "rows": rows_sel, "cols": cols_sel, "norm_wy": wy}

@@ -70,6 +70,7 @@ def _load():
         "ce_fused_plan": (st, [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]),
         "ce_get_status": (st, [vp, ctypes.POINTER(ctypes.c_uint32), vp]),
+        "ce_select_variant": (st, [P, vp, ctypes.POINTER(ctypes.c_int32)]),
         "ce_gemm_bf16": (st, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int64, ctypes.c_int32,
                               vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int64, vp, vp]),
         "flce_workspace_size": (st, [P, ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(sz)]),
@@ -221,6 +222,14 @@ def ce_fwd_bwd(logits, target, *, grad_output=None, weight=None, ignore_index=-1
     _check(_lib.ce_fwd_bwd(ctypes.byref(p), _ptr(logits), _ptr(target), _ptr(loss),
                            _ptr(grad_output), _ptr(ws), wsb, _stream(stream)), "ce_fwd_bwd")
     return loss
+
+
+def auto_variant(logits, target, *, weight=None, label_smoothing=0.0) -> str:
+    """The kernel path ce_fwd_bwd(variant="auto") takes for these tensors."""
+    p = make_params(logits, target, weight=weight, label_smoothing=label_smoothing)
+    out = ctypes.c_int32()
+    _check(_lib.ce_select_variant(ctypes.byref(p), _ptr(logits), ctypes.byref(out)), "ce_select_variant")
+    return {v: k for k, v in VARIANTS.items()}[out.value]
 
 
 def ce_scale_grad(grad, grad_output, *, reduction="mean", vocab=None, stream=None):

@@ -139,9 +139,27 @@ bool fused_layout_ok(const ce_params *p, const void *x) {
     return true;
 }
 
+// The path of CE_VARIANT_AUTO: the one-kernel row pass (HBM read once, the
+// second read served by L2) is the fastest measured path on GB300 for every
+// row size; the split path remains for callers that ask for it.
+int auto_path(const ce_params *p, const void *x) {
+    (void)p;
+    (void)x;
+    return CE_VARIANT_ROWPASS;
+}
+
 }  // namespace
 
 extern "C" {
+
+ce_status ce_select_variant(const ce_params *p, const void *logits, int32_t *variant) {
+    ce_status st = check_params(p);
+    if (st != CE_OK) return st;
+    if (!variant) return CE_ERR_INVALID_ARG;
+    const int path = p->variant & 0xff;
+    *variant = path == CE_VARIANT_AUTO ? auto_path(p, logits) : path;
+    return CE_OK;
+}
 
 const char *ce_version(void) { return "ce-gb300 1.0 (sm_103a)"; }
 
@@ -223,8 +241,9 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
     if (st != CE_OK) return st;
     if ((st = check_ws(p, ws, ws_bytes)) != CE_OK) return st;
     if (!loss || (p->n_rows > 0 && (!logits_inout || !target))) return CE_ERR_INVALID_ARG;
-    const int path = p->variant & 0xff;
+    int path = p->variant & 0xff;
     if (p->variant & ~(0xffff | CE_VARIANT_PREPARED)) return CE_ERR_INVALID_ARG;
+    if (path == CE_VARIANT_AUTO) path = auto_path(p, logits_inout);
     if (path != CE_VARIANT_AUTO && path != CE_VARIANT_SPLIT && path != CE_VARIANT_FUSED &&
         path != CE_VARIANT_ROWPASS)
         return CE_ERR_INVALID_ARG;

@@ -107,7 +107,8 @@ def test_flce_small_against_oracle(ce, reduction, chunk, with_bias):
 def test_flce_full_size_sampled(ce):
     """hidden 8192 x 4096, W 128256 x 4096: loss over all rows, grad_hidden on
     256 sampled rows and grad_weight on 256 sampled vocabulary rows against
-    the fp64 oracle."""
+    the fp64 oracle, with the same rounding bound as the small cases
+    (dZ rounded once to bf16: |error| <= 2^-8 sum |dZ| |operand|)."""
     cfg = FLCE_CONFIGS["flce"]
     inp = make_flce_inputs(cfg, device="cuda")
     h, W, t = inp["hidden"], inp["weight"], inp["target"]
@@ -116,14 +117,16 @@ def test_flce_full_size_sampled(ce):
     gen = torch.Generator().manual_seed(77)
     rows = torch.randperm(cfg.n_rows, generator=gen)[:256].sort().values
     cols = torch.randperm(cfg.vocab, generator=gen)[:256].sort().values
-    ref = oracle.flce(h.cpu(), W.cpu(), t.cpu(), reduction="mean", sample_rows=rows, sample_cols=cols)
+    ref = oracle.flce(h.cpu(), W.cpu(), t.cpu(), reduction="mean", sample_rows=rows, sample_cols=cols,
+                      abs_sums=True)
     assert abs(float(loss.item()) - ref["loss"]) <= 1e-4 * abs(ref["loss"])
     gh_s = gh[rows.cuda()].double().cpu()
     gw_s = gw[cols.cuda()].double().cpu()
-    # relative to each row's / column's max norm (the oracle's dZ is fp64)
-    eh = (gh_s - ref["grad_hidden"]).abs().max(dim=1).values / ref["grad_hidden"].abs().max(dim=1).values.clamp_min(1e-30)
-    ew = (gw_s - ref["grad_weight"]).abs().max(dim=1).values / ref["grad_weight"].abs().max(dim=1).values.clamp_min(1e-30)
+    err_h = (gh_s - ref["grad_hidden"]).abs()
+    bound_h = ref["grad_hidden_abs"] * 2.0 ** -8 + ref["grad_hidden"].abs() * 2.0 ** -7
+    assert (err_h <= bound_h).all(), f"grad_hidden: {int((err_h > bound_h).sum())} elements off"
+    err_w = (gw_s - ref["grad_weight"]).abs()
+    bound_w = ref["grad_weight_abs"] * 2.0 ** -8 + ref["grad_weight"].abs() * 2.0 ** -20
+    assert (err_w <= bound_w).all(), f"grad_weight: {int((err_w > bound_w).sum())} elements off"
     valid = t.cpu()[rows] >= 0
-    assert eh[valid].max() <= 2e-2, f"grad_hidden rel err {float(eh.max()):.3e}"
-    assert ew.max() <= 1e-3, f"grad_weight rel err {float(ew.max()):.3e}"
     assert torch.count_nonzero(gh_s[~valid]) == 0
