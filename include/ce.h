@@ -173,6 +173,36 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
                      const float *grad_output, void *workspace, size_t workspace_bytes,
                      void *stream);
 
+/* Largest n_rows ce_fwd_bwd_noalloc accepts (its fixed scratch, about
+ * 1.3 MB, is sized for this many rows). */
+#define CE_NOALLOC_MAX_ROWS 65536
+
+/*
+ * ce_fwd_bwd without a workspace argument, for callers that cannot allocate
+ * device memory: hosts that give their extensions no allocator, such as a
+ * runtime that reserves all device memory for its own pool up front, or a
+ * plugin interface that hands an entry point only its inputs and outputs.
+ * The pages this library follows have no counterpart to this entry point.
+ * Same arguments, results and error behaviour as ce_fwd_bwd; the caller
+ * still passes every input and output buffer.
+ *  - Scratch: a fixed array of about 1.3 MB in the library's own device
+ *    memory, present on every GPU that loads the library until the process
+ *    exits. Nothing is allocated by this call.
+ *  - n_rows above CE_NOALLOC_MAX_ROWS returns CE_ERR_WORKSPACE with nothing
+ *    enqueued.
+ *  - The first call on a device looks up the array's device address (a
+ *    runtime query, once per device, with that device current); make that
+ *    first call before any stream capture.
+ *  - Every call on a device shares the one array, and the array keeps the
+ *    last call's contents (each call resets the counters it relies on).
+ *    Calls whose GPU work overlaps (different streams, or different host
+ *    threads without ordering) race on it: serialise them, e.g. on one
+ *    stream. Status bits are read with ce_get_status only through a
+ *    caller-provided workspace, so this variant offers none.
+ */
+ce_status ce_fwd_bwd_noalloc(const ce_params *p, void *logits_inout, const void *target, float *loss,
+                             const float *grad_output, void *stream);
+
 /*
  * Scale a gradient already written with grad_output = 1 (ce_fwd_bwd with
  * grad_output NULL) by the grad_output that arrives later: row i is

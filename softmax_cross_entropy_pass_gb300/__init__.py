@@ -66,6 +66,7 @@ def _load():
         "ce_forward": (st, [P, vp, vp, vp, vp, vp, sz, vp]),
         "ce_backward": (st, [P, vp, vp, vp, vp, vp, sz, vp]),
         "ce_fwd_bwd": (st, [P, vp, vp, vp, vp, vp, sz, vp]),
+        "ce_fwd_bwd_noalloc": (st, [P, vp, vp, vp, vp, vp]),
         "ce_scale_grad": (st, [P, vp, vp, vp]),
         "ce_fused_plan": (st, [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]),
@@ -221,6 +222,25 @@ def ce_fwd_bwd(logits, target, *, grad_output=None, weight=None, ignore_index=-1
     ws, wsb = _ws(ws, n, logits.device)
     _check(_lib.ce_fwd_bwd(ctypes.byref(p), _ptr(logits), _ptr(target), _ptr(loss),
                            _ptr(grad_output), _ptr(ws), wsb, _stream(stream)), "ce_fwd_bwd")
+    return loss
+
+
+CE_NOALLOC_MAX_ROWS = 65536
+
+
+def ce_fwd_bwd_noalloc(logits, target, *, grad_output=None, weight=None, ignore_index=-100,
+                       label_smoothing=0.0, reduction="mean", variant="auto", loss=None, stream=None):
+    """ce_fwd_bwd without a workspace: for callers that cannot allocate device
+    memory, the library uses its own fixed scratch (n_rows <= CE_NOALLOC_MAX_ROWS).
+    Calls whose GPU work overlaps race on that scratch: keep them on one stream."""
+    _check_dev(logits, target, grad_output, weight)
+    p = make_params(logits, target, weight=weight, ignore_index=ignore_index,
+                    label_smoothing=label_smoothing, reduction=reduction, variant=variant)
+    if loss is None:
+        loss = torch.empty(logits.shape[0] if reduction == "none" else 1, dtype=torch.float32,
+                           device=logits.device)
+    _check(_lib.ce_fwd_bwd_noalloc(ctypes.byref(p), _ptr(logits), _ptr(target), _ptr(loss),
+                                   _ptr(grad_output), _stream(stream)), "ce_fwd_bwd_noalloc")
     return loss
 
 
