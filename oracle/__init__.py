@@ -59,6 +59,9 @@ def _load():
             lib.ce_oracle_rows.restype = i32
             lib.ce_oracle_rows.argtypes = [vp, i32, i64, i64, i64, vp, i32, i64, vp, dbl, i32,
                                            vp, i32, dbl, dbl, vp, vp, vp, i32]
+            lib.ce_oracle_rows_ex.restype = i32
+            lib.ce_oracle_rows_ex.argtypes = [vp, i32, i64, i64, i64, vp, i32, i64, vp, dbl, i32,
+                                              vp, i32, dbl, dbl, vp, vp, vp, i32, dbl, dbl, vp]
             lib.ce_oracle_reduce.restype = dbl
             lib.ce_oracle_reduce.argtypes = [vp, i64, i32, dbl]
             _lib = lib
@@ -96,11 +99,15 @@ def normalizers(target: torch.Tensor, vocab: int, ignore_index: int = -100,
 def rows(logits: torch.Tensor, target: torch.Tensor, *, weight=None, ignore_index: int = -100,
          label_smoothing: float = 0.0, reduction: str = "mean", grad_output=None,
          norm_wy: float | None = None, w_all: float | None = None, want_grad: bool = True,
-         want_stats: bool = True, n_threads: int | None = None) -> dict:
+         want_stats: bool = True, n_threads: int | None = None, softcap: float = 0.0,
+         z_loss: float = 0.0) -> dict:
     """Per-row oracle on a block of rows. ``logits`` is a CPU (or device,
     copied here) [R, V] tensor in f32/bf16/f16/f64, possibly a row-strided
     view. ``norm_wy`` / ``w_all`` default to the normalisers of this block;
-    pass the whole batch's values when the block is a sample."""
+    pass the whole batch's values when the block is a sample. ``softcap``
+    (c > 0: logits become c tanh(x / c)) and ``z_loss`` (lambda LSE^2 per valid
+    row) are off at 0; ``argmax`` (first column of the row maximum) is
+    always returned."""
     lib = _load()
     x = logits.detach().to("cpu")
     if x.dim() != 2 or x.stride(1) != 1:
@@ -128,15 +135,17 @@ def rows(logits: torch.Tensor, target: torch.Tensor, *, weight=None, ignore_inde
     row_loss = torch.zeros(R, dtype=torch.float64)
     stats = torch.zeros(R, 4, dtype=torch.float64) if want_stats else None
     grad = torch.zeros(R, V, dtype=torch.float64) if want_grad else None
-    rc = lib.ce_oracle_rows(
+    argmax = torch.zeros(R, dtype=torch.int64)
+    rc = lib.ce_oracle_rows_ex(
         x.data_ptr(), _DT[x.dtype], R, V, ld, tgt.data_ptr(), is32, ignore_index,
         w.data_ptr() if w is not None else None, float(label_smoothing), _RED[reduction],
         g.data_ptr() if g is not None else None, per_row, float(norm_wy), float(w_all),
         row_loss.data_ptr(), stats.data_ptr() if stats is not None else None,
-        grad.data_ptr() if grad is not None else None, n_threads or default_threads())
+        grad.data_ptr() if grad is not None else None, n_threads or default_threads(),
+        float(softcap), float(z_loss), argmax.data_ptr())
     if rc != 0:
         raise RuntimeError(f"ce_oracle_rows failed with code {rc}")
-    return {"row_loss": row_loss, "stats": stats, "grad": grad,
+    return {"row_loss": row_loss, "stats": stats, "grad": grad, "argmax": argmax,
             "norm_wy": norm_wy, "w_all": w_all}
 
 
@@ -149,18 +158,30 @@ def reduce(row_loss: torch.Tensor, reduction: str, norm_wy: float):
     return lib.ce_oracle_reduce(rl.data_ptr(), rl.numel(), _RED[reduction], float(norm_wy))
 
 
+def accuracy(argmax: torch.Tensor, target: torch.Tensor, vocab: int, ignore_index: int = -100) -> float:
+    """Token accuracy: the share of valid rows whose argmax is the target (0
+    when no row is valid)."""
+    t = _cpu(target).to(torch.int64)
+    valid = (t != ignore_index) & (t >= 0) & (t < vocab)
+    n = int(valid.sum())
+    return float((argmax[valid] == t[valid]).sum()) / n if n else 0.0
+
+
 def ce(logits, target, *, weight=None, ignore_index: int = -100, label_smoothing: float = 0.0,
        reduction: str = "mean", grad_output=None, want_grad: bool = True,
-       n_threads: int | None = None) -> dict:
-    """Whole-batch oracle: loss (reduced as asked), per-row losses, stats and
-    the fp64 gradient of (grad_output * loss) with respect to the logits."""
+       n_threads: int | None = None, softcap: float = 0.0, z_loss: float = 0.0) -> dict:
+    """Whole-batch oracle: loss (reduced as asked), per-row losses, stats, the
+    fp64 gradient of (grad_output * loss) with respect to the logits, the
+    per-row argmax and the token accuracy."""
     V = logits.shape[1]
     n, wy, wall, bad = normalizers(target, V, ignore_index, weight)
     out = rows(logits, target, weight=weight, ignore_index=ignore_index,
                label_smoothing=label_smoothing, reduction=reduction, grad_output=grad_output,
-               norm_wy=wy, w_all=wall, want_grad=want_grad, n_threads=n_threads)
+               norm_wy=wy, w_all=wall, want_grad=want_grad, n_threads=n_threads,
+               softcap=softcap, z_loss=z_loss)
     out["loss"] = reduce(out["row_loss"], reduction, wy)
     out["n_valid"], out["n_out_of_range"] = n, bad
+    out["accuracy"] = accuracy(out["argmax"], target, V, ignore_index)
     return out
 
 

@@ -37,6 +37,19 @@
  *  Mean with every row ignored is read as loss 0, gradient 0 (the pages are
  *  silent there; this oracle and the CUDA path agree on that reading).
  *
+ * Options (next to the method on the Liger-Kernel #1268 page, whose CE suite
+ * covers "class weights, softcap, label smoothing, z-loss, and ignore_index"
+ * and whose dx_y correction keeps "softcap factors"; the pages name them but
+ * do not define them, so the plain definitions are taken):
+ *   softcap c > 0: every logit is replaced by z = c * tanh(x / c) before the
+ *     loss; the gradient with respect to x is the gradient with respect to z
+ *     times dz/dx = 1 - tanh^2(x / c).
+ *   z-loss lambda > 0: loss_i += lambda * LSE_i^2 on valid rows (LSE over the
+ *     capped logits), reduced like the other terms; its gradient adds
+ *     s_i * 2 * lambda * LSE_i * p_ic.
+ *   argmax: the first column holding the row maximum (token accuracy is the
+ *     share of valid rows whose argmax is the target).
+ *
  * Per-row statistics returned for the forward/backward split:
  *   stats[i] = { m_i, s_i, x_{i,t_i}, r_i } with
  *   s_i = sum_{c != t_i} exp(x_ic - m_i)   (all c on invalid rows)
@@ -128,6 +141,12 @@ int64_t ce_oracle_normalizers(const void *target, int target_is_int32, int64_t n
 }
 
 typedef struct {
+    double softcap;      /* 0: off */
+    double z_loss;       /* lambda, 0: off */
+    int64_t *argmax;     /* [n_rows] or NULL */
+} or_opts;
+
+typedef struct {
     const void *logits;
     int dtype;
     int64_t vocab, ld;
@@ -142,23 +161,32 @@ typedef struct {
     double norm_wy, w_all;
     double *row_loss, *stats, *grad;
     int64_t row_begin, row_end;
+    or_opts opt;
 } or_job;
 
 static void or_one_row(const or_job *J, int64_t i, double *xbuf)
 {
     const int64_t V = J->vocab;
     const double eps = J->eps;
-    for (int64_t c = 0; c < V; ++c)
-        xbuf[c] = or_load(J->logits, J->dtype, i * J->ld + c);
+    const double cap = J->opt.softcap;
+    for (int64_t c = 0; c < V; ++c) {
+        double x = or_load(J->logits, J->dtype, i * J->ld + c);
+        xbuf[c] = cap > 0.0 ? cap * tanh(x / cap) : x;
+    }
 
     int64_t t = or_target(J->target, J->target_is_int32, i);
     int valid = or_valid(t, J->ignore_index, V);
 
-    /* pass 1: max */
+    /* pass 1: max (and its first column) */
     double m = -INFINITY;
+    int64_t am = 0;
     for (int64_t c = 0; c < V; ++c)
-        if (xbuf[c] > m)
+        if (xbuf[c] > m) {
             m = xbuf[c];
+            am = c;
+        }
+    if (J->opt.argmax)
+        J->opt.argmax[i] = am;
     /* pass 2: exp-sum, off-target exp-sum, smoothing sum */
     double S = 0.0, s_off = 0.0, r = 0.0;
     for (int64_t c = 0; c < V; ++c) {
@@ -185,6 +213,7 @@ static void or_one_row(const or_job *J, int64_t i, double *xbuf)
         for (int64_t c = 0; c < V; ++c)
             smooth += (J->w ? J->w[c] : 1.0) * (xbuf[c] - lse);
         loss = -(1.0 - eps) * wy * (xbuf[t] - lse) - (eps / (double)V) * smooth;
+        loss += J->opt.z_loss * lse * lse;
     }
     if (J->row_loss)
         J->row_loss[i] = loss;
@@ -208,6 +237,12 @@ static void or_one_row(const or_job *J, int64_t i, double *xbuf)
             double onehot = (c == t) ? 1.0 : 0.0;
             double wc = J->w ? J->w[c] : 1.0;
             double G = (1.0 - eps) * wy * (p - onehot) + (eps / (double)V) * (p * J->w_all - wc);
+            G += 2.0 * J->opt.z_loss * lse * p;
+            if (cap > 0.0) {
+                /* chain rule through z = cap * tanh(x / cap): dz/dx = 1 - (z / cap)^2 */
+                double th = xbuf[c] / cap;
+                G *= 1.0 - th * th;
+            }
             gr[c] = scale * G;
         }
     }
@@ -233,11 +268,12 @@ static void *or_worker(void *arg)
  * NULL. grad_output is [1] (or [n_rows] with grad_output_per_row) or NULL
  * for 1.0. Returns 0 on success.
  */
-int ce_oracle_rows(const void *logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
-                   const void *target, int target_is_int32, int64_t ignore_index,
-                   const double *class_weight, double label_smoothing, int reduction,
-                   const double *grad_output, int grad_output_per_row, double norm_wy,
-                   double w_all, double *row_loss, double *stats, double *grad, int n_threads)
+int ce_oracle_rows_ex(const void *logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
+                      const void *target, int target_is_int32, int64_t ignore_index,
+                      const double *class_weight, double label_smoothing, int reduction,
+                      const double *grad_output, int grad_output_per_row, double norm_wy,
+                      double w_all, double *row_loss, double *stats, double *grad, int n_threads,
+                      double softcap, double z_loss, int64_t *argmax)
 {
     if (n_rows < 0 || vocab < 1 || ld < vocab)
         return 1;
@@ -274,6 +310,9 @@ int ce_oracle_rows(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
         J->grad = grad;
         J->row_begin = n_rows * k / n_threads;
         J->row_end = n_rows * (k + 1) / n_threads;
+        J->opt.softcap = softcap;
+        J->opt.z_loss = z_loss;
+        J->opt.argmax = argmax;
     }
     int started = 0;
     for (int k = 1; k < n_threads; ++k) {
@@ -299,6 +338,14 @@ int ce_oracle_rows(const void *logits, int dtype, int64_t n_rows, int64_t vocab,
     return rc == 3 ? 0 : rc;
 }
 
+/* ce_oracle_rows with the options (softcap, z-loss, argmax output). */
+int ce_oracle_rows_ex(const void *logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
+                      const void *target, int target_is_int32, int64_t ignore_index,
+                      const double *class_weight, double label_smoothing, int reduction,
+                      const double *grad_output, int grad_output_per_row, double norm_wy,
+                      double w_all, double *row_loss, double *stats, double *grad, int n_threads,
+                      double softcap, double z_loss, int64_t *argmax);
+
 /* mean: sum / norm_wy (0 when norm_wy is 0), sum: sum, none: not reduced. */
 double ce_oracle_reduce(const double *row_loss, int64_t n_rows, int reduction, double norm_wy)
 {
@@ -308,4 +355,15 @@ double ce_oracle_reduce(const double *row_loss, int64_t n_rows, int reduction, d
     if (reduction == OR_MEAN)
         return norm_wy != 0.0 ? s / norm_wy : 0.0;
     return s;
+}
+
+int ce_oracle_rows(const void *logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
+                   const void *target, int target_is_int32, int64_t ignore_index,
+                   const double *class_weight, double label_smoothing, int reduction,
+                   const double *grad_output, int grad_output_per_row, double norm_wy,
+                   double w_all, double *row_loss, double *stats, double *grad, int n_threads)
+{
+    return ce_oracle_rows_ex(logits, dtype, n_rows, vocab, ld, target, target_is_int32, ignore_index,
+                             class_weight, label_smoothing, reduction, grad_output, grad_output_per_row,
+                             norm_wy, w_all, row_loss, stats, grad, n_threads, 0.0, 0.0, NULL);
 }

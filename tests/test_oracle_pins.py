@@ -338,3 +338,97 @@ def test_peak_memory_table_is_one_logits_tensor():
     for key, esz in (("bf16_bt_sweep_v128256", 2), ("fp32_bt_sweep_v128256", 4)):
         for bt, mb in d[key].items():
             assert -1 <= mb - int(bt) * 128256 * esz / 2 ** 20 <= 3
+
+
+# ----------------------------------------------------------------- softcap, z-loss, accuracy
+@pytest.mark.parametrize("weighted", [False, True])
+@pytest.mark.parametrize("red", ["mean", "sum", "none"])
+def test_softcap_zloss_against_torch_autograd(weighted, red):
+    """Softcap and z-loss against torch autograd through the composed library
+    routines: z = c tanh(x / c), cross_entropy(z) + lambda * logsumexp(z)^2 on
+    the valid rows (reduced with the cross-entropy's normaliser)."""
+    R, V = 13, 97
+    c, lam, eps = 3.0, 1e-3, 0.1
+    x = _rand(R, V, 31, scale=4.0)
+    t = make_targets(R, V, 0.2, 31)
+    w = make_weights(V, 31).double() if weighted else None
+    g = torch.rand(R, dtype=torch.float64, generator=torch.Generator().manual_seed(2)) if red == "none" \
+        else torch.tensor([0.6], dtype=torch.float64)
+    xr = x.clone().requires_grad_(True)
+    z = c * torch.tanh(xr / c)
+    ce_l = F.cross_entropy(z, t, weight=w, ignore_index=IGNORE_INDEX, label_smoothing=eps, reduction="none")
+    valid = t != IGNORE_INDEX
+    zl = lam * torch.logsumexp(z, dim=1) ** 2 * valid
+    if red == "none":
+        loss = ce_l + zl
+        (loss * g).sum().backward()
+    else:
+        denom = (w[t.clamp_min(0)] * valid).sum() if weighted else valid.sum()
+        base = F.cross_entropy(z, t, weight=w, ignore_index=IGNORE_INDEX, label_smoothing=eps, reduction=red)
+        loss = base + (zl.sum() / denom if red == "mean" else zl.sum())
+        (loss * g[0]).backward()
+    out = oracle.ce(x, t, weight=w, label_smoothing=eps, reduction=red, grad_output=g, softcap=c, z_loss=lam)
+    if red == "none":
+        assert torch.allclose(out["row_loss"], loss.detach(), rtol=1e-12, atol=1e-14)
+    else:
+        assert out["loss"] == pytest.approx(loss.item(), rel=1e-12)
+    assert torch.allclose(out["grad"], xr.grad, rtol=1e-10, atol=1e-16)
+
+
+def test_huge_softcap_is_no_softcap():
+    x = _rand(6, 40, 5, scale=2.0)
+    t = make_targets(6, 40, 0.0, 5)
+    a = oracle.ce(x, t, label_smoothing=0.1)
+    b = oracle.ce(x, t, label_smoothing=0.1, softcap=1e7)
+    assert b["loss"] == pytest.approx(a["loss"], rel=1e-12)
+    assert torch.allclose(a["grad"], b["grad"], rtol=1e-10, atol=1e-13)
+
+
+def test_zloss_uniform_logits_closed_form():
+    """All logits x0: LSE = x0 + log V, so loss = log V + lambda (x0 + log V)^2
+    and every off-target gradient is (1 + 2 lambda LSE) / (V N)."""
+    R, V, x0, lam = 4, 50, 0.3, 0.01
+    x = torch.full((R, V), x0, dtype=torch.float64)
+    t = torch.tensor([0, 7, 49, 3])
+    out = oracle.ce(x, t, z_loss=lam)
+    lse = x0 + math.log(V)
+    assert out["loss"] == pytest.approx(math.log(V) + lam * lse * lse, rel=1e-13)
+    off = (1 + 2 * lam * lse) / (V * R)
+    g = out["grad"][1].clone()
+    g[7] = off
+    assert torch.allclose(g, torch.full((V,), off, dtype=torch.float64), rtol=1e-12, atol=0)
+
+
+@pytest.mark.parametrize("z_loss", [0.0, 1e-4])
+def test_zloss_and_softcap_finite_differences(z_loss):
+    R, V = 4, 7
+    x = _rand(R, V, 8, scale=2.0)
+    t = torch.tensor([1, IGNORE_INDEX, 6, 0])
+    g = torch.tensor([0.9], dtype=torch.float64)
+    grad = oracle.ce(x, t, label_smoothing=0.2, grad_output=g, softcap=2.5, z_loss=z_loss)["grad"]
+    h = 1e-6
+    fd = torch.zeros_like(x)
+    for i in range(R):
+        for c in range(V):
+            xp, xm = x.clone(), x.clone()
+            xp[i, c] += h
+            xm[i, c] -= h
+            lp = oracle.ce(xp, t, label_smoothing=0.2, softcap=2.5, z_loss=z_loss, want_grad=False)["loss"]
+            lm = oracle.ce(xm, t, label_smoothing=0.2, softcap=2.5, z_loss=z_loss, want_grad=False)["loss"]
+            fd[i, c] = 0.9 * (lp - lm) / (2 * h)
+    assert torch.allclose(grad, fd, rtol=1e-6, atol=1e-9)
+
+
+def test_argmax_and_accuracy_against_torch_argmax():
+    R, V = 40, 300
+    x = _rand(R, V, 77, scale=2.0).to(torch.bfloat16)   # bf16 makes ties common enough
+    x[3, 10] = x[3, 20] = 50.0                            # a tie: the first column wins
+    t = torch.argmax(x.double(), dim=1)
+    t[::3] = make_targets(R, V, 0.0, 77)[::3]
+    t[5] = IGNORE_INDEX
+    out = oracle.ce(x, t, want_grad=False)
+    assert torch.equal(out["argmax"], torch.argmax(x.double(), dim=1))
+    assert out["argmax"][3] == 10
+    valid = t != IGNORE_INDEX
+    expect = float((torch.argmax(x.double(), dim=1)[valid] == t[valid]).double().mean())
+    assert out["accuracy"] == pytest.approx(expect, rel=0, abs=1e-15)
