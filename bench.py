@@ -150,6 +150,14 @@ def reduce_max(value: float, world: int, device):
     return float(t.item())
 
 
+def aggregate_throughput(rows_per_rank: int, steps: int, local_total_ms: float, world: int, device):
+    """Whole-job tokens/s of N replicas: every rank's rows over the slowest
+    rank's time (max over ranks). Returns (tokens_per_s, ms_per_step)."""
+    total_ms = reduce_max(local_total_ms, world, device)
+    ms_per_step = total_ms / steps
+    return rows_per_rank * world / (ms_per_step / 1e3), ms_per_step
+
+
 def barrier(world: int):
     if world > 1:
         import torch.distributed as dist
@@ -157,22 +165,27 @@ def barrier(world: int):
 
 
 # --------------------------------------------------------------------------- CPU oracle arm
-def oracle_sample_run(cfg, n_rows: int, threads: int):
-    """Oracle forward + backward (loss, statistics, fp64 gradient) on the
-    first n_rows of the workload's synthetic batch, normalised with the whole
-    batch's normalisers; returns seconds."""
-    import torch
-
+def oracle_sample_run(cfg, n_rows: int, threads: int, block: int = 1024):
+    """Oracle forward + backward (loss, statistics, fp64 gradient) on n_rows
+    rows of the workload (its targets; synthetic logits of its distribution),
+    normalised with the whole batch's normalisers, in blocks of ``block``
+    rows so that host memory stays bounded; returns seconds of oracle work."""
     import oracle
     from workloads import IGNORE_INDEX, make_logits, make_targets
-    x = make_logits(n_rows, cfg.vocab, cfg.dtype, cfg.sigma, cfg.seed + 1000)
     t_all = make_targets(cfg.n_rows, cfg.vocab, cfg.ignore_frac, cfg.seed)
-    t = t_all[:n_rows].clone()
     n, wy, wall, _ = oracle.normalizers(t_all, cfg.vocab, IGNORE_INDEX, None)
-    t0 = time.perf_counter()
-    oracle.rows(x, t, label_smoothing=cfg.label_smoothing, reduction=cfg.reduction, norm_wy=wy,
-                w_all=wall, want_grad=True, n_threads=threads)
-    return time.perf_counter() - t0
+    secs = 0.0
+    for r0 in range(0, n_rows, block):
+        r = min(block, n_rows - r0)
+        x = make_logits(r, cfg.vocab, cfg.dtype, cfg.sigma, cfg.seed + 1000 + r0)
+        t = t_all[(r0 + 0) % cfg.n_rows:(r0 % cfg.n_rows) + r].clone()
+        if t.numel() < r:
+            t = make_targets(r, cfg.vocab, cfg.ignore_frac, cfg.seed + r0)
+        t0 = time.perf_counter()
+        oracle.rows(x, t, label_smoothing=cfg.label_smoothing, reduction=cfg.reduction, norm_wy=wy,
+                    w_all=wall, want_grad=True, n_threads=threads)
+        secs += time.perf_counter() - t0
+    return secs
 
 
 def run_reference(args):
@@ -198,7 +211,8 @@ def run_reference(args):
         "data": "synthetic",
         "config": {"workload": f"{WORKLOAD}: BT=8192, V=128256, bf16 logits N(0,1), 5% ignore_index=-100, "
                                "label_smoothing=0.1, mean, grad_output=1",
-                   "sample": f"{rows} rows of the batch per step (normalised with all 8192 rows' targets)"},
+                   "sample": f"{rows} rows of the batch per step (in 1024-row blocks, normalised with all "
+                             f"8192 rows' targets)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows} rows x 128256 per step, forward + fp64 gradient"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -297,12 +311,51 @@ def measure_flce(ce, device, steps: int, chunk_rows: int):
             "gemm_tflops_whole_step": flop / step_ms / 1e9, "gemm_chunk": per}
 
 
+def measure_gemm(ce, device, spec: str, steps: int, warmup: int):
+    """One tcgen05 GEMM alone: spec "M,N,K,a_mn,b_mn" (bf16 in, fp32 out)."""
+    import torch
+    M, N, K, a_mn, b_mn = (int(v) for v in spec.split(","))
+    g = torch.Generator(device=device).manual_seed(9)
+    A = torch.randn(K, M, generator=g, device=device).to(torch.bfloat16) if a_mn else \
+        torch.randn(M, K, generator=g, device=device).to(torch.bfloat16)
+    B = torch.randn(K, N, generator=g, device=device).to(torch.bfloat16) if b_mn else \
+        torch.randn(N, K, generator=g, device=device).to(torch.bfloat16)
+    D = torch.empty(M, N, device=device)
+    for _ in range(warmup):
+        ce.ce_gemm_bf16(A, B, a_mn_major=bool(a_mn), b_mn_major=bool(b_mn), out=D)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        ce.ce_gemm_bf16(A, B, a_mn_major=bool(a_mn), b_mn_major=bool(b_mn), out=D)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    tflops = 2.0 * M * N * K / ms / 1e9
+    peak = read_bf16_peak()
+    return {"M": M, "N": N, "K": K, "a_mn_major": a_mn, "b_mn_major": b_mn, "ms": ms, "tflops": tflops,
+            "peak_tflops": peak, "frac": tflops / peak}
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_ours(args):
     import torch
     world, rank, local = dist_setup()
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    if args.gemm_only:
+        import softmax_cross_entropy_pass_gb300 as ce
+        print(json.dumps({"gemm": measure_gemm(ce, device, args.gemm_only, max(1, args.steps), args.warmup)}),
+              flush=True)
+        return 0
+    if args.flce_only:
+        import softmax_cross_entropy_pass_gb300 as ce
+        flce = measure_flce(ce, device, max(1, args.steps), args.flce_chunk)
+        peak_tf = read_bf16_peak()
+        flce["peak_tflops"] = peak_tf
+        flce["frac_whole_step"] = flce["gemm_tflops_whole_step"] / peak_tf
+        print(json.dumps({"flce": flce}), flush=True)
+        return 0
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
@@ -323,7 +376,7 @@ def run_ours(args):
     stream = torch.cuda.current_stream(device)
     weight = inp["weight"]
     kw = dict(label_smoothing=cfg.label_smoothing, reduction=cfg.reduction, grad_output=g, loss=loss,
-              ws=ws, stream=stream, variant=args.variant, cluster=args.cluster, weight=weight)
+              ws=ws, stream=stream, variant=args.variant, cluster=args.cluster, weight=weight, tune=args.tune)
 
     def step():
         return ce.ce_fwd_bwd(work, target, **kw)
@@ -345,6 +398,7 @@ def run_ours(args):
     reads = n_valid + (R if path == "split" else 0)
     algo_bytes = (reads + R) * V * esz + 2 * R * 8
     kernel_name = {"fused": f"ce_fused_kernel<{cfg.dtype}>", "rowpass": f"ce_rowpass_kernel<{cfg.dtype}>",
+                   "stream": f"ce_stream_kernel<{cfg.dtype}>",
                    "split": f"ce_stats_kernel + ce_grad_kernel <{cfg.dtype}>"}[path]
 
     sampler = ClockSampler(local)
@@ -389,7 +443,7 @@ def run_ours(args):
     if not args.no_e2e:
         e2e_ms = measure_e2e(ce, pristine, target, work, flush, loss, kw, stream, args.steps)
 
-    total_ms = reduce_max(total_ms, world, device)
+    value, ms_per_step = aggregate_throughput(R, args.steps, total_ms, world, device)
     e2e_ms = reduce_max(e2e_ms, world, device)
     kernel_avg_s = reduce_max(kernel_avg_s, world, device)
     if rank != 0:
@@ -398,8 +452,6 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
 
-    ms_per_step = total_ms / args.steps
-    value = R * world / (ms_per_step / 1e3)
     peak, peak_kind = read_peaks()
     achieved = algo_bytes / kernel_avg_s / 1e9
     traffic = read_traffic()
@@ -420,9 +472,13 @@ def run_ours(args):
         oracle.build()
         threads = oracle.default_threads()
         secs = oracle_sample_run(cfg, args.cpu_rows, threads)
+        one_rows = max(16, args.cpu_rows // 64)
+        secs1 = oracle_sample_run(cfg, one_rows, 1)
         cpu = {"value": args.cpu_rows / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-               "sample": f"{args.cpu_rows} rows x {V} of the headline batch, forward + fp64 gradient, "
-                         f"{secs:.2f} s"}
+               "sample": f"{args.cpu_rows} rows x {V} (the whole batch of the workload, in 1024-row "
+                         f"blocks), forward + fp64 gradient, {secs:.2f} s on {threads} threads",
+               "single_core": {"value": one_rows / secs1, "unit": "tokens/s", "cores": 1,
+                               "sample": f"{one_rows} rows, {secs1:.2f} s"}}
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -433,7 +489,7 @@ def run_ours(args):
                                f"{cfg.reduction}, grad_output={cfg.grad_output}, "
                                f"{'class weights, ' if cfg.weighted else ''}gradient in place",
                    "global_batch": R * world, "seq_len": None, "parallelism": f"replicas x{world}",
-                   "variant": args.variant, "path": path, "fused_plan": plan,
+                   "variant": args.variant, "path": path, "tune": args.tune, "fused_plan": plan,
                    "l2": "inputs 2.1 GB > 129 MB L2; logits restored and a 256 MB buffer written "
                          "before every step, outside the timed region"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -462,14 +518,17 @@ def main():
     ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--variant", choices=["auto", "fused", "split", "rowpass"], default="auto")
+    ap.add_argument("--variant", choices=["auto", "fused", "split", "rowpass", "stream"], default="auto")
     ap.add_argument("--cluster", type=int, default=0)
-    ap.add_argument("--cpu-rows", type=int, default=2048)
-    ap.add_argument("--ref-rows", type=int, default=512)
+    ap.add_argument("--tune", type=int, default=0, help="stream-kernel tuning bits (see include/ce.h)")
+    ap.add_argument("--cpu-rows", type=int, default=8192)
+    ap.add_argument("--ref-rows", type=int, default=2048)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-flce", action="store_true", help="skip the fused-linear measurement")
-    ap.add_argument("--flce-chunk", type=int, default=2048)
+    ap.add_argument("--flce-chunk", type=int, default=4096)
+    ap.add_argument("--flce-only", action="store_true", help="only the fused-linear measurement")
+    ap.add_argument("--gemm-only", default="", help="only one GEMM: M,N,K,a_mn,b_mn")
     ap.add_argument("--rows", type=int, default=0, help="rows of a smaller case of the workload (profiling)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="CE workload of workloads.CONFIGS (the default is the headline metric's)")

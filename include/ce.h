@@ -76,17 +76,25 @@ typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
 #define CE_FLAG_WAIT_TIMEOUT 0x4u        /* a device-side wait gave up (results invalid) */
 
 /* ce_params.variant: which kernels ce_fwd_bwd uses */
-#define CE_VARIANT_AUTO 0   /* the library picks (ce_select_variant): the row-pass kernel */
+#define CE_VARIANT_AUTO 0   /* the library picks (ce_select_variant) */
 #define CE_VARIANT_SPLIT 1  /* ce_forward then ce_backward kernels (row read twice) */
 #define CE_VARIANT_FUSED 2  /* fused kernel; CE_ERR_UNSUPPORTED if the rows do not allow it */
 #define CE_VARIANT_ROWPASS 3 /* one kernel, each row read twice, the second read from L2 */
+#define CE_VARIANT_STREAM 4  /* as ROWPASS, the two passes streamed through a shared-memory
+                                ring by bulk copies; 16-byte aligned rows only */
 /* bits 8..15 of variant: fused-kernel cluster size override, or CTAs per SM
- * of the row-pass kernel (0 = automatic) */
+ * of the row-pass and stream kernels (0 = automatic) */
 #define CE_VARIANT_CLUSTER_SHIFT 8
 /* the workspace already holds this batch's normalisers from ce_prepare (same
  * target, weights, n_rows and reduction): ce_forward / ce_backward /
  * ce_fwd_bwd skip their own normaliser kernel */
 #define CE_VARIANT_PREPARED 0x10000
+/* bits 20..24 of variant: stream-kernel tuning (0 = the library's choice):
+ * 1 = 16 consumer warps and one CTA per SM, 2 = second pass over each row's
+ * chunks in reverse order, 4 = first pass without the L2 evict-last policy,
+ * 8 = a cluster of two CTAs per row (each streams half the row),
+ * 16 = three CTAs per SM with a smaller ring */
+#define CE_VARIANT_TUNE_SHIFT 20
 
 typedef struct ce_params {
     int64_t n_rows;             /* BT >= 0 */
@@ -100,7 +108,18 @@ typedef struct ce_params {
     int32_t target_is_int32;    /* 0: int64 targets, 1: int32 targets */
     int32_t variant;            /* CE_VARIANT_* (ce_fwd_bwd only) */
     int32_t reserved;           /* must be 0 */
-} ce_params; /* 64 bytes */
+    /* Options named next to the method on the Liger-Kernel #1268 page (its CE
+     * suite: "class weights, softcap, label smoothing, z-loss"; its dx_y
+     * correction keeps the "softcap factors") without a definition there;
+     * this library takes the plain ones. Supported by ce_forward /
+     * ce_backward and ce_fwd_bwd's row-pass and split paths (ce_fwd_bwd
+     * picks the row pass when an option is set); the cluster variant and
+     * flce_fwd_bwd return CE_ERR_UNSUPPORTED with an option set. */
+    float softcap;              /* c > 0: every logit becomes c*tanh(x/c); 0 = off */
+    float z_loss;               /* lambda >= 0: loss_i += lambda*LSE_i^2 on valid rows */
+    float *accuracy;            /* device fp32 [1] or NULL: share of valid rows whose argmax
+                                   (first column of the row maximum) is the target */
+} ce_params; /* 80 bytes */
 
 /* Library version string, e.g. "ce-gb300 1.0". */
 const char *ce_version(void);
@@ -227,10 +246,20 @@ ce_status ce_fused_plan(const ce_params *p, int32_t *cluster_size, int32_t *n_cl
 
 /*
  * The kernel path ce_fwd_bwd takes for p->variant == CE_VARIANT_AUTO (host
- * query, no GPU work): CE_VARIANT_ROWPASS, CE_VARIANT_FUSED or
- * CE_VARIANT_SPLIT in *variant. `logits` is only inspected for alignment.
+ * query, no GPU work): one of the CE_VARIANT_* paths in *variant. `logits`
+ * is only inspected for alignment.
  */
 ce_status ce_select_variant(const ce_params *p, const void *logits, int32_t *variant);
+
+/*
+ * Self-test of the device-side bounded wait every kernel of this library
+ * uses on its mbarriers: one block waits on an mbarrier that nothing ever
+ * arrives on, gives up after about limit_ns nanoseconds, and writes
+ * CE_FLAG_WAIT_TIMEOUT to *device_flags (device uint32). Lets a caller
+ * check that a failed wait ends with a status instead of a hang, and that
+ * the context stays usable. limit_ns in [1e6, 5e9].
+ */
+ce_status ce_selftest_wait_timeout(uint64_t limit_ns, uint32_t *device_flags, void *stream);
 
 /*
  * Synchronises `stream`, then copies the workspace status word (CE_FLAG_*

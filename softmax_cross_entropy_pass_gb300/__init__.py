@@ -32,7 +32,7 @@ CE_OK, CE_ERR_INVALID_ARG, CE_ERR_UNSUPPORTED, CE_ERR_CUDA, CE_ERR_WORKSPACE = 0
 CE_RED = {"none": 0, "mean": 1, "sum": 2}
 CE_DT = {torch.float32: 0, torch.bfloat16: 1, torch.float16: 2}
 CE_FLAG_TARGET_OUT_OF_RANGE, CE_FLAG_NO_VALID_ROWS, CE_FLAG_WAIT_TIMEOUT = 1, 2, 4
-VARIANTS = {"auto": 0, "split": 1, "fused": 2, "rowpass": 3}
+VARIANTS = {"auto": 0, "split": 1, "fused": 2, "rowpass": 3, "stream": 4}
 CE_VARIANT_PREPARED = 0x10000
 
 
@@ -45,10 +45,11 @@ class ce_params(ctypes.Structure):
                 ("ignore_index", ctypes.c_int64), ("class_weight", ctypes.c_void_p),
                 ("label_smoothing", ctypes.c_float), ("dtype", ctypes.c_int32),
                 ("reduction", ctypes.c_int32), ("target_is_int32", ctypes.c_int32),
-                ("variant", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("variant", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("softcap", ctypes.c_float), ("z_loss", ctypes.c_float), ("accuracy", ctypes.c_void_p)]
 
 
-assert ctypes.sizeof(ce_params) == 64
+assert ctypes.sizeof(ce_params) == 80
 
 
 def _load():
@@ -72,6 +73,7 @@ def _load():
                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]),
         "ce_get_status": (st, [vp, ctypes.POINTER(ctypes.c_uint32), vp]),
         "ce_select_variant": (st, [P, vp, ctypes.POINTER(ctypes.c_int32)]),
+        "ce_selftest_wait_timeout": (st, [ctypes.c_uint64, vp, vp]),
         "ce_gemm_bf16": (st, [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, vp, ctypes.c_int64, ctypes.c_int32,
                               vp, ctypes.c_int64, ctypes.c_int32, ctypes.c_int32, vp, ctypes.c_int64, vp, vp]),
         "flce_workspace_size": (st, [P, ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(sz)]),
@@ -111,7 +113,8 @@ def _stream(stream) -> ctypes.c_void_p:
 
 def make_params(logits: torch.Tensor, target: torch.Tensor, *, weight=None, ignore_index: int = -100,
                 label_smoothing: float = 0.0, reduction: str = "mean", variant="auto",
-                cluster: int = 0) -> ce_params:
+                cluster: int = 0, tune: int = 0, softcap: float = 0.0, z_loss: float = 0.0,
+                accuracy=None) -> ce_params:
     if logits.dim() != 2 or logits.stride(1) != 1:
         raise ValueError("logits must be a 2-D tensor with unit column stride")
     if logits.dtype not in CE_DT:
@@ -132,8 +135,15 @@ def make_params(logits: torch.Tensor, target: torch.Tensor, *, weight=None, igno
     p.dtype = CE_DT[logits.dtype]
     p.reduction = CE_RED[reduction]
     p.target_is_int32 = 1 if target.dtype == torch.int32 else 0
-    p.variant = (VARIANTS[variant] if isinstance(variant, str) else int(variant)) | (int(cluster) << 8)
+    p.variant = ((VARIANTS[variant] if isinstance(variant, str) else int(variant)) | (int(cluster) << 8)
+                 | (int(tune) << 20))
     p.reserved = 0
+    p.softcap = float(softcap)
+    p.z_loss = float(z_loss)
+    if accuracy is not None:
+        if accuracy.dtype != torch.float32 or not accuracy.is_cuda:
+            raise ValueError("accuracy must be a device fp32 tensor")
+        p.accuracy = accuracy.data_ptr()
     return p
 
 
@@ -175,11 +185,13 @@ def ce_prepare(logits, target, *, weight=None, ignore_index=-100, label_smoothin
 
 
 def ce_forward(logits, target, *, weight=None, ignore_index=-100, label_smoothing=0.0,
-               reduction="mean", stats=None, loss=None, ws=None, stream=None):
+               reduction="mean", stats=None, loss=None, ws=None, stream=None, softcap=0.0, z_loss=0.0,
+               accuracy=None):
     """Loss and per-row statistics [n_rows, 4] (m, off-target exp-sum, x_y, smoothing sum)."""
     _check_dev(logits, target, weight)
     p = make_params(logits, target, weight=weight, ignore_index=ignore_index,
-                    label_smoothing=label_smoothing, reduction=reduction)
+                    label_smoothing=label_smoothing, reduction=reduction, softcap=softcap, z_loss=z_loss,
+                    accuracy=accuracy)
     n = logits.shape[0]
     if loss is None:
         loss = torch.empty(n if reduction == "none" else 1, dtype=torch.float32, device=logits.device)
@@ -192,11 +204,11 @@ def ce_forward(logits, target, *, weight=None, ignore_index=-100, label_smoothin
 
 
 def ce_backward(logits, target, stats, *, grad_output=None, weight=None, ignore_index=-100,
-                label_smoothing=0.0, reduction="mean", ws=None, stream=None):
+                label_smoothing=0.0, reduction="mean", ws=None, stream=None, softcap=0.0, z_loss=0.0):
     """Writes the gradient over ``logits`` (in place) and returns it."""
     _check_dev(logits, target, stats, grad_output, weight)
     p = make_params(logits, target, weight=weight, ignore_index=ignore_index,
-                    label_smoothing=label_smoothing, reduction=reduction)
+                    label_smoothing=label_smoothing, reduction=reduction, softcap=softcap, z_loss=z_loss)
     ws, wsb = _ws(ws, logits.shape[0], logits.device)
     _check(_lib.ce_backward(ctypes.byref(p), _ptr(logits), _ptr(target), _ptr(stats),
                             _ptr(grad_output), _ptr(ws), wsb, _stream(stream)), "ce_backward")
@@ -205,13 +217,13 @@ def ce_backward(logits, target, stats, *, grad_output=None, weight=None, ignore_
 
 def ce_fwd_bwd(logits, target, *, grad_output=None, weight=None, ignore_index=-100,
                label_smoothing=0.0, reduction="mean", variant="auto", cluster=0, loss=None,
-               ws=None, stream=None, prepared=False):
+               ws=None, stream=None, prepared=False, tune=0, softcap=0.0, z_loss=0.0, accuracy=None):
     """Loss; the gradient (times grad_output, or 1) is written over ``logits``.
     ``prepared``: ``ws`` already holds this batch's normalisers (ce_prepare)."""
     _check_dev(logits, target, grad_output, weight)
     p = make_params(logits, target, weight=weight, ignore_index=ignore_index,
                     label_smoothing=label_smoothing, reduction=reduction, variant=variant,
-                    cluster=cluster)
+                    cluster=cluster, tune=tune, softcap=softcap, z_loss=z_loss, accuracy=accuracy)
     if prepared:
         if ws is None:
             raise ValueError("prepared=True needs the prepared workspace")
@@ -290,6 +302,15 @@ def ce_fused_plan(n_rows: int, vocab: int, dtype=torch.bfloat16, *, weighted=Fal
     return c.value, ncl.value, per_sm.value, sb.value
 
 
+def ce_selftest_wait_timeout(limit_ns: int = 100_000_000, stream=None) -> int:
+    """Runs the bounded-wait self-test (a wait nothing satisfies) and returns
+    the flags it reported (CE_FLAG_WAIT_TIMEOUT expected); synchronises."""
+    flags = torch.zeros(1, dtype=torch.int32, device="cuda")
+    _check(_lib.ce_selftest_wait_timeout(int(limit_ns), _ptr(flags), _stream(stream)), "ce_selftest_wait_timeout")
+    torch.cuda.synchronize()
+    return int(flags.item())
+
+
 def ce_get_status(ws, stream=None) -> int:
     """Synchronises the stream and returns the CE_FLAG_* bits of the last call on ``ws``."""
     out = ctypes.c_uint32()
@@ -362,7 +383,7 @@ def flce_workspace_size(n_rows: int, hidden: int, vocab: int, chunk_rows: int) -
 
 
 def flce_fwd_bwd(hidden, weight, target, *, bias=None, class_weight=None, ignore_index=-100,
-                 label_smoothing=0.0, reduction="mean", grad_output=None, chunk_rows=2048, loss=None,
+                 label_smoothing=0.0, reduction="mean", grad_output=None, chunk_rows=4096, loss=None,
                  grad_hidden=None, grad_weight=None, grad_bias=None, ws=None, stream=None):
     """Fused-linear cross-entropy: returns (loss, grad_hidden [BT, H] bf16,
     grad_weight [V, H] fp32, grad_bias [V] fp32 or None)."""

@@ -41,8 +41,14 @@ ce_status check_params(const ce_params *p) {
     if (p->target_is_int32 != 0 && p->target_is_int32 != 1) return CE_ERR_INVALID_ARG;
     if (p->reserved != 0) return CE_ERR_INVALID_ARG;
     if (p->class_weight && !aligned(p->class_weight, 4)) return CE_ERR_INVALID_ARG;
+    if (!(p->softcap >= 0.f && p->softcap < INFINITY) || !(p->z_loss >= 0.f && p->z_loss < INFINITY))
+        return CE_ERR_INVALID_ARG;
+    if (p->accuracy && !aligned(p->accuracy, 4)) return CE_ERR_INVALID_ARG;
     return CE_OK;
 }
+
+// softcap, z-loss or token accuracy asked for
+bool has_options(const ce_params *p) { return p->softcap > 0.f || p->z_loss > 0.f || p->accuracy; }
 
 size_t workspace_bytes_for(int64_t n_rows) { return ws_bytes(n_rows); }
 
@@ -96,6 +102,9 @@ RowArgs row_args(const ce_params *p, const void *target, void *ws) {
     a.eps = p->label_smoothing;
     a.row_loss = ws_row_loss(ws);
     a.ctl = reinterpret_cast<WsCtl *>(ws);
+    a.softcap = p->softcap;
+    a.z_loss = p->z_loss;
+    a.accuracy = p->accuracy;
     return a;
 }
 
@@ -142,10 +151,11 @@ bool fused_layout_ok(const ce_params *p, const void *x) {
 // The path of CE_VARIANT_AUTO: the one-kernel row pass (HBM read once, the
 // second read served by L2) is the fastest measured path on GB300 for every
 // row size; the split path remains for callers that ask for it.
+bool fused_layout_ok(const ce_params *p, const void *x);
+
 int auto_path(const ce_params *p, const void *x) {
-    (void)p;
-    (void)x;
-    return CE_VARIANT_ROWPASS;
+    if (has_options(p)) return CE_VARIANT_ROWPASS;  // the options live in the row-pass and split kernels
+    return fused_layout_ok(p, x) ? CE_VARIANT_STREAM : CE_VARIANT_ROWPASS;
 }
 
 }  // namespace
@@ -242,12 +252,31 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
     if ((st = check_ws(p, ws, ws_bytes)) != CE_OK) return st;
     if (!loss || (p->n_rows > 0 && (!logits_inout || !target))) return CE_ERR_INVALID_ARG;
     int path = p->variant & 0xff;
-    if (p->variant & ~(0xffff | CE_VARIANT_PREPARED)) return CE_ERR_INVALID_ARG;
+    if (p->variant & ~(0xffff | CE_VARIANT_PREPARED | (0x1f << CE_VARIANT_TUNE_SHIFT))) return CE_ERR_INVALID_ARG;
     if (path == CE_VARIANT_AUTO) path = auto_path(p, logits_inout);
     if (path != CE_VARIANT_AUTO && path != CE_VARIANT_SPLIT && path != CE_VARIANT_FUSED &&
-        path != CE_VARIANT_ROWPASS)
+        path != CE_VARIANT_ROWPASS && path != CE_VARIANT_STREAM)
         return CE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    if ((path == CE_VARIANT_STREAM || path == CE_VARIANT_FUSED) && has_options(p)) return CE_ERR_UNSUPPORTED;
+    if (path == CE_VARIANT_STREAM) {
+        if (!fused_layout_ok(p, logits_inout)) return CE_ERR_UNSUPPORTED;
+        cudaError_t e = enqueue_prep(p, target, ws, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+        if (p->n_rows == 0) {
+            if (p->reduction != CE_RED_NONE && (e = cudaMemsetAsync(loss, 0, sizeof(float), s)) != cudaSuccess)
+                return cuda_fail(e);
+            return CE_OK;
+        }
+        RowArgs a = row_args(p, target, ws);
+        a.grad = logits_inout;
+        a.loss = loss;
+        a.grad_output = grad_output;
+        e = launch_stream(a, p->dtype, smoothing_mode(p), (p->variant >> CE_VARIANT_CLUSTER_SHIFT) & 0xff,
+                          (p->variant >> CE_VARIANT_TUNE_SHIFT) & 0x1f, (p->variant & CE_VARIANT_PREPARED) == 0, s);
+        return e == cudaSuccess ? CE_OK : cuda_fail(e);
+    }
 
     if (path == CE_VARIANT_ROWPASS) {
         cudaError_t e = enqueue_prep(p, target, ws, s);
@@ -355,6 +384,13 @@ ce_status ce_fused_plan(const ce_params *p, int32_t *cluster_size, int32_t *n_cl
     if (ctas_per_sm) *ctas_per_sm = plan.ctas_per_sm;
     if (slice_bytes) *slice_bytes = plan.slice_elems * elem_bytes(p->dtype);
     return CE_OK;
+}
+
+ce_status ce_selftest_wait_timeout(uint64_t limit_ns, uint32_t *device_flags, void *stream) {
+    if (!device_flags || !aligned(device_flags, 4)) return CE_ERR_INVALID_ARG;
+    if (limit_ns < 1000000ull || limit_ns > 5000000000ull) return CE_ERR_INVALID_ARG;
+    cudaError_t e = launch_wait_selftest(limit_ns, device_flags, reinterpret_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? CE_OK : cuda_fail(e);
 }
 
 ce_status ce_get_status(const void *ws, uint32_t *flags, void *stream) {

@@ -22,7 +22,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 struct WsCtl {
     unsigned int status;      // CE_FLAG_* bits of the current call
     unsigned int done;        // blocks finished (last-block reduction)
-    unsigned int pad0[2];
+    unsigned int n_correct;   // rows whose argmax is the target (token accuracy)
+    unsigned int pad0;
     float n_valid;            // number of valid rows
     float w_y;                // sum of w_{t_i} over valid rows (n_valid when unweighted)
     float w_all;              // sum_c w_c (vocab when unweighted)
@@ -277,6 +278,35 @@ __device__ inline float row_state_rel_sum(const RowState &st) {
     return st.n > 0.f ? __fsub_rn(st.r, __fmul_rn(st.n, st.m)) : 0.f;
 }
 
+// ------------------------------------------------------------------ softcap and argmax
+// z = c tanh(x / c) with the accurate tanh (an approximate tanh would move
+// exp(z) by more than half a bf16 ulp), and dz/dx = 1 - (z / c)^2.
+__device__ inline float softcap_logit(float x, float c) { return c * tanhf(x / c); }
+__device__ inline float softcap_deriv(float z, float c) {
+    const float u = z / c;
+    return fmaf(-u, u, 1.f);
+}
+
+// The first column holding the maximum (ties go to the smaller column).
+struct ArgMax {
+    float v;
+    int i;
+};
+__device__ inline ArgMax argmax_merge(const ArgMax &a, const ArgMax &b) {
+    if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
+    return a;
+}
+__device__ inline ArgMax warp_argmax(ArgMax a) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        ArgMax o;
+        o.v = __shfl_xor_sync(0xffffffffu, a.v, off);
+        o.i = __shfl_xor_sync(0xffffffffu, a.i, off);
+        a = argmax_merge(a, o);
+    }
+    return a;
+}
+
 // ------------------------------------------------------------------ per-row scalars
 // Everything the gradient and the loss of one row need, formed once in fp32
 // from the row statistics (m, s, x_y, r) and the batch normalisers.
@@ -298,7 +328,7 @@ __device__ inline float softplus_f(float t) {
 // scale = s_i of the gradient; valid = row has a usable target.
 __device__ inline RowScalars make_row_scalars(float m, float s, float xy, float r, bool valid,
                                               int64_t y, float wy, float w_all, float eps,
-                                              float inv_v, float scale) {
+                                              float inv_v, float scale, float z_loss = 0.f) {
     RowScalars o;
     o.m = m;
     if (!valid) {
@@ -318,6 +348,14 @@ __device__ inline RowScalars make_row_scalars(float m, float s, float xy, float 
     // LSE - x_y = log1p(s * exp(m - x_y)) = softplus(log s + m - x_y)
     const float nll = (s > 0.f) ? softplus_f(logf(s) + (m - xy)) : 0.f;
     o.loss = (1.f - eps) * wy * nll + eps_v * (w_all * log_d - r);
+    if (z_loss > 0.f) {
+        // lambda LSE^2: loss term, and 2 lambda LSE p in the gradient
+        const float lse = m + log_d;
+        o.loss += z_loss * lse * lse;
+        const float zc = scale * 2.f * z_loss * lse;
+        o.a += zc;
+        o.dxy += zc * p_y;
+    }
     o.y = y;
     return o;
 }

@@ -41,6 +41,9 @@ struct RowArgs {
     float *stats;              // [n_rows][4] (stats: out, grad: in)
     float *row_loss;           // workspace per-row loss (mean / sum)
     WsCtl *ctl;
+    float softcap;             // > 0: logits become c tanh(x / c)
+    float z_loss;              // lambda of lambda LSE^2
+    float *accuracy;           // token accuracy out [1] or NULL
 };
 
 struct ScaleArgs {
@@ -81,11 +84,18 @@ constexpr int kMaxCluster = 16;
 constexpr int kFusedSmemFixed = 2048;
 
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s);
+cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned int *flags, cudaStream_t s);
 cudaError_t launch_stats(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s);
 cudaError_t launch_grad(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s);
+// true when softcap, z-loss or token accuracy is asked for (row-pass / split kernels only)
+inline bool row_features(const RowArgs &a) { return a.softcap > 0.f || a.z_loss > 0.f || a.accuracy; }
 cudaError_t launch_scale(const ScaleArgs &a, int dtype, int grid, cudaStream_t s);
 // one-kernel forward + backward, two passes per row (second from L2)
 cudaError_t launch_rowpass(const RowArgs &a, int dtype, int mode, int ctas_per_sm, cudaStream_t s);
+// the same two passes streamed through a shared-memory ring by bulk copies
+// (16-byte aligned rows only)
+cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm, int tune, bool after_prep,
+                          cudaStream_t s);
 
 // Fused kernel plan / launch. `mode`: 0 no smoothing, 1 smoothing, 2 weighted smoothing.
 struct FusedPlan {

@@ -81,6 +81,7 @@ __global__ void __launch_bounds__(kPrepThreads) ce_prep_kernel(PrepArgs a) {
         if (a.reduction == CE_RED_MEAN && y == 0.0) status |= CE_FLAG_NO_VALID_ROWS;
         ctl->status = status;
         ctl->done = 0u;
+        ctl->n_correct = 0u;
         ctl->n_valid = static_cast<float>(c);
         ctl->w_y = static_cast<float>(y);
         ctl->w_all = a.weight ? static_cast<float>(w) : static_cast<float>(a.vocab);
@@ -111,6 +112,8 @@ __device__ inline float grad_scale(const RowArgs &a, const WsCtl *ctl, int64_t r
 // Last block to finish reduces the per-row losses in a fixed order (double
 // accumulation) and resets the counter. Thread 0 of each block must have
 // written its rows' losses before calling.
+__device__ inline void finish_accuracy(const RowArgs &a, WsCtl *ctl);
+
 __device__ inline void finish_loss(const RowArgs &a, WsCtl *ctl, unsigned n_blocks) {
     __shared__ unsigned sh_last;
     __shared__ double sh_sum[32];
@@ -123,6 +126,11 @@ __device__ inline void finish_loss(const RowArgs &a, WsCtl *ctl, unsigned n_bloc
     __syncthreads();
     if (!sh_last) return;
     __threadfence();
+    finish_accuracy(a, ctl);
+    if (a.reduction == CE_RED_NONE) {
+        if (threadIdx.x == 0) ctl->done = 0u;
+        return;
+    }
     const float *rl = a.row_loss;
     double s = 0.0;
     for (int64_t i = threadIdx.x; i < a.n_rows; i += blockDim.x) s += static_cast<double>(__ldcg(rl + i));
@@ -142,6 +150,49 @@ __device__ inline void finish_loss(const RowArgs &a, WsCtl *ctl, unsigned n_bloc
     }
 }
 
+// Last-block token accuracy: correct rows over valid rows (0 with none).
+__device__ inline void finish_accuracy(const RowArgs &a, WsCtl *ctl) {
+    if (threadIdx.x == 0 && a.accuracy) {
+        const float n = ctl->n_valid;
+        a.accuracy[0] = n > 0.f ? static_cast<float>(__ldcg(&ctl->n_correct)) / n : 0.f;
+    }
+}
+
+// Statistics of one vector with the options on: the logits are capped
+// first (the statistics describe the capped logits z), the argmax follows
+// the raw logits (tanh is monotonic, so it is the same column).
+template <int VEC, bool SMOOTH>
+__device__ inline void feat_add(RowState &st, ArgMax &am, const float *xraw, int64_t col0, int skip,
+                                const float *w, float cap, bool want_am) {
+    float z[VEC];
+    float zmax = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < VEC; ++j) {
+        z[j] = cap > 0.f ? softcap_logit(xraw[j], cap) : xraw[j];
+        zmax = fmaxf(zmax, z[j]);
+    }
+    if (want_am) {
+#pragma unroll
+        for (int j = 0; j < VEC; ++j) am = argmax_merge(am, ArgMax{xraw[j], static_cast<int>(col0 + j)});
+    }
+    row_state_add<VEC, SMOOTH>(st, z, zmax, skip, w);
+}
+
+// Block-wide argmax; the result is valid in thread 0.
+__device__ inline ArgMax block_argmax(ArgMax am, ArgMax *sh /*[32]*/) {
+    am = warp_argmax(am);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    __syncthreads();
+    if (lane == 0) sh[warp] = am;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        am = lane < nw ? sh[lane] : ArgMax{-INFINITY, 0x7fffffff};
+        am = warp_argmax(am);
+    }
+    return am;
+}
+
 // Block-wide merge of per-thread states; the result is valid in thread 0.
 __device__ inline RowState block_merge(RowState st, RowState *sh /*[32]*/) {
     st = warp_merge(st);
@@ -157,13 +208,16 @@ __device__ inline RowState block_merge(RowState st, RowState *sh /*[32]*/) {
 }
 
 // ------------------------------------------------------------------ forward: row statistics
-template <int DT, int MODE>
+template <int DT, int MODE, bool FEAT>
 __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
     using F = Fmt<DT>;
     constexpr int VEC = F::kVec;
     constexpr bool SMOOTH = MODE != 0;
     constexpr int UNROLL = 4;
     __shared__ RowState sh[32];
+    __shared__ ArgMax sh_am[32];
+    const float cap = FEAT ? a.softcap : 0.f;
+    const bool want_am = FEAT && a.accuracy != nullptr;
     WsCtl *ctl = a.ctl;
     const float inv_v = 1.f / static_cast<float>(a.vocab);
     pdl_wait();
@@ -181,11 +235,13 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
         const int64_t tail0 = head + nvec * VEC;
 
         RowState st = row_state_empty();
+        ArgMax am{-INFINITY, 0x7fffffff};
         // scalar head (< 16 bytes before the first aligned vector) and tail
         if (const int64_t c = scalar_col(threadIdx.x, head, tail0, V); c >= 0) {
             float x = F::load1(rowp, c);
             float w = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
-            row_state_add<1, SMOOTH>(st, &x, x, (c == y) ? 0 : -1, MODE == 2 ? &w : nullptr);
+            if constexpr (FEAT) feat_add<1, SMOOTH>(st, am, &x, c, (c == y) ? 0 : -1, MODE == 2 ? &w : nullptr, cap, want_am);
+            else row_state_add<1, SMOOTH>(st, &x, x, (c == y) ? 0 : -1, MODE == 2 ? &w : nullptr);
         }
         // 16-byte vectors
         const uint4 *vp = reinterpret_cast<const uint4 *>(rowp + head * F::kBytes);
@@ -209,17 +265,23 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) w[j] = __ldg(a.weight + base + j);
                 }
-                row_state_add<VEC, SMOOTH>(st, x, F::vmax(raw[u]), skip, MODE == 2 ? w : nullptr);
+                if constexpr (FEAT) feat_add<VEC, SMOOTH>(st, am, x, base, skip, MODE == 2 ? w : nullptr, cap, want_am);
+                else row_state_add<VEC, SMOOTH>(st, x, F::vmax(raw[u]), skip, MODE == 2 ? w : nullptr);
             }
+        }
+        if constexpr (FEAT) {
+            if (want_am) am = block_argmax(am, sh_am);
         }
         st = block_merge(st, sh);
         if (threadIdx.x == 0) {
-            const float xy = valid ? F::load1(rowp, y) : 0.f;
+            float xy = valid ? F::load1(rowp, y) : 0.f;
+            if (FEAT && cap > 0.f) xy = softcap_logit(xy, cap);
             const float wy = valid ? (a.weight ? __ldg(a.weight + y) : 1.f) : 0.f;
             // the loss needs no gradient scale
             const float rrel = SMOOTH ? row_state_rel_sum(st) : 0.f;
             RowScalars rs = make_row_scalars(st.m, st.s, xy, rrel, valid, y, wy, ctl->w_all,
-                                             a.eps, inv_v, 1.f);
+                                             a.eps, inv_v, 1.f, FEAT ? a.z_loss : 0.f);
+            if (want_am && valid && am.i == y) atomicAdd(&ctl->n_correct, 1u);
             if (a.stats) {
                 float4 s4 = make_float4(st.m, st.s, xy, rrel);
                 reinterpret_cast<float4 *>(a.stats)[row] = s4;
@@ -229,15 +291,16 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
         }
         __syncthreads();
     }
-    if (a.reduction != CE_RED_NONE) finish_loss(a, ctl, gridDim.x);
+    if (a.reduction != CE_RED_NONE || (FEAT && a.accuracy)) finish_loss(a, ctl, gridDim.x);
 }
 
 // ------------------------------------------------------------------ backward: gradient in place
-template <int DT, int MODE>
+template <int DT, int MODE, bool FEAT>
 __global__ void __launch_bounds__(kRowThreads, 3) ce_grad_kernel(RowArgs a) {
     using F = Fmt<DT>;
     constexpr int VEC = F::kVec;
     constexpr int UNROLL = 4;
+    const float cap = FEAT ? a.softcap : 0.f;
     const WsCtl *ctl = a.ctl;
     const float inv_v = 1.f / static_cast<float>(a.vocab);
     pdl_wait();
@@ -251,7 +314,7 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_grad_kernel(RowArgs a) {
         const float4 s4 = __ldg(reinterpret_cast<const float4 *>(a.stats) + row);
         const float wy = valid ? (a.weight ? __ldg(a.weight + y) : 1.f) : 0.f;
         const RowScalars rs = make_row_scalars(s4.x, s4.y, s4.z, s4.w, valid, y, wy, w_all, a.eps,
-                                               inv_v, grad_scale(a, ctl, row));
+                                               inv_v, grad_scale(a, ctl, row), FEAT ? a.z_loss : 0.f);
         const int64_t V = a.vocab;
         const uintptr_t addr = reinterpret_cast<uintptr_t>(rowp);
         int64_t head = static_cast<int64_t>(((16u - (addr & 15u)) & 15u) / F::kBytes);
@@ -263,7 +326,10 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_grad_kernel(RowArgs a) {
             float g = 0.f;
             if (valid) {
                 float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
-                g = (c == y) ? rs.dxy : grad_elem(rs, F::load1(rowp, c), wc);
+                float x = F::load1(rowp, c);
+                if (FEAT && cap > 0.f) x = softcap_logit(x, cap);
+                g = (c == y) ? rs.dxy : grad_elem(rs, x, wc);
+                if (FEAT && cap > 0.f) g *= softcap_deriv(x, cap);
             }
             F::store1(rowp, c, g);
         }
@@ -287,6 +353,10 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_grad_kernel(RowArgs a) {
                 float x[VEC], g[VEC];
                 F::unpack(raw[u], x);
                 const int64_t base = head + v * VEC;
+                if (FEAT && cap > 0.f) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) x[j] = softcap_logit(x[j], cap);
+                }
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) {
                     float wc = (MODE == 2) ? __ldg(a.weight + base + j) : 1.f;
@@ -295,6 +365,10 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_grad_kernel(RowArgs a) {
                 if (static_cast<uint64_t>(y - base) < static_cast<uint64_t>(VEC)) {
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) g[e] = (base + e == y) ? rs.dxy : g[e];
+                }
+                if (FEAT && cap > 0.f) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) g[j] *= softcap_deriv(x[j], cap);
                 }
                 st_stream(vp + v, F::pack(g));
             }
@@ -322,14 +396,17 @@ __device__ inline uint64_t policy_evict_last() {
     return p;
 }
 
-template <int DT, int MODE>
+template <int DT, int MODE, bool FEAT>
 __global__ void __launch_bounds__(kRowpassThreads, 2) ce_rowpass_kernel(RowArgs a) {
     using F = Fmt<DT>;
     constexpr int VEC = F::kVec;
     constexpr bool SMOOTH = MODE != 0;
     constexpr int UNROLL = 4;
     __shared__ RowState sh[32];
+    __shared__ ArgMax sh_am[32];
     __shared__ RowScalars sh_rs;
+    const float cap = FEAT ? a.softcap : 0.f;
+    const bool want_am = FEAT && a.accuracy != nullptr;
     WsCtl *ctl = a.ctl;
     const float inv_v = 1.f / static_cast<float>(a.vocab);
     const uint64_t keep = policy_evict_last(), drop = policy_evict_first();
@@ -362,10 +439,12 @@ __global__ void __launch_bounds__(kRowpassThreads, 2) ce_rowpass_kernel(RowArgs 
         }
         // ---------------------------------------------------------------- pass 1: statistics
         RowState st = row_state_empty();
+        ArgMax am{-INFINITY, 0x7fffffff};
         if (const int64_t c = scalar_col(threadIdx.x, head, tail0, V); c >= 0) {
             float x = F::load1(rowp, c);
             float w = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
-            row_state_add<1, SMOOTH>(st, &x, x, (c == y) ? 0 : -1, MODE == 2 ? &w : nullptr);
+            if constexpr (FEAT) feat_add<1, SMOOTH>(st, am, &x, c, (c == y) ? 0 : -1, MODE == 2 ? &w : nullptr, cap, want_am);
+            else row_state_add<1, SMOOTH>(st, &x, x, (c == y) ? 0 : -1, MODE == 2 ? &w : nullptr);
         }
         for (int v0 = threadIdx.x; v0 < nvec; v0 += blockDim.x * UNROLL) {
             uint4 raw[UNROLL];
@@ -387,26 +466,37 @@ __global__ void __launch_bounds__(kRowpassThreads, 2) ce_rowpass_kernel(RowArgs 
 #pragma unroll
                     for (int j = 0; j < VEC; ++j) w[j] = __ldg(a.weight + head + vb + j);
                 }
-                row_state_add<VEC, SMOOTH>(st, x, F::vmax(raw[u]), skip, MODE == 2 ? w : nullptr);
+                if constexpr (FEAT) feat_add<VEC, SMOOTH>(st, am, x, head + vb, skip, MODE == 2 ? w : nullptr, cap, want_am);
+                else row_state_add<VEC, SMOOTH>(st, x, F::vmax(raw[u]), skip, MODE == 2 ? w : nullptr);
             }
+        }
+        if constexpr (FEAT) {
+            if (want_am) am = block_argmax(am, sh_am);
         }
         st = block_merge(st, sh);
         if (threadIdx.x == 0) {
-            const float xy = F::load1(rowp, y);
+            float xy = F::load1(rowp, y);
+            if (FEAT && cap > 0.f) xy = softcap_logit(xy, cap);
             const float wy = a.weight ? __ldg(a.weight + y) : 1.f;
             const float rrel = SMOOTH ? row_state_rel_sum(st) : 0.f;
-            const RowScalars rl = make_row_scalars(st.m, st.s, xy, rrel, true, y, wy, w_all, a.eps, inv_v, 1.f);
+            const float zl = FEAT ? a.z_loss : 0.f;
+            const RowScalars rl = make_row_scalars(st.m, st.s, xy, rrel, true, y, wy, w_all, a.eps, inv_v, 1.f, zl);
             if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
             else a.row_loss[row] = rl.loss;
             sh_rs = make_row_scalars(st.m, st.s, xy, rrel, true, y, wy, w_all, a.eps, inv_v,
-                                     grad_scale(a, ctl, row));
+                                     grad_scale(a, ctl, row), zl);
+            if (want_am && am.i == y) atomicAdd(&ctl->n_correct, 1u);
         }
         __syncthreads();
         const RowScalars rs = sh_rs;
         // ---------------------------------------------------------------- pass 2: gradient in place
         if (const int64_t c = scalar_col(threadIdx.x, head, tail0, V); c >= 0) {
             const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
-            F::store1(rowp, c, (c == y) ? rs.dxy : grad_elem(rs, F::load1(rowp, c), wc));
+            float x = F::load1(rowp, c);
+            if (FEAT && cap > 0.f) x = softcap_logit(x, cap);
+            float g = (c == y) ? rs.dxy : grad_elem(rs, x, wc);
+            if (FEAT && cap > 0.f) g *= softcap_deriv(x, cap);
+            F::store1(rowp, c, g);
         }
         for (int v0 = threadIdx.x; v0 < nvec; v0 += blockDim.x * UNROLL) {
             uint4 raw[UNROLL];
@@ -422,6 +512,10 @@ __global__ void __launch_bounds__(kRowpassThreads, 2) ce_rowpass_kernel(RowArgs 
                 float x[VEC], g[VEC];
                 F::unpack(raw[u], x);
                 const int vb = v * VEC;
+                if (FEAT && cap > 0.f) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) x[j] = softcap_logit(x[j], cap);
+                }
 #pragma unroll
                 for (int j = 0; j < VEC; ++j) {
                     const float wc = (MODE == 2) ? __ldg(a.weight + head + vb + j) : 1.f;
@@ -431,12 +525,16 @@ __global__ void __launch_bounds__(kRowpassThreads, 2) ce_rowpass_kernel(RowArgs 
 #pragma unroll
                     for (int e = 0; e < VEC; ++e) g[e] = (vb + e == y_rel) ? rs.dxy : g[e];
                 }
+                if (FEAT && cap > 0.f) {
+#pragma unroll
+                    for (int j = 0; j < VEC; ++j) g[j] *= softcap_deriv(x[j], cap);
+                }
                 st_stream(vp + v, F::pack(g));
             }
         }
         __syncthreads();  // sh / sh_rs are reused by the next row
     }
-    if (a.reduction != CE_RED_NONE) finish_loss(a, ctl, gridDim.x);
+    if (a.reduction != CE_RED_NONE || (FEAT && a.accuracy)) finish_loss(a, ctl, gridDim.x);
 }
 
 // ------------------------------------------------------------------ grad_output scaling in place
@@ -470,6 +568,28 @@ __global__ void __launch_bounds__(kRowThreads) ce_scale_kernel(ScaleArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ bounded-wait self-test
+// Waits on an mbarrier that nothing arrives on; the bounded wait gives up
+// after limit_ns and the block reports CE_FLAG_WAIT_TIMEOUT.
+__global__ void ce_wait_selftest_kernel(uint64_t limit_ns, unsigned int *flags) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(&bar), 1);
+        abort_flag = 0;
+        fence_mbar_init_cluster();
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_bounded<false>(smem_u32(&bar), 0u, &abort_flag, limit_ns);
+    __syncthreads();
+    if (threadIdx.x == 0) *flags = (!ok || abort_flag) ? CE_FLAG_WAIT_TIMEOUT : 0u;
+}
+
+cudaError_t launch_wait_selftest(uint64_t limit_ns, unsigned int *flags, cudaStream_t s) {
+    void *args[] = {&limit_ns, &flags};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(&ce_wait_selftest_kernel), dim3(1), dim3(32), args, 0, s);
+}
+
 // ------------------------------------------------------------------ launchers
 // cudaLaunchKernel reports the status of this launch itself (a <<<>>> launch
 // followed by cudaGetLastError could return an earlier, unrelated error).
@@ -492,21 +612,31 @@ static cudaError_t launch(const void *fn, int grid, int block, const Args &a, cu
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
-template <int DT>
+template <int DT, bool FEAT>
 static const void *stats_fn(int mode) {
     switch (mode) {
-    case 0: return reinterpret_cast<const void *>(&ce_stats_kernel<DT, 0>);
-    case 1: return reinterpret_cast<const void *>(&ce_stats_kernel<DT, 1>);
-    default: return reinterpret_cast<const void *>(&ce_stats_kernel<DT, 2>);
+    case 0: return reinterpret_cast<const void *>(&ce_stats_kernel<DT, 0, FEAT>);
+    case 1: return reinterpret_cast<const void *>(&ce_stats_kernel<DT, 1, FEAT>);
+    default: return reinterpret_cast<const void *>(&ce_stats_kernel<DT, 2, FEAT>);
     }
 }
-template <int DT>
+template <int DT, bool FEAT>
 static const void *grad_fn(int mode) {
     switch (mode) {
-    case 0: return reinterpret_cast<const void *>(&ce_grad_kernel<DT, 0>);
-    case 1: return reinterpret_cast<const void *>(&ce_grad_kernel<DT, 1>);
-    default: return reinterpret_cast<const void *>(&ce_grad_kernel<DT, 2>);
+    case 0: return reinterpret_cast<const void *>(&ce_grad_kernel<DT, 0, FEAT>);
+    case 1: return reinterpret_cast<const void *>(&ce_grad_kernel<DT, 1, FEAT>);
+    default: return reinterpret_cast<const void *>(&ce_grad_kernel<DT, 2, FEAT>);
     }
+}
+template <bool FEAT>
+static const void *stats_fn_dt(int dtype, int mode) {
+    return dtype == CE_DT_F32 ? stats_fn<CE_DT_F32, FEAT>(mode)
+         : dtype == CE_DT_BF16 ? stats_fn<CE_DT_BF16, FEAT>(mode) : stats_fn<CE_DT_F16, FEAT>(mode);
+}
+template <bool FEAT>
+static const void *grad_fn_dt(int dtype, int mode) {
+    return dtype == CE_DT_F32 ? grad_fn<CE_DT_F32, FEAT>(mode)
+         : dtype == CE_DT_BF16 ? grad_fn<CE_DT_BF16, FEAT>(mode) : grad_fn<CE_DT_F16, FEAT>(mode);
 }
 
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s) {
@@ -514,29 +644,31 @@ cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s) {
 }
 
 cudaError_t launch_stats(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s) {
-    const void *fn = dtype == CE_DT_F32 ? stats_fn<CE_DT_F32>(mode)
-                   : dtype == CE_DT_BF16 ? stats_fn<CE_DT_BF16>(mode) : stats_fn<CE_DT_F16>(mode);
+    const void *fn = row_features(a) ? stats_fn_dt<true>(dtype, mode) : stats_fn_dt<false>(dtype, mode);
     return launch(fn, grid, kRowThreads, a, s);
 }
 
 cudaError_t launch_grad(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s) {
-    const void *fn = dtype == CE_DT_F32 ? grad_fn<CE_DT_F32>(mode)
-                   : dtype == CE_DT_BF16 ? grad_fn<CE_DT_BF16>(mode) : grad_fn<CE_DT_F16>(mode);
+    const void *fn = row_features(a) ? grad_fn_dt<true>(dtype, mode) : grad_fn_dt<false>(dtype, mode);
     return launch(fn, grid, kRowThreads, a, s);
 }
 
-template <int DT>
+template <int DT, bool FEAT>
 static const void *rowpass_fn(int mode) {
     switch (mode) {
-    case 0: return reinterpret_cast<const void *>(&ce_rowpass_kernel<DT, 0>);
-    case 1: return reinterpret_cast<const void *>(&ce_rowpass_kernel<DT, 1>);
-    default: return reinterpret_cast<const void *>(&ce_rowpass_kernel<DT, 2>);
+    case 0: return reinterpret_cast<const void *>(&ce_rowpass_kernel<DT, 0, FEAT>);
+    case 1: return reinterpret_cast<const void *>(&ce_rowpass_kernel<DT, 1, FEAT>);
+    default: return reinterpret_cast<const void *>(&ce_rowpass_kernel<DT, 2, FEAT>);
     }
+}
+template <bool FEAT>
+static const void *rowpass_fn_dt(int dtype, int mode) {
+    return dtype == CE_DT_F32 ? rowpass_fn<CE_DT_F32, FEAT>(mode)
+         : dtype == CE_DT_BF16 ? rowpass_fn<CE_DT_BF16, FEAT>(mode) : rowpass_fn<CE_DT_F16, FEAT>(mode);
 }
 
 cudaError_t launch_rowpass(const RowArgs &a, int dtype, int mode, int ctas_per_sm, cudaStream_t s) {
-    const void *fn = dtype == CE_DT_F32 ? rowpass_fn<CE_DT_F32>(mode)
-                   : dtype == CE_DT_BF16 ? rowpass_fn<CE_DT_BF16>(mode) : rowpass_fn<CE_DT_F16>(mode);
+    const void *fn = row_features(a) ? rowpass_fn_dt<true>(dtype, mode) : rowpass_fn_dt<false>(dtype, mode);
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;

@@ -1,0 +1,494 @@
+// ce_stream.cu -- streaming forward + backward: each CTA owns whole rows and
+// a producer warp streams every row through a ring of shared-memory chunks
+// twice, with 1-D bulk async copies:
+//   pass 1 (statistics): the row comes from HBM; its lines are marked
+//          evict-last in L2;
+//   pass 2 (gradient):   the same bytes again, now served by L2 (marked
+//          evict-first), while consumer warps write the fp32 gradient,
+//          rounded once, over the logits.
+// The ring is not tied to a row: while the consumers merge a row's
+// statistics, the producer keeps copying (the row's pass-2 chunks and the
+// next row's pass-1 chunks), so the memory system never idles between
+// phases, and the bytes in flight are set by the ring, not by registers.
+// HBM sees one read and one write per element, as the cluster kernel does,
+// without a cluster exchange; the L2 holds about one row per CTA.
+//
+// With a cluster of two CTAs per row, each CTA streams half of the row and
+// the two halves' statistics are exchanged through distributed shared
+// memory (st.shared::cluster + a remote mbarrier arrive), which halves the
+// bytes each CTA keeps waiting in L2 for its second pass.
+//
+// Requires 16-byte aligned row starts (ce_fwd_bwd falls back to the
+// register row-pass kernel otherwise). Every wait is bounded.
+#include "ce_device.cuh"
+#include "ce_kernels.h"
+
+namespace ce {
+
+// Three shapes: 8 consumer warps and a 6-slot ring (two CTAs per SM);
+// 16 consumer warps and a 12-slot ring (one CTA per SM, half the rows
+// waiting in L2 for their second pass); 8 consumer warps and a 4-slot ring
+// (three CTAs per SM, more warps to cover a cluster exchange).
+constexpr int kStreamChunk = 16384;  // bytes per ring slot
+constexpr int kStreamMaxSlots = 12;
+template <int SHAPE> struct StreamShape {
+    static constexpr int kWarps = SHAPE == 1 ? 16 : 8;
+    static constexpr int kThreads = (kWarps + 1) * 32;
+    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : 4);
+    static constexpr int kCtasPerSm = SHAPE == 0 ? 2 : (SHAPE == 1 ? 1 : 3);
+    static constexpr int kSmem = kSlots * kStreamChunk + 1024;
+};
+
+struct StreamXSlot {      // one CTA's partial of one row (32 bytes)
+    float m, s, r, n;
+    float xy, pad0, pad1, pad2;
+};
+
+struct StreamSmem {
+    uint64_t full[kStreamMaxSlots];
+    uint64_t empty[kStreamMaxSlots];
+    uint64_t xbar[2];
+    StreamXSlot slot[2][2];
+    RowState red[16];
+    RowScalars rs;
+    float xy;
+    int abort;
+};
+static_assert(sizeof(StreamSmem) <= 1024, "stream control block too large");
+
+// tuning bits (ce_params.variant >> CE_VARIANT_TUNE_SHIFT)
+constexpr int kTuneWide = 1;       // 16 consumer warps, one CTA per SM
+constexpr int kTuneReverse = 2;    // second pass walks the row's chunks last to first
+constexpr int kTuneNoKeep = 4;     // first pass without the L2 evict-last policy
+constexpr int kTuneCluster2 = 8;   // a cluster of two CTAs per row, each streaming half
+constexpr int kTuneThree = 16;     // three CTAs per SM with a 4-slot ring
+
+template <int NCW>
+__device__ inline void stream_consumer_sync() {
+    asm volatile("bar.sync 1, %0;" :: "n"(NCW * 32) : "memory");
+}
+
+__device__ inline void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
+}
+__device__ inline uint64_t createpolicy_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ inline uint64_t policy_keep() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+template <int DT, int MODE, int SHAPE, int CL>
+__global__ void __launch_bounds__(StreamShape<SHAPE>::kThreads, StreamShape<SHAPE>::kCtasPerSm)
+ce_stream_kernel(RowArgs a, int tune) {
+    using F = Fmt<DT>;
+    using SH = StreamShape<SHAPE>;
+    constexpr int NCW = SH::kWarps;
+    constexpr int VEC = F::kVec;
+    constexpr bool SMOOTH = MODE != 0;
+    constexpr int kStreamConsumerWarps = NCW;
+    constexpr int kStreamSlots = SH::kSlots;
+    constexpr int NCT = NCW * 32;
+    constexpr int VPC = kStreamChunk / 16;          // vectors per full chunk
+    constexpr int VPT = VPC / NCT;                  // vectors per thread per full chunk
+    static_assert(VPC % NCT == 0, "chunk must split evenly over the consumers");
+    static_assert(CL == 1 || CL == 2, "one or two CTAs per row");
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    StreamSmem &S = *reinterpret_cast<StreamSmem *>(smem + kStreamSlots * kStreamChunk);
+    const uint32_t ring = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t V = a.vocab;
+    // this CTA's columns [lo, hi) of every row: all of it, or one half
+    const uint32_t rank = CL == 1 ? 0u : cluster_ctarank();
+    const int64_t q0 = CL == 1 ? blockIdx.x : cluster_id_x();
+    const int64_t nq = CL == 1 ? gridDim.x : nclusters_x();
+    const int64_t half = CL == 1 ? V : ((V + 1) / 2 + VEC - 1) / VEC * VEC;
+    const int64_t lo = rank * half;
+    const int64_t hi = (lo + half < V) ? lo + half : V;
+    const int64_t L = hi > lo ? hi - lo : 0;
+    const int64_t Lb16 = (L * F::kBytes) & ~static_cast<int64_t>(15);  // bytes moved by bulk copies
+    const int nvec = static_cast<int>(Lb16 / 16);
+    const int64_t tail0 = lo + Lb16 / F::kBytes;                       // first column of the scalar tail
+    const int ntail = static_cast<int>(hi - tail0);
+    const int nch = static_cast<int>((Lb16 + kStreamChunk - 1) / kStreamChunk);
+    const size_t row_bytes = static_cast<size_t>(a.ld) * F::kBytes;
+    char *const xbase = reinterpret_cast<char *>(a.grad);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStreamSlots; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 1);
+            mbar_init(smem_u32(&S.empty[s]), kStreamConsumerWarps);
+        }
+        mbar_init(smem_u32(&S.xbar[0]), CL);
+        mbar_init(smem_u32(&S.xbar[1]), CL);
+        S.abort = 0;
+        fence_mbar_init_cluster();
+    }
+    __syncthreads();
+    if (CL > 1) cluster_sync_all();  // the peer's barriers exist before any remote arrive
+    volatile int *abort = &S.abort;
+
+    const bool reverse = (tune & kTuneReverse) != 0;
+    if (warp == kStreamConsumerWarps) {
+        // -------------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t drop = policy_evict_first();
+            const uint64_t keep = (tune & kTuneNoKeep) ? createpolicy_normal() : policy_keep();
+            uint32_t it = 0;
+            for (int64_t row = q0; row < a.n_rows; row += nq) {
+                const int64_t t = load_target(a.target, a.tgt32, row);
+                if (!target_valid(t, a.ignore_index, V)) continue;
+                const char *src = xbase + row * row_bytes + lo * F::kBytes;
+                for (int pass = 0; pass < 2; ++pass) {
+                    const uint64_t pol = pass == 0 ? keep : drop;
+                    for (int k = 0; k < nch; ++k, ++it) {
+                        const int c = (pass == 1 && reverse) ? nch - 1 - k : k;
+                        const uint32_t s = it % kStreamSlots, r = it / kStreamSlots;
+                        if (r > 0) mbar_wait_bounded<false>(smem_u32(&S.empty[s]), (r - 1) & 1u, abort);
+                        const int64_t off = static_cast<int64_t>(c) * kStreamChunk;
+                        const uint32_t bytes = static_cast<uint32_t>(Lb16 - off < kStreamChunk ? Lb16 - off : kStreamChunk);
+                        mbar_expect_tx(smem_u32(&S.full[s]), bytes);
+                        bulk_g2s_hint(ring + s * kStreamChunk, src + off, bytes, smem_u32(&S.full[s]), pol);
+                    }
+                }
+            }
+            // drain: every issued copy has landed before the CTA may exit
+            for (uint32_t k = 0; k < kStreamSlots && k < it; ++k) {
+                const uint32_t i = it - 1 - k;
+                mbar_wait_bounded<false>(smem_u32(&S.full[i % kStreamSlots]), (i / kStreamSlots) & 1u, abort);
+            }
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------------- consumers
+        const float inv_v = 1.f / static_cast<float>(V);
+        const float eps = a.eps;
+        bool have_norm = false;
+        float w_all = 0.f, w_y_sum = 0.f, g_all = 1.f;  // batch constants, read once
+        uint32_t it = 0, j = 0;  // ring position; valid rows done (exchange parity)
+        for (int64_t row = q0; row < a.n_rows; row += nq) {
+            const int64_t t = load_target(a.target, a.tgt32, row);
+            const bool valid = target_valid(t, a.ignore_index, V);
+            char *rowp = xbase + row * row_bytes;
+            uint4 *vp = reinterpret_cast<uint4 *>(rowp + lo * F::kBytes);
+            if (!valid) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                for (int v = tid; v < nvec; v += NCT) st_stream(vp + v, z);
+                if (tid < ntail) F::store1(rowp, tail0 + tid, 0.f);
+                if (tid == 0 && rank == 0) {
+                    if (a.reduction == CE_RED_NONE) a.loss[row] = 0.f;
+                    else a.row_loss[row] = 0.f;
+                }
+                continue;
+            }
+            const int yg = static_cast<int>(t);                 // target column in the row
+            const int y = (t >= lo && t < hi) ? static_cast<int>(t - lo) : -(1 << 30);  // in this slice
+            // per-row values the merge needs, fetched now so their latency hides under pass 1
+            const float g_row = (a.grad_output && a.reduction == CE_RED_NONE) ? __ldg(a.grad_output + row) : 0.f;
+            const float wy = a.weight ? __ldg(a.weight + yg) : 1.f;
+            // ------------------------------------------------ pass 1: statistics
+            RowState st = row_state_empty();
+            for (int c = 0; c < nch; ++c, ++it) {
+                const uint32_t s = it % kStreamSlots;
+                mbar_wait_bounded<false>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
+                const uint32_t base_s = ring + s * kStreamChunk;
+                const int v0 = c * VPC;
+                const int nv = min(VPC, nvec - v0);
+                // does one of this thread's vectors hold the target column?
+                const unsigned q = static_cast<unsigned>(y / VEC - v0 - tid);
+                const bool mine = q < static_cast<unsigned>(VPT * NCT) && (q % NCT) == 0;
+                if (nv == VPC && !mine && MODE != 2) {
+                    // full chunk, no target: one max per chunk, four independent sums
+                    uint4 raw[VPT];
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k) raw[k] = ld_shared_v4(base_s + 16u * (tid + k * NCT));
+                    float cm = F::vmax(raw[0]);
+#pragma unroll
+                    for (int k = 1; k < VPT; ++k) cm = fmaxf(cm, F::vmax(raw[k]));
+                    if (cm > st.m) {
+                        if (st.m != -INFINITY) st.s *= ex2_hw((st.m - cm) * kLog2e);
+                        st.m = cm;
+                    }
+                    if (st.m != -INFINITY) {
+                        const float mL = st.m * kLog2e;
+                        float acc[4] = {0.f, 0.f, 0.f, 0.f}, racc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) {
+                            float x[VEC];
+                            F::unpack(raw[k], x);
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) {
+                                acc[j & 3] += ex2_hw(fmaf(x[j], kLog2e, -mL));
+                                if (SMOOTH) racc[j & 3] += x[j];
+                            }
+                        }
+                        st.s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                        if (SMOOTH) {
+                            st.r += (racc[0] + racc[1]) + (racc[2] + racc[3]);
+                            st.n += static_cast<float>(VPT * VEC);
+                        }
+                    } else if (SMOOTH) {
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) {
+                            float x[VEC];
+                            F::unpack(raw[k], x);
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) st.r += x[j];
+                        }
+                        st.n += static_cast<float>(VPT * VEC);
+                    }
+                } else {
+                    for (int v = tid; v < nv; v += NCT) {
+                        const uint4 raw = ld_shared_v4(base_s + 16u * v);
+                        const int vb = (v0 + v) * VEC;
+                        float x[VEC];
+                        F::unpack(raw, x);
+                        const int skip = (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) ? y - vb : -1;
+                        if (skip >= 0) {
+                            float xv = 0.f;
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) xv = (j == skip) ? x[j] : xv;
+                            S.xy = xv;  // the target logit, for the merge
+                        }
+                        float w[VEC];
+                        if (MODE == 2) {
+                            const float4 *wp = reinterpret_cast<const float4 *>(a.weight + lo + vb);
+#pragma unroll
+                            for (int h = 0; h < VEC / 4; ++h) {
+                                const float4 w4 = __ldg(wp + h);
+                                w[4 * h] = w4.x; w[4 * h + 1] = w4.y; w[4 * h + 2] = w4.z; w[4 * h + 3] = w4.w;
+                            }
+                        }
+                        row_state_add<VEC, SMOOTH>(st, x, F::vmax(raw), skip, MODE == 2 ? w : nullptr);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
+            }
+            if (tid < ntail) {
+                const int64_t c = tail0 + tid;
+                float x = F::load1(rowp, c);
+                float w = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
+                if (c == yg) S.xy = x;
+                row_state_add<1, SMOOTH>(st, &x, x, (c == yg) ? 0 : -1, MODE == 2 ? &w : nullptr);
+            }
+            // ------------------------------------------------ merge and row scalars
+            st = warp_merge(st);
+            if (lane == 0) S.red[warp] = st;
+            stream_consumer_sync<NCW>();
+            if (warp == 0) {
+                RowState m = lane < kStreamConsumerWarps ? S.red[lane] : row_state_empty();
+                m = warp_merge(m);
+                float xy_mine = 0.f;
+                if (lane == 0) xy_mine = S.xy;
+                if (CL > 1 && lane == 0) {
+                    // push this half's partial into both CTAs, then merge both in rank order
+                    const uint32_t par = j & 1u;
+                    const uint32_t my_slot = smem_u32(&S.slot[par][rank]);
+                    const uint32_t my_bar = smem_u32(&S.xbar[par]);
+                    for (uint32_t d = 0; d < static_cast<uint32_t>(CL); ++d) {
+                        const uint32_t rs_addr = mapa_shared(my_slot, d);
+                        st_cluster_v4(rs_addr, m.m, m.s, m.r, m.n);
+                        st_cluster_v4(rs_addr + 16u, xy_mine, 0.f, 0.f, 0.f);
+                        mbar_arrive_remote(mapa_shared(my_bar, d));
+                    }
+                    mbar_wait_bounded<true>(my_bar, (j >> 1) & 1u, abort);
+                    RowState tot = row_state_empty();
+                    for (int d = 0; d < CL; ++d) {
+                        const StreamXSlot &xs = S.slot[par][d];
+                        tot = row_state_merge(tot, RowState{xs.m, xs.s, xs.r, xs.n});
+                    }
+                    m = tot;
+                    xy_mine = S.slot[par][yg >= half ? 1 : 0].xy;
+                }
+                if (lane == 0) {
+                    if (!have_norm) {
+                        pdl_wait();
+                        w_all = a.ctl->w_all;
+                        w_y_sum = a.ctl->w_y;
+                        g_all = a.grad_output ? __ldg(a.grad_output) : 1.f;
+                        have_norm = true;
+                    }
+                    const float xy = xy_mine;
+                    const float rrel = SMOOTH ? row_state_rel_sum(m) : 0.f;
+                    const float g = a.reduction == CE_RED_NONE ? (a.grad_output ? g_row : 1.f) : g_all;
+                    float scale = g;
+                    if (a.reduction == CE_RED_MEAN) scale = w_y_sum != 0.f ? g / w_y_sum : 0.f;
+                    if (rank == 0) {
+                        const RowScalars rl = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f);
+                        if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
+                        else a.row_loss[row] = rl.loss;
+                    }
+                    S.rs = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, scale);
+                }
+            }
+            stream_consumer_sync<NCW>();
+            const RowScalars rs = S.rs;
+            // ------------------------------------------------ pass 2: gradient in place
+            for (int k = 0; k < nch; ++k, ++it) {
+                const int c = reverse ? nch - 1 - k : k;
+                const uint32_t s = it % kStreamSlots;
+                mbar_wait_bounded<false>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
+                const uint32_t base_s = ring + s * kStreamChunk;
+                const int v0 = c * VPC;
+                const int nv = min(VPC, nvec - v0);
+                for (int v = tid; v < nv; v += NCT) {
+                    float x[VEC], gr[VEC];
+                    F::unpack(ld_shared_v4(base_s + 16u * v), x);
+                    const int vb = (v0 + v) * VEC;
+                    if (MODE == 2) {
+                        const float4 *wp = reinterpret_cast<const float4 *>(a.weight + lo + vb);
+#pragma unroll
+                        for (int h = 0; h < VEC / 4; ++h) {
+                            const float4 w4 = __ldg(wp + h);
+                            gr[4 * h] = grad_elem(rs, x[4 * h], w4.x);
+                            gr[4 * h + 1] = grad_elem(rs, x[4 * h + 1], w4.y);
+                            gr[4 * h + 2] = grad_elem(rs, x[4 * h + 2], w4.z);
+                            gr[4 * h + 3] = grad_elem(rs, x[4 * h + 3], w4.w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) gr[e] = grad_elem(rs, x[e], 1.f);
+                    }
+                    if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
+                    }
+                    st_stream(vp + v0 + v, F::pack(gr));  // vp points at this CTA's slice
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
+            }
+            if (tid < ntail) {
+                const int64_t c = tail0 + tid;
+                const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
+                F::store1(rowp, c, (c == yg) ? rs.dxy : grad_elem(rs, F::load1(rowp, c), wc));
+            }
+            ++j;
+        }
+        // ---------------------------------------------------- batch reduction (last CTA)
+        if (a.reduction != CE_RED_NONE) {
+            __shared__ unsigned sh_last;
+            __shared__ double sh_sum[kStreamConsumerWarps];
+            if (!have_norm) pdl_wait();
+            stream_consumer_sync<NCW>();
+            if (tid == 0) {
+                __threadfence();
+                const unsigned prev = atomicAdd(&a.ctl->done, 1u);
+                sh_last = (prev == gridDim.x - 1) ? 1u : 0u;
+            }
+            stream_consumer_sync<NCW>();
+            if (sh_last) {
+                __threadfence();
+                double sum = 0.0;
+                for (int64_t i = tid; i < a.n_rows; i += NCT) sum += static_cast<double>(__ldcg(a.row_loss + i));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                if (lane == 0) sh_sum[warp] = sum;
+                stream_consumer_sync<NCW>();
+                if (tid == 0) {
+                    double tot = 0.0;
+                    for (int k = 0; k < kStreamConsumerWarps; ++k) tot += sh_sum[k];
+                    if (a.reduction == CE_RED_MEAN) {
+                        const float wys = a.ctl->w_y;  // after the normaliser kernel (waited above)
+                        tot = wys != 0.f ? tot / static_cast<double>(wys) : 0.0;
+                    }
+                    a.loss[0] = static_cast<float>(tot);
+                    a.ctl->done = 0u;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && S.abort) {
+        pdl_wait();
+        atomicOr(&a.ctl->status, CE_FLAG_WAIT_TIMEOUT);
+    }
+    if (CL > 1) cluster_sync_all();  // no CTA leaves while its peer may still write into it
+}
+
+template <int DT, int SHAPE, int CL>
+static const void *stream_fn(int mode) {
+    switch (mode) {
+    case 0: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 0, SHAPE, CL>);
+    case 1: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 1, SHAPE, CL>);
+    default: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 2, SHAPE, CL>);
+    }
+}
+
+template <int SHAPE, int CL>
+static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, int ctas_per_sm, int tune,
+                                       bool after_prep, cudaStream_t s) {
+    using SH = StreamShape<SHAPE>;
+    RowArgs a = a0;
+    const void *fn = dtype == CE_DT_F32 ? stream_fn<CE_DT_F32, SHAPE, CL>(mode)
+                   : dtype == CE_DT_BF16 ? stream_fn<CE_DT_BF16, SHAPE, CL>(mode) : stream_fn<CE_DT_F16, SHAPE, CL>(mode);
+    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SH::kSmem);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    int64_t grid = static_cast<int64_t>(sms) * (ctas_per_sm > 0 ? ctas_per_sm : SH::kCtasPerSm);
+    if (grid > a.n_rows * CL) grid = a.n_rows * CL;
+    grid = grid / CL * CL;
+    if (grid < CL) grid = CL;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(SH::kThreads);
+    cfg.dynamicSmemBytes = SH::kSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (CL > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = CL;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    if (after_prep) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n;
+    void *args[] = {&a, &tune};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm, int tune, bool after_prep,
+                          cudaStream_t s) {
+    // Library choice by row size (GB300 measurements, CUDA events, L2 flushed):
+    //  rows <= 96 KB: three CTAs per SM, one CTA per row (4096 x 32000 bf16:
+    //    0.107 ms vs 0.121 ms with two CTAs per SM);
+    //  rows <= 384 KB: three CTAs per SM, a pair of CTAs per row, so the
+    //    second pass is served by L2 without misses (8192 x 128256 bf16:
+    //    0.759 ms vs 0.775 ms unpaired, vs 0.827 ms paired at two per SM);
+    //  larger rows: the same, second pass last chunk first (16384 x 256000
+    //    bf16: 5.25 ms per step vs 5.81 ms with one wide CTA per SM).
+    if (tune == 0) {
+        const int64_t row_bytes = a.vocab * (dtype == CE_DT_F32 ? 4 : 2);
+        tune = row_bytes <= 96 * 1024 ? kTuneThree
+             : row_bytes <= 384 * 1024 ? (kTuneThree | kTuneCluster2)
+                                      : (kTuneThree | kTuneCluster2 | kTuneReverse);
+    }
+    const bool pair = (tune & kTuneCluster2) && a.vocab >= 2 * (dtype == CE_DT_F32 ? 4 : 8);
+    if (tune & kTuneWide)
+        return pair ? launch_stream_shape<1, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+                    : launch_stream_shape<1, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
+    if (tune & kTuneThree)
+        return pair ? launch_stream_shape<2, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+                    : launch_stream_shape<2, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
+    return pair ? launch_stream_shape<0, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+                : launch_stream_shape<0, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
+}
+
+}  // namespace ce

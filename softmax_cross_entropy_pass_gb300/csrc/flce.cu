@@ -403,6 +403,7 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
     if (!(p->label_smoothing >= 0.f && p->label_smoothing <= 1.f) || p->reserved != 0) return CE_ERR_INVALID_ARG;
     if (p->target_is_int32 != 0 && p->target_is_int32 != 1) return CE_ERR_INVALID_ARG;
     if (p->class_weight && (reinterpret_cast<uintptr_t>(p->class_weight) & 15u)) return CE_ERR_INVALID_ARG;
+    if (p->softcap != 0.f || p->z_loss != 0.f || p->accuracy) return CE_ERR_UNSUPPORTED;
     if (!loss || !ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CE_ERR_INVALID_ARG;
     const int64_t BT = p->n_rows, V = p->vocab;
     if (BT > INT32_MAX || V > INT32_MAX || H > INT32_MAX) return CE_ERR_UNSUPPORTED;

@@ -39,9 +39,15 @@ def rne(v64: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:
 
 
 def magnitude_T(x: torch.Tensor, target: torch.Tensor, stats64: torch.Tensor, weight, eps: float,
-                w_all: float, scale: torch.Tensor) -> torch.Tensor:
-    """|s_i| * T_ic for every element, in fp64 (rows not valid: 0)."""
+                w_all: float, scale: torch.Tensor, softcap: float = 0.0, z_loss: float = 0.0) -> torch.Tensor:
+    """|s_i| * T_ic for every element, in fp64 (rows not valid: 0). With a
+    softcap the terms are those of the capped logits times dz/dx; z-loss adds
+    its |2 lambda LSE p| term."""
     xd = x.double()
+    deriv = None
+    if softcap > 0:
+        xd = softcap * torch.tanh(xd / softcap)
+        deriv = 1.0 - (xd / softcap) ** 2
     R, V = xd.shape
     m, s, xy = stats64[:, 0:1], stats64[:, 1:2], stats64[:, 2:3]
     lse = m + torch.log(s + torch.exp(xy - m))
@@ -53,6 +59,10 @@ def magnitude_T(x: torch.Tensor, target: torch.Tensor, stats64: torch.Tensor, we
     onehot = torch.zeros(R, V, dtype=torch.float64)
     onehot[torch.arange(R), tt] = 1.0
     T = (1 - eps) * wy * (p + onehot) + (eps / V) * (p * w_all + w[None, :])
+    if z_loss > 0:
+        T = T + (2 * z_loss * lse).abs() * p
+    if deriv is not None:
+        T = T * deriv
     T = T * scale.abs().reshape(-1, 1).double()
     T[~valid] = 0.0
     return T

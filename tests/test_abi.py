@@ -55,8 +55,9 @@ def test_version_and_status_strings(lib):
 
 def test_params_layout(lib):
     P = lib.ce_params
-    assert ctypes.sizeof(P) == 64
+    assert ctypes.sizeof(P) == 80
     assert P.class_weight.offset == 32 and P.label_smoothing.offset == 40 and P.reserved.offset == 60
+    assert P.softcap.offset == 64 and P.z_loss.offset == 68 and P.accuracy.offset == 72
 
 
 def _params(lib, **kw):
@@ -65,12 +66,13 @@ def _params(lib, **kw):
     p.label_smoothing = kw.get("eps", 0.0)
     p.dtype, p.reduction = kw.get("dtype", 1), kw.get("reduction", 1)
     p.variant, p.reserved = kw.get("variant", 0), kw.get("reserved", 0)
+    p.softcap, p.z_loss = kw.get("softcap", 0.0), kw.get("z_loss", 0.0)
     return p
 
 
 @pytest.mark.parametrize("bad", [dict(vocab=0), dict(ld=5), dict(n_rows=-1), dict(eps=1.5),
                                  dict(eps=float("nan")), dict(dtype=7), dict(reduction=9),
-                                 dict(reserved=1)])
+                                 dict(reserved=1), dict(softcap=-1.0), dict(z_loss=float("inf"))])
 def test_invalid_params_rejected_on_host(lib, bad):
     p = _params(lib, **bad)
     fake = ctypes.c_void_p(0x1000)
@@ -96,3 +98,22 @@ def test_workspace_is_o_rows_and_far_below_one_logits_tensor(lib):
     assert ws <= 20 * 8192 + 512
     assert ws / 2 ** 20 < 0.001 * mb
     assert lib.ce_workspace_size(16384) - lib.ce_workspace_size(8192) == 20 * 8192
+
+
+def test_automatic_path_choice_is_host_logic(lib):
+    """ce_select_variant (no GPU work): 16-byte aligned rows take the stream
+    kernel, other row layouts the register row-pass kernel; explicit
+    variants are returned as asked."""
+    out = ctypes.c_int32()
+    p = _params(lib, n_rows=4, vocab=128256, ld=128256)
+    assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
+    assert out.value == lib.VARIANTS["stream"]
+    p = _params(lib, n_rows=4, vocab=1001, ld=1001)   # 2002-byte rows: not 16-byte aligned
+    assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
+    assert out.value == lib.VARIANTS["rowpass"]
+    p = _params(lib, n_rows=4, vocab=128256, ld=128256)
+    assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10008), ctypes.byref(out)) == 0
+    assert out.value == lib.VARIANTS["rowpass"]
+    p = _params(lib, variant=lib.VARIANTS["split"])
+    assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
+    assert out.value == lib.VARIANTS["split"]

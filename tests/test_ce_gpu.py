@@ -32,14 +32,15 @@ def _oracle(x, t, w, eps, red, g):
                      reduction=red, grad_output=None if g is None else g.cpu())
 
 
-def _check_all(got_x, t, w, eps, red, g, ref, got_loss, x_in):
+def _check_all(got_x, t, w, eps, red, g, ref, got_loss, x_in, softcap=0.0, z_loss=0.0):
     R, V = got_x.shape
     if red == "none":
         check_loss_rows(got_loss.cpu(), ref["row_loss"])
     else:
         check_loss_reduced(float(got_loss.cpu()[0]), ref["loss"])
     scale = row_scale(red, g, R, ref["norm_wy"])
-    T = magnitude_T(x_in, t.cpu(), ref["stats"], None if w is None else w.cpu(), eps, ref["w_all"], scale)
+    T = magnitude_T(x_in, t.cpu(), ref["stats"], None if w is None else w.cpu(), eps, ref["w_all"], scale,
+                    softcap, z_loss)
     bad, n_floor, worst = grad_mismatch(got_x.cpu(), ref["grad"], T)
     assert bad == 0, f"{bad} gradient elements outside tolerance (worst {worst:.2f} ulp, floor used {n_floor})"
     # dx_y of every valid row
@@ -68,7 +69,7 @@ SMALL = [
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: f"{s[0]}x{s[1]}+{s[2]}")
 @pytest.mark.parametrize("opt", ["plain", "smooth", "weighted_smooth"])
 @pytest.mark.parametrize("red", ["mean", "sum", "none"])
-@pytest.mark.parametrize("api", ["fused", "split", "rowpass", "fwd+bwd calls"])
+@pytest.mark.parametrize("api", ["fused", "split", "rowpass", "stream", "stream-pair", "fwd+bwd calls"])
 def test_parity_small(ce, dtype, shape, opt, red, api):
     R, V, extra = shape
     dev = torch.device("cuda")
@@ -93,18 +94,18 @@ def test_parity_small(ce, dtype, shape, opt, red, api):
         assert torch.equal(st[valid, 2], ref["stats"][valid, 2].float().double())  # x_y is exact
         assert torch.allclose(st[:, 1], ref["stats"][:, 1], rtol=2e-5, atol=0)
     else:
-        variant = api
+        variant, tune = (api, 0) if api != "stream-pair" else ("stream", 8)
         ld = x.stride(0) if R > 1 else V
         fusable = x.data_ptr() % 16 == 0 and (R == 1 or (ld * x.element_size()) % 16 == 0)
-        if variant == "fused" and not fusable:
+        if variant in ("fused", "stream") and not fusable:
             with pytest.raises(ce.CEError):
                 ce.ce_fwd_bwd(x, t, grad_output=g, weight=w, label_smoothing=eps, reduction=red,
-                              variant="fused")
+                              variant=variant)
             return
         if variant == "fused" and ce.ce_fused_plan(R, V, DT[dtype]) is None:
             pytest.skip("fused kernel does not take this shape")
         loss = ce.ce_fwd_bwd(x, t, grad_output=g, weight=w, label_smoothing=eps, reduction=red,
-                             variant=variant)
+                             variant=variant, tune=tune)
         torch.cuda.synchronize()
     _check_all(x, t, w, eps, red, g, ref, loss, x_in)
     if extra:
@@ -309,8 +310,9 @@ def _full_size_check(ce, cfg, variant, sample_rows=48, check_dxy_thirds=False):
     n, wy, wall, _ = oracle.normalizers(t_host, V, IGNORE_INDEX, w_host)
     full = oracle.rows(x_host, t_host, weight=w_host, label_smoothing=cfg.label_smoothing,
                        reduction=cfg.reduction, norm_wy=wy, w_all=wall, want_grad=False)
+    variant, tune = (variant, 0) if variant != "stream-pair" else ("stream", 8)
     loss = ce.ce_fwd_bwd(x, t, weight=w, label_smoothing=cfg.label_smoothing, reduction=cfg.reduction,
-                         grad_output=g, variant=variant)
+                         grad_output=g, variant=variant, tune=tune)
     torch.cuda.synchronize()
     if cfg.reduction == "none":
         check_loss_rows(loss.cpu(), full["row_loss"])
@@ -342,7 +344,7 @@ def _full_size_check(ce, cfg, variant, sample_rows=48, check_dxy_thirds=False):
     return out
 
 
-@pytest.mark.parametrize("variant", ["fused", "split", "rowpass"])
+@pytest.mark.parametrize("variant", ["fused", "split", "rowpass", "stream"])
 def test_confident_full_size_dxy(ce, variant):
     """4096 x 32000 bf16, softmax(x_y) near 0.9 / 0.99 / 0.999: dx_y within
     0.4% of the oracle in every third (the #1329 accuracy table's workload)."""
@@ -362,7 +364,7 @@ def test_confident_full_size_dxy(ce, variant):
         assert rel[sel].max() <= DXY_RTOL, f"third {k}: dx_y max rel err {float(rel[sel].max()):.4%}"
 
 
-@pytest.mark.parametrize("variant", ["fused", "split", "rowpass"])
+@pytest.mark.parametrize("variant", ["fused", "split", "rowpass", "stream", "stream-pair"])
 def test_headline_full_size(ce, variant):
     _full_size_check(ce, CONFIGS["headline"], variant)
 
@@ -381,3 +383,96 @@ def test_tiny_config(ce):
     loss = ce.ce_fwd_bwd(x, t)
     torch.cuda.synchronize()
     _check_all(x, t, None, 0.0, "mean", None, ref, loss, x_in)
+
+
+@pytest.mark.parametrize("tune", [0, 1, 2, 3, 4, 8, 9, 10, 12, 15, 16, 24, 26])
+@pytest.mark.parametrize("shape", [(70, 128256), (33, 33008), (9, 256000), (5, 1000)])
+def test_stream_tuning_variants(ce, tune, shape):
+    """Every stream-kernel tuning combination (wide CTA, reversed second
+    pass, no L2 evict-last) against the oracle."""
+    R, V = shape
+    x = make_logits(R, V, "bf16", 1.5, 300 + tune, device="cuda")
+    t = make_targets(R, V, 0.1, 300 + tune, device="cuda")
+    w = make_weights(V, 300 + tune, device="cuda") if tune % 2 else None
+    x_in = x.cpu()
+    g = torch.tensor([0.37], device="cuda")
+    ref = _oracle(x, t, w, 0.05, "sum", g)
+    loss = ce.ce_fwd_bwd(x, t, weight=w, label_smoothing=0.05, reduction="sum", grad_output=g,
+                         variant="stream", tune=tune)
+    torch.cuda.synchronize()
+    _check_all(x, t, w, 0.05, "sum", g, ref, loss, x_in)
+
+
+def test_bounded_wait_gives_up_with_status_and_context_survives(ce):
+    """A device wait that nothing satisfies ends after its limit with
+    CE_FLAG_WAIT_TIMEOUT, and the context keeps working."""
+    t0 = time.perf_counter()
+    flags = ce.ce_selftest_wait_timeout(100_000_000)
+    elapsed = time.perf_counter() - t0
+    assert flags & ce.CE_FLAG_WAIT_TIMEOUT
+    assert 0.09 <= elapsed < 5.0
+    x = make_logits(8, 512, "bf16", 1.0, 1, device="cuda")
+    t = make_targets(8, 512, 0.0, 1, device="cuda")
+    ws = ce.workspace(8)
+    ce.ce_fwd_bwd(x, t, ws=ws)
+    assert ce.ce_get_status(ws) == 0
+
+
+@pytest.mark.parametrize("api", ["auto", "split", "fwd+bwd calls"])
+@pytest.mark.parametrize("dtype", ["bf16", "f32"])
+@pytest.mark.parametrize("red", ["mean", "sum", "none"])
+@pytest.mark.parametrize("opts", [(15.0, 0.0), (0.0, 1e-4), (30.0, 1e-4)], ids=["softcap", "zloss", "both"])
+@pytest.mark.parametrize("shape", [(17, 1000), (9, 33000), (5, 7), (6, 1001)], ids=lambda s: f"{s[0]}x{s[1]}")
+def test_softcap_zloss_accuracy(ce, api, dtype, red, opts, shape):
+    """Softcap, z-loss and token accuracy against the oracle (the row-pass
+    and split kernels carry the options)."""
+    R, V = shape
+    cap, zl = opts
+    seed = zlib.crc32(repr((R, V, dtype, red, opts)).encode()) % 9973
+    x = make_logits(R, V, dtype, 6.0, seed, device="cuda")   # wide logits: the cap bites
+    t = make_targets(R, V, 0.2, seed, device="cuda")
+    t[0] = int(torch.argmax(x[0].float()))                    # at least one correct row
+    w = make_weights(V, seed, device="cuda") if red == "sum" else None
+    g = (torch.rand(R, generator=torch.Generator().manual_seed(seed)).to("cuda") if red == "none"
+         else torch.tensor([0.37], device="cuda"))
+    x_in = x.cpu()
+    ref = oracle.ce(x_in, t.cpu(), weight=None if w is None else w.cpu(), label_smoothing=0.1, reduction=red,
+                    grad_output=g.cpu(), softcap=cap, z_loss=zl)
+    acc = torch.zeros(1, device="cuda")
+    if api == "fwd+bwd calls":
+        loss, stats = ce.ce_forward(x, t, weight=w, label_smoothing=0.1, reduction=red, softcap=cap, z_loss=zl,
+                                    accuracy=acc)
+        ce.ce_backward(x, t, stats, grad_output=g, weight=w, label_smoothing=0.1, reduction=red, softcap=cap,
+                       z_loss=zl)
+    else:
+        loss = ce.ce_fwd_bwd(x, t, grad_output=g, weight=w, label_smoothing=0.1, reduction=red,
+                             variant=api, softcap=cap, z_loss=zl, accuracy=acc)
+    torch.cuda.synchronize()
+    _check_all(x, t, w, 0.1, red, g, ref, loss, x_in, softcap=cap, z_loss=zl)
+    assert float(acc.item()) == pytest.approx(ref["accuracy"], abs=1e-7)
+
+
+def test_options_refused_where_not_implemented(ce):
+    x = make_logits(4, 1024, "bf16", 1.0, 1, device="cuda")
+    t = make_targets(4, 1024, 0.0, 1, device="cuda")
+    for variant in ("fused", "stream"):
+        with pytest.raises(ce.CEError, match="UNSUPPORTED"):
+            ce.ce_fwd_bwd(x, t, variant=variant, softcap=10.0)
+
+
+@pytest.mark.parametrize("variant", ["auto", "fused", "split", "rowpass", "stream", "stream-pair"])
+@pytest.mark.parametrize("V", [1000, 33000, 128256])
+def test_nothing_written_past_the_buffer(ce, variant, V):
+    """The logits sit at the start of a larger allocation whose tail holds a
+    canary pattern; after the call the canary is intact (no write past
+    n_rows x ld)."""
+    R = 7
+    canary_len = 1 << 16
+    base = make_logits(1, R * V + canary_len, "bf16", 1.0, 55, device="cuda").reshape(-1)
+    base[R * V:] = 123.0
+    x = base[:R * V].view(R, V)
+    t = make_targets(R, V, 0.0, 55, device="cuda")
+    var, tune = (variant, 0) if variant != "stream-pair" else ("stream", 8)
+    ce.ce_fwd_bwd(x, t, label_smoothing=0.1, variant=var, tune=tune)
+    torch.cuda.synchronize()
+    assert torch.all(base[R * V:] == 123.0)
