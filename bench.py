@@ -35,8 +35,8 @@ sys.path.insert(0, ROOT)
 WORKLOAD = "headline"
 METRIC = "CE fwd+bwd tokens/s at BT=8192 V=128256 bf16; achieved HBM GB/s vs peak"
 FALLBACK_HBM_GBS = 6800.0
-TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ce_fused_headline_traffic.json")
-KERNEL_SOURCES = ["softmax_cross_entropy_pass_gb300/csrc/ce_fused.cu",
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ce_stream_kernel_headline_traffic.json")
+KERNEL_SOURCES = ["softmax_cross_entropy_pass_gb300/csrc/ce_stream.cu",
                   "softmax_cross_entropy_pass_gb300/csrc/ce_device.cuh"]
 
 
@@ -66,9 +66,12 @@ def read_bf16_peak():
         return 1900.0
 
 
-def read_traffic():
-    """ncu DRAM bytes per launch of the fused kernel, if captured on the
-    current kernel source (else None)."""
+def read_traffic(path: str, workload: str):
+    """ncu DRAM bytes (read + write) per launch of the stream kernel on the
+    headline workload, when the capture was taken on the current kernel
+    source (else None)."""
+    if path != "stream" or workload != WORKLOAD:
+        return None
     try:
         with open(TRAFFIC_FILE) as f:
             d = json.load(f)
@@ -76,7 +79,7 @@ def read_traffic():
         return None
     if d.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return float(d["dram_bytes_per_launch_full_size"])
+    return float(d["dram_bytes_per_launch"])
 
 
 class ClockSampler:
@@ -454,7 +457,7 @@ def run_ours(args):
 
     peak, peak_kind = read_peaks()
     achieved = algo_bytes / kernel_avg_s / 1e9
-    traffic = read_traffic()
+    traffic = read_traffic(path, cfg.name)
 
     flce = None
     if not args.no_flce:
@@ -532,7 +535,11 @@ def main():
     ap.add_argument("--rows", type=int, default=0, help="rows of a smaller case of the workload (profiling)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="CE workload of workloads.CONFIGS (the default is the headline metric's)")
+    ap.add_argument("--print-kernel-hash", action="store_true")
     args = ap.parse_args()
+    if args.print_kernel_hash:
+        print(kernel_source_hash())
+        return 0
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
     if args.impl == "reference":
