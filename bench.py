@@ -272,16 +272,22 @@ def measure_flce(ce, device, steps: int, chunk_rows: int):
     gw = torch.empty(V, H, dtype=torch.float32, device=device)
     ws = torch.empty(ce.flce_workspace_size(BT, H, V, chunk_rows), dtype=torch.uint8, device=device)
     kw = dict(reduction="mean", chunk_rows=chunk_rows, loss=loss, grad_hidden=gh, grad_weight=gw, ws=ws)
-    for _ in range(2):
-        ce.flce_fwd_bwd(h, W, t, **kw)
-    torch.cuda.synchronize()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
-    for a, b in ev:
-        a.record()
-        ce.flce_fwd_bwd(h, W, t, **kw)
-        b.record()
-    torch.cuda.synchronize()
-    step_ms = sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    def timed(dense):
+        for _ in range(2):
+            ce.flce_fwd_bwd(h, W, t, dense=dense, **kw)
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for a, b in ev:
+            a.record()
+            ce.flce_fwd_bwd(h, W, t, dense=dense, **kw)
+            b.record()
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+    step_ms = timed(False)          # the default: ignored rows compacted away on the device
+    dense_ms = timed(True)          # every row through every GEMM
+    n_valid = int(((t >= 0) & (t < V)).sum().item())
     flop = 3 * 2.0 * BT * V * H
     # the three GEMMs of one chunk, each timed alone
     c = min(chunk_rows, BT)
@@ -311,7 +317,10 @@ def measure_flce(ce, device, steps: int, chunk_rows: int):
     return {"workload": f"flce: hidden [{BT}, {H}] bf16 N(0,1), weight [{V}, {H}] bf16 N(0, 0.02^2), "
                         f"5% ignore_index, mean, chunk_rows={chunk_rows}",
             "ms_per_step": step_ms, "tokens_per_s": BT / (step_ms / 1e3),
-            "gemm_tflops_whole_step": flop / step_ms / 1e9, "gemm_chunk": per}
+            "gemm_tflops_whole_step": flop / step_ms / 1e9,
+            "valid_rows": n_valid, "gemm_tflops_executed": 3 * 2.0 * n_valid * V * H / step_ms / 1e9,
+            "ms_per_step_dense": dense_ms, "gemm_tflops_dense": flop / dense_ms / 1e9,
+            "gemm_chunk": per}
 
 
 def measure_gemm(ce, device, spec: str, steps: int, warmup: int):
@@ -357,6 +366,8 @@ def run_ours(args):
         peak_tf = read_bf16_peak()
         flce["peak_tflops"] = peak_tf
         flce["frac_whole_step"] = flce["gemm_tflops_whole_step"] / peak_tf
+        flce["frac_executed"] = flce["gemm_tflops_executed"] / peak_tf
+        flce["frac_dense"] = flce["gemm_tflops_dense"] / peak_tf
         print(json.dumps({"flce": flce}), flush=True)
         return 0
     if world > 1:
@@ -466,6 +477,8 @@ def run_ours(args):
         peak_tf = read_bf16_peak()
         flce["peak_tflops"] = peak_tf
         flce["frac_whole_step"] = flce["gemm_tflops_whole_step"] / peak_tf
+        flce["frac_executed"] = flce["gemm_tflops_executed"] / peak_tf
+        flce["frac_dense"] = flce["gemm_tflops_dense"] / peak_tf
         for v in flce["gemm_chunk"].values():
             v["frac"] = v["tflops"] / peak_tf
 

@@ -298,15 +298,22 @@ ce_status ce_gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t l
                        const void *B, int64_t ldb, int32_t b_mn_major, int32_t out_kind, void *D,
                        int64_t ldd, const float *bias, void *stream);
 
+/* ce_params.variant of flce_fwd_bwd: 0 compacts the valid rows first (the
+ * default), CE_FLCE_DENSE runs every row through every GEMM. */
+#define CE_FLCE_DENSE 1
+
 /* Workspace bytes of flce_fwd_bwd for these sizes (the fp32 logits chunk,
- * the bf16 logits-gradient chunk and the cross-entropy workspace). */
+ * the bf16 logits-gradient chunk and the cross-entropy workspace; with
+ * compaction also a compacted copy of hidden, BT x H bf16, and 24 bytes per
+ * row of maps, targets and grad_output). */
 ce_status flce_workspace_size(const ce_params *p, int64_t hidden_dim, int64_t chunk_rows, size_t *bytes);
 
 /*
  * Fused-linear cross-entropy forward and backward.
  *   p            n_rows = BT, vocab = V, dtype = CE_DT_BF16 (hidden and
  *                weight), ignore_index, class_weight, label_smoothing,
- *                reduction; ld and variant are ignored.
+ *                reduction; variant 0 or CE_FLCE_DENSE (else
+ *                CE_ERR_INVALID_ARG); ld is ignored.
  *   hidden       device bf16 [BT, H] row-major.
  *   weight       device bf16 [V, H] row-major (the lm head).
  *   bias         device fp32 [V] or NULL.
@@ -322,6 +329,14 @@ ce_status flce_workspace_size(const ce_params *p, int64_t hidden_dim, int64_t ch
  * turns Z into dZ (bf16, one rounding) with the batch's normalisers;
  * grad_hidden_c = dZ W; grad_weight (+)= dZ^T hidden_c. H and V multiples
  * of 8.
+ * Ignored rows (target == ignore_index, or out of range: status bit) add
+ * nothing to the loss or grad_weight and get zero grad_hidden rows. By
+ * default they are also skipped, without a host sync (the device-side form
+ * of Liger-Kernel PR #1554's ignored-row skip): one kernel gathers the valid
+ * rows of hidden and their targets to the front of the workspace, and the
+ * GEMMs and the chunk kernels read the valid-row count from device memory,
+ * so chunks and tiles past it do no work. The host still launches every
+ * chunk. Results equal the dense path's up to the order of fp32 sums.
  */
 ce_status flce_fwd_bwd(const ce_params *p, int64_t hidden_dim, const void *hidden, const void *weight,
                        const float *bias, const void *target, float *loss, const float *grad_output,

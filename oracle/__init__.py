@@ -200,7 +200,8 @@ def flce_logits(hidden: torch.Tensor, weight: torch.Tensor, bias=None, row_block
 
 def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
          label_smoothing: float = 0.0, reduction: str = "mean", sample_rows=None,
-         sample_cols=None, abs_sums: bool = False, n_threads: int | None = None) -> dict:
+         sample_cols=None, abs_sums: bool = False, n_threads: int | None = None,
+         class_weight=None, grad_output=None) -> dict:
     """Fused-linear cross-entropy reference (fp64).
 
     Returns the reduced loss, the per-row losses, grad_hidden on
@@ -208,10 +209,15 @@ def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
     (all vocabulary rows if None): grad_hidden = dZ @ W, grad_weight = dZ^T @ h
     with dZ the oracle gradient of the loss with respect to z = h W^T + b.
     With ``abs_sums`` it also returns |dZ| @ |W| and |dZ|^T @ |h| on the same
-    samples (the magnitudes that bound rounding errors of dZ in the tests)."""
+    samples (the magnitudes that bound rounding errors of dZ in the tests).
+    ``class_weight`` and ``grad_output`` (scalar, or one value per row for
+    reduction none) are handed to the row oracle unchanged."""
     BT, H = hidden.shape
     V = weight.shape[0]
-    n, wy, wall, bad = normalizers(target, V, ignore_index, None)
+    n, wy, wall, bad = normalizers(target, V, ignore_index, class_weight)
+    g_all = None
+    if grad_output is not None:
+        g_all = _cpu(torch.as_tensor(grad_output), torch.float64).reshape(-1)
     Wd = _cpu(weight, torch.float64)
     hd = _cpu(hidden, torch.float64)
     tgt = _cpu(target).to(torch.int64)
@@ -229,9 +235,12 @@ def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
     abs_w = torch.zeros(len(cols_sel), H, dtype=torch.float64) if abs_sums else None
     for r0, z in flce_logits(hidden, weight, bias):
         r1 = r0 + z.shape[0]
-        res = rows(z, tgt[r0:r1], ignore_index=ignore_index, label_smoothing=label_smoothing,
-                   reduction=reduction, norm_wy=wy, w_all=wall, want_grad=True,
-                   want_stats=False, n_threads=n_threads)
+        g = None
+        if g_all is not None:
+            g = g_all[r0:r1] if reduction == "none" else g_all
+        res = rows(z, tgt[r0:r1], weight=class_weight, ignore_index=ignore_index,
+                   label_smoothing=label_smoothing, reduction=reduction, grad_output=g,
+                   norm_wy=wy, w_all=wall, want_grad=True, want_stats=False, n_threads=n_threads)
         row_loss[r0:r1] = res["row_loss"]
         dz = res["grad"]
         grad_w += dz[:, cols_sel].T @ hd[r0:r1]

@@ -93,6 +93,12 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
     const int vec_per_chunk = a.chunk_bytes / 16;
     const int tid = threadIdx.x;
     const int warp = tid >> 5, lane = tid & 31;
+    int64_t n_rows = a.n_rows;
+    if (a.row_limit) {
+        const int64_t left = static_cast<int64_t>(__ldg(a.row_limit)) - a.row_limit_off;
+        const int64_t blk = left > 0 ? (left + 63) / 64 * 64 : 0;
+        n_rows = blk < n_rows ? blk : n_rows;
+    }
 
     if (tid == 0) {
         for (int k = 0; k < nch; ++k) {
@@ -118,7 +124,7 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
             uint32_t j = 0;
-            for (int64_t row = q; row < a.n_rows; row += nq) {
+            for (int64_t row = q; row < n_rows; row += nq) {
                 const int64_t t = load_target(a.target, a.tgt32, row);
                 if (!target_valid(t, a.ignore_index, V)) continue;
                 const char *src = xbase + row * row_bytes + lo * F::kBytes;
@@ -144,7 +150,7 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
         float w_all = 0.f, w_y_sum = 0.f;   // batch normalisers, read after the normaliser kernel ends
         bool have_norm = false;
         uint32_t j = 0;
-        for (int64_t row = q; row < a.n_rows; row += nq) {
+        for (int64_t row = q; row < n_rows; row += nq) {
             const int64_t t = load_target(a.target, a.tgt32, row);
             const bool valid = target_valid(t, a.ignore_index, V);
             char *rowp = xbase + row * row_bytes;
@@ -310,7 +316,7 @@ __global__ void __launch_bounds__(kFusedThreads, 3) ce_fused_kernel(FusedArgs a)
             if (sh_last) {
                 __threadfence();
                 double s = 0.0;
-                for (int64_t i = tid; i < a.n_rows; i += NCT) s += static_cast<double>(__ldcg(a.row_loss + i));
+                for (int64_t i = tid; i < n_rows; i += NCT) s += static_cast<double>(__ldcg(a.row_loss + i));
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xffffffffu, s, off);
                 if (lane == 0) sh_sum[warp] = s;

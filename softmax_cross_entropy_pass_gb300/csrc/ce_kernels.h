@@ -73,6 +73,13 @@ struct FusedArgs {
     void *out;                 // gradient destination (== x for in place)
     int64_t ld_out;            // row stride of out in elements of the output dtype
     int32_t finalize;          // 1: the last CTA reduces the row losses into loss[0]
+    // Device-side row count (NULL: n_rows). The kernel handles rows
+    // [0, min(n_rows, round_up(max(0, *row_limit - row_limit_off), 64))):
+    // rows past the count but inside its 64-row block are expected to carry
+    // ignored targets and come out as zero gradient rows, so a GEMM that
+    // reduces over them in 64-row steps sees zeros.
+    const int *row_limit;
+    int64_t row_limit_off;
 };
 
 constexpr int kFusedConsumerWarps = 8;

@@ -48,6 +48,13 @@ struct GemmArgs {
     int tiles_m, tiles_n;
     int m_fastest;         // tile order: consecutive tiles step along M
     unsigned int *status;
+    // Device-side size (NULL: the sizes above). The kernel reads
+    // n = clamp(*dyn_count - dyn_off, 0, size) and uses it as M (dyn_dim 0)
+    // or K (dyn_dim 1); the launch must be stream-ordered after the kernel
+    // that writes the count.
+    const int *dyn_count;
+    int dyn_off, dyn_dim;
+    const int *row_map;    // output row r is stored at row row_map[r] (NULL: r)
 };
 
 __device__ inline void tile_coords(const GemmArgs &g, int t, int &tm, int &tn) {
@@ -56,11 +63,12 @@ __device__ inline void tile_coords(const GemmArgs &g, int t, int &tm, int &tn) {
 }
 
 // One thread's 32 consecutive accumulator columns of one output row.
-__device__ inline void epilogue_store(const GemmArgs &g, int row, int col0, const uint32_t (&v)[32]) {
+// `orow` is the row of the output the tile row `row` is stored at.
+__device__ inline void epilogue_store(const GemmArgs &g, int row, int orow, int col0, const uint32_t (&v)[32]) {
     if (row >= g.M) return;
     const bool full = col0 + 32 <= g.N;
     if (g.out_kind == OUT_BF16_STORE) {
-        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(g.out) + static_cast<int64_t>(row) * g.ldo + col0;
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(g.out) + static_cast<int64_t>(orow) * g.ldo + col0;
         if (full && (g.ldo % 8) == 0) {
             uint4 *o4 = reinterpret_cast<uint4 *>(o);
 #pragma unroll
@@ -79,7 +87,7 @@ __device__ inline void epilogue_store(const GemmArgs &g, int row, int col0, cons
         }
         return;
     }
-    float *o = reinterpret_cast<float *>(g.out) + static_cast<int64_t>(row) * g.ldo + col0;
+    float *o = reinterpret_cast<float *>(g.out) + static_cast<int64_t>(orow) * g.ldo + col0;
     const bool accum = g.out_kind == OUT_F32_ACCUM;
     if (full && (g.ldo % 4) == 0) {
         float4 *o4 = reinterpret_cast<float4 *>(o);
@@ -111,6 +119,34 @@ __device__ inline void epilogue_store(const GemmArgs &g, int row, int col0, cons
 
 __global__ void __launch_bounds__(GB_THREADS, 1)
 flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+    if (g.dyn_count) {
+        int n = __ldg(g.dyn_count) - g.dyn_off;
+        if (g.dyn_dim == 0) {
+            g.M = n < 0 ? 0 : (n < g.M ? n : g.M);
+            g.tiles_m = (g.M + GB_M - 1) / GB_M;
+        } else {
+            g.K = n < 0 ? 0 : (n < g.K ? n : g.K);
+        }
+    }
+    const int num_tiles = g.tiles_m * g.tiles_n;
+    const int kiters = (g.K + GB_K - 1) / GB_K;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (num_tiles == 0) return;
+    if (kiters == 0) {
+        // empty reduction: D = 0 (+ bias) in the store modes, nothing to add in accumulate mode
+        if (g.out_kind != OUT_F32_ACCUM && warp >= 2) {
+            const int q = warp & 3;
+            const uint32_t zero[32] = {};
+            for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
+                int tm, tn;
+                tile_coords(g, t, tm, tn);
+                const int row = tm * GB_M + q * 32 + lane;
+                const int orow = (g.row_map && row < g.M) ? __ldg(g.row_map + row) : row;
+                for (int c0 = 0; c0 < GB_N; c0 += 32) epilogue_store(g, row, orow, tn * GB_N + c0, zero);
+            }
+        }
+        return;
+    }
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = smem_u32(smem_raw);
     const uint32_t base = (raw + 1023u) & ~1023u;   // 128-byte swizzle atoms need 1 KB alignment
@@ -123,7 +159,6 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
     volatile int *abort = abort_flag;
 
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         for (int s = 0; s < GB_STAGES; ++s) { mbar_init(smem_u32(&full[s]), 1); mbar_init(smem_u32(&empty[s]), 1); }
         for (int a = 0; a < 2; ++a) { mbar_init(smem_u32(&tfull[a]), 1); mbar_init(smem_u32(&tempty[a]), 4); }
@@ -140,9 +175,6 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-
-    const int num_tiles = g.tiles_m * g.tiles_n;
-    const int kiters = (g.K + GB_K - 1) / GB_K;
 
     if (warp == 0) {
         if (lane == 0) {
@@ -205,13 +237,14 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             mbar_wait_bounded<false>(smem_u32(&tfull[acc]), u & 1u, abort);
             tc_fence_after();
             const int row = tm * GB_M + q * 32 + lane;
+            const int orow = (g.row_map && row < g.M) ? __ldg(g.row_map + row) : row;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * GB_N;
 #pragma unroll 1
             for (int c0 = 0; c0 < GB_N; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(taddr + c0, v);
                 tmem_ld_wait();
-                epilogue_store(g, row, tn * GB_N + c0, v);
+                epilogue_store(g, row, orow, tn * GB_N + c0, v);
             }
             tc_fence_before();
             __syncwarp();
@@ -227,19 +260,117 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
 }
 
 // ------------------------------------------------------------------ small kernels
+// Rows past a device-side count are skipped: n = clamp(*count - off, 0, n).
+__device__ inline int64_t dyn_rows(int64_t n, const int *count, int64_t off) {
+    if (!count) return n;
+    const int64_t left = static_cast<int64_t>(__ldg(count)) - off;
+    return left < 0 ? 0 : (left < n ? left : n);
+}
+
 // grad_bias[c] (+)= sum over rows of dZ[r, c]
-__global__ void flce_colsum_kernel(const __nv_bfloat16 *dz, int64_t ldd, int rows, int64_t V, float *gb, int accumulate) {
+__global__ void flce_colsum_kernel(const __nv_bfloat16 *dz, int64_t ldd, int rows, int64_t V, float *gb, int accumulate,
+                                   const int *count, int off) {
     const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (c >= V) return;
+    const int n = static_cast<int>(dyn_rows(rows, count, off));
     float s = 0.f;
-    for (int r = 0; r < rows; ++r) s += __bfloat162float(dz[static_cast<int64_t>(r) * ldd + c]);
+    for (int r = 0; r < n; ++r) s += __bfloat162float(dz[static_cast<int64_t>(r) * ldd + c]);
     gb[c] = accumulate ? gb[c] + s : s;
 }
 
-// loss[0] = sum of the row losses (/ W_y for mean), fixed order, fp64
-__global__ void __launch_bounds__(256) flce_reduce_kernel(const float *row_loss, int64_t n, int reduction,
-                                                          const WsCtl *ctl, float *loss) {
+// Ignored-row compaction (the device-side form of Liger-Kernel PR #1554's
+// skip of ignored rows: no host sync). One block scans the targets in order
+// and writes, for the n rows whose target is valid, idx[k] = the k-th valid
+// row and tgt_c[k] = its target; pos[i] = k for a valid row i, -1 otherwise;
+// tgt_c[k] = ignore_index for k >= n; *count = n.
+constexpr int kCompactThreads = 1024;
+__global__ void __launch_bounds__(kCompactThreads) flce_compact_kernel(const void *target, int tgt32, int64_t n_rows,
+                                                                      int64_t vocab, int64_t ignore_index, int *idx,
+                                                                      int *pos, int64_t *tgt_c, int *count) {
+    __shared__ int warp_off[kCompactThreads / 32];
+    __shared__ int total;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    int base = 0;
+    for (int64_t r0 = 0; r0 < n_rows; r0 += kCompactThreads) {
+        const int64_t i = r0 + tid;
+        int64_t t = 0;
+        bool v = false;
+        if (i < n_rows) {
+            t = load_target(target, tgt32, i);
+            v = target_valid(t, ignore_index, vocab);
+        }
+        const unsigned b = __ballot_sync(0xffffffffu, v);
+        if (lane == 0) warp_off[warp] = __popc(b);
+        __syncthreads();
+        if (warp == 0) {
+            const int c = warp_off[lane];
+            int x = c;
+#pragma unroll
+            for (int d = 1; d < 32; d <<= 1) {
+                const int y = __shfl_up_sync(0xffffffffu, x, d);
+                if (lane >= d) x += y;
+            }
+            warp_off[lane] = x - c;  // exclusive prefix over warps
+            if (lane == 31) total = x;
+        }
+        __syncthreads();
+        const int k = base + warp_off[warp] + __popc(b & ((1u << lane) - 1u));
+        if (i < n_rows) {
+            if (v) {
+                idx[k] = static_cast<int>(i);
+                tgt_c[k] = t;
+            }
+            pos[i] = v ? k : -1;
+        }
+        base += total;
+        __syncthreads();  // warp_off and total are rewritten by the next tile
+    }
+    for (int64_t k = base + tid; k < n_rows; k += kCompactThreads) {
+        tgt_c[k] = ignore_index;
+        idx[k] = -1;
+    }
+    if (tid == 0) *count = base;
+}
+
+// h_c[k] = hidden[idx[k]] for k < n and 0 beyond (so that a GEMM reducing
+// over the compacted rows in 64-row steps meets zeros past n); the gradient
+// rows of the rows left out are zeroed; for reduction none the per-row
+// grad_output is gathered the same way.
+__global__ void __launch_bounds__(256) flce_gather_kernel(const uint4 *hidden, int64_t row16, int64_t n_rows,
+                                                          const int *idx, const int *pos, const int *count, uint4 *hc,
+                                                          uint4 *grad_hidden, const float *g_in, float *g_c) {
+    const int64_t n = __ldg(count);
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (int64_t r = blockIdx.x; r < n_rows; r += gridDim.x) {
+        uint4 *dst = hc + r * row16;
+        if (r < n) {
+            const uint4 *src = hidden + static_cast<int64_t>(__ldg(idx + r)) * row16;
+            for (int64_t j = threadIdx.x; j < row16; j += blockDim.x) dst[j] = __ldg(src + j);
+        } else {
+            for (int64_t j = threadIdx.x; j < row16; j += blockDim.x) dst[j] = zero;
+        }
+        if (__ldg(pos + r) < 0) {
+            uint4 *gh = grad_hidden + r * row16;
+            for (int64_t j = threadIdx.x; j < row16; j += blockDim.x) gh[j] = zero;
+        }
+        if (g_in && threadIdx.x == 0) g_c[r] = r < n ? __ldg(g_in + __ldg(idx + r)) : 0.f;
+    }
+}
+
+// reduction none after compaction: loss[i] = the compacted row's loss, 0 for rows left out
+__global__ void flce_scatter_loss_kernel(const int *pos, const float *row_loss_c, int64_t n_rows, float *loss) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i >= n_rows) return;
+    const int k = __ldg(pos + i);
+    loss[i] = k >= 0 ? __ldg(row_loss_c + k) : 0.f;
+}
+
+// loss[0] = sum of the row losses (/ W_y for mean), fixed order, fp64; with
+// `count`, only the first *count row losses (the compacted rows).
+__global__ void __launch_bounds__(256) flce_reduce_kernel(const float *row_loss, int64_t n0, int reduction,
+                                                          const WsCtl *ctl, float *loss, const int *count) {
     __shared__ double sh[8];
+    const int64_t n = dyn_rows(n0, count, 0);
     double s = 0.0;
     for (int64_t i = threadIdx.x; i < n; i += blockDim.x) s += static_cast<double>(row_loss[i]);
 #pragma unroll
@@ -301,7 +432,7 @@ static int sm_count() {
 // memory [K, M] (lda >= M). B: K-major = memory [N, K]; MN-major = memory [K, N].
 cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B, int64_t ldb,
                       int b_mn, int out_kind, void *out, int64_t ldo, const float *bias, unsigned int *status,
-                      cudaStream_t s) {
+                      cudaStream_t s, const GemmDyn *dyn) {
     if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
     CUtensorMap ta, tb;
     cudaError_t e;
@@ -319,6 +450,12 @@ cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn,
     g.tiles_n = (N + GB_N - 1) / GB_N;
     g.m_fastest = g.tiles_m <= g.tiles_n ? 1 : 0;  // the operand of the short side stays in L2
     g.status = status;
+    if (dyn) {
+        g.dyn_count = dyn->count;
+        g.dyn_off = dyn->off;
+        g.dyn_dim = dyn->dim;
+        g.row_map = dyn->row_map;
+    }
     static bool attr_set = false;
     if (!attr_set) {
         e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&flce_gemm_kernel),
@@ -347,9 +484,12 @@ int64_t round_up(int64_t a, int64_t b) { return (a + b - 1) / b * b; }
 struct FlceLayout {
     size_t ce_ws, z_off, dz_off, total;
     int64_t ldz, ldd;
+    // ignored-row compaction: compacted hidden rows, the maps, the compacted
+    // targets and per-row grad_output, the valid-row count
+    size_t hc_off, idx_off, pos_off, tgt_off, gc_off, cnt_off;
 };
 
-FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk) {
+FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk, int64_t hidden, bool compact) {
     FlceLayout L{};
     L.ce_ws = round_up(static_cast<int64_t>(ws_bytes(n_rows)), 1024);
     L.ldz = round_up(vocab, 4);
@@ -357,8 +497,19 @@ FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk) {
     L.z_off = L.ce_ws;
     L.dz_off = L.z_off + round_up(chunk * L.ldz * 4, 1024);
     L.total = L.dz_off + round_up(chunk * L.ldd * 2, 1024);
+    if (compact) {
+        L.hc_off = L.total;
+        L.idx_off = L.hc_off + round_up(n_rows * hidden * 2, 1024);
+        L.pos_off = L.idx_off + round_up(n_rows * 4, 256);
+        L.tgt_off = L.pos_off + round_up(n_rows * 4, 256);
+        L.gc_off = L.tgt_off + round_up(n_rows * 8, 256);
+        L.cnt_off = L.gc_off + round_up(n_rows * 4, 256);
+        L.total = L.cnt_off + 256;
+    }
     return L;
 }
+
+bool flce_compacts(const ce_params *p) { return (p->variant & CE_FLCE_DENSE) == 0; }
 
 ce_status flce_cuda_fail(cudaError_t e) {
     (void)cudaGetLastError();
@@ -388,7 +539,7 @@ ce_status ce_gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t l
 ce_status flce_workspace_size(const ce_params *p, int64_t hidden_dim, int64_t chunk_rows, size_t *bytes) {
     if (!p || !bytes || p->n_rows < 0 || p->vocab < 1 || hidden_dim < 1 || chunk_rows < 1) return CE_ERR_INVALID_ARG;
     int64_t chunk = chunk_rows < p->n_rows ? chunk_rows : (p->n_rows > 0 ? p->n_rows : 1);
-    *bytes = flce_layout(p->n_rows, p->vocab, chunk).total;
+    *bytes = flce_layout(p->n_rows, p->vocab, chunk, hidden_dim, flce_compacts(p)).total;
     return CE_OK;
 }
 
@@ -404,11 +555,13 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
     if (p->target_is_int32 != 0 && p->target_is_int32 != 1) return CE_ERR_INVALID_ARG;
     if (p->class_weight && (reinterpret_cast<uintptr_t>(p->class_weight) & 15u)) return CE_ERR_INVALID_ARG;
     if (p->softcap != 0.f || p->z_loss != 0.f || p->accuracy) return CE_ERR_UNSUPPORTED;
+    if ((p->variant & ~CE_FLCE_DENSE) != 0) return CE_ERR_INVALID_ARG;
     if (!loss || !ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CE_ERR_INVALID_ARG;
     const int64_t BT = p->n_rows, V = p->vocab;
     if (BT > INT32_MAX || V > INT32_MAX || H > INT32_MAX) return CE_ERR_UNSUPPORTED;
     const int64_t C = chunk_rows < BT ? chunk_rows : (BT > 0 ? BT : 1);
-    const FlceLayout L = flce_layout(BT, V, C);
+    const bool compact = flce_compacts(p);
+    const FlceLayout L = flce_layout(BT, V, C, H, compact);
     if (ws_bytes < L.total) return CE_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (BT > 0 && (!hidden || !weight || !target || !grad_hidden || !grad_weight)) return CE_ERR_INVALID_ARG;
@@ -420,6 +573,7 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
     float *Z = reinterpret_cast<float *>(wsb + L.z_off);
     __nv_bfloat16 *dZ = reinterpret_cast<__nv_bfloat16 *>(wsb + L.dz_off);
     float *row_loss = ws_row_loss(ws);
+    const bool none = p->reduction == CE_RED_NONE;
 
     // batch normalisers over every row (the mean's W_y spans all chunks)
     PrepArgs pa{};
@@ -429,7 +583,7 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
     cudaError_t e = launch_prep(pa, s);
     if (e != cudaSuccess) return flce_cuda_fail(e);
     if (BT == 0) {
-        if (p->reduction != CE_RED_NONE && (e = cudaMemsetAsync(loss, 0, sizeof(float), s)) != cudaSuccess)
+        if (!none && (e = cudaMemsetAsync(loss, 0, sizeof(float), s)) != cudaSuccess)
             return flce_cuda_fail(e);
         if ((e = cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * H * 4, s)) != cudaSuccess)
             return flce_cuda_fail(e);
@@ -442,36 +596,93 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
     bool ok = false;
     if ((e = fused_plan_f32_to_bf16(mode, C, V, &plan, &ok)) != cudaSuccess) return flce_cuda_fail(e);
     if (!ok) return CE_ERR_UNSUPPORTED;
-    const int tgt_bytes = p->target_is_int32 ? 4 : 8;
+
+    // Rows whose target is ignored (or out of range) add nothing to the loss
+    // or to grad_weight and have a zero grad_hidden row. With compaction the
+    // valid rows are gathered to the front on the device, every kernel of the
+    // chunk loop reads the valid-row count from device memory, and the work
+    // past it is skipped; the host never learns the count.
+    const void *h_src = hidden;
+    const void *tgt_src = target;
+    int tgt32 = p->target_is_int32;
+    const float *g_rows = grad_output;     // reduction none: per-row grad_output in chunk row order
+    float *loss_rows = loss;               // reduction none: per-row loss in chunk row order
+    const int *count = nullptr, *idx = nullptr, *pos = nullptr;
+    if (compact) {
+        int *idx_w = reinterpret_cast<int *>(wsb + L.idx_off);
+        int *pos_w = reinterpret_cast<int *>(wsb + L.pos_off);
+        int64_t *tgt_c = reinterpret_cast<int64_t *>(wsb + L.tgt_off);
+        float *g_c = reinterpret_cast<float *>(wsb + L.gc_off);
+        int *cnt = reinterpret_cast<int *>(wsb + L.cnt_off);
+        {
+            const void *tg = target;
+            int t32 = p->target_is_int32;
+            int64_t n = BT, vv = V, ign = p->ignore_index;
+            void *args[] = {&tg, &t32, &n, &vv, &ign, &idx_w, &pos_w, &tgt_c, &cnt};
+            e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_compact_kernel), dim3(1),
+                                 dim3(kCompactThreads), args, 0, s);
+            if (e != cudaSuccess) return flce_cuda_fail(e);
+        }
+        uint4 *hc = reinterpret_cast<uint4 *>(wsb + L.hc_off);
+        {
+            const uint4 *hid = reinterpret_cast<const uint4 *>(hidden);
+            int64_t row16 = H * 2 / 16, n = BT;
+            const int *ci = idx_w, *cp = pos_w, *cc = cnt;
+            uint4 *gh = reinterpret_cast<uint4 *>(grad_hidden);
+            const float *gi = (none && grad_output) ? grad_output : nullptr;
+            float *gc = g_c;
+            void *args[] = {&hid, &row16, &n, &ci, &cp, &cc, &hc, &gh, &gi, &gc};
+            const int64_t want = static_cast<int64_t>(sm_count()) * 8;
+            const int blocks = static_cast<int>(BT < want ? BT : want);
+            e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_gather_kernel), dim3(blocks), dim3(256), args,
+                                 0, s);
+            if (e != cudaSuccess) return flce_cuda_fail(e);
+        }
+        h_src = hc;
+        tgt_src = tgt_c;
+        tgt32 = 0;
+        if (none && grad_output) g_rows = g_c;
+        if (none) loss_rows = row_loss;
+        count = cnt;
+        idx = idx_w;
+        pos = pos_w;
+    }
+    const int tgt_bytes = tgt32 ? 4 : 8;
 
     for (int64_t r0 = 0; r0 < BT; r0 += C) {
         const int64_t c = (BT - r0) < C ? (BT - r0) : C;
-        const char *h_c = reinterpret_cast<const char *>(hidden) + r0 * H * 2;
+        const char *h_c = reinterpret_cast<const char *>(h_src) + r0 * H * 2;
+        const GemmDyn rows_m{count, static_cast<int>(r0), 0, nullptr};
+        const GemmDyn rows_k{count, static_cast<int>(r0), 1, nullptr};
+        const GemmDyn rows_out{count, static_cast<int>(r0), 0, idx ? idx + r0 : nullptr};
         // Z = h_c W^T (+ b), fp32
         e = gemm_bf16(static_cast<int>(c), static_cast<int>(V), static_cast<int>(H), h_c, H, 0, weight, H, 0,
-                      0, Z, L.ldz, bias, &ctl->status, s);
+                      0, Z, L.ldz, bias, &ctl->status, s, compact ? &rows_m : nullptr);
         if (e != cudaSuccess) return flce_cuda_fail(e);
         // cross-entropy forward + backward on the chunk: dZ (bf16) and row losses
         FusedArgs a{};
         a.x = Z; a.n_rows = c; a.vocab = V; a.ld = L.ldz;
-        a.target = reinterpret_cast<const char *>(target) + r0 * tgt_bytes;
-        a.tgt32 = p->target_is_int32; a.reduction = p->reduction; a.ignore_index = p->ignore_index;
+        a.target = reinterpret_cast<const char *>(tgt_src) + r0 * tgt_bytes;
+        a.tgt32 = tgt32; a.reduction = p->reduction; a.ignore_index = p->ignore_index;
         a.weight = p->class_weight; a.eps = p->label_smoothing;
-        a.grad_output = grad_output ? (p->reduction == CE_RED_NONE ? grad_output + r0 : grad_output) : nullptr;
-        a.loss = p->reduction == CE_RED_NONE ? loss + r0 : loss;
+        a.grad_output = g_rows ? (none ? g_rows + r0 : g_rows) : nullptr;
+        a.loss = none ? loss_rows + r0 : loss;
         a.row_loss = row_loss + r0;
         a.ctl = ctl;
         a.out = dZ; a.ld_out = L.ldd; a.finalize = 0;
+        a.row_limit = count; a.row_limit_off = r0;
         FusedPlan pl = plan;
         if (pl.n_clusters > c) pl.n_clusters = static_cast<int>(c);
         if ((e = launch_fused_f32_to_bf16(a, pl, mode, s)) != cudaSuccess) return flce_cuda_fail(e);
-        // grad_hidden_c = dZ W   (A = dZ K-major, B = W stored [V, H] = [K, N]: MN-major)
+        // grad_hidden rows = dZ W   (A = dZ K-major, B = W stored [V, H] = [K, N]: MN-major);
+        // compacted rows are stored back at their own rows
+        void *gh = compact ? grad_hidden : reinterpret_cast<char *>(grad_hidden) + r0 * H * 2;
         e = gemm_bf16(static_cast<int>(c), static_cast<int>(H), static_cast<int>(V), dZ, L.ldd, 0, weight, H, 1,
-                      2, reinterpret_cast<char *>(grad_hidden) + r0 * H * 2, H, nullptr, &ctl->status, s);
+                      2, gh, H, nullptr, &ctl->status, s, compact ? &rows_out : nullptr);
         if (e != cudaSuccess) return flce_cuda_fail(e);
         // grad_weight (+)= dZ^T h_c   (A = dZ stored [c, V] = [K, M]: MN-major; B = h_c [K, N]: MN-major)
         e = gemm_bf16(static_cast<int>(V), static_cast<int>(H), static_cast<int>(c), dZ, L.ldd, 1, h_c, H, 1,
-                      r0 == 0 ? 0 : 1, grad_weight, H, nullptr, &ctl->status, s);
+                      r0 == 0 ? 0 : 1, grad_weight, H, nullptr, &ctl->status, s, compact ? &rows_k : nullptr);
         if (e != cudaSuccess) return flce_cuda_fail(e);
         if (grad_bias) {
             const int threads = 256;
@@ -481,19 +692,30 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
             int rows = static_cast<int>(c);
             int64_t vv = V;
             int accum = r0 == 0 ? 0 : 1;
-            void *args[] = {&dzc, &ldd, &rows, &vv, &grad_bias, &accum};
+            const int *cc = count;
+            int off = static_cast<int>(r0);
+            void *args[] = {&dzc, &ldd, &rows, &vv, &grad_bias, &accum, &cc, &off};
             e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_colsum_kernel), dim3(blocks), dim3(threads),
                                  args, 0, s);
             if (e != cudaSuccess) return flce_cuda_fail(e);
         }
     }
-    if (p->reduction != CE_RED_NONE) {
+    if (!none) {
         const float *rl = row_loss;
         int64_t n = BT;
         int red = p->reduction;
         const WsCtl *cc = ctl;
-        void *args[] = {&rl, &n, &red, &cc, &loss};
+        const int *cnt = count;
+        void *args[] = {&rl, &n, &red, &cc, &loss, &cnt};
         e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_reduce_kernel), dim3(1), dim3(256), args, 0, s);
+        if (e != cudaSuccess) return flce_cuda_fail(e);
+    } else if (compact) {
+        const int *pp = pos;
+        const float *rl = row_loss;
+        int64_t n = BT;
+        void *args[] = {&pp, &rl, &n, &loss};
+        e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_scatter_loss_kernel),
+                             dim3(static_cast<unsigned>((BT + 255) / 256)), dim3(256), args, 0, s);
         if (e != cudaSuccess) return flce_cuda_fail(e);
     }
     return CE_OK;

@@ -11,8 +11,18 @@ namespace ce {
 // a_mn / b_mn: operand stored MN-major (A as [K, M], B as [K, N]) instead of
 // K-major (A as [M, K], B as [N, K]). out_kind: 0 fp32 store (+ bias[N]),
 // 1 fp32 accumulate, 2 bf16 store.
+// `dyn` (optional) makes M or K a device-side value: the kernel uses
+// clamp(*count - off, 0, M or K) (dim 0: M, 1: K), and `row_map` sends output
+// row r to row row_map[r]. The sizes passed here are then upper bounds.
+struct GemmDyn {
+    const int *count;
+    int off;
+    int dim;
+    const int *row_map;
+};
+
 cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B,
                       int64_t ldb, int b_mn, int out_kind, void *out, int64_t ldo, const float *bias,
-                      unsigned int *status, cudaStream_t s);
+                      unsigned int *status, cudaStream_t s, const GemmDyn *dyn = nullptr);
 
 }  // namespace ce

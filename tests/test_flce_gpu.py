@@ -103,6 +103,82 @@ def test_flce_small_against_oracle(ce, reduction, chunk, with_bias):
         assert (err_b <= dz.abs().sum(0) * 2.0 ** -8 + 1e-30).all()
 
 
+def _ignored_case(case, BT, V):
+    """Targets, reduction, chunk rows, label smoothing, class weights and
+    grad_output of one ignored-row case (seeded)."""
+    seeds = {"mixed": 21, "all_ignored": 22, "mostly_ignored": 23, "none_rows": 24, "int32_out_of_range": 25}
+    g = torch.Generator().manual_seed(seeds[case])
+    t = torch.randint(0, V, (BT,), generator=g)
+    perm = torch.randperm(BT, generator=g)
+    red, chunk, eps, weighted, go = "mean", 128, 0.0, False, None
+    if case == "mixed":          # 5% ignored, valid count not a multiple of 64
+        t[perm[:27]] = -100
+    elif case == "all_ignored":
+        t[:] = -100
+        chunk = 200
+    elif case == "mostly_ignored":  # whole chunks past the valid count
+        t[perm[:int(0.8 * BT)]] = -100
+        red, chunk = "sum", 64
+        go = torch.tensor([0.37])
+    elif case == "none_rows":    # per-row loss and grad_output, weights, smoothing
+        t[perm[:int(0.3 * BT)]] = -100
+        red, chunk, eps, weighted = "none", 100, 0.1, True
+        go = torch.rand(BT, generator=g)
+    elif case == "int32_out_of_range":
+        t[perm[:40]] = -100
+        t[perm[40]] = V + 5
+        t = t.to(torch.int32)
+    w = (torch.rand(V, generator=g) + 0.5) if weighted else None
+    return t, red, chunk, eps, w, go
+
+
+@pytest.mark.parametrize("dense", [False, True])
+@pytest.mark.parametrize("case", ["mixed", "all_ignored", "mostly_ignored", "none_rows", "int32_out_of_range"])
+def test_flce_ignored_rows_against_oracle(ce, case, dense):
+    """Ignored (and out-of-range) rows, with and without the device-side
+    compaction of the valid rows: every output against the fp64 oracle with
+    the dZ-rounding bound; workspace and outputs start as NaN so nothing a
+    kernel skips can leak into a result."""
+    BT, H, V = 520, 128, 1000
+    h = _rand_bf16(BT, H, seed=11)
+    W = _rand_bf16(V, H, seed=12, scale=0.05)
+    t, red, chunk, eps, w, go = _ignored_case(case, BT, V)
+    dev = "cuda"
+    ws = torch.full((ce.flce_workspace_size(BT, H, V, chunk, dense),), 0xFF, dtype=torch.uint8, device=dev)
+    loss = torch.full((BT if red == "none" else 1,), float("nan"), device=dev)
+    gh = torch.full((BT, H), float("nan"), dtype=torch.bfloat16, device=dev)
+    gw = torch.full((V, H), float("nan"), device=dev)
+    out = ce.flce_fwd_bwd(h.to(dev), W.to(dev), t.to(dev), class_weight=None if w is None else w.to(dev),
+                          label_smoothing=eps, reduction=red, grad_output=None if go is None else go.to(dev),
+                          chunk_rows=chunk, loss=loss, grad_hidden=gh, grad_weight=gw, ws=ws, dense=dense)
+    flags = ce.ce_get_status(ws)
+    ref = oracle.flce(h, W, t, label_smoothing=eps, reduction=red, class_weight=w, grad_output=go,
+                      abs_sums=True)
+    want_flags = (ce.CE_FLAG_TARGET_OUT_OF_RANGE if case == "int32_out_of_range" else 0) | \
+        (ce.CE_FLAG_NO_VALID_ROWS if case == "all_ignored" and red == "mean" else 0)
+    assert flags == want_flags, f"status flags {flags:#x}, expected {want_flags:#x}"
+    loss_c = out[0].double().cpu()
+    if red == "none":
+        err = (loss_c - ref["loss"]).abs()
+        assert (err <= 1e-4 * ref["loss"].abs() + 1e-6).all(), f"row losses: max err {float(err.max()):.3e}"
+    else:
+        assert abs(float(loss_c[0]) - ref["loss"]) <= 1e-4 * abs(ref["loss"]) + 1e-30
+    gh_c = gh.double().cpu()
+    gw_c = gw.double().cpu()
+    assert torch.isfinite(gh_c).all() and torch.isfinite(gw_c).all()
+    err_h = (gh_c - ref["grad_hidden"]).abs()
+    assert (err_h <= ref["grad_hidden_abs"] * 2.0 ** -8 + ref["grad_hidden"].abs() * 2.0 ** -7).all(), \
+        f"grad_hidden max err {float(err_h.max()):.3e}"
+    err_w = (gw_c - ref["grad_weight"]).abs()
+    assert (err_w <= ref["grad_weight_abs"] * 2.0 ** -8 + ref["grad_weight"].abs() * 2.0 ** -20).all(), \
+        f"grad_weight max err {float(err_w.max()):.3e}"
+    tt = t.to(torch.int64)
+    skipped = (tt < 0) | (tt >= V)
+    assert torch.count_nonzero(gh_c[skipped]) == 0
+    if red == "none":
+        assert torch.count_nonzero(loss_c[skipped]) == 0
+
+
 @pytest.mark.slow
 def test_flce_full_size_sampled(ce):
     """hidden 8192 x 4096, W 128256 x 4096: loss over all rows, grad_hidden on

@@ -281,6 +281,31 @@ def test_flce_against_torch_autograd_fp64():
     assert torch.allclose(out["grad_bias"], br.grad[cols], rtol=1e-10, atol=1e-15)
 
 
+@pytest.mark.parametrize("reduction", ["mean", "none"])
+def test_flce_class_weight_grad_output_against_torch_autograd_fp64(reduction):
+    """The fused-linear reference with class weights, label smoothing and a
+    grad_output (per row for none) vs torch autograd of the same composition."""
+    BT, H, V = 36, 16, 50
+    g = torch.Generator().manual_seed(4)
+    h = torch.randn(BT, H, generator=g, dtype=torch.float64)
+    W = torch.randn(V, H, generator=g, dtype=torch.float64) * 0.3
+    w = torch.rand(V, generator=g, dtype=torch.float64) + 0.5
+    t = make_targets(BT, V, 0.2, 4)
+    go = torch.rand(BT, generator=g, dtype=torch.float64) if reduction == "none" else torch.tensor(0.37,
+                                                                                                 dtype=torch.float64)
+    hr, Wr = (a.clone().requires_grad_(True) for a in (h, W))
+    loss = F.cross_entropy(F.linear(hr, Wr), t, weight=w, ignore_index=IGNORE_INDEX, label_smoothing=0.1,
+                           reduction=reduction)
+    loss.backward(go)
+    out = oracle.flce(h, W, t, label_smoothing=0.1, reduction=reduction, class_weight=w, grad_output=go)
+    if reduction == "none":
+        assert torch.allclose(out["loss"], loss.detach(), rtol=1e-12, atol=1e-15)
+    else:
+        assert out["loss"] == pytest.approx(loss.item(), rel=1e-12)
+    assert torch.allclose(out["grad_hidden"], hr.grad, rtol=1e-10, atol=1e-15)
+    assert torch.allclose(out["grad_weight"], Wr.grad, rtol=1e-10, atol=1e-15)
+
+
 # ----------------------------------------------------------------- the pages' numbers
 def _bf16_round(v: torch.Tensor) -> torch.Tensor:
     return v.to(torch.float32).to(torch.bfloat16).to(torch.float64)
