@@ -273,20 +273,23 @@ def measure_flce(ce, device, steps: int, chunk_rows: int):
     ws = torch.empty(ce.flce_workspace_size(BT, H, V, chunk_rows), dtype=torch.uint8, device=device)
     kw = dict(reduction="mean", chunk_rows=chunk_rows, loss=loss, grad_hidden=gh, grad_weight=gw, ws=ws)
 
-    def timed(dense):
+    def timed(**variant):
         for _ in range(2):
-            ce.flce_fwd_bwd(h, W, t, dense=dense, **kw)
+            ce.flce_fwd_bwd(h, W, t, **variant, **kw)
         torch.cuda.synchronize()
         ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
         for a, b in ev:
             a.record()
-            ce.flce_fwd_bwd(h, W, t, dense=dense, **kw)
+            ce.flce_fwd_bwd(h, W, t, **variant, **kw)
             b.record()
         torch.cuda.synchronize()
         return sum(a.elapsed_time(b) for a, b in ev) / steps
 
-    step_ms = timed(False)          # the default: ignored rows compacted away on the device
-    dense_ms = timed(True)          # every row through every GEMM
+    # the default: ignored rows compacted away on the device, chunk cross-entropy
+    # from the logits GEMM's row statistics + one streaming map
+    step_ms = timed()
+    dense_ms = timed(dense=True)            # every row through every GEMM
+    cluster_ms = timed(ce_cluster=True)     # chunk cross-entropy by the cluster kernel
     n_valid = int(((t >= 0) & (t < V)).sum().item())
     flop = 3 * 2.0 * BT * V * H
     # the three GEMMs of one chunk, each timed alone
@@ -320,6 +323,7 @@ def measure_flce(ce, device, steps: int, chunk_rows: int):
             "gemm_tflops_whole_step": flop / step_ms / 1e9,
             "valid_rows": n_valid, "gemm_tflops_executed": 3 * 2.0 * n_valid * V * H / step_ms / 1e9,
             "ms_per_step_dense": dense_ms, "gemm_tflops_dense": flop / dense_ms / 1e9,
+            "ms_per_step_ce_cluster": cluster_ms,
             "gemm_chunk": per}
 
 

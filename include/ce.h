@@ -291,16 +291,21 @@ ce_status ce_get_status(const void *workspace, uint32_t *flags, void *stream);
  *      [K, N] (ldb >= N).
  *   D  device fp32 or bf16 (out_kind) [M, N], row stride ldd elements.
  *   bias device fp32 [N] added in CE_GEMM_F32_STORE mode, or NULL.
- * Base pointers 16-byte aligned and lda/ldb multiples of 8 (TMA rules),
- * else CE_ERR_INVALID_ARG.
+ * Base pointers (A, B and bias) 16-byte aligned and lda/ldb multiples of 8
+ * (TMA rules), else CE_ERR_INVALID_ARG.
  */
 ce_status ce_gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t lda, int32_t a_mn_major,
                        const void *B, int64_t ldb, int32_t b_mn_major, int32_t out_kind, void *D,
                        int64_t ldd, const float *bias, void *stream);
 
-/* ce_params.variant of flce_fwd_bwd: 0 compacts the valid rows first (the
- * default), CE_FLCE_DENSE runs every row through every GEMM. */
+/* ce_params.variant of flce_fwd_bwd (bits, 0 = the defaults):
+ * CE_FLCE_DENSE runs every row through every GEMM instead of compacting the
+ * valid rows first; CE_FLCE_CE_CLUSTER runs each chunk's cross-entropy with
+ * the cluster kernel (row held in shared memory) instead of the default:
+ * row statistics formed in the logits GEMM's epilogue, then one streaming
+ * map from the fp32 logits to dZ. */
 #define CE_FLCE_DENSE 1
+#define CE_FLCE_CE_CLUSTER 2
 
 /* Workspace bytes of flce_fwd_bwd for these sizes (the fp32 logits chunk,
  * the bf16 logits-gradient chunk and the cross-entropy workspace; with
@@ -312,11 +317,11 @@ ce_status flce_workspace_size(const ce_params *p, int64_t hidden_dim, int64_t ch
  * Fused-linear cross-entropy forward and backward.
  *   p            n_rows = BT, vocab = V, dtype = CE_DT_BF16 (hidden and
  *                weight), ignore_index, class_weight, label_smoothing,
- *                reduction; variant 0 or CE_FLCE_DENSE (else
- *                CE_ERR_INVALID_ARG); ld is ignored.
+ *                reduction; variant a combination of the CE_FLCE_*
+ *                bits (else CE_ERR_INVALID_ARG); ld is ignored.
  *   hidden       device bf16 [BT, H] row-major.
  *   weight       device bf16 [V, H] row-major (the lm head).
- *   bias         device fp32 [V] or NULL.
+ *   bias         device fp32 [V] (16-byte aligned) or NULL.
  *   target       device [BT] int64 / int32.
  *   loss         device fp32 [1] (mean/sum) or [BT] (none).
  *   grad_output  device fp32 [1] / [BT] or NULL for 1.0, applied to dZ.

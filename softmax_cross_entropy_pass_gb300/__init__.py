@@ -374,13 +374,18 @@ def ce_gemm_bf16(A, B, *, a_mn_major=False, b_mn_major=False, out=None, out_kind
     return out
 
 
-CE_FLCE_DENSE = 1
+CE_FLCE_DENSE, CE_FLCE_CE_CLUSTER = 1, 2
 
 
-def flce_workspace_size(n_rows: int, hidden: int, vocab: int, chunk_rows: int, dense: bool = False) -> int:
+def _flce_variant(dense: bool, ce_cluster: bool) -> int:
+    return (CE_FLCE_DENSE if dense else 0) | (CE_FLCE_CE_CLUSTER if ce_cluster else 0)
+
+
+def flce_workspace_size(n_rows: int, hidden: int, vocab: int, chunk_rows: int, dense: bool = False,
+                        ce_cluster: bool = False) -> int:
     p = ce_params()
     p.n_rows, p.vocab, p.ld, p.dtype = n_rows, vocab, vocab, CE_DT[torch.bfloat16]
-    p.variant = CE_FLCE_DENSE if dense else 0
+    p.variant = _flce_variant(dense, ce_cluster)
     out = ctypes.c_size_t()
     _check(_lib.flce_workspace_size(ctypes.byref(p), hidden, chunk_rows, ctypes.byref(out)), "flce_workspace_size")
     return out.value
@@ -388,10 +393,13 @@ def flce_workspace_size(n_rows: int, hidden: int, vocab: int, chunk_rows: int, d
 
 def flce_fwd_bwd(hidden, weight, target, *, bias=None, class_weight=None, ignore_index=-100,
                  label_smoothing=0.0, reduction="mean", grad_output=None, chunk_rows=4096, loss=None,
-                 grad_hidden=None, grad_weight=None, grad_bias=None, ws=None, stream=None, dense=False):
+                 grad_hidden=None, grad_weight=None, grad_bias=None, ws=None, stream=None, dense=False,
+                 ce_cluster=False):
     """Fused-linear cross-entropy: returns (loss, grad_hidden [BT, H] bf16,
     grad_weight [V, H] fp32, grad_bias [V] fp32 or None). ``dense=True``
-    runs every row through the GEMMs instead of skipping ignored rows."""
+    runs every row through the GEMMs instead of skipping ignored rows;
+    ``ce_cluster=True`` runs each chunk's cross-entropy with the cluster
+    kernel instead of the GEMM-epilogue statistics and the streaming map."""
     _check_dev(hidden, weight, target, bias, class_weight, grad_output)
     BT, H = hidden.shape
     V = weight.shape[0]
@@ -403,7 +411,7 @@ def flce_fwd_bwd(hidden, weight, target, *, bias=None, class_weight=None, ignore
     p.dtype = CE_DT[torch.bfloat16]
     p.reduction = CE_RED[reduction]
     p.target_is_int32 = 1 if target.dtype == torch.int32 else 0
-    p.variant = CE_FLCE_DENSE if dense else 0
+    p.variant = _flce_variant(dense, ce_cluster)
     dev = hidden.device
     if loss is None:
         loss = torch.empty(BT if reduction == "none" else 1, dtype=torch.float32, device=dev)
@@ -414,7 +422,8 @@ def flce_fwd_bwd(hidden, weight, target, *, bias=None, class_weight=None, ignore
     if bias is not None and grad_bias is None:
         grad_bias = torch.empty(V, dtype=torch.float32, device=dev)
     if ws is None:
-        ws = torch.empty(flce_workspace_size(BT, H, V, chunk_rows, dense), dtype=torch.uint8, device=dev)
+        ws = torch.empty(flce_workspace_size(BT, H, V, chunk_rows, dense, ce_cluster), dtype=torch.uint8,
+                         device=dev)
     _check(_lib.flce_fwd_bwd(ctypes.byref(p), H, _ptr(hidden), _ptr(weight), _ptr(bias), _ptr(target), _ptr(loss),
                              _ptr(grad_output), _ptr(grad_hidden), _ptr(grad_weight), _ptr(grad_bias), chunk_rows,
                              _ptr(ws), ws.numel(), _stream(stream)), "flce_fwd_bwd")

@@ -30,6 +30,7 @@
 namespace ce {
 
 constexpr int GB_M = 128, GB_N = 256, GB_K = 64, GB_STAGES = 4;
+static_assert(GB_N == kGemmTileN, "the row statistics are kept per 256-column tile");
 constexpr int GB_A_BYTES = GB_M * GB_K * 2;  // 16 KB
 constexpr int GB_B_BYTES = GB_N * GB_K * 2;  // 32 KB
 constexpr int GB_THREADS = 192;
@@ -55,6 +56,15 @@ struct GemmArgs {
     const int *dyn_count;
     int dyn_off, dyn_dim;
     const int *row_map;    // output row r is stored at row row_map[r] (NULL: r)
+    // Row statistics of the fp32 output (logits GEMM of the fused-linear
+    // path): per row and column tile, the running softmax state of the tile's
+    // columns {max m, exp-sum s without the target column, smoothing sum r,
+    // weight sum n}, stored at part[row * tiles_n + tile].
+    float4 *part;
+    const void *st_target;
+    int st_tgt32;
+    int64_t st_ignore;
+    const float *st_weight;
 };
 
 __device__ inline void tile_coords(const GemmArgs &g, int t, int &tm, int &tn) {
@@ -117,6 +127,60 @@ __device__ inline void epilogue_store(const GemmArgs &g, int row, int orow, int 
     }
 }
 
+// Statistics epilogue: store 32 fp32 logits (+ bias) of one row and fold
+// them into the row's softmax state over the current column tile. `skip` is
+// the target's position among the 32 columns (-1: not among them). SMODE 0:
+// no smoothing sums; 1: sum of the logits; 2: class-weighted sum.
+template <int SMODE>
+__device__ inline void epilogue_stats(const GemmArgs &g, int row, int col0, const uint32_t (&v)[32], RowState &st,
+                                      int skip) {
+    const int nv = g.N - col0;
+    if (nv <= 0) return;
+    float x[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) x[j] = __uint_as_float(v[j]);
+    float *o = reinterpret_cast<float *>(g.out) + static_cast<int64_t>(row) * g.ldo + col0;
+    if (nv >= 32 && (g.ldo % 4) == 0) {
+        if (g.bias) {
+            const float4 *b4 = reinterpret_cast<const float4 *>(g.bias + col0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 bb = __ldg(b4 + q);
+                x[4 * q] += bb.x; x[4 * q + 1] += bb.y; x[4 * q + 2] += bb.z; x[4 * q + 3] += bb.w;
+            }
+        }
+        float4 *o4 = reinterpret_cast<float4 *>(o);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) o4[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+        float vmax = x[0];
+#pragma unroll
+        for (int j = 1; j < 32; ++j) vmax = fmaxf(vmax, x[j]);
+        float w[32];
+        if (SMODE == 2) {
+            const float4 *w4 = reinterpret_cast<const float4 *>(g.st_weight + col0);
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const float4 ww = __ldg(w4 + q);
+                w[4 * q] = ww.x; w[4 * q + 1] = ww.y; w[4 * q + 2] = ww.z; w[4 * q + 3] = ww.w;
+            }
+        }
+        row_state_add<32, SMODE != 0>(st, x, vmax, skip, SMODE == 2 ? w : nullptr);
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            if (j < nv) {
+                float xv = x[j] + (g.bias ? __ldg(g.bias + col0 + j) : 0.f);
+                o[j] = xv;
+                float wj = SMODE == 2 ? __ldg(g.st_weight + col0 + j) : 1.f;
+                row_state_add<1, SMODE != 0>(st, &xv, xv, skip == j ? 0 : -1, SMODE == 2 ? &wj : nullptr);
+            }
+        }
+    }
+}
+
+// EPI 0: the plain epilogue (epilogue_store); 1..3: fp32 store with row
+// statistics (epilogue_stats, smoothing mode EPI - 1).
+template <int EPI>
 __global__ void __launch_bounds__(GB_THREADS, 1)
 flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
     if (g.dyn_count) {
@@ -239,13 +303,26 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int row = tm * GB_M + q * 32 + lane;
             const int orow = (g.row_map && row < g.M) ? __ldg(g.row_map + row) : row;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * GB_N;
+            RowState st = row_state_empty();
+            int y_rel = -(1 << 30);   // target column relative to the tile (none: far outside)
+            if (EPI != 0 && row < g.M) {
+                const int64_t y = load_target(g.st_target, g.st_tgt32, row);
+                if (target_valid(y, g.st_ignore, g.N)) y_rel = static_cast<int>(y - static_cast<int64_t>(tn) * GB_N);
+            }
 #pragma unroll 1
             for (int c0 = 0; c0 < GB_N; c0 += 32) {
                 uint32_t v[32];
                 tmem_ld_32x32b_x32(taddr + c0, v);
                 tmem_ld_wait();
-                epilogue_store(g, row, orow, tn * GB_N + c0, v);
+                if (EPI == 0) {
+                    epilogue_store(g, row, orow, tn * GB_N + c0, v);
+                } else if (row < g.M) {
+                    const int skip = (static_cast<unsigned>(y_rel - c0) < 32u) ? y_rel - c0 : -1;
+                    epilogue_stats<(EPI > 0 ? EPI - 1 : 0)>(g, row, tn * GB_N + c0, v, st, skip);
+                }
             }
+            if (EPI != 0 && row < g.M)
+                g.part[static_cast<int64_t>(row) * g.tiles_n + tn] = make_float4(st.m, st.s, st.r, st.n);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
@@ -365,6 +442,152 @@ __global__ void flce_scatter_loss_kernel(const int *pos, const float *row_loss_c
     loss[i] = k >= 0 ? __ldg(row_loss_c + k) : 0.f;
 }
 
+// ------------------------------------------------------------------ cross-entropy on a logits chunk
+// The rows a chunk kernel handles: all n rows, or with a device-side count
+// only min(n, round_up(max(0, *count - off), 64)) (the rows past the count
+// in that 64-row block carry ignored targets and become zero rows, which the
+// grad_weight GEMM's 64-row K steps then read).
+__device__ inline int64_t chunk_rows_64(int64_t n, const int *count, int64_t off) {
+    if (!count) return n;
+    const int64_t left = static_cast<int64_t>(__ldg(count)) - off;
+    const int64_t blk = left > 0 ? (left + 63) / 64 * 64 : 0;
+    return blk < n ? blk : n;
+}
+
+// What the map kernel needs of one row (32 bytes): p = 2^((z - m) log2e +
+// neg_log2d), gradient a p - b w_c off the target, dxy at the target column
+// y; y = -1 marks a row whose gradient is all zeros.
+struct MapRow {
+    float neg_log2d, m, a, b;
+    float dxy;
+    int y;
+    float pad0, pad1;
+};
+static_assert(sizeof(MapRow) == 32, "two 16-byte loads per row");
+
+struct ChunkArgs {
+    const float *z;            // logits chunk [n_rows, ldz] fp32
+    int64_t ldz;
+    const float4 *part;        // [n_rows, tiles] partial row states of the logits GEMM
+    int tiles;
+    int64_t n_rows, vocab;
+    const void *target;
+    int tgt32;
+    int64_t ignore_index;
+    const float *weight;
+    float eps;
+    int reduction;
+    const float *grad_output;  // [1], or [n_rows] for none, or NULL
+    float *loss;               // reduction none: [n_rows]
+    float *row_loss;           // mean / sum: [n_rows]
+    const WsCtl *ctl;
+    MapRow *rows;
+    __nv_bfloat16 *out;        // dZ [n_rows, ld_out] bf16
+    int64_t ld_out;
+    const int *row_limit;
+    int64_t row_limit_off;
+};
+
+// One warp per row: merge the row's tile states, read x_y from the logits,
+// form the loss and the gradient scalars.
+__global__ void __launch_bounds__(256) flce_row_scalars_kernel(ChunkArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t n = chunk_rows_64(a.n_rows, a.row_limit, a.row_limit_off);
+    const int64_t V = a.vocab;
+    const float inv_v = 1.f / static_cast<float>(V);
+    for (int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + warp; row < n; row += static_cast<int64_t>(gridDim.x) * 8) {
+        const int64_t t = load_target(a.target, a.tgt32, row);
+        const bool valid = target_valid(t, a.ignore_index, V);
+        RowState st = row_state_empty();
+        if (valid) {
+            const float4 *pp = a.part + row * a.tiles;
+            for (int j = lane; j < a.tiles; j += 32) {
+                const float4 q = __ldg(pp + j);
+                st = row_state_merge(st, RowState{q.x, q.y, q.z, q.w});
+            }
+            st = warp_merge(st);
+        }
+        if (lane != 0) continue;
+        MapRow mr{};
+        float loss = 0.f;
+        mr.y = -1;
+        if (valid) {
+            const float xy = __ldg(a.z + row * a.ldz + t);
+            const float w_all = a.ctl->w_all, w_y_sum = a.ctl->w_y;
+            const float wy = a.weight ? __ldg(a.weight + t) : 1.f;
+            const float g = a.grad_output ? __ldg(a.grad_output + (a.reduction == CE_RED_NONE ? row : 0)) : 1.f;
+            float scale = g;
+            if (a.reduction == CE_RED_MEAN) scale = (w_y_sum != 0.f) ? g / w_y_sum : 0.f;
+            const float rrel = row_state_rel_sum(st);
+            const RowScalars rs = make_row_scalars(st.m, st.s, xy, rrel, true, t, wy, w_all, a.eps, inv_v, scale);
+            loss = make_row_scalars(st.m, st.s, xy, rrel, true, t, wy, w_all, a.eps, inv_v, 1.f).loss;
+            mr.neg_log2d = rs.neg_log2d; mr.m = rs.m; mr.a = rs.a; mr.b = rs.b; mr.dxy = rs.dxy;
+            mr.y = static_cast<int>(t);
+        }
+        a.rows[row] = mr;
+        if (a.reduction == CE_RED_NONE) a.loss[row] = loss;
+        else a.row_loss[row] = loss;
+    }
+}
+
+// dZ = the gradient of every element, rounded once to bf16: a flat map over
+// the chunk's 8-element vectors (every thread two vectors per step), logits
+// read once with streaming loads, dZ written with streaming stores.
+template <bool WEIGHTED>
+__device__ inline uint4 map_vec(const ChunkArgs &a, uint32_t row, uint32_t col, const MapRow &mr, const uint4 &u0,
+                                const uint4 &u1) {
+    float x[8] = {__uint_as_float(u0.x), __uint_as_float(u0.y), __uint_as_float(u0.z), __uint_as_float(u0.w),
+                  __uint_as_float(u1.x), __uint_as_float(u1.y), __uint_as_float(u1.z), __uint_as_float(u1.w)};
+    float w[8];
+    if (WEIGHTED) {
+        const float4 w0 = __ldg(reinterpret_cast<const float4 *>(a.weight + col));
+        const float4 w1 = __ldg(reinterpret_cast<const float4 *>(a.weight + col) + 1);
+        w[0] = w0.x; w[1] = w0.y; w[2] = w0.z; w[3] = w0.w; w[4] = w1.x; w[5] = w1.y; w[6] = w1.z; w[7] = w1.w;
+    }
+    RowScalars rs;
+    rs.neg_log2d = mr.neg_log2d; rs.m = mr.m; rs.a = mr.a; rs.b = mr.b;
+    const int yr = mr.y - static_cast<int>(col);
+    float gr[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        gr[e] = grad_elem(rs, x[e], WEIGHTED ? w[e] : 1.f);
+        gr[e] = (e == yr) ? mr.dxy : gr[e];
+    }
+    return Fmt<CE_DT_BF16>::pack(gr);
+}
+
+template <bool WEIGHTED>
+__global__ void __launch_bounds__(256) flce_map_kernel(ChunkArgs a) {
+    const int64_t n = chunk_rows_64(a.n_rows, a.row_limit, a.row_limit_off);
+    const uint32_t vpr = static_cast<uint32_t>(a.vocab / 8);
+    const uint32_t total = static_cast<uint32_t>(n) * vpr;   // < 2^31 (host check)
+    const uint32_t stride = gridDim.x * blockDim.x;
+    const uint4 zero = make_uint4(0u, 0u, 0u, 0u);
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < total; i += 2u * stride) {
+        const uint32_t i1 = i + stride;
+        const bool has1 = i1 < total;
+        const uint32_t r0 = i / vpr, c0 = (i - r0 * vpr) * 8u;
+        const uint32_t r1 = has1 ? i1 / vpr : r0, c1 = has1 ? (i1 - r1 * vpr) * 8u : c0;
+        const float4 *m0p = reinterpret_cast<const float4 *>(a.rows + r0);
+        const float4 *m1p = reinterpret_cast<const float4 *>(a.rows + r1);
+        const float4 p0a = __ldg(m0p), p0b = __ldg(m0p + 1);
+        const float4 p1a = __ldg(m1p), p1b = __ldg(m1p + 1);
+        const MapRow mr0{p0a.x, p0a.y, p0a.z, p0a.w, p0b.x, __float_as_int(p0b.y), 0.f, 0.f};
+        const MapRow mr1{p1a.x, p1a.y, p1a.z, p1a.w, p1b.x, __float_as_int(p1b.y), 0.f, 0.f};
+        const float *z0 = a.z + static_cast<int64_t>(r0) * a.ldz + c0;
+        const float *z1 = a.z + static_cast<int64_t>(r1) * a.ldz + c1;
+        uint4 u00 = zero, u01 = zero, u10 = zero, u11 = zero;
+        if (mr0.y >= 0) { u00 = ld_stream_ro(z0); u01 = ld_stream_ro(z0 + 4); }
+        if (has1 && mr1.y >= 0) { u10 = ld_stream_ro(z1); u11 = ld_stream_ro(z1 + 4); }
+        const uint4 o0 = mr0.y >= 0 ? map_vec<WEIGHTED>(a, r0, c0, mr0, u00, u01) : zero;
+        st_stream(a.out + static_cast<int64_t>(r0) * a.ld_out + c0, o0);
+        if (has1) {
+            const uint4 o1 = mr1.y >= 0 ? map_vec<WEIGHTED>(a, r1, c1, mr1, u10, u11) : zero;
+            st_stream(a.out + static_cast<int64_t>(r1) * a.ld_out + c1, o1);
+        }
+    }
+}
+
 // loss[0] = sum of the row losses (/ W_y for mean), fixed order, fp64; with
 // `count`, only the first *count row losses (the compacted rows).
 __global__ void __launch_bounds__(256) flce_reduce_kernel(const float *row_loss, int64_t n0, int reduction,
@@ -432,8 +655,9 @@ static int sm_count() {
 // memory [K, M] (lda >= M). B: K-major = memory [N, K]; MN-major = memory [K, N].
 cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B, int64_t ldb,
                       int b_mn, int out_kind, void *out, int64_t ldo, const float *bias, unsigned int *status,
-                      cudaStream_t s, const GemmDyn *dyn) {
+                      cudaStream_t s, const GemmDyn *dyn, const GemmStats *stats) {
     if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
+    if (stats && out_kind != OUT_F32_STORE) return cudaErrorInvalidValue;
     CUtensorMap ta, tb;
     cudaError_t e;
     if (!a_mn) e = make_tmap(&ta, A, M, K, lda, GB_K, GB_M);
@@ -456,18 +680,35 @@ cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn,
         g.dyn_dim = dyn->dim;
         g.row_map = dyn->row_map;
     }
-    static bool attr_set = false;
-    if (!attr_set) {
-        e = cudaFuncSetAttribute(reinterpret_cast<const void *>(&flce_gemm_kernel),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(GB_SMEM));
+    int epi = 0;
+    if (stats) {
+        g.part = stats->part;
+        g.st_target = stats->target;
+        g.st_tgt32 = stats->tgt32;
+        g.st_ignore = stats->ignore_index;
+        g.st_weight = stats->weight;
+        epi = 1 + stats->smooth_mode;
+        if (stats->smooth_mode < 0 || stats->smooth_mode > 2 || (stats->smooth_mode == 2 && !stats->weight))
+            return cudaErrorInvalidValue;
+    }
+    static const void *const kernels[4] = {
+        reinterpret_cast<const void *>(&flce_gemm_kernel<0>), reinterpret_cast<const void *>(&flce_gemm_kernel<1>),
+        reinterpret_cast<const void *>(&flce_gemm_kernel<2>), reinterpret_cast<const void *>(&flce_gemm_kernel<3>)};
+    // the shared-memory limit is a per-device attribute of each kernel: set it once per device
+    static uint64_t attr_set[4] = {};
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
+    if (!bit || !(attr_set[epi] & bit)) {
+        e = cudaFuncSetAttribute(kernels[epi], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(GB_SMEM));
         if (e != cudaSuccess) return e;
-        attr_set = true;
+        attr_set[epi] |= bit;
     }
     const int tiles = g.tiles_m * g.tiles_n;
     const int grid = tiles < sm_count() ? tiles : sm_count();
     void *args[] = {&ta, &tb, &g};
-    return cudaLaunchKernel(reinterpret_cast<const void *>(&flce_gemm_kernel), dim3(grid), dim3(GB_THREADS), args,
-                            GB_SMEM, s);
+    return cudaLaunchKernel(kernels[epi], dim3(grid), dim3(GB_THREADS), args, GB_SMEM, s);
 }
 
 }  // namespace ce
@@ -487,9 +728,12 @@ struct FlceLayout {
     // ignored-row compaction: compacted hidden rows, the maps, the compacted
     // targets and per-row grad_output, the valid-row count
     size_t hc_off, idx_off, pos_off, tgt_off, gc_off, cnt_off;
+    // statistics path: the logits GEMM's per-tile row states and the per-row map scalars
+    size_t part_off, rows_off;
+    int tiles;
 };
 
-FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk, int64_t hidden, bool compact) {
+FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk, int64_t hidden, bool compact, bool map_ce) {
     FlceLayout L{};
     L.ce_ws = round_up(static_cast<int64_t>(ws_bytes(n_rows)), 1024);
     L.ldz = round_up(vocab, 4);
@@ -506,10 +750,23 @@ FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk, int64_t hid
         L.cnt_off = L.gc_off + round_up(n_rows * 4, 256);
         L.total = L.cnt_off + 256;
     }
+    if (map_ce) {
+        L.tiles = static_cast<int>((vocab + kGemmTileN - 1) / kGemmTileN);
+        L.part_off = L.total;
+        L.rows_off = L.part_off + round_up(chunk * L.tiles * 16, 1024);
+        L.total = L.rows_off + round_up(chunk * static_cast<int64_t>(sizeof(MapRow)), 1024);
+    }
     return L;
 }
 
 bool flce_compacts(const ce_params *p) { return (p->variant & CE_FLCE_DENSE) == 0; }
+
+// The cross-entropy of each chunk runs as the logits GEMM's statistics
+// epilogue + a row-scalar kernel + a flat map, unless the caller asks for
+// the cluster kernel or the chunk has 2^31 or more 8-element vectors.
+bool flce_maps(const ce_params *p, int64_t chunk) {
+    return (p->variant & CE_FLCE_CE_CLUSTER) == 0 && chunk * (p->vocab / 8) < (static_cast<int64_t>(1) << 31);
+}
 
 ce_status flce_cuda_fail(cudaError_t e) {
     (void)cudaGetLastError();
@@ -529,7 +786,7 @@ ce_status ce_gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t l
     if (M == 0 || N == 0) return CE_OK;
     if (!A || !B || !D || !al16(A) || !al16(B)) return CE_ERR_INVALID_ARG;
     if ((lda % 8) || (ldb % 8) || lda < (a_mn ? M : K) || ldb < (b_mn ? N : K) || ldd < N) return CE_ERR_INVALID_ARG;
-    if (bias && out_kind != CE_GEMM_F32_STORE) return CE_ERR_INVALID_ARG;
+    if (bias && (out_kind != CE_GEMM_F32_STORE || !al16(bias))) return CE_ERR_INVALID_ARG;
     if (K == 0) return CE_ERR_UNSUPPORTED;
     cudaError_t e = gemm_bf16(static_cast<int>(M), static_cast<int>(N), static_cast<int>(K), A, lda, a_mn, B, ldb,
                               b_mn, out_kind, D, ldd, bias, nullptr, reinterpret_cast<cudaStream_t>(stream));
@@ -539,7 +796,7 @@ ce_status ce_gemm_bf16(int64_t M, int64_t N, int64_t K, const void *A, int64_t l
 ce_status flce_workspace_size(const ce_params *p, int64_t hidden_dim, int64_t chunk_rows, size_t *bytes) {
     if (!p || !bytes || p->n_rows < 0 || p->vocab < 1 || hidden_dim < 1 || chunk_rows < 1) return CE_ERR_INVALID_ARG;
     int64_t chunk = chunk_rows < p->n_rows ? chunk_rows : (p->n_rows > 0 ? p->n_rows : 1);
-    *bytes = flce_layout(p->n_rows, p->vocab, chunk, hidden_dim, flce_compacts(p)).total;
+    *bytes = flce_layout(p->n_rows, p->vocab, chunk, hidden_dim, flce_compacts(p), flce_maps(p, chunk)).total;
     return CE_OK;
 }
 
@@ -555,13 +812,15 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
     if (p->target_is_int32 != 0 && p->target_is_int32 != 1) return CE_ERR_INVALID_ARG;
     if (p->class_weight && (reinterpret_cast<uintptr_t>(p->class_weight) & 15u)) return CE_ERR_INVALID_ARG;
     if (p->softcap != 0.f || p->z_loss != 0.f || p->accuracy) return CE_ERR_UNSUPPORTED;
-    if ((p->variant & ~CE_FLCE_DENSE) != 0) return CE_ERR_INVALID_ARG;
+    if ((p->variant & ~(CE_FLCE_DENSE | CE_FLCE_CE_CLUSTER)) != 0) return CE_ERR_INVALID_ARG;
+    if (bias && !al16(bias)) return CE_ERR_INVALID_ARG;
     if (!loss || !ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CE_ERR_INVALID_ARG;
     const int64_t BT = p->n_rows, V = p->vocab;
     if (BT > INT32_MAX || V > INT32_MAX || H > INT32_MAX) return CE_ERR_UNSUPPORTED;
     const int64_t C = chunk_rows < BT ? chunk_rows : (BT > 0 ? BT : 1);
     const bool compact = flce_compacts(p);
-    const FlceLayout L = flce_layout(BT, V, C, H, compact);
+    const bool map_ce = flce_maps(p, C);
+    const FlceLayout L = flce_layout(BT, V, C, H, compact, map_ce);
     if (ws_bytes < L.total) return CE_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (BT > 0 && (!hidden || !weight || !target || !grad_hidden || !grad_weight)) return CE_ERR_INVALID_ARG;
@@ -593,9 +852,11 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
     }
     const int mode = p->label_smoothing <= 0.f ? 0 : (p->class_weight ? 2 : 1);
     FusedPlan plan{};
-    bool ok = false;
-    if ((e = fused_plan_f32_to_bf16(mode, C, V, &plan, &ok)) != cudaSuccess) return flce_cuda_fail(e);
-    if (!ok) return CE_ERR_UNSUPPORTED;
+    if (!map_ce) {
+        bool ok = false;
+        if ((e = fused_plan_f32_to_bf16(mode, C, V, &plan, &ok)) != cudaSuccess) return flce_cuda_fail(e);
+        if (!ok) return CE_ERR_UNSUPPORTED;
+    }
 
     // Rows whose target is ignored (or out of range) add nothing to the loss
     // or to grad_weight and have a zero grad_hidden row. With compaction the
@@ -655,25 +916,57 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
         const GemmDyn rows_m{count, static_cast<int>(r0), 0, nullptr};
         const GemmDyn rows_k{count, static_cast<int>(r0), 1, nullptr};
         const GemmDyn rows_out{count, static_cast<int>(r0), 0, idx ? idx + r0 : nullptr};
-        // Z = h_c W^T (+ b), fp32
-        e = gemm_bf16(static_cast<int>(c), static_cast<int>(V), static_cast<int>(H), h_c, H, 0, weight, H, 0,
-                      0, Z, L.ldz, bias, &ctl->status, s, compact ? &rows_m : nullptr);
-        if (e != cudaSuccess) return flce_cuda_fail(e);
-        // cross-entropy forward + backward on the chunk: dZ (bf16) and row losses
-        FusedArgs a{};
-        a.x = Z; a.n_rows = c; a.vocab = V; a.ld = L.ldz;
-        a.target = reinterpret_cast<const char *>(tgt_src) + r0 * tgt_bytes;
-        a.tgt32 = tgt32; a.reduction = p->reduction; a.ignore_index = p->ignore_index;
-        a.weight = p->class_weight; a.eps = p->label_smoothing;
-        a.grad_output = g_rows ? (none ? g_rows + r0 : g_rows) : nullptr;
-        a.loss = none ? loss_rows + r0 : loss;
-        a.row_loss = row_loss + r0;
-        a.ctl = ctl;
-        a.out = dZ; a.ld_out = L.ldd; a.finalize = 0;
-        a.row_limit = count; a.row_limit_off = r0;
-        FusedPlan pl = plan;
-        if (pl.n_clusters > c) pl.n_clusters = static_cast<int>(c);
-        if ((e = launch_fused_f32_to_bf16(a, pl, mode, s)) != cudaSuccess) return flce_cuda_fail(e);
+        const void *tgt_chunk = reinterpret_cast<const char *>(tgt_src) + r0 * tgt_bytes;
+        if (map_ce) {
+            // Z = h_c W^T (+ b), fp32, with the per-tile row states; then the
+            // row scalars and the flat map to dZ (bf16) and the row losses
+            float4 *part = reinterpret_cast<float4 *>(wsb + L.part_off);
+            const GemmStats gs{part, tgt_chunk, tgt32, p->ignore_index, mode, p->class_weight};
+            e = gemm_bf16(static_cast<int>(c), static_cast<int>(V), static_cast<int>(H), h_c, H, 0, weight, H, 0,
+                          0, Z, L.ldz, bias, &ctl->status, s, compact ? &rows_m : nullptr, &gs);
+            if (e != cudaSuccess) return flce_cuda_fail(e);
+            ChunkArgs ca{};
+            ca.z = Z; ca.ldz = L.ldz; ca.part = part; ca.tiles = L.tiles;
+            ca.n_rows = c; ca.vocab = V; ca.target = tgt_chunk; ca.tgt32 = tgt32; ca.ignore_index = p->ignore_index;
+            ca.weight = p->class_weight; ca.eps = p->label_smoothing; ca.reduction = p->reduction;
+            ca.grad_output = g_rows ? (none ? g_rows + r0 : g_rows) : nullptr;
+            ca.loss = none ? loss_rows + r0 : loss;
+            ca.row_loss = row_loss + r0;
+            ca.ctl = ctl;
+            ca.rows = reinterpret_cast<MapRow *>(wsb + L.rows_off);
+            ca.out = dZ; ca.ld_out = L.ldd;
+            ca.row_limit = count; ca.row_limit_off = r0;
+            void *cargs[] = {&ca};
+            const int64_t want = static_cast<int64_t>(sm_count()) * 8;
+            const int64_t sblk = (c + 7) / 8;
+            e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_row_scalars_kernel),
+                                 dim3(static_cast<unsigned>(sblk < want ? sblk : want)), dim3(256), cargs, 0, s);
+            if (e != cudaSuccess) return flce_cuda_fail(e);
+            const void *mk = mode == 2 ? reinterpret_cast<const void *>(&flce_map_kernel<true>)
+                                              : reinterpret_cast<const void *>(&flce_map_kernel<false>);
+            e = cudaLaunchKernel(mk, dim3(static_cast<unsigned>(want)), dim3(256), cargs, 0, s);
+            if (e != cudaSuccess) return flce_cuda_fail(e);
+        } else {
+            // Z = h_c W^T (+ b), fp32
+            e = gemm_bf16(static_cast<int>(c), static_cast<int>(V), static_cast<int>(H), h_c, H, 0, weight, H, 0,
+                          0, Z, L.ldz, bias, &ctl->status, s, compact ? &rows_m : nullptr);
+            if (e != cudaSuccess) return flce_cuda_fail(e);
+            // cross-entropy forward + backward on the chunk: dZ (bf16) and row losses
+            FusedArgs a{};
+            a.x = Z; a.n_rows = c; a.vocab = V; a.ld = L.ldz;
+            a.target = tgt_chunk;
+            a.tgt32 = tgt32; a.reduction = p->reduction; a.ignore_index = p->ignore_index;
+            a.weight = p->class_weight; a.eps = p->label_smoothing;
+            a.grad_output = g_rows ? (none ? g_rows + r0 : g_rows) : nullptr;
+            a.loss = none ? loss_rows + r0 : loss;
+            a.row_loss = row_loss + r0;
+            a.ctl = ctl;
+            a.out = dZ; a.ld_out = L.ldd; a.finalize = 0;
+            a.row_limit = count; a.row_limit_off = r0;
+            FusedPlan pl = plan;
+            if (pl.n_clusters > c) pl.n_clusters = static_cast<int>(c);
+            if ((e = launch_fused_f32_to_bf16(a, pl, mode, s)) != cudaSuccess) return flce_cuda_fail(e);
+        }
         // grad_hidden rows = dZ W   (A = dZ K-major, B = W stored [V, H] = [K, N]: MN-major);
         // compacted rows are stored back at their own rows
         void *gh = compact ? grad_hidden : reinterpret_cast<char *>(grad_hidden) + r0 * H * 2;

@@ -21,8 +21,24 @@ struct GemmDyn {
     const int *row_map;
 };
 
+// `stats` (optional, fp32 store only) also writes, for every output row and
+// 256-column tile, the tile's softmax state {max, exp-sum without the
+// row's target column, smoothing sum, weight sum} to part[row * tiles + t]
+// (tiles = ceil(N / 256)); smooth_mode 0: no smoothing sums, 1: plain sum
+// of the logits, 2: class-weighted (weight[N]).
+struct GemmStats {
+    float4 *part;
+    const void *target;
+    int tgt32;
+    int64_t ignore_index;
+    int smooth_mode;
+    const float *weight;
+};
+constexpr int kGemmTileN = 256;
+
 cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B,
                       int64_t ldb, int b_mn, int out_kind, void *out, int64_t ldo, const float *bias,
-                      unsigned int *status, cudaStream_t s, const GemmDyn *dyn = nullptr);
+                      unsigned int *status, cudaStream_t s, const GemmDyn *dyn = nullptr,
+                      const GemmStats *stats = nullptr);
 
 }  // namespace ce

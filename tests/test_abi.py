@@ -117,3 +117,35 @@ def test_automatic_path_choice_is_host_logic(lib):
     p = _params(lib, variant=lib.VARIANTS["split"])
     assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
     assert out.value == lib.VARIANTS["split"]
+
+
+def test_gemm_and_flce_argument_errors_on_host(lib):
+    """Misaligned bias pointers and unknown fused-linear variant bits are
+    refused before any CUDA call."""
+    L = lib._lib
+    fake = ctypes.c_void_p(0x100000)
+    st = L.ce_gemm_bf16(128, 256, 64, fake, 64, 0, fake, 64, 0, 0, fake, 256, ctypes.c_void_p(0x100004), None)
+    assert st == 1
+    p = lib.ce_params()
+    p.n_rows, p.vocab, p.ld, p.dtype, p.reduction, p.ignore_index = 64, 1024, 1024, 1, 1, -100
+    for variant, bias in ((4, None), (0, ctypes.c_void_p(0x100008))):
+        p.variant = variant
+        st = L.flce_fwd_bwd(ctypes.byref(p), 64, fake, fake, bias, fake, fake, None, fake, fake, fake, 64,
+                            ctypes.c_void_p(0x200000), 1 << 40, None)
+        assert st == 1, (variant, bias)
+
+
+def test_flce_workspace_by_variant(lib):
+    """The compacted path adds a copy of hidden (BT x H bf16) and a few bytes
+    per row; the statistics path adds 16 bytes per row and 256-column tile of
+    a chunk plus 32 bytes per chunk row; all stay far below the logits."""
+    BT, H, V, C = 8192, 4096, 128256, 4096
+    base = lib.flce_workspace_size(BT, H, V, C, dense=True, ce_cluster=True)
+    compact = lib.flce_workspace_size(BT, H, V, C, dense=False, ce_cluster=True)
+    stats = lib.flce_workspace_size(BT, H, V, C, dense=True, ce_cluster=False)
+    both = lib.flce_workspace_size(BT, H, V, C)
+    assert compact - base >= BT * H * 2 and compact - base <= BT * H * 2 + BT * 32 + 8192
+    tiles = (V + 255) // 256
+    assert stats - base >= C * tiles * 16 + C * 32 and stats - base <= C * tiles * 16 + C * 32 + 4096
+    assert both == base + (compact - base) + (stats - base)
+    assert base >= C * V * 6                       # fp32 logits chunk + bf16 dZ chunk

@@ -132,27 +132,35 @@ def _ignored_case(case, BT, V):
     return t, red, chunk, eps, w, go
 
 
-@pytest.mark.parametrize("dense", [False, True])
+@pytest.mark.parametrize("ce_cluster", [False, True], ids=["stats_map", "cluster"])
+@pytest.mark.parametrize("dense", [False, True], ids=["compact", "dense"])
 @pytest.mark.parametrize("case", ["mixed", "all_ignored", "mostly_ignored", "none_rows", "int32_out_of_range"])
-def test_flce_ignored_rows_against_oracle(ce, case, dense):
+def test_flce_ignored_rows_against_oracle(ce, case, dense, ce_cluster):
     """Ignored (and out-of-range) rows, with and without the device-side
-    compaction of the valid rows: every output against the fp64 oracle with
-    the dZ-rounding bound; workspace and outputs start as NaN so nothing a
-    kernel skips can leak into a result."""
+    compaction of the valid rows, and with either chunk cross-entropy (the
+    logits GEMM's row statistics + streaming map, or the cluster kernel):
+    every output against the fp64 oracle with the dZ-rounding bound;
+    workspace and outputs start as NaN so nothing a kernel skips can leak
+    into a result. V = 1000 leaves a ragged last column tile (232 columns)."""
     BT, H, V = 520, 128, 1000
     h = _rand_bf16(BT, H, seed=11)
     W = _rand_bf16(V, H, seed=12, scale=0.05)
     t, red, chunk, eps, w, go = _ignored_case(case, BT, V)
+    bias = (torch.randn(V, generator=torch.Generator().manual_seed(13)) * 0.2) if case == "mixed" else None
     dev = "cuda"
-    ws = torch.full((ce.flce_workspace_size(BT, H, V, chunk, dense),), 0xFF, dtype=torch.uint8, device=dev)
+    ws = torch.full((ce.flce_workspace_size(BT, H, V, chunk, dense, ce_cluster),), 0xFF, dtype=torch.uint8,
+                    device=dev)
     loss = torch.full((BT if red == "none" else 1,), float("nan"), device=dev)
     gh = torch.full((BT, H), float("nan"), dtype=torch.bfloat16, device=dev)
     gw = torch.full((V, H), float("nan"), device=dev)
-    out = ce.flce_fwd_bwd(h.to(dev), W.to(dev), t.to(dev), class_weight=None if w is None else w.to(dev),
+    gb = torch.full((V,), float("nan"), device=dev) if bias is not None else None
+    out = ce.flce_fwd_bwd(h.to(dev), W.to(dev), t.to(dev), bias=None if bias is None else bias.to(dev),
+                          class_weight=None if w is None else w.to(dev),
                           label_smoothing=eps, reduction=red, grad_output=None if go is None else go.to(dev),
-                          chunk_rows=chunk, loss=loss, grad_hidden=gh, grad_weight=gw, ws=ws, dense=dense)
+                          chunk_rows=chunk, loss=loss, grad_hidden=gh, grad_weight=gw, grad_bias=gb, ws=ws,
+                          dense=dense, ce_cluster=ce_cluster)
     flags = ce.ce_get_status(ws)
-    ref = oracle.flce(h, W, t, label_smoothing=eps, reduction=red, class_weight=w, grad_output=go,
+    ref = oracle.flce(h, W, t, bias=bias, label_smoothing=eps, reduction=red, class_weight=w, grad_output=go,
                       abs_sums=True)
     want_flags = (ce.CE_FLAG_TARGET_OUT_OF_RANGE if case == "int32_out_of_range" else 0) | \
         (ce.CE_FLAG_NO_VALID_ROWS if case == "all_ignored" and red == "mean" else 0)
@@ -172,6 +180,11 @@ def test_flce_ignored_rows_against_oracle(ce, case, dense):
     err_w = (gw_c - ref["grad_weight"]).abs()
     assert (err_w <= ref["grad_weight_abs"] * 2.0 ** -8 + ref["grad_weight"].abs() * 2.0 ** -20).all(), \
         f"grad_weight max err {float(err_w.max()):.3e}"
+    if bias is not None:
+        z = h.double() @ W.double().T + bias.double()
+        dz = oracle.rows(z, t, label_smoothing=eps, reduction=red, norm_wy=ref["norm_wy"], want_stats=False)["grad"]
+        err_b = (gb.double().cpu() - ref["grad_bias"]).abs()
+        assert (err_b <= dz.abs().sum(0) * 2.0 ** -8 + 1e-30).all(), f"grad_bias max err {float(err_b.max()):.3e}"
     tt = t.to(torch.int64)
     skipped = (tt < 0) | (tt >= V)
     assert torch.count_nonzero(gh_c[skipped]) == 0
