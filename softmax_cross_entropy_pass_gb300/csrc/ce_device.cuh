@@ -196,6 +196,49 @@ __device__ inline float ex2_hw(float x) {
     return y;
 }
 
+// ------------------------------------------------------------------ packed fp32 pairs
+// Two fp32 values in one 64-bit register pair, operated on by the packed
+// fp32 instructions of sm_100-class GPUs (add / sub / fma .rn.f32x2): each
+// lane is rounded exactly as the scalar instruction would round it, so a
+// loop rewritten over pairs gives bit-identical results with half the FP32
+// instructions.
+struct F2 {
+    uint64_t v;
+};
+__device__ inline F2 f2(float lo, float hi) {
+    F2 r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r.v) : "f"(lo), "f"(hi));
+    return r;
+}
+__device__ inline void f2_split(F2 a, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(a.v));
+}
+__device__ inline F2 f2_add(F2 a, F2 b) {
+    F2 r;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ inline F2 f2_sub(F2 a, F2 b) {
+    F2 r;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ inline F2 f2_mul(F2 a, F2 b) {
+    F2 r;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r.v) : "l"(a.v), "l"(b.v));
+    return r;
+}
+__device__ inline F2 f2_fma(F2 a, F2 b, F2 c) {
+    F2 r;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r.v) : "l"(a.v), "l"(b.v), "l"(c.v));
+    return r;
+}
+__device__ inline F2 f2_ex2(F2 a) {
+    float lo, hi;
+    f2_split(a, lo, hi);
+    return f2(ex2_hw(lo), ex2_hw(hi));
+}
+
 // ------------------------------------------------------------------ online softmax state
 // One thread's (or block's) running statistics over a set of columns:
 //   m = max x, s = sum exp(x - m) over non-target columns,

@@ -217,21 +217,30 @@ ce_stream_kernel(RowArgs a, int tune) {
                         st.m = cm;
                     }
                     if (st.m != -INFINITY) {
+                        // four accumulators, column j into sum j mod 4, held as two packed
+                        // pairs {0,1} {2,3}: the pair ops round each lane as the scalar ops do
                         const float mL = st.m * kLog2e;
-                        float acc[4] = {0.f, 0.f, 0.f, 0.f}, racc[4] = {0.f, 0.f, 0.f, 0.f};
+                        const F2 l2 = f2(kLog2e, kLog2e), nm = f2(-mL, -mL);
+                        F2 acc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)}, racc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
 #pragma unroll
                         for (int k = 0; k < VPT; ++k) {
                             float x[VEC];
                             F::unpack(raw[k], x);
 #pragma unroll
-                            for (int j = 0; j < VEC; ++j) {
-                                acc[j & 3] += ex2_hw(fmaf(x[j], kLog2e, -mL));
-                                if (SMOOTH) racc[j & 3] += x[j];
+                            for (int p = 0; p < VEC / 2; ++p) {
+                                const F2 xx = f2(x[2 * p], x[2 * p + 1]);
+                                acc[p & 1] = f2_add(acc[p & 1], f2_ex2(f2_fma(xx, l2, nm)));
+                                if (SMOOTH) racc[p & 1] = f2_add(racc[p & 1], xx);
                             }
                         }
-                        st.s += (acc[0] + acc[1]) + (acc[2] + acc[3]);
+                        float a0, a1, a2, a3;
+                        f2_split(acc[0], a0, a1);
+                        f2_split(acc[1], a2, a3);
+                        st.s += (a0 + a1) + (a2 + a3);
                         if (SMOOTH) {
-                            st.r += (racc[0] + racc[1]) + (racc[2] + racc[3]);
+                            f2_split(racc[0], a0, a1);
+                            f2_split(racc[1], a2, a3);
+                            st.r += (a0 + a1) + (a2 + a3);
                             st.n += static_cast<float>(VPT * VEC);
                         }
                     } else if (SMOOTH) {
@@ -331,6 +340,9 @@ ce_stream_kernel(RowArgs a, int tune) {
             }
             stream_consumer_sync<NCW>();
             const RowScalars rs = S.rs;
+            // grad_elem over packed pairs: p = 2^((x - m) log2e - log2 d), g = a p - b w
+            const F2 rs_m = f2(rs.m, rs.m), rs_l2 = f2(kLog2e, kLog2e), rs_nl = f2(rs.neg_log2d, rs.neg_log2d);
+            const F2 rs_a = f2(rs.a, rs.a), rs_nb = f2(-rs.b, -rs.b);
             // ------------------------------------------------ pass 2: gradient in place
             for (int k = 0; k < nch; ++k, ++it) {
                 const int c = reverse ? nch - 1 - k : k;
@@ -348,14 +360,18 @@ ce_stream_kernel(RowArgs a, int tune) {
 #pragma unroll
                         for (int h = 0; h < VEC / 4; ++h) {
                             const float4 w4 = __ldg(wp + h);
-                            gr[4 * h] = grad_elem(rs, x[4 * h], w4.x);
-                            gr[4 * h + 1] = grad_elem(rs, x[4 * h + 1], w4.y);
-                            gr[4 * h + 2] = grad_elem(rs, x[4 * h + 2], w4.z);
-                            gr[4 * h + 3] = grad_elem(rs, x[4 * h + 3], w4.w);
+                            const F2 nbw0 = f2_mul(rs_nb, f2(w4.x, w4.y)), nbw1 = f2_mul(rs_nb, f2(w4.z, w4.w));
+                            const F2 p0 = f2_ex2(f2_fma(f2_sub(f2(x[4 * h], x[4 * h + 1]), rs_m), rs_l2, rs_nl));
+                            const F2 p1 = f2_ex2(f2_fma(f2_sub(f2(x[4 * h + 2], x[4 * h + 3]), rs_m), rs_l2, rs_nl));
+                            f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
+                            f2_split(f2_fma(p1, rs_a, nbw1), gr[4 * h + 2], gr[4 * h + 3]);
                         }
                     } else {
 #pragma unroll
-                        for (int e = 0; e < VEC; ++e) gr[e] = grad_elem(rs, x[e], 1.f);
+                        for (int p = 0; p < VEC / 2; ++p) {
+                            const F2 pp = f2_ex2(f2_fma(f2_sub(f2(x[2 * p], x[2 * p + 1]), rs_m), rs_l2, rs_nl));
+                            f2_split(f2_fma(pp, rs_a, rs_nb), gr[2 * p], gr[2 * p + 1]);
+                        }
                     }
                     if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
 #pragma unroll
