@@ -381,9 +381,9 @@ def run_ours(args):
     import softmax_cross_entropy_pass_gb300 as ce
     from workloads import CONFIGS, make_ce_inputs
     cfg = CONFIGS[args.workload]
-    if args.rows:
+    if args.rows or args.vocab:
         import dataclasses
-        cfg = dataclasses.replace(cfg, n_rows=args.rows)
+        cfg = dataclasses.replace(cfg, n_rows=args.rows or cfg.n_rows, vocab=args.vocab or cfg.vocab)
     R, V = cfg.n_rows, cfg.vocab
     inp = make_ce_inputs(cfg, device=device)
     pristine, target, g = inp["logits"], inp["target"], inp["grad_output"]
@@ -550,6 +550,8 @@ def main():
     ap.add_argument("--flce-only", action="store_true", help="only the fused-linear measurement")
     ap.add_argument("--gemm-only", default="", help="only one GEMM: M,N,K,a_mn,b_mn")
     ap.add_argument("--rows", type=int, default=0, help="rows of a smaller case of the workload (profiling)")
+    ap.add_argument("--vocab", type=int, default=0,
+                    help="another vocabulary size for the workload (e.g. one that leaves rows unaligned)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="CE workload of workloads.CONFIGS (the default is the headline metric's)")
     ap.add_argument("--print-kernel-hash", action="store_true")

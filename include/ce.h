@@ -81,7 +81,9 @@ typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
 #define CE_VARIANT_FUSED 2  /* fused kernel; CE_ERR_UNSUPPORTED if the rows do not allow it */
 #define CE_VARIANT_ROWPASS 3 /* one kernel, each row read twice, the second read from L2 */
 #define CE_VARIANT_STREAM 4  /* as ROWPASS, the two passes streamed through a shared-memory
-                                ring by bulk copies; 16-byte aligned rows only */
+                                ring by bulk copies (any row alignment: the part of a row
+                                before its first and after its last 16-byte boundary goes
+                                through plain accesses) */
 /* bits 8..15 of variant: fused-kernel cluster size override, or CTAs per SM
  * of the row-pass and stream kernels (0 = automatic) */
 #define CE_VARIANT_CLUSTER_SHIFT 8
@@ -99,7 +101,9 @@ typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
 typedef struct ce_params {
     int64_t n_rows;             /* BT >= 0 */
     int64_t vocab;              /* V >= 1 */
-    int64_t ld;                 /* row stride of logits in elements, >= vocab */
+    int64_t ld;                 /* row stride of logits in elements, >= vocab; the logits
+                                   pointer is aligned to its element size, else
+                                   CE_ERR_INVALID_ARG (rows need no other alignment) */
     int64_t ignore_index;       /* targets equal to this are ignored (torch default -100) */
     const float *class_weight;  /* device [vocab] fp32, or NULL for all ones */
     float label_smoothing;      /* eps in [0, 1] */

@@ -148,14 +148,14 @@ bool fused_layout_ok(const ce_params *p, const void *x) {
     return true;
 }
 
-// The path of CE_VARIANT_AUTO: the one-kernel row pass (HBM read once, the
-// second read served by L2) is the fastest measured path on GB300 for every
-// row size; the split path remains for callers that ask for it.
-bool fused_layout_ok(const ce_params *p, const void *x);
-
-int auto_path(const ce_params *p, const void *x) {
+// The path of CE_VARIANT_AUTO: the stream kernel (HBM read once, the second
+// read served by L2 through a bulk-copy ring) is the fastest measured path
+// on GB300 for every row size and takes any row alignment (the unaligned
+// head and tail of a row go through plain accesses); the row pass carries
+// the options; the split path remains for callers that ask for it.
+int auto_path(const ce_params *p, const void *) {
     if (has_options(p)) return CE_VARIANT_ROWPASS;  // the options live in the row-pass and split kernels
-    return fused_layout_ok(p, x) ? CE_VARIANT_STREAM : CE_VARIANT_ROWPASS;
+    return CE_VARIANT_STREAM;
 }
 
 }  // namespace
@@ -209,6 +209,7 @@ ce_status ce_forward(const ce_params *p, const void *logits, const void *target,
     if (st != CE_OK) return st;
     if ((st = check_ws(p, ws, ws_bytes)) != CE_OK) return st;
     if (!loss || (p->n_rows > 0 && (!logits || !target))) return CE_ERR_INVALID_ARG;
+    if (!aligned(logits, elem_bytes(p->dtype))) return CE_ERR_INVALID_ARG;
     if (stats && !aligned(stats, 16)) return CE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = enqueue_prep(p, target, ws, s);
@@ -232,6 +233,7 @@ ce_status ce_backward(const ce_params *p, void *logits_inout, const void *target
     if (st != CE_OK) return st;
     if ((st = check_ws(p, ws, ws_bytes)) != CE_OK) return st;
     if (p->n_rows > 0 && (!logits_inout || !target || !stats)) return CE_ERR_INVALID_ARG;
+    if (!aligned(logits_inout, elem_bytes(p->dtype))) return CE_ERR_INVALID_ARG;
     if (stats && !aligned(stats, 16)) return CE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     cudaError_t e = enqueue_prep(p, target, ws, s);
@@ -251,6 +253,7 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
     if (st != CE_OK) return st;
     if ((st = check_ws(p, ws, ws_bytes)) != CE_OK) return st;
     if (!loss || (p->n_rows > 0 && (!logits_inout || !target))) return CE_ERR_INVALID_ARG;
+    if (!aligned(logits_inout, elem_bytes(p->dtype))) return CE_ERR_INVALID_ARG;
     int path = p->variant & 0xff;
     if (p->variant & ~(0xffff | CE_VARIANT_PREPARED | (0x1f << CE_VARIANT_TUNE_SHIFT))) return CE_ERR_INVALID_ARG;
     if (path == CE_VARIANT_AUTO) path = auto_path(p, logits_inout);
@@ -261,7 +264,6 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
 
     if ((path == CE_VARIANT_STREAM || path == CE_VARIANT_FUSED) && has_options(p)) return CE_ERR_UNSUPPORTED;
     if (path == CE_VARIANT_STREAM) {
-        if (!fused_layout_ok(p, logits_inout)) return CE_ERR_UNSUPPORTED;
         cudaError_t e = enqueue_prep(p, target, ws, s);
         if (e != cudaSuccess) return cuda_fail(e);
         if (p->n_rows == 0) {

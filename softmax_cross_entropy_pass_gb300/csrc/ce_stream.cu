@@ -84,6 +84,37 @@ __device__ inline uint64_t policy_keep() {
     return p;
 }
 
+// Where one row's slice [lo, lo + L) sits against 16-byte boundaries: the
+// head (columns before the first boundary, at most 15 bytes) and the tail
+// (after the last) are read and written with plain accesses; the interior
+// [vlo, tail0) moves with bulk copies and 16-byte vectors. Rows whose start
+// is 16-byte aligned have no head.
+struct RowGeom {
+    int64_t vlo, tail0;  // first column of the interior, first column of the tail
+    int nhead, ntail, nvec, nch;
+    int64_t bytes;       // interior bytes (a multiple of 16)
+};
+template <int KB>
+__device__ inline RowGeom row_geom(const char *slice, int64_t lo, int64_t L) {
+    RowGeom g;
+    const int64_t hb = static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(slice) & 15u)) & 15u);
+    const int64_t nh = hb / KB < L ? hb / KB : L;
+    g.nhead = static_cast<int>(nh);
+    g.vlo = lo + nh;
+    g.bytes = ((L - nh) * KB) & ~static_cast<int64_t>(15);
+    g.nvec = static_cast<int>(g.bytes / 16);
+    g.tail0 = g.vlo + g.bytes / KB;
+    g.ntail = static_cast<int>(lo + L - g.tail0);
+    g.nch = static_cast<int>((g.bytes + kStreamChunk - 1) / kStreamChunk);
+    return g;
+}
+
+// 4 class weights starting at column c (c a multiple of 4 when vec4)
+__device__ inline float4 load_w4(const float *w, int64_t c, bool vec4) {
+    if (vec4) return __ldg(reinterpret_cast<const float4 *>(w + c));
+    return make_float4(__ldg(w + c), __ldg(w + c + 1), __ldg(w + c + 2), __ldg(w + c + 3));
+}
+
 template <int DT, int MODE, int SHAPE, int CL>
 __global__ void __launch_bounds__(StreamShape<SHAPE>::kThreads, StreamShape<SHAPE>::kCtasPerSm)
 ce_stream_kernel(RowArgs a, int tune) {
@@ -113,13 +144,10 @@ ce_stream_kernel(RowArgs a, int tune) {
     const int64_t lo = rank * half;
     const int64_t hi = (lo + half < V) ? lo + half : V;
     const int64_t L = hi > lo ? hi - lo : 0;
-    const int64_t Lb16 = (L * F::kBytes) & ~static_cast<int64_t>(15);  // bytes moved by bulk copies
-    const int nvec = static_cast<int>(Lb16 / 16);
-    const int64_t tail0 = lo + Lb16 / F::kBytes;                       // first column of the scalar tail
-    const int ntail = static_cast<int>(hi - tail0);
-    const int nch = static_cast<int>((Lb16 + kStreamChunk - 1) / kStreamChunk);
     const size_t row_bytes = static_cast<size_t>(a.ld) * F::kBytes;
     char *const xbase = reinterpret_cast<char *>(a.grad);
+    // weights as float4 when the base allows it (each row's interior start decides the rest)
+    const bool w_base16 = (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
 
     if (tid == 0) {
         for (int s = 0; s < kStreamSlots; ++s) {
@@ -145,7 +173,10 @@ ce_stream_kernel(RowArgs a, int tune) {
             for (int64_t row = q0; row < a.n_rows; row += nq) {
                 const int64_t t = load_target(a.target, a.tgt32, row);
                 if (!target_valid(t, a.ignore_index, V)) continue;
-                const char *src = xbase + row * row_bytes + lo * F::kBytes;
+                const char *slice = xbase + row * row_bytes + lo * F::kBytes;
+                const RowGeom gm = row_geom<F::kBytes>(slice, lo, L);
+                const char *src = slice + static_cast<int64_t>(gm.nhead) * F::kBytes;
+                const int nch = gm.nch;
                 for (int pass = 0; pass < 2; ++pass) {
                     const uint64_t pol = pass == 0 ? keep : drop;
                     for (int k = 0; k < nch; ++k, ++it) {
@@ -153,7 +184,8 @@ ce_stream_kernel(RowArgs a, int tune) {
                         const uint32_t s = it % kStreamSlots, r = it / kStreamSlots;
                         if (r > 0) mbar_wait_bounded<false>(smem_u32(&S.empty[s]), (r - 1) & 1u, abort);
                         const int64_t off = static_cast<int64_t>(c) * kStreamChunk;
-                        const uint32_t bytes = static_cast<uint32_t>(Lb16 - off < kStreamChunk ? Lb16 - off : kStreamChunk);
+                        const uint32_t bytes =
+                            static_cast<uint32_t>(gm.bytes - off < kStreamChunk ? gm.bytes - off : kStreamChunk);
                         mbar_expect_tx(smem_u32(&S.full[s]), bytes);
                         bulk_g2s_hint(ring + s * kStreamChunk, src + off, bytes, smem_u32(&S.full[s]), pol);
                     }
@@ -177,11 +209,17 @@ ce_stream_kernel(RowArgs a, int tune) {
             const int64_t t = load_target(a.target, a.tgt32, row);
             const bool valid = target_valid(t, a.ignore_index, V);
             char *rowp = xbase + row * row_bytes;
-            uint4 *vp = reinterpret_cast<uint4 *>(rowp + lo * F::kBytes);
+            const RowGeom gm = row_geom<F::kBytes>(rowp + lo * F::kBytes, lo, L);
+            const int nvec = gm.nvec, nch = gm.nch, nedge = gm.nhead + gm.ntail;
+            const int64_t vlo = gm.vlo;
+            // the column a plain-access thread owns: head columns first, then the tail
+            const int64_t edge_c = tid < gm.nhead ? lo + tid : gm.tail0 + (tid - gm.nhead);
+            uint4 *vp = reinterpret_cast<uint4 *>(rowp + vlo * F::kBytes);
+            const bool w4 = w_base16 && (vlo & 3) == 0;
             if (!valid) {
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 for (int v = tid; v < nvec; v += NCT) st_stream(vp + v, z);
-                if (tid < ntail) F::store1(rowp, tail0 + tid, 0.f);
+                if (tid < nedge) F::store1(rowp, edge_c, 0.f);
                 if (tid == 0 && rank == 0) {
                     if (a.reduction == CE_RED_NONE) a.loss[row] = 0.f;
                     else a.row_loss[row] = 0.f;
@@ -189,7 +227,8 @@ ce_stream_kernel(RowArgs a, int tune) {
                 continue;
             }
             const int yg = static_cast<int>(t);                 // target column in the row
-            const int y = (t >= lo && t < hi) ? static_cast<int>(t - lo) : -(1 << 30);  // in this slice
+            // target column relative to the interior (far outside when it is not in it)
+            const int y = (t >= vlo && t < gm.tail0) ? static_cast<int>(t - vlo) : -(1 << 30);
             // per-row values the merge needs, fetched now so their latency hides under pass 1
             const float g_row = (a.grad_output && a.reduction == CE_RED_NONE) ? __ldg(a.grad_output + row) : 0.f;
             const float wy = a.weight ? __ldg(a.weight + yg) : 1.f;
@@ -268,11 +307,10 @@ ce_stream_kernel(RowArgs a, int tune) {
                         }
                         float w[VEC];
                         if (MODE == 2) {
-                            const float4 *wp = reinterpret_cast<const float4 *>(a.weight + lo + vb);
 #pragma unroll
                             for (int h = 0; h < VEC / 4; ++h) {
-                                const float4 w4 = __ldg(wp + h);
-                                w[4 * h] = w4.x; w[4 * h + 1] = w4.y; w[4 * h + 2] = w4.z; w[4 * h + 3] = w4.w;
+                                const float4 wv = load_w4(a.weight, vlo + vb + 4 * h, w4);
+                                w[4 * h] = wv.x; w[4 * h + 1] = wv.y; w[4 * h + 2] = wv.z; w[4 * h + 3] = wv.w;
                             }
                         }
                         row_state_add<VEC, SMOOTH>(st, x, F::vmax(raw), skip, MODE == 2 ? w : nullptr);
@@ -281,8 +319,8 @@ ce_stream_kernel(RowArgs a, int tune) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
             }
-            if (tid < ntail) {
-                const int64_t c = tail0 + tid;
+            if (tid < nedge) {
+                const int64_t c = edge_c;
                 float x = F::load1(rowp, c);
                 float w = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
                 if (c == yg) S.xy = x;
@@ -356,11 +394,10 @@ ce_stream_kernel(RowArgs a, int tune) {
                     F::unpack(ld_shared_v4(base_s + 16u * v), x);
                     const int vb = (v0 + v) * VEC;
                     if (MODE == 2) {
-                        const float4 *wp = reinterpret_cast<const float4 *>(a.weight + lo + vb);
 #pragma unroll
                         for (int h = 0; h < VEC / 4; ++h) {
-                            const float4 w4 = __ldg(wp + h);
-                            const F2 nbw0 = f2_mul(rs_nb, f2(w4.x, w4.y)), nbw1 = f2_mul(rs_nb, f2(w4.z, w4.w));
+                            const float4 wv = load_w4(a.weight, vlo + vb + 4 * h, w4);
+                            const F2 nbw0 = f2_mul(rs_nb, f2(wv.x, wv.y)), nbw1 = f2_mul(rs_nb, f2(wv.z, wv.w));
                             const F2 p0 = f2_ex2(f2_fma(f2_sub(f2(x[4 * h], x[4 * h + 1]), rs_m), rs_l2, rs_nl));
                             const F2 p1 = f2_ex2(f2_fma(f2_sub(f2(x[4 * h + 2], x[4 * h + 3]), rs_m), rs_l2, rs_nl));
                             f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
@@ -382,8 +419,8 @@ ce_stream_kernel(RowArgs a, int tune) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
             }
-            if (tid < ntail) {
-                const int64_t c = tail0 + tid;
+            if (tid < nedge) {
+                const int64_t c = edge_c;
                 const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
                 F::store1(rowp, c, (c == yg) ? rs.dxy : grad_elem(rs, F::load1(rowp, c), wc));
             }

@@ -101,18 +101,22 @@ def test_workspace_is_o_rows_and_far_below_one_logits_tensor(lib):
 
 
 def test_automatic_path_choice_is_host_logic(lib):
-    """ce_select_variant (no GPU work): 16-byte aligned rows take the stream
-    kernel, other row layouts the register row-pass kernel; explicit
-    variants are returned as asked."""
+    """ce_select_variant (no GPU work): every row layout takes the stream
+    kernel (aligned or ragged rows), calls with softcap / z-loss / accuracy
+    the register row-pass kernel; explicit variants are returned as asked."""
     out = ctypes.c_int32()
     p = _params(lib, n_rows=4, vocab=128256, ld=128256)
     assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
     assert out.value == lib.VARIANTS["stream"]
     p = _params(lib, n_rows=4, vocab=1001, ld=1001)   # 2002-byte rows: not 16-byte aligned
     assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
-    assert out.value == lib.VARIANTS["rowpass"]
+    assert out.value == lib.VARIANTS["stream"]
     p = _params(lib, n_rows=4, vocab=128256, ld=128256)
     assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10008), ctypes.byref(out)) == 0
+    assert out.value == lib.VARIANTS["stream"]
+    p = _params(lib, n_rows=4, vocab=128256, ld=128256)
+    p.softcap = 30.0
+    assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
     assert out.value == lib.VARIANTS["rowpass"]
     p = _params(lib, variant=lib.VARIANTS["split"])
     assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
@@ -149,3 +153,14 @@ def test_flce_workspace_by_variant(lib):
     assert stats - base >= C * tiles * 16 + C * 32 and stats - base <= C * tiles * 16 + C * 32 + 4096
     assert both == base + (compact - base) + (stats - base)
     assert base >= C * V * 6                       # fp32 logits chunk + bf16 dZ chunk
+
+
+def test_logits_not_element_aligned_rejected_on_host(lib):
+    """A bf16 logits pointer at an odd address is refused by every entry point."""
+    L = lib._lib
+    p = _params(lib, n_rows=4, vocab=1000, ld=1000)
+    fake, odd = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x100001)
+    ws, nb = ctypes.c_void_p(0x200000), 1 << 20
+    assert L.ce_fwd_bwd(ctypes.byref(p), odd, fake, fake, None, ws, nb, None) == 1
+    assert L.ce_forward(ctypes.byref(p), odd, fake, fake, fake, ws, nb, None) == 1
+    assert L.ce_backward(ctypes.byref(p), odd, fake, fake, None, ws, nb, None) == 1

@@ -65,6 +65,47 @@ SMALL = [
 ]
 
 
+RAGGED = [
+    # (rows, vocab, ld, first column of the view inside a wider buffer)
+    (7, 1001, 1001, 0), (5, 4099, 4103, 3), (3, 3, 5, 1), (9, 65537, 65537, 1), (4, 20000, 20011, 5),
+    (2, 9, 9, 7),
+]
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("shape", RAGGED, ids=lambda s: f"{s[0]}x{s[1]}ld{s[2]}@{s[3]}")
+@pytest.mark.parametrize("opt", ["plain", "weighted_smooth"])
+@pytest.mark.parametrize("tune", [0, 8, 16, 24], ids=lambda t: f"tune{t}")
+def test_stream_ragged_rows(ce, dtype, shape, opt, tune):
+    """The stream kernel on rows that do not start on a 16-byte boundary: the
+    head and tail of each row (and of each half row for a CTA pair) go
+    through plain accesses, the interior through the bulk-copy ring; the
+    view starts inside a wider buffer so the base itself is misaligned."""
+    R, V, ld, off = shape
+    dev = torch.device("cuda")
+    seed = zlib.crc32(repr((R, V, ld, off, dtype, opt)).encode()) % 10007
+    buf = make_logits(R, ld + off, dtype, 2.0, seed, device=dev)
+    x = buf[:, off:off + V]
+    t = make_targets(R, V, 0.25, seed, device=dev)
+    if R > 2:
+        t[1] = V - 1
+        t[2] = 0
+    w = make_weights(V, seed, device=dev) if opt == "weighted_smooth" else None
+    eps = 0.0 if opt == "plain" else 0.1
+    g = torch.tensor([0.37], device=dev)
+    x_in = x.cpu()
+    ref = _oracle(x, t, w, eps, "mean", g)
+    outside = buf.clone()
+    loss = ce.ce_fwd_bwd(x, t, grad_output=g, weight=w, label_smoothing=eps, reduction="mean",
+                         variant="stream", tune=tune)
+    torch.cuda.synchronize()
+    _check_all(x, t, w, eps, "mean", g, ref, loss, x_in)
+    # columns of the buffer outside the view are untouched
+    keep = torch.ones(ld + off, dtype=torch.bool)
+    keep[off:off + V] = False
+    assert torch.equal(buf[:, keep.to(dev)].cpu(), outside[:, keep.to(dev)].cpu())
+
+
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("shape", SMALL, ids=lambda s: f"{s[0]}x{s[1]}+{s[2]}")
 @pytest.mark.parametrize("opt", ["plain", "smooth", "weighted_smooth"])
@@ -97,7 +138,7 @@ def test_parity_small(ce, dtype, shape, opt, red, api):
         variant, tune = (api, 0) if api != "stream-pair" else ("stream", 8)
         ld = x.stride(0) if R > 1 else V
         fusable = x.data_ptr() % 16 == 0 and (R == 1 or (ld * x.element_size()) % 16 == 0)
-        if variant in ("fused", "stream") and not fusable:
+        if variant == "fused" and not fusable:
             with pytest.raises(ce.CEError):
                 ce.ce_fwd_bwd(x, t, grad_output=g, weight=w, label_smoothing=eps, reduction=red,
                               variant=variant)
