@@ -36,7 +36,8 @@ WORKLOAD = "headline"
 METRIC = "CE fwd+bwd tokens/s at BT=8192 V=128256 bf16; achieved HBM GB/s vs peak"
 FALLBACK_HBM_GBS = 6800.0
 TRAFFIC_FILE = os.path.join(ROOT, "profiles", "ce_stream_kernel_headline_traffic.json")
-KERNEL_SOURCES = ["softmax_cross_entropy_pass_gb300/csrc/ce_stream.cu",
+KERNEL_SOURCES = ["softmax_cross_entropy_pass_gb300/csrc/ce_stream.cuh",
+                  "softmax_cross_entropy_pass_gb300/csrc/ce_stream.cu",
                   "softmax_cross_entropy_pass_gb300/csrc/ce_device.cuh"]
 
 

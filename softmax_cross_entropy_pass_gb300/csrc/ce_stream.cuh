@@ -1,0 +1,609 @@
+// ce_stream.cuh -- streaming forward + backward: each CTA owns whole rows and
+// a producer warp streams every row through a ring of shared-memory chunks
+// twice, with 1-D bulk async copies:
+//   pass 1 (statistics): the row comes from HBM; its lines are marked
+//          evict-last in L2;
+//   pass 2 (gradient):   the same bytes again, now served by L2 (marked
+//          evict-first), while consumer warps write the fp32 gradient,
+//          rounded once, over the logits.
+// The ring is not tied to a row: while the consumers merge a row's
+// statistics, the producer keeps copying (the row's pass-2 chunks and the
+// next row's pass-1 chunks), so the memory system never idles between
+// phases, and the bytes in flight are set by the ring, not by registers.
+// HBM sees one read and one write per element, as the cluster kernel does,
+// without a cluster exchange; the L2 holds about one row per CTA.
+//
+// With a cluster of two CTAs per row, each CTA streams half of the row and
+// the two halves' statistics are exchanged through distributed shared
+// memory (st.shared::cluster + a remote mbarrier arrive), which halves the
+// bytes each CTA keeps waiting in L2 for its second pass.
+//
+// Requires 16-byte aligned row starts (ce_fwd_bwd falls back to the
+// register row-pass kernel otherwise). Every wait is bounded.
+#pragma once
+
+#include "ce_device.cuh"
+#include "ce_kernels.h"
+
+namespace ce {
+
+// Three shapes: 8 consumer warps and a 6-slot ring (two CTAs per SM);
+// 16 consumer warps and a 12-slot ring (one CTA per SM, half the rows
+// waiting in L2 for their second pass); 8 consumer warps and a 4-slot ring
+// (three CTAs per SM, more warps to cover a cluster exchange).
+constexpr int kStreamChunk = 16384;  // bytes per ring slot
+constexpr int kStreamMaxSlots = 12;
+template <int SHAPE> struct StreamShape {
+    static constexpr int kWarps = SHAPE == 1 ? 16 : 8;
+    static constexpr int kThreads = (kWarps + 1) * 32;
+    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : 4);
+    static constexpr int kCtasPerSm = SHAPE == 0 ? 2 : (SHAPE == 1 ? 1 : 3);
+    static constexpr int kSmem = kSlots * kStreamChunk + 1024;
+};
+
+struct StreamXSlot {      // one CTA's partial of one row (32 bytes)
+    float m, s, r, n;
+    float xy, pad0, pad1, pad2;
+};
+
+struct StreamSmem {
+    uint64_t full[kStreamMaxSlots];
+    uint64_t empty[kStreamMaxSlots];
+    uint64_t xbar[2];
+    StreamXSlot slot[2][2];
+    RowState red[16];
+    float2 defer[16];     // class-weighted smoothing: per-warp {sum w x, sum w} of the last row
+    RowScalars rs;
+    float xy;
+    int abort;
+};
+static_assert(sizeof(StreamSmem) <= 1024, "stream control block too large");
+
+// tuning bits (ce_params.variant >> CE_VARIANT_TUNE_SHIFT)
+constexpr int kTuneWide = 1;       // 16 consumer warps, one CTA per SM
+constexpr int kTuneReverse = 2;    // second pass walks the row's chunks last to first
+constexpr int kTuneNoKeep = 4;     // first pass without the L2 evict-last policy
+constexpr int kTuneCluster2 = 8;   // a cluster of two CTAs per row, each streaming half
+constexpr int kTuneThree = 16;     // three CTAs per SM with a 4-slot ring
+
+template <int NCW>
+__device__ inline void stream_consumer_sync() {
+    asm volatile("bar.sync 1, %0;" :: "n"(NCW * 32) : "memory");
+}
+
+__device__ inline void bulk_g2s_hint(uint32_t dst, const void *src, uint32_t bytes, uint32_t bar, uint64_t pol) {
+    asm volatile("cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+                 " [%0], [%1], %2, [%3], %4;"
+                 :: "r"(dst), "l"(src), "r"(bytes), "r"(bar), "l"(pol) : "memory");
+}
+__device__ inline uint64_t createpolicy_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+__device__ inline uint64_t policy_keep() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Where one row's slice [lo, lo + L) sits against 16-byte boundaries: the
+// head (columns before the first boundary, at most 15 bytes) and the tail
+// (after the last) are read and written with plain accesses; the interior
+// [vlo, tail0) moves with bulk copies and 16-byte vectors. Rows whose start
+// is 16-byte aligned have no head.
+struct RowGeom {
+    int64_t vlo, tail0;  // first column of the interior, first column of the tail
+    int nhead, ntail, nvec, nch;
+    int64_t bytes;       // interior bytes (a multiple of 16)
+};
+template <int KB>
+__device__ inline RowGeom row_geom(const char *slice, int64_t lo, int64_t L) {
+    RowGeom g;
+    const int64_t hb = static_cast<int64_t>((16u - (reinterpret_cast<uintptr_t>(slice) & 15u)) & 15u);
+    const int64_t nh = hb / KB < L ? hb / KB : L;
+    g.nhead = static_cast<int>(nh);
+    g.vlo = lo + nh;
+    g.bytes = ((L - nh) * KB) & ~static_cast<int64_t>(15);
+    g.nvec = static_cast<int>(g.bytes / 16);
+    g.tail0 = g.vlo + g.bytes / KB;
+    g.ntail = static_cast<int>(lo + L - g.tail0);
+    g.nch = static_cast<int>((g.bytes + kStreamChunk - 1) / kStreamChunk);
+    return g;
+}
+
+// the same for a slice that starts on a 16-byte boundary
+template <int KB>
+__device__ inline RowGeom row_geom_aligned(int64_t lo, int64_t L) {
+    RowGeom g;
+    g.nhead = 0;
+    g.vlo = lo;
+    g.bytes = (L * KB) & ~static_cast<int64_t>(15);
+    g.nvec = static_cast<int>(g.bytes / 16);
+    g.tail0 = g.vlo + g.bytes / KB;
+    g.ntail = static_cast<int>(lo + L - g.tail0);
+    g.nch = static_cast<int>((g.bytes + kStreamChunk - 1) / kStreamChunk);
+    return g;
+}
+
+// 4 class weights starting at column c (c a multiple of 4 when vec4)
+__device__ inline float4 load_w4(const float *w, int64_t c, bool vec4) {
+    if (vec4) return __ldg(reinterpret_cast<const float4 *>(w + c));
+    return make_float4(__ldg(w + c), __ldg(w + c + 1), __ldg(w + c + 2), __ldg(w + c + 3));
+}
+
+// The loss of a row whose class-weighted smoothing sums (r = sum w x,
+// n = sum w over the whole row) arrived after its gradient pass; written by
+// the first CTA of the row.
+__device__ inline void finish_deferred_loss(const RowArgs &a, uint32_t rank, int64_t row, float m, float s, float xy,
+                                            float r, float n, int yg, float wy, float w_all, float eps,
+                                            float inv_v) {
+    if (rank != 0) return;
+    const float rrel = n > 0.f ? __fsub_rn(r, __fmul_rn(n, m)) : 0.f;
+    const RowScalars rl = make_row_scalars(m, s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f);
+    if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
+    else a.row_loss[row] = rl.loss;
+}
+
+// RAG: rows may start off a 16-byte boundary (per-row head and tail);
+// without it every row of the launch is 16-byte aligned and the geometry is
+// fixed for the whole launch.
+template <int DT, int MODE, int SHAPE, int CL, bool RAG>
+__global__ void __launch_bounds__(StreamShape<SHAPE>::kThreads, StreamShape<SHAPE>::kCtasPerSm)
+ce_stream_kernel(RowArgs a, int tune) {
+    using F = Fmt<DT>;
+    using SH = StreamShape<SHAPE>;
+    constexpr int NCW = SH::kWarps;
+    constexpr int VEC = F::kVec;
+    constexpr bool SMOOTH = MODE != 0;
+    // Class-weighted smoothing needs sum_c w_c x_c, which only the loss uses:
+    // it is summed in pass 2 (where w_c is loaded for the gradient anyway)
+    // instead of pass 1, and the row's loss is completed at the next row's
+    // merge (or after the last row), so pass 1 reads no weights.
+    constexpr bool DEFER = MODE == 2;
+    constexpr bool P1S = SMOOTH && !DEFER;   // smoothing sums in pass 1
+    constexpr int kStreamConsumerWarps = NCW;
+    constexpr int kStreamSlots = SH::kSlots;
+    constexpr int NCT = NCW * 32;
+    constexpr int VPC = kStreamChunk / 16;          // vectors per full chunk
+    constexpr int VPT = VPC / NCT;                  // vectors per thread per full chunk
+    static_assert(VPC % NCT == 0, "chunk must split evenly over the consumers");
+    static_assert(CL == 1 || CL == 2, "one or two CTAs per row");
+
+    extern __shared__ __align__(128) uint8_t smem[];
+    StreamSmem &S = *reinterpret_cast<StreamSmem *>(smem + kStreamSlots * kStreamChunk);
+    const uint32_t ring = smem_u32(smem);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int64_t V = a.vocab;
+    // this CTA's columns [lo, hi) of every row: all of it, or one half
+    const uint32_t rank = CL == 1 ? 0u : cluster_ctarank();
+    const int64_t q0 = CL == 1 ? blockIdx.x : cluster_id_x();
+    const int64_t nq = CL == 1 ? gridDim.x : nclusters_x();
+    const int64_t half = CL == 1 ? V : ((V + 1) / 2 + VEC - 1) / VEC * VEC;
+    const int64_t lo = rank * half;
+    const int64_t hi = (lo + half < V) ? lo + half : V;
+    const int64_t L = hi > lo ? hi - lo : 0;
+    const size_t row_bytes = static_cast<size_t>(a.ld) * F::kBytes;
+    char *const xbase = reinterpret_cast<char *>(a.grad);
+    // weights as float4 when the base allows it (each row's interior start decides the rest)
+    const bool w_base16 = (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
+    const RowGeom g_aligned = row_geom_aligned<F::kBytes>(lo, L);
+
+    if (tid == 0) {
+        for (int s = 0; s < kStreamSlots; ++s) {
+            mbar_init(smem_u32(&S.full[s]), 1);
+            mbar_init(smem_u32(&S.empty[s]), kStreamConsumerWarps);
+        }
+        mbar_init(smem_u32(&S.xbar[0]), CL);
+        mbar_init(smem_u32(&S.xbar[1]), CL);
+        S.abort = 0;
+        fence_mbar_init_cluster();
+    }
+    __syncthreads();
+    if (CL > 1) cluster_sync_all();  // the peer's barriers exist before any remote arrive
+    volatile int *abort = &S.abort;
+
+    const bool reverse = (tune & kTuneReverse) != 0;
+    if (warp == kStreamConsumerWarps) {
+        // -------------------------------------------------------------- producer
+        if (lane == 0) {
+            const uint64_t drop = policy_evict_first();
+            const uint64_t keep = (tune & kTuneNoKeep) ? createpolicy_normal() : policy_keep();
+            uint32_t it = 0;
+            // each row's target is loaded one row ahead, so its latency hides under the previous row
+            int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;
+            for (int64_t row = q0; row < a.n_rows; row += nq) {
+                const int64_t t = t_next;
+                if (row + nq < a.n_rows) t_next = load_target(a.target, a.tgt32, row + nq);
+                if (!target_valid(t, a.ignore_index, V)) continue;
+                const char *slice = xbase + row * row_bytes + lo * F::kBytes;
+                const RowGeom gm = RAG ? row_geom<F::kBytes>(slice, lo, L) : g_aligned;
+                const char *src = slice + static_cast<int64_t>(gm.nhead) * F::kBytes;
+                const int nch = gm.nch;
+                for (int pass = 0; pass < 2; ++pass) {
+                    const uint64_t pol = pass == 0 ? keep : drop;
+                    for (int k = 0; k < nch; ++k, ++it) {
+                        const int c = (pass == 1 && reverse) ? nch - 1 - k : k;
+                        const uint32_t s = it % kStreamSlots, r = it / kStreamSlots;
+                        if (r > 0) mbar_wait_bounded<false>(smem_u32(&S.empty[s]), (r - 1) & 1u, abort);
+                        const int64_t off = static_cast<int64_t>(c) * kStreamChunk;
+                        const uint32_t bytes =
+                            static_cast<uint32_t>(gm.bytes - off < kStreamChunk ? gm.bytes - off : kStreamChunk);
+                        mbar_expect_tx(smem_u32(&S.full[s]), bytes);
+                        bulk_g2s_hint(ring + s * kStreamChunk, src + off, bytes, smem_u32(&S.full[s]), pol);
+                    }
+                }
+            }
+            // drain: every issued copy has landed before the CTA may exit
+            for (uint32_t k = 0; k < kStreamSlots && k < it; ++k) {
+                const uint32_t i = it - 1 - k;
+                mbar_wait_bounded<false>(smem_u32(&S.full[i % kStreamSlots]), (i / kStreamSlots) & 1u, abort);
+            }
+        }
+        __syncwarp();
+    } else {
+        // -------------------------------------------------------------- consumers
+        const float inv_v = 1.f / static_cast<float>(V);
+        const float eps = a.eps;
+        bool have_norm = false;
+        float w_all = 0.f, w_y_sum = 0.f, g_all = 1.f;  // batch constants, read once
+        // the row whose loss still waits for its deferred smoothing sums (class weights)
+        bool pend = false;
+        int64_t pend_row = 0;
+        float pend_m = 0.f, pend_s = 0.f, pend_xy = 0.f, pend_wy = 0.f;
+        int pend_yg = 0;
+        uint32_t it = 0, j = 0;  // ring position; valid rows done (exchange parity)
+        int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;  // one row ahead
+        for (int64_t row = q0; row < a.n_rows; row += nq) {
+            const int64_t t = t_next;
+            if (row + nq < a.n_rows) t_next = load_target(a.target, a.tgt32, row + nq);
+            const bool valid = target_valid(t, a.ignore_index, V);
+            char *rowp = xbase + row * row_bytes;
+            const RowGeom gm = RAG ? row_geom<F::kBytes>(rowp + lo * F::kBytes, lo, L) : g_aligned;
+            const int nvec = gm.nvec, nch = gm.nch, nedge = gm.nhead + gm.ntail;
+            const int64_t vlo = gm.vlo;
+            // the column a plain-access thread owns: head columns first, then the tail
+            const int64_t edge_c = tid < gm.nhead ? lo + tid : gm.tail0 + (tid - gm.nhead);
+            uint4 *vp = reinterpret_cast<uint4 *>(rowp + vlo * F::kBytes);
+            const bool w4 = w_base16 && (vlo & 3) == 0;
+            if (!valid) {
+                const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+                for (int v = tid; v < nvec; v += NCT) st_stream(vp + v, z);
+                if (tid < nedge) F::store1(rowp, edge_c, 0.f);
+                if (tid == 0 && rank == 0) {
+                    if (a.reduction == CE_RED_NONE) a.loss[row] = 0.f;
+                    else a.row_loss[row] = 0.f;
+                }
+                continue;
+            }
+            const int yg = static_cast<int>(t);                 // target column in the row
+            // target column relative to the interior (far outside when it is not in it)
+            const int y = (t >= vlo && t < gm.tail0) ? static_cast<int>(t - vlo) : -(1 << 30);
+            // per-row values the merge needs, fetched now so their latency hides under pass 1
+            const float g_row = (a.grad_output && a.reduction == CE_RED_NONE) ? __ldg(a.grad_output + row) : 0.f;
+            const float wy = a.weight ? __ldg(a.weight + yg) : 1.f;
+            // ------------------------------------------------ pass 1: statistics
+            RowState st = row_state_empty();
+            for (int c = 0; c < nch; ++c, ++it) {
+                const uint32_t s = it % kStreamSlots;
+                mbar_wait_bounded<false>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
+                const uint32_t base_s = ring + s * kStreamChunk;
+                const int v0 = c * VPC;
+                const int nv = min(VPC, nvec - v0);
+                // does one of this thread's vectors hold the target column?
+                const unsigned q = static_cast<unsigned>(y / VEC - v0 - tid);
+                const bool mine = q < static_cast<unsigned>(VPT * NCT) && (q % NCT) == 0;
+                if (nv == VPC && !mine) {
+                    // full chunk, no target: one max per chunk, four independent sums
+                    uint4 raw[VPT];
+#pragma unroll
+                    for (int k = 0; k < VPT; ++k) raw[k] = ld_shared_v4(base_s + 16u * (tid + k * NCT));
+                    float cm = F::vmax(raw[0]);
+#pragma unroll
+                    for (int k = 1; k < VPT; ++k) cm = fmaxf(cm, F::vmax(raw[k]));
+                    if (cm > st.m) {
+                        if (st.m != -INFINITY) st.s *= ex2_hw((st.m - cm) * kLog2e);
+                        st.m = cm;
+                    }
+                    if (st.m != -INFINITY) {
+                        // four accumulators, column j into sum j mod 4, held as two packed
+                        // pairs {0,1} {2,3}: the pair ops round each lane as the scalar ops do
+                        const float mL = st.m * kLog2e;
+                        const F2 l2 = f2(kLog2e, kLog2e), nm = f2(-mL, -mL);
+                        F2 acc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)}, racc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) {
+                            float x[VEC];
+                            F::unpack(raw[k], x);
+#pragma unroll
+                            for (int p = 0; p < VEC / 2; ++p) {
+                                const F2 xx = f2(x[2 * p], x[2 * p + 1]);
+                                acc[p & 1] = f2_add(acc[p & 1], f2_ex2(f2_fma(xx, l2, nm)));
+                                if (P1S) racc[p & 1] = f2_add(racc[p & 1], xx);
+                            }
+                        }
+                        float a0, a1, a2, a3;
+                        f2_split(acc[0], a0, a1);
+                        f2_split(acc[1], a2, a3);
+                        st.s += (a0 + a1) + (a2 + a3);
+                        if (P1S) {
+                            f2_split(racc[0], a0, a1);
+                            f2_split(racc[1], a2, a3);
+                            st.r += (a0 + a1) + (a2 + a3);
+                            st.n += static_cast<float>(VPT * VEC);
+                        }
+                    } else if (P1S) {
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) {
+                            float x[VEC];
+                            F::unpack(raw[k], x);
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) st.r += x[j];
+                        }
+                        st.n += static_cast<float>(VPT * VEC);
+                    }
+                } else {
+                    for (int v = tid; v < nv; v += NCT) {
+                        const uint4 raw = ld_shared_v4(base_s + 16u * v);
+                        const int vb = (v0 + v) * VEC;
+                        float x[VEC];
+                        F::unpack(raw, x);
+                        const int skip = (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) ? y - vb : -1;
+                        if (skip >= 0) {
+                            float xv = 0.f;
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) xv = (j == skip) ? x[j] : xv;
+                            S.xy = xv;  // the target logit, for the merge
+                        }
+                        row_state_add<VEC, P1S>(st, x, F::vmax(raw), skip, nullptr);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
+            }
+            if (tid < nedge) {
+                const int64_t c = edge_c;
+                float x = F::load1(rowp, c);
+                if (c == yg) S.xy = x;
+                row_state_add<1, P1S>(st, &x, x, (c == yg) ? 0 : -1, nullptr);
+            }
+            // ------------------------------------------------ merge and row scalars
+            st = warp_merge(st);
+            if (lane == 0) S.red[warp] = st;
+            stream_consumer_sync<NCW>();
+            if (warp == 0) {
+                RowState m = lane < kStreamConsumerWarps ? S.red[lane] : row_state_empty();
+                m = warp_merge(m);
+                float xy_mine = 0.f;
+                if (lane == 0) xy_mine = S.xy;
+                if (DEFER && lane == 0) {
+                    // r and n of this state carry the previous row's deferred sums (this CTA's
+                    // part, then both CTAs' after the exchange); pass 1 left them at 0
+                    float pr = 0.f, pn = 0.f;
+                    if (pend)
+                        for (int k = 0; k < kStreamConsumerWarps; ++k) { pr += S.defer[k].x; pn += S.defer[k].y; }
+                    m.r = pr;
+                    m.n = pn;
+                }
+                if (CL > 1 && lane == 0) {
+                    // push this half's partial into both CTAs, then merge both in rank order
+                    const uint32_t par = j & 1u;
+                    const uint32_t my_slot = smem_u32(&S.slot[par][rank]);
+                    const uint32_t my_bar = smem_u32(&S.xbar[par]);
+                    for (uint32_t d = 0; d < static_cast<uint32_t>(CL); ++d) {
+                        const uint32_t rs_addr = mapa_shared(my_slot, d);
+                        st_cluster_v4(rs_addr, m.m, m.s, m.r, m.n);
+                        st_cluster_v4(rs_addr + 16u, xy_mine, 0.f, 0.f, 0.f);
+                        mbar_arrive_remote(mapa_shared(my_bar, d));
+                    }
+                    mbar_wait_bounded<true>(my_bar, (j >> 1) & 1u, abort);
+                    RowState tot = row_state_empty();
+                    for (int d = 0; d < CL; ++d) {
+                        const StreamXSlot &xs = S.slot[par][d];
+                        tot = row_state_merge(tot, RowState{xs.m, xs.s, xs.r, xs.n});
+                    }
+                    m = tot;
+                    xy_mine = S.slot[par][yg >= half ? 1 : 0].xy;
+                }
+                if (lane == 0) {
+                    if (!have_norm) {
+                        pdl_wait();
+                        w_all = a.ctl->w_all;
+                        w_y_sum = a.ctl->w_y;
+                        g_all = a.grad_output ? __ldg(a.grad_output) : 1.f;
+                        have_norm = true;
+                    }
+                    const float xy = xy_mine;
+                    float rrel = SMOOTH ? row_state_rel_sum(m) : 0.f;
+                    if (DEFER) {
+                        if (pend) finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, m.r, m.n,
+                                                       pend_yg, pend_wy, w_all, eps, inv_v);
+                        rrel = 0.f;  // the gradient does not use it; this row's loss waits for pass 2
+                        pend_row = row; pend_m = m.m; pend_s = m.s; pend_xy = xy; pend_yg = yg; pend_wy = wy;
+                    }
+                    const float g = a.reduction == CE_RED_NONE ? (a.grad_output ? g_row : 1.f) : g_all;
+                    float scale = g;
+                    if (a.reduction == CE_RED_MEAN) scale = w_y_sum != 0.f ? g / w_y_sum : 0.f;
+                    if (rank == 0 && !DEFER) {
+                        const RowScalars rl = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f);
+                        if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
+                        else a.row_loss[row] = rl.loss;
+                    }
+                    S.rs = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, scale);
+                }
+            }
+            stream_consumer_sync<NCW>();
+            const RowScalars rs = S.rs;
+            // grad_elem over packed pairs: p = 2^((x - m) log2e - log2 d), g = a p - b w
+            const F2 rs_m = f2(rs.m, rs.m), rs_l2 = f2(kLog2e, kLog2e), rs_nl = f2(rs.neg_log2d, rs.neg_log2d);
+            const F2 rs_a = f2(rs.a, rs.a), rs_nb = f2(-rs.b, -rs.b);
+            F2 dr[2] = {f2(0.f, 0.f), f2(0.f, 0.f)}, dn[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // deferred sums
+            // ------------------------------------------------ pass 2: gradient in place
+            for (int k = 0; k < nch; ++k, ++it) {
+                const int c = reverse ? nch - 1 - k : k;
+                const uint32_t s = it % kStreamSlots;
+                mbar_wait_bounded<false>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
+                const uint32_t base_s = ring + s * kStreamChunk;
+                const int v0 = c * VPC;
+                const int nv = min(VPC, nvec - v0);
+                for (int v = tid; v < nv; v += NCT) {
+                    float x[VEC], gr[VEC];
+                    F::unpack(ld_shared_v4(base_s + 16u * v), x);
+                    const int vb = (v0 + v) * VEC;
+                    if (MODE == 2) {
+#pragma unroll
+                        for (int h = 0; h < VEC / 4; ++h) {
+                            const float4 wv = load_w4(a.weight, vlo + vb + 4 * h, w4);
+                            const F2 w01 = f2(wv.x, wv.y), w23 = f2(wv.z, wv.w);
+                            const F2 x01 = f2(x[4 * h], x[4 * h + 1]), x23 = f2(x[4 * h + 2], x[4 * h + 3]);
+                            const F2 nbw0 = f2_mul(rs_nb, w01), nbw1 = f2_mul(rs_nb, w23);
+                            const F2 p0 = f2_ex2(f2_fma(f2_sub(x01, rs_m), rs_l2, rs_nl));
+                            const F2 p1 = f2_ex2(f2_fma(f2_sub(x23, rs_m), rs_l2, rs_nl));
+                            dr[0] = f2_fma(w01, x01, dr[0]);
+                            dr[1] = f2_fma(w23, x23, dr[1]);
+                            dn[0] = f2_add(dn[0], w01);
+                            dn[1] = f2_add(dn[1], w23);
+                            f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
+                            f2_split(f2_fma(p1, rs_a, nbw1), gr[4 * h + 2], gr[4 * h + 3]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < VEC / 2; ++p) {
+                            const F2 pp = f2_ex2(f2_fma(f2_sub(f2(x[2 * p], x[2 * p + 1]), rs_m), rs_l2, rs_nl));
+                            f2_split(f2_fma(pp, rs_a, rs_nb), gr[2 * p], gr[2 * p + 1]);
+                        }
+                    }
+                    if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
+#pragma unroll
+                        for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
+                    }
+                    st_stream(vp + v0 + v, F::pack(gr));  // vp points at this CTA's slice
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
+            }
+            float er = 0.f, en = 0.f;
+            if (tid < nedge) {
+                const int64_t c = edge_c;
+                const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
+                const float xe = F::load1(rowp, c);
+                er = wc * xe;
+                en = wc;
+                F::store1(rowp, c, (c == yg) ? rs.dxy : grad_elem(rs, xe, wc));
+            }
+            if (DEFER) {
+                // this thread's, then this warp's, deferred sums (fixed order), for the next merge
+                float r0, r1, r2, r3, n0, n1, n2, n3;
+                f2_split(dr[0], r0, r1);
+                f2_split(dr[1], r2, r3);
+                f2_split(dn[0], n0, n1);
+                f2_split(dn[1], n2, n3);
+                float rr = ((r0 + r1) + (r2 + r3)) + er, nn = ((n0 + n1) + (n2 + n3)) + en;
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    rr += __shfl_xor_sync(0xffffffffu, rr, off);
+                    nn += __shfl_xor_sync(0xffffffffu, nn, off);
+                }
+                if (lane == 0) S.defer[warp] = make_float2(rr, nn);
+            }
+            pend = true;
+            ++j;
+        }
+        // ---------------------------------------------------- the last row's deferred loss
+        if (DEFER && pend) {
+            stream_consumer_sync<NCW>();  // every warp's sums of the last row are in S.defer
+            if (warp == 0 && lane == 0) {
+                float pr = 0.f, pn = 0.f;
+                for (int k = 0; k < kStreamConsumerWarps; ++k) { pr += S.defer[k].x; pn += S.defer[k].y; }
+                if (CL > 1) {
+                    // one more exchange (the next parity) carrying only the sums
+                    const uint32_t par = j & 1u;
+                    const uint32_t my_slot = smem_u32(&S.slot[par][rank]);
+                    const uint32_t my_bar = smem_u32(&S.xbar[par]);
+                    for (uint32_t d = 0; d < static_cast<uint32_t>(CL); ++d) {
+                        const uint32_t rs_addr = mapa_shared(my_slot, d);
+                        st_cluster_v4(rs_addr, -INFINITY, 0.f, pr, pn);
+                        st_cluster_v4(rs_addr + 16u, 0.f, 0.f, 0.f, 0.f);
+                        mbar_arrive_remote(mapa_shared(my_bar, d));
+                    }
+                    mbar_wait_bounded<true>(my_bar, (j >> 1) & 1u, abort);
+                    RowState tot = row_state_empty();
+                    for (int d = 0; d < CL; ++d) {
+                        const StreamXSlot &xs = S.slot[par][d];
+                        tot = row_state_merge(tot, RowState{xs.m, xs.s, xs.r, xs.n});
+                    }
+                    pr = tot.r;
+                    pn = tot.n;
+                }
+                finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, pr, pn, pend_yg, pend_wy, w_all,
+                                     eps, inv_v);
+            }
+        }
+        // ---------------------------------------------------- batch reduction (last CTA)
+        if (a.reduction != CE_RED_NONE) {
+            __shared__ unsigned sh_last;
+            __shared__ double sh_sum[kStreamConsumerWarps];
+            if (!have_norm) pdl_wait();
+            stream_consumer_sync<NCW>();
+            if (tid == 0) {
+                __threadfence();
+                const unsigned prev = atomicAdd(&a.ctl->done, 1u);
+                sh_last = (prev == gridDim.x - 1) ? 1u : 0u;
+            }
+            stream_consumer_sync<NCW>();
+            if (sh_last) {
+                __threadfence();
+                double sum = 0.0;
+                for (int64_t i = tid; i < a.n_rows; i += NCT) sum += static_cast<double>(__ldcg(a.row_loss + i));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                if (lane == 0) sh_sum[warp] = sum;
+                stream_consumer_sync<NCW>();
+                if (tid == 0) {
+                    double tot = 0.0;
+                    for (int k = 0; k < kStreamConsumerWarps; ++k) tot += sh_sum[k];
+                    if (a.reduction == CE_RED_MEAN) {
+                        const float wys = a.ctl->w_y;  // after the normaliser kernel (waited above)
+                        tot = wys != 0.f ? tot / static_cast<double>(wys) : 0.0;
+                    }
+                    a.loss[0] = static_cast<float>(tot);
+                    a.ctl->done = 0u;
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (tid == 0 && S.abort) {
+        pdl_wait();
+        atomicOr(&a.ctl->status, CE_FLAG_WAIT_TIMEOUT);
+    }
+    if (CL > 1) cluster_sync_all();  // no CTA leaves while its peer may still write into it
+}
+
+// Kernel entry of one instantiation (the aligned ones are compiled in
+// ce_stream.cu, the ragged ones in ce_stream_ragged.cu).
+template <int DT, int SHAPE, int CL, bool RAG>
+const void *stream_fn(int mode) {
+    switch (mode) {
+    case 0: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 0, SHAPE, CL, RAG>);
+    case 1: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 1, SHAPE, CL, RAG>);
+    default: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 2, SHAPE, CL, RAG>);
+    }
+}
+
+template <bool RAG>
+const void *stream_kernel_for(int dtype, int mode, int shape, int cl) {
+#define CE_STREAM_PICK(S, C)                                                                  \
+    if (shape == S && cl == C)                                                                \
+        return dtype == CE_DT_F32 ? stream_fn<CE_DT_F32, S, C, RAG>(mode)                     \
+             : dtype == CE_DT_BF16 ? stream_fn<CE_DT_BF16, S, C, RAG>(mode) : stream_fn<CE_DT_F16, S, C, RAG>(mode);
+    CE_STREAM_PICK(0, 1) CE_STREAM_PICK(0, 2) CE_STREAM_PICK(1, 1) CE_STREAM_PICK(1, 2)
+    CE_STREAM_PICK(2, 1) CE_STREAM_PICK(2, 2)
+#undef CE_STREAM_PICK
+    return nullptr;
+}
+
+// defined in ce_stream_ragged.cu
+const void *stream_kernel_ragged(int dtype, int mode, int shape, int cl);
+
+}  // namespace ce
