@@ -33,12 +33,13 @@ namespace ce {
 // (three CTAs per SM, more warps to cover a cluster exchange).
 constexpr int kStreamChunk = 16384;  // bytes per ring slot
 constexpr int kStreamMaxSlots = 12;
+constexpr int kStreamCtlBytes = 2048;  // control block after the ring
 template <int SHAPE> struct StreamShape {
     static constexpr int kWarps = SHAPE == 1 ? 16 : 8;
     static constexpr int kThreads = (kWarps + 1) * 32;
     static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : 4);
     static constexpr int kCtasPerSm = SHAPE == 0 ? 2 : (SHAPE == 1 ? 1 : 3);
-    static constexpr int kSmem = kSlots * kStreamChunk + 1024;
+    static constexpr int kSmem = kSlots * kStreamChunk + kStreamCtlBytes;
 };
 
 struct StreamXSlot {      // one CTA's partial of one row (32 bytes)
@@ -51,13 +52,15 @@ struct StreamSmem {
     uint64_t empty[kStreamMaxSlots];
     uint64_t xbar[2];
     StreamXSlot slot[2][2];
-    RowState red[16];
-    float2 defer[16];     // class-weighted smoothing: per-warp {sum w x, sum w} of the last row
-    RowScalars rs;
-    float xy;
+    // per row parity: a warp may write the next row's values while a slower
+    // warp still reads this row's (never further ahead: the row's barrier
+    // waits for every warp)
+    RowState red[2][16];    // per-warp partial states of pass 1
+    float2 defer[2][16];    // class-weighted smoothing: per-warp {sum w x, sum w} of pass 2
+    float xy[2];            // the target logit
     int abort;
 };
-static_assert(sizeof(StreamSmem) <= 1024, "stream control block too large");
+static_assert(sizeof(StreamSmem) <= kStreamCtlBytes, "stream control block too large");
 
 // tuning bits (ce_params.variant >> CE_VARIANT_TUNE_SHIFT)
 constexpr int kTuneWide = 1;       // 16 consumer warps, one CTA per SM
@@ -277,6 +280,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                 continue;
             }
             const int yg = static_cast<int>(t);                 // target column in the row
+            const uint32_t rp = j & 1u;                         // parity of this valid row
             // target column relative to the interior (far outside when it is not in it)
             const int y = (t >= vlo && t < gm.tail0) ? static_cast<int>(t - vlo) : -(1 << 30);
             // per-row values the merge needs, fetched now so their latency hides under pass 1
@@ -353,7 +357,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                             float xv = 0.f;
 #pragma unroll
                             for (int j = 0; j < VEC; ++j) xv = (j == skip) ? x[j] : xv;
-                            S.xy = xv;  // the target logit, for the merge
+                            S.xy[rp] = xv;  // the target logit, for the merge
                         }
                         row_state_add<VEC, P1S>(st, x, F::vmax(raw), skip, nullptr);
                     }
@@ -364,76 +368,81 @@ ce_stream_kernel(RowArgs a, int tune) {
             if (tid < nedge) {
                 const int64_t c = edge_c;
                 float x = F::load1(rowp, c);
-                if (c == yg) S.xy = x;
+                if (c == yg) S.xy[rp] = x;
                 row_state_add<1, P1S>(st, &x, x, (c == yg) ? 0 : -1, nullptr);
             }
             // ------------------------------------------------ merge and row scalars
+            // Every warp merges the CTA's partials and forms the row scalars itself
+            // (the same operations in the same order, so every thread holds the
+            // same values): one barrier per row, no thread waits on another's
+            // scalar work.
             st = warp_merge(st);
-            if (lane == 0) S.red[warp] = st;
+            if (lane == 0) S.red[rp][warp] = st;
             stream_consumer_sync<NCW>();
-            if (warp == 0) {
-                RowState m = lane < kStreamConsumerWarps ? S.red[lane] : row_state_empty();
-                m = warp_merge(m);
-                float xy_mine = 0.f;
-                if (lane == 0) xy_mine = S.xy;
-                if (DEFER && lane == 0) {
-                    // r and n of this state carry the previous row's deferred sums (this CTA's
-                    // part, then both CTAs' after the exchange); pass 1 left them at 0
-                    float pr = 0.f, pn = 0.f;
-                    if (pend)
-                        for (int k = 0; k < kStreamConsumerWarps; ++k) { pr += S.defer[k].x; pn += S.defer[k].y; }
-                    m.r = pr;
-                    m.n = pn;
-                }
-                if (CL > 1 && lane == 0) {
-                    // push this half's partial into both CTAs, then merge both in rank order
-                    const uint32_t par = j & 1u;
+            RowState m = lane < kStreamConsumerWarps ? S.red[rp][lane] : row_state_empty();
+            m = warp_merge(m);
+            float xy = S.xy[rp];
+            if (DEFER) {
+                // r and n of this state carry the previous row's deferred sums (this CTA's
+                // part, then both CTAs' after the exchange); pass 1 left them at 0
+                float pr = 0.f, pn = 0.f;
+                if (pend)
+                    for (int k = 0; k < kStreamConsumerWarps; ++k) {
+                        pr += S.defer[rp ^ 1u][k].x;
+                        pn += S.defer[rp ^ 1u][k].y;
+                    }
+                m.r = pr;
+                m.n = pn;
+            }
+            if (CL > 1) {
+                // one thread pushes this half's partial into both CTAs; every thread
+                // waits for both and merges them in rank order
+                const uint32_t par = rp;
+                const uint32_t my_bar = smem_u32(&S.xbar[par]);
+                if (warp == 0 && lane == 0) {
                     const uint32_t my_slot = smem_u32(&S.slot[par][rank]);
-                    const uint32_t my_bar = smem_u32(&S.xbar[par]);
                     for (uint32_t d = 0; d < static_cast<uint32_t>(CL); ++d) {
                         const uint32_t rs_addr = mapa_shared(my_slot, d);
                         st_cluster_v4(rs_addr, m.m, m.s, m.r, m.n);
-                        st_cluster_v4(rs_addr + 16u, xy_mine, 0.f, 0.f, 0.f);
+                        st_cluster_v4(rs_addr + 16u, xy, 0.f, 0.f, 0.f);
                         mbar_arrive_remote(mapa_shared(my_bar, d));
                     }
-                    mbar_wait_bounded<true>(my_bar, (j >> 1) & 1u, abort);
-                    RowState tot = row_state_empty();
-                    for (int d = 0; d < CL; ++d) {
-                        const StreamXSlot &xs = S.slot[par][d];
-                        tot = row_state_merge(tot, RowState{xs.m, xs.s, xs.r, xs.n});
-                    }
-                    m = tot;
-                    xy_mine = S.slot[par][yg >= half ? 1 : 0].xy;
                 }
-                if (lane == 0) {
-                    if (!have_norm) {
-                        pdl_wait();
-                        w_all = a.ctl->w_all;
-                        w_y_sum = a.ctl->w_y;
-                        g_all = a.grad_output ? __ldg(a.grad_output) : 1.f;
-                        have_norm = true;
-                    }
-                    const float xy = xy_mine;
-                    float rrel = SMOOTH ? row_state_rel_sum(m) : 0.f;
-                    if (DEFER) {
-                        if (pend) finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, m.r, m.n,
-                                                       pend_yg, pend_wy, w_all, eps, inv_v);
-                        rrel = 0.f;  // the gradient does not use it; this row's loss waits for pass 2
-                        pend_row = row; pend_m = m.m; pend_s = m.s; pend_xy = xy; pend_yg = yg; pend_wy = wy;
-                    }
-                    const float g = a.reduction == CE_RED_NONE ? (a.grad_output ? g_row : 1.f) : g_all;
-                    float scale = g;
-                    if (a.reduction == CE_RED_MEAN) scale = w_y_sum != 0.f ? g / w_y_sum : 0.f;
-                    if (rank == 0 && !DEFER) {
-                        const RowScalars rl = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f);
-                        if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
-                        else a.row_loss[row] = rl.loss;
-                    }
-                    S.rs = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, scale);
+                mbar_wait_bounded<true>(my_bar, (j >> 1) & 1u, abort);
+                RowState tot = row_state_empty();
+                for (int d = 0; d < CL; ++d) {
+                    const StreamXSlot &xs = S.slot[par][d];
+                    tot = row_state_merge(tot, RowState{xs.m, xs.s, xs.r, xs.n});
                 }
+                m = tot;
+                xy = S.slot[par][yg >= half ? 1 : 0].xy;
             }
-            stream_consumer_sync<NCW>();
-            const RowScalars rs = S.rs;
+            if (!have_norm) {
+                pdl_wait();
+                w_all = a.ctl->w_all;
+                w_y_sum = a.ctl->w_y;
+                g_all = a.grad_output ? __ldg(a.grad_output) : 1.f;
+                have_norm = true;
+            }
+            float rrel = SMOOTH ? row_state_rel_sum(m) : 0.f;
+            const bool writer = warp == 0 && lane == 0;
+            if (DEFER) {
+                if (writer) {
+                    if (pend) finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, m.r, m.n,
+                                                   pend_yg, pend_wy, w_all, eps, inv_v);
+                    pend_row = row; pend_m = m.m; pend_s = m.s; pend_xy = xy; pend_yg = yg; pend_wy = wy;
+                }
+                rrel = 0.f;  // the gradient does not use it; this row's loss waits for pass 2
+            }
+            const float g = a.reduction == CE_RED_NONE ? (a.grad_output ? g_row : 1.f) : g_all;
+            float scale = g;
+            if (a.reduction == CE_RED_MEAN) scale = w_y_sum != 0.f ? g / w_y_sum : 0.f;
+            if (writer && rank == 0 && !DEFER) {
+                const RowScalars rl = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f);
+                if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
+                else a.row_loss[row] = rl.loss;
+            }
+            const RowScalars rs = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, scale);
             // grad_elem over packed pairs: p = 2^((x - m) log2e - log2 d), g = a p - b w
             const F2 rs_m = f2(rs.m, rs.m), rs_l2 = f2(kLog2e, kLog2e), rs_nl = f2(rs.neg_log2d, rs.neg_log2d);
             const F2 rs_a = f2(rs.a, rs.a), rs_nb = f2(-rs.b, -rs.b);
@@ -504,7 +513,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                     rr += __shfl_xor_sync(0xffffffffu, rr, off);
                     nn += __shfl_xor_sync(0xffffffffu, nn, off);
                 }
-                if (lane == 0) S.defer[warp] = make_float2(rr, nn);
+                if (lane == 0) S.defer[rp][warp] = make_float2(rr, nn);
             }
             pend = true;
             ++j;
@@ -514,7 +523,8 @@ ce_stream_kernel(RowArgs a, int tune) {
             stream_consumer_sync<NCW>();  // every warp's sums of the last row are in S.defer
             if (warp == 0 && lane == 0) {
                 float pr = 0.f, pn = 0.f;
-                for (int k = 0; k < kStreamConsumerWarps; ++k) { pr += S.defer[k].x; pn += S.defer[k].y; }
+                const uint32_t lp = (j - 1u) & 1u;  // parity of the last row
+                for (int k = 0; k < kStreamConsumerWarps; ++k) { pr += S.defer[lp][k].x; pn += S.defer[lp][k].y; }
                 if (CL > 1) {
                     // one more exchange (the next parity) carrying only the sums
                     const uint32_t par = j & 1u;
