@@ -1,8 +1,30 @@
 // ce_stream.cu -- launch of the streaming forward + backward kernel
 // (ce_stream.cuh) and its instantiations for 16-byte aligned rows.
+#include <mutex>
+
 #include "ce_stream.cuh"
 
 namespace ce {
+
+// Resident clusters of a kernel on a device (0 if unknown), asked once per
+// kernel and device.
+static int max_active_clusters(const void *fn, int dev, const cudaLaunchConfig_t &cfg) {
+    struct Entry {
+        const void *fn;
+        int dev, n;
+    };
+    static Entry cache[128];
+    static int used = 0;
+    static std::mutex mu;
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].fn == fn && cache[i].dev == dev) return cache[i].n;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+    (void)cudaGetLastError();
+    if (used < 128) cache[used++] = Entry{fn, dev, n};
+    return n;
+}
 
 template <int SHAPE, int CL>
 static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, int ctas_per_sm, int tune,
@@ -20,14 +42,29 @@ static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, i
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
     int64_t grid = static_cast<int64_t>(sms) * (ctas_per_sm > 0 ? ctas_per_sm : SH::kCtasPerSm);
-    if (grid > a.n_rows * CL) grid = a.n_rows * CL;
-    grid = grid / CL * CL;
-    if (grid < CL) grid = CL;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(SH::kThreads);
     cfg.dynamicSmemBytes = SH::kSmem;
     cfg.stream = s;
+    cudaLaunchAttribute cl_attr;
+    if (CL > 1) {
+        // the kernel is persistent: no more clusters than can be resident at once
+        // (clusters are placed within a GPC, so fewer may fit than SMs x CTAs per SM)
+        cl_attr.id = cudaLaunchAttributeClusterDimension;
+        cl_attr.val.clusterDim.x = CL;
+        cl_attr.val.clusterDim.y = 1;
+        cl_attr.val.clusterDim.z = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(grid / CL * CL));
+        cfg.attrs = &cl_attr;
+        cfg.numAttrs = 1;
+        const int max_clusters = max_active_clusters(fn, dev, cfg);
+        if (max_clusters > 0 && static_cast<int64_t>(max_clusters) * CL < grid)
+            grid = static_cast<int64_t>(max_clusters) * CL;
+    }
+    if (grid > a.n_rows * CL) grid = a.n_rows * CL;
+    grid = grid / CL * CL;
+    if (grid < CL) grid = CL;
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cudaLaunchAttribute attr[2];
     int n = 0;
     if (CL > 1) {

@@ -182,7 +182,8 @@ ce_stream_kernel(RowArgs a, int tune) {
     const uint32_t rank = CL == 1 ? 0u : cluster_ctarank();
     const int64_t q0 = CL == 1 ? blockIdx.x : cluster_id_x();
     const int64_t nq = CL == 1 ? gridDim.x : nclusters_x();
-    const int64_t half = CL == 1 ? V : ((V + 1) / 2 + VEC - 1) / VEC * VEC;
+    // columns per CTA (a multiple of the vector width, so every part starts on a vector)
+    const int64_t half = CL == 1 ? V : ((V + CL - 1) / CL + VEC - 1) / VEC * VEC;
     const int64_t lo = rank * half;
     const int64_t hi = (lo + half < V) ? lo + half : V;
     const int64_t L = hi > lo ? hi - lo : 0;
@@ -415,7 +416,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                     tot = row_state_merge(tot, RowState{xs.m, xs.s, xs.r, xs.n});
                 }
                 m = tot;
-                xy = S.slot[par][yg >= half ? 1 : 0].xy;
+                xy = S.slot[par][yg / half].xy;
             }
             if (!have_norm) {
                 pdl_wait();

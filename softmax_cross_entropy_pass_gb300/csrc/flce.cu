@@ -56,6 +56,11 @@ struct GemmArgs {
     const int *dyn_count;
     int dyn_off, dyn_dim;
     const int *row_map;    // output row r is stored at row row_map[r] (NULL: r)
+    // Split-K: every output tile is computed as ksplit partial products over
+    // consecutive K ranges; partial s is stored (fp32) split_stride elements
+    // after partial s - 1 (ksplit 1: one product, the usual output).
+    int ksplit;
+    int64_t split_stride;
     // Row statistics of the fp32 output (logits GEMM of the fused-linear
     // path): per row and column tile, the running softmax state of the tile's
     // columns {max m, exp-sum s without the target column, smoothing sum r,
@@ -74,11 +79,12 @@ __device__ inline void tile_coords(const GemmArgs &g, int t, int &tm, int &tn) {
 
 // One thread's 32 consecutive accumulator columns of one output row.
 // `orow` is the row of the output the tile row `row` is stored at.
-__device__ inline void epilogue_store(const GemmArgs &g, int row, int orow, int col0, const uint32_t (&v)[32]) {
+__device__ inline void epilogue_store(const GemmArgs &g, int row, int orow, int col0, const uint32_t (&v)[32],
+                                      int64_t base = 0) {
     if (row >= g.M) return;
     const bool full = col0 + 32 <= g.N;
     if (g.out_kind == OUT_BF16_STORE) {
-        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(g.out) + static_cast<int64_t>(orow) * g.ldo + col0;
+        __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(g.out) + base + static_cast<int64_t>(orow) * g.ldo + col0;
         if (full && (g.ldo % 8) == 0) {
             uint4 *o4 = reinterpret_cast<uint4 *>(o);
 #pragma unroll
@@ -97,7 +103,7 @@ __device__ inline void epilogue_store(const GemmArgs &g, int row, int orow, int 
         }
         return;
     }
-    float *o = reinterpret_cast<float *>(g.out) + static_cast<int64_t>(orow) * g.ldo + col0;
+    float *o = reinterpret_cast<float *>(g.out) + base + static_cast<int64_t>(orow) * g.ldo + col0;
     const bool accum = g.out_kind == OUT_F32_ACCUM;
     if (full && (g.ldo % 4) == 0) {
         float4 *o4 = reinterpret_cast<float4 *>(o);
@@ -192,8 +198,13 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             g.K = n < 0 ? 0 : (n < g.K ? n : g.K);
         }
     }
-    const int num_tiles = g.tiles_m * g.tiles_n;
+    const int ksplit = g.ksplit > 1 ? g.ksplit : 1;
+    // tiles run K part by K part (all output tiles of part 0, then part 1, ...), so
+    // the CTAs of a wave share one K range of the operands in L2
+    const int mn_tiles = g.tiles_m * g.tiles_n;
+    const int num_tiles = mn_tiles * ksplit;
     const int kiters = (g.K + GB_K - 1) / GB_K;
+    const int kper = (kiters + ksplit - 1) / ksplit;   // K steps of one split (the last may have fewer)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (num_tiles == 0) return;
     if (kiters == 0) {
@@ -203,10 +214,11 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const uint32_t zero[32] = {};
             for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
                 int tm, tn;
-                tile_coords(g, t, tm, tn);
+                tile_coords(g, t % mn_tiles, tm, tn);
                 const int row = tm * GB_M + q * 32 + lane;
                 const int orow = (g.row_map && row < g.M) ? __ldg(g.row_map + row) : row;
-                for (int c0 = 0; c0 < GB_N; c0 += 32) epilogue_store(g, row, orow, tn * GB_N + c0, zero);
+                const int64_t base = static_cast<int64_t>(t / mn_tiles) * g.split_stride;
+                for (int c0 = 0; c0 < GB_N; c0 += 32) epilogue_store(g, row, orow, tn * GB_N + c0, zero, base);
             }
         }
         return;
@@ -246,8 +258,9 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             uint32_t it = 0;
             for (int t = blockIdx.x; t < num_tiles; t += gridDim.x) {
                 int tm, tn;
-                tile_coords(g, t, tm, tn);
-                for (int k = 0; k < kiters; ++k, ++it) {
+                tile_coords(g, t % mn_tiles, tm, tn);
+                const int kb = (t / mn_tiles) * kper, ke = min(kiters, kb + kper);
+                for (int k = kb; k < ke; ++k, ++it) {
                     const uint32_t s = it % GB_STAGES, r = it / GB_STAGES;
                     if (r > 0) mbar_wait_bounded<false>(smem_u32(&empty[s]), (r - 1) & 1u, abort);
                     const uint32_t fb = smem_u32(&full[s]);
@@ -275,7 +288,8 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 if (u > 0) mbar_wait_bounded<false>(smem_u32(&tempty[acc]), (u - 1) & 1u, abort);
                 tc_fence_after();
                 const uint32_t d = tmem + acc * GB_N;
-                for (int k = 0; k < kiters; ++k, ++it) {
+                const int kb = (t / mn_tiles) * kper, ke = min(kiters, kb + kper);
+                for (int k = kb; k < ke; ++k, ++it) {
                     const uint32_t s = it % GB_STAGES, r = it / GB_STAGES;
                     mbar_wait_bounded<false>(smem_u32(&full[s]), r & 1u, abort);
                     tc_fence_after();
@@ -283,7 +297,7 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     for (int kk = 0; kk < GB_K / 16; ++kk) {
                         const uint64_t ad = smem_desc_sw128(sA + s * GB_A_BYTES + kk * a_kstep, a_lbo, 1024);
                         const uint64_t bd = smem_desc_sw128(sB + s * GB_B_BYTES + kk * b_kstep, b_lbo, 1024);
-                        mma_bf16(d, ad, bd, idesc, (k | kk) ? 1u : 0u);
+                        mma_bf16(d, ad, bd, idesc, (k > kb || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(smem_u32(&empty[s]));
                 }
@@ -296,7 +310,8 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
         uint32_t lt = 0;
         for (int t = blockIdx.x; t < num_tiles; t += gridDim.x, ++lt) {
             int tm, tn;
-            tile_coords(g, t, tm, tn);
+            tile_coords(g, t % mn_tiles, tm, tn);
+            const int64_t base = static_cast<int64_t>(t / mn_tiles) * g.split_stride;
             const uint32_t acc = lt & 1u, u = lt >> 1;
             mbar_wait_bounded<false>(smem_u32(&tfull[acc]), u & 1u, abort);
             tc_fence_after();
@@ -315,7 +330,7 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                 tmem_ld_32x32b_x32(taddr + c0, v);
                 tmem_ld_wait();
                 if (EPI == 0) {
-                    epilogue_store(g, row, orow, tn * GB_N + c0, v);
+                    epilogue_store(g, row, orow, tn * GB_N + c0, v, base);
                 } else if (row < g.M) {
                     const int skip = (static_cast<unsigned>(y_rel - c0) < 32u) ? y_rel - c0 : -1;
                     epilogue_stats<(EPI > 0 ? EPI - 1 : 0)>(g, row, tn * GB_N + c0, v, st, skip);
@@ -588,6 +603,33 @@ __global__ void __launch_bounds__(256) flce_map_kernel(ChunkArgs a) {
     }
 }
 
+// grad_hidden rows from the split-K partials of dZ W: the parts summed in
+// fp32 in a fixed order, rounded once to bf16, stored at row_map[r] (or r)
+// for the rows below the device-side count.
+__global__ void __launch_bounds__(256) flce_splitk_sum_kernel(const float *part, int ksplit, int64_t split_stride,
+                                                              int64_t n_rows, int64_t H, const int *count, int64_t off,
+                                                              const int *row_map, __nv_bfloat16 *out, int64_t ldo) {
+    const int64_t n = dyn_rows(n_rows, count, off);
+    const int64_t vpr = H / 8;
+    const int64_t total = n * vpr;
+    for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t r = i / vpr, c = (i - r * vpr) * 8;
+        const float *p = part + r * H + c;
+        float4 a = __ldcs(reinterpret_cast<const float4 *>(p)), b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+        for (int k = 1; k < ksplit; ++k) {
+            const float4 *q = reinterpret_cast<const float4 *>(p + k * split_stride);
+            const float4 a2 = __ldcs(q), b2 = __ldcs(q + 1);
+            a.x += a2.x; a.y += a2.y; a.z += a2.z; a.w += a2.w;
+            b.x += b2.x; b.y += b2.y; b.z += b2.z; b.w += b2.w;
+        }
+        using FB = Fmt<CE_DT_BF16>;
+        const uint4 o = make_uint4(FB::pack2(a.x, a.y), FB::pack2(a.z, a.w), FB::pack2(b.x, b.y), FB::pack2(b.z, b.w));
+        const int64_t orow = row_map ? static_cast<int64_t>(__ldg(row_map + r)) : r;
+        st_stream(out + orow * ldo + c, o);
+    }
+}
+
 // loss[0] = sum of the row losses (/ W_y for mean), fixed order, fp64; with
 // `count`, only the first *count row losses (the compacted rows).
 __global__ void __launch_bounds__(256) flce_reduce_kernel(const float *row_loss, int64_t n0, int reduction,
@@ -651,13 +693,29 @@ static int sm_count() {
     return n;
 }
 
+int gemm_fit_ksplit(int K, int ksplit) {
+    const int kiters = (K + GB_K - 1) / GB_K;
+    if (ksplit > kiters) ksplit = kiters > 0 ? kiters : 1;
+    while (ksplit > 1) {
+        const int kper = (kiters + ksplit - 1) / ksplit;
+        if ((ksplit - 1) * kper < kiters) break;  // the last part is not empty
+        --ksplit;
+    }
+    return ksplit;
+}
+
 // D[M,N] = A[M,K] B[K,N]. A: K-major = memory [M, K] (lda >= K); MN-major =
 // memory [K, M] (lda >= M). B: K-major = memory [N, K]; MN-major = memory [K, N].
 cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B, int64_t ldb,
                       int b_mn, int out_kind, void *out, int64_t ldo, const float *bias, unsigned int *status,
-                      cudaStream_t s, const GemmDyn *dyn, const GemmStats *stats) {
+                      cudaStream_t s, const GemmDyn *dyn, const GemmStats *stats, int ksplit,
+                      int64_t split_stride) {
     if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
     if (stats && out_kind != OUT_F32_STORE) return cudaErrorInvalidValue;
+    if (ksplit < 1) ksplit = 1;
+    if (ksplit > 1 && (out_kind != OUT_F32_STORE || stats || (dyn && dyn->dim == 1) || bias ||
+                       gemm_fit_ksplit(K, ksplit) != ksplit))
+        return cudaErrorInvalidValue;
     CUtensorMap ta, tb;
     cudaError_t e;
     if (!a_mn) e = make_tmap(&ta, A, M, K, lda, GB_K, GB_M);
@@ -674,6 +732,8 @@ cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn,
     g.tiles_n = (N + GB_N - 1) / GB_N;
     g.m_fastest = g.tiles_m <= g.tiles_n ? 1 : 0;  // the operand of the short side stays in L2
     g.status = status;
+    g.ksplit = ksplit;
+    g.split_stride = split_stride;
     if (dyn) {
         g.dyn_count = dyn->count;
         g.dyn_off = dyn->off;
@@ -705,7 +765,7 @@ cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn,
         if (e != cudaSuccess) return e;
         attr_set[epi] |= bit;
     }
-    const int tiles = g.tiles_m * g.tiles_n;
+    const int tiles = g.tiles_m * g.tiles_n * ksplit;
     const int grid = tiles < sm_count() ? tiles : sm_count();
     void *args[] = {&ta, &tb, &g};
     return cudaLaunchKernel(kernels[epi], dim3(grid), dim3(GB_THREADS), args, GB_SMEM, s);
@@ -731,7 +791,20 @@ struct FlceLayout {
     // statistics path: the logits GEMM's per-tile row states and the per-row map scalars
     size_t part_off, rows_off;
     int tiles;
+    // split-K parts of grad_hidden = dZ W (fp32, dh_splits x chunk x H)
+    size_t dhp_off;
+    int dh_splits;
 };
+
+// Split count of the grad_hidden GEMM: its output has few tiles (chunk x H)
+// and a long K (V), so one product per tile leaves the last of few waves
+// mostly idle; 4 parts below 1024 tiles, 2 below 2048 (host rule, no device
+// query, so the workspace size is a function of the sizes alone).
+int flce_dh_splits(int64_t chunk, int64_t H, int64_t V) {
+    const int64_t tiles = ((chunk + 127) / 128) * ((H + 255) / 256);
+    const int want = tiles >= 2048 ? 1 : (tiles >= 1024 ? 2 : 4);
+    return gemm_fit_ksplit(static_cast<int>(V), want);
+}
 
 FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk, int64_t hidden, bool compact, bool map_ce) {
     FlceLayout L{};
@@ -749,6 +822,11 @@ FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk, int64_t hid
         L.gc_off = L.tgt_off + round_up(n_rows * 8, 256);
         L.cnt_off = L.gc_off + round_up(n_rows * 4, 256);
         L.total = L.cnt_off + 256;
+    }
+    L.dh_splits = flce_dh_splits(chunk, hidden, vocab);
+    if (L.dh_splits > 1) {
+        L.dhp_off = L.total;
+        L.total = L.dhp_off + round_up(static_cast<int64_t>(L.dh_splits) * chunk * hidden * 4, 1024);
     }
     if (map_ce) {
         L.tiles = static_cast<int>((vocab + kGemmTileN - 1) / kGemmTileN);
@@ -970,8 +1048,28 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
         // grad_hidden rows = dZ W   (A = dZ K-major, B = W stored [V, H] = [K, N]: MN-major);
         // compacted rows are stored back at their own rows
         void *gh = compact ? grad_hidden : reinterpret_cast<char *>(grad_hidden) + r0 * H * 2;
-        e = gemm_bf16(static_cast<int>(c), static_cast<int>(H), static_cast<int>(V), dZ, L.ldd, 0, weight, H, 1,
-                      2, gh, H, nullptr, &ctl->status, s, compact ? &rows_out : nullptr);
+        if (L.dh_splits > 1) {
+            // split-K parts in fp32, then one kernel sums them (fixed order), rounds once
+            // to bf16 and stores each row at its own position
+            float *dhp = reinterpret_cast<float *>(wsb + L.dhp_off);
+            const int64_t stride = c * H;
+            e = gemm_bf16(static_cast<int>(c), static_cast<int>(H), static_cast<int>(V), dZ, L.ldd, 0, weight, H, 1,
+                          0, dhp, H, nullptr, &ctl->status, s, compact ? &rows_m : nullptr, nullptr, L.dh_splits,
+                          stride);
+            if (e != cudaSuccess) return flce_cuda_fail(e);
+            const float *pp = dhp;
+            int ks = L.dh_splits;
+            int64_t st = stride, nr = c, hh = H, off = r0, ldo = H;
+            const int *cc = count;
+            const int *rm = compact ? idx + r0 : nullptr;
+            __nv_bfloat16 *o = reinterpret_cast<__nv_bfloat16 *>(gh);
+            void *args[] = {&pp, &ks, &st, &nr, &hh, &cc, &off, &rm, &o, &ldo};
+            e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_splitk_sum_kernel),
+                                 dim3(static_cast<unsigned>(sm_count() * 8)), dim3(256), args, 0, s);
+        } else {
+            e = gemm_bf16(static_cast<int>(c), static_cast<int>(H), static_cast<int>(V), dZ, L.ldd, 0, weight, H, 1,
+                          2, gh, H, nullptr, &ctl->status, s, compact ? &rows_out : nullptr);
+        }
         if (e != cudaSuccess) return flce_cuda_fail(e);
         // grad_weight (+)= dZ^T h_c   (A = dZ stored [c, V] = [K, M]: MN-major; B = h_c [K, N]: MN-major)
         e = gemm_bf16(static_cast<int>(V), static_cast<int>(H), static_cast<int>(c), dZ, L.ldd, 1, h_c, H, 1,

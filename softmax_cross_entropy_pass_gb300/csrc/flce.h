@@ -21,6 +21,9 @@ struct GemmDyn {
     const int *row_map;
 };
 
+// `ksplit` > 1 (fp32 store only, static K) computes every tile as ksplit
+// partial products over consecutive K ranges, partial p stored at
+// out + p * split_stride.
 // `stats` (optional, fp32 store only) also writes, for every output row and
 // 256-column tile, the tile's softmax state {max, exp-sum without the
 // row's target column, smoothing sum, weight sum} to part[row * tiles + t]
@@ -39,6 +42,10 @@ constexpr int kGemmTileN = 256;
 cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B,
                       int64_t ldb, int b_mn, int out_kind, void *out, int64_t ldo, const float *bias,
                       unsigned int *status, cudaStream_t s, const GemmDyn *dyn = nullptr,
-                      const GemmStats *stats = nullptr);
+                      const GemmStats *stats = nullptr, int ksplit = 1, int64_t split_stride = 0);
+
+// K steps of 64 per split-K part: ksplit parts over kiters steps, each
+// non-empty (the split count actually used, <= ksplit).
+int gemm_fit_ksplit(int K, int ksplit);
 
 }  // namespace ce

@@ -75,7 +75,7 @@ RAGGED = [
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("shape", RAGGED, ids=lambda s: f"{s[0]}x{s[1]}ld{s[2]}@{s[3]}")
 @pytest.mark.parametrize("opt", ["plain", "weighted_smooth"])
-@pytest.mark.parametrize("tune", [0, 8, 16, 24], ids=lambda t: f"tune{t}")
+@pytest.mark.parametrize("tune", [0, 8, 9, 16, 24], ids=lambda t: f"tune{t}")
 def test_stream_ragged_rows(ce, dtype, shape, opt, tune):
     """The stream kernel on rows that do not start on a 16-byte boundary: the
     head and tail of each row (and of each half row for a CTA pair) go

@@ -193,6 +193,35 @@ def test_flce_ignored_rows_against_oracle(ce, case, dense, ce_cluster):
 
 
 @pytest.mark.slow
+def test_flce_grad_hidden_without_split_k(ce):
+    """A chunk whose grad_hidden GEMM has 2048 output tiles (16384 rows x H
+    4096) takes one product per tile (no split-K) and stores bf16 rows
+    through the compaction's row map in the GEMM epilogue: sampled rows and
+    vocabulary rows against the fp64 oracle."""
+    BT, H, V = 16384, 4096, 1024
+    g = torch.Generator(device="cuda").manual_seed(31)
+    h = torch.randn(BT, H, generator=g, device="cuda").to(torch.bfloat16)
+    W = (torch.randn(V, H, generator=g, device="cuda") * 0.02).to(torch.bfloat16)
+    t = make_targets(BT, V, 0.05, 31, device="cuda")
+    loss, gh, gw, _ = ce.flce_fwd_bwd(h, W, t, reduction="mean", chunk_rows=BT)
+    torch.cuda.synchronize()
+    gen = torch.Generator().manual_seed(32)
+    rows = torch.randperm(BT, generator=gen)[:128].sort().values
+    cols = torch.randperm(V, generator=gen)[:64].sort().values
+    ref = oracle.flce(h.cpu(), W.cpu(), t.cpu(), reduction="mean", sample_rows=rows, sample_cols=cols,
+                      abs_sums=True)
+    assert abs(float(loss.item()) - ref["loss"]) <= 1e-4 * abs(ref["loss"])
+    gh_s = gh[rows.cuda()].double().cpu()
+    err_h = (gh_s - ref["grad_hidden"]).abs()
+    assert (err_h <= ref["grad_hidden_abs"] * 2.0 ** -8 + ref["grad_hidden"].abs() * 2.0 ** -7).all()
+    gw_s = gw[cols.cuda()].double().cpu()
+    err_w = (gw_s - ref["grad_weight"]).abs()
+    assert (err_w <= ref["grad_weight_abs"] * 2.0 ** -8 + ref["grad_weight"].abs() * 2.0 ** -20).all()
+    valid = t.cpu()[rows] >= 0
+    assert torch.count_nonzero(gh_s[~valid]) == 0
+
+
+@pytest.mark.slow
 def test_flce_full_size_sampled(ce):
     """hidden 8192 x 4096, W 128256 x 4096: loss over all rows, grad_hidden on
     256 sampled rows and grad_weight on 256 sampled vocabulary rows against
