@@ -227,6 +227,31 @@ ce_status ce_fwd_bwd_noalloc(const ce_params *p, void *logits_inout, const void 
                              const float *grad_output, void *stream);
 
 /*
+ * ce_fwd_bwd for logits that start in host memory: the rows are copied to
+ * logits_dev in n_parts blocks on copy_stream, and each block's forward +
+ * backward (the stream kernel, with the whole batch's normalisers computed
+ * first on `stream`) runs on `stream` as soon as its copy has landed, so the
+ * transfer and the kernels overlap (Liger-Kernel #1622 counts the
+ * host-device traffic around the loss; this call hides the kernels under
+ * it). Same results as ce_fwd_bwd on the device copy.
+ *   logits_host  host [n_rows, ld] of p->dtype, page-locked (cudaHostAlloc
+ *                or registered) for the copies to be asynchronous; it must
+ *                stay valid and unchanged until `stream` has passed this call.
+ *   logits_dev   device [n_rows, ld]: receives the logits, then the gradient.
+ *   target, loss, grad_output, workspace: as in ce_fwd_bwd.
+ *   copy_stream  a stream other than `stream` (not the legacy default
+ *                stream, which would serialise the two); it first waits for
+ *                the work already queued on `stream`.
+ *   n_parts      >= 1 blocks of rows (clamped to n_rows); 8 is a good choice.
+ * p->variant must be 0; softcap, z-loss and accuracy give
+ * CE_ERR_UNSUPPORTED. Allocates no device memory; creates and releases CUDA
+ * events.
+ */
+ce_status ce_fwd_bwd_from_host(const ce_params *p, const void *logits_host, void *logits_dev, const void *target,
+                               float *loss, const float *grad_output, void *workspace, size_t workspace_bytes,
+                               void *stream, void *copy_stream, int32_t n_parts);
+
+/*
  * Scale a gradient already written with grad_output = 1 (ce_fwd_bwd with
  * grad_output NULL) by the grad_output that arrives later: row i is
  * multiplied by g ([1]) or g_i ([n_rows], reduction none). With a [1]

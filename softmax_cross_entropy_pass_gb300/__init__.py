@@ -68,6 +68,7 @@ def _load():
         "ce_backward": (st, [P, vp, vp, vp, vp, vp, sz, vp]),
         "ce_fwd_bwd": (st, [P, vp, vp, vp, vp, vp, sz, vp]),
         "ce_fwd_bwd_noalloc": (st, [P, vp, vp, vp, vp, vp]),
+        "ce_fwd_bwd_from_host": (st, [P, vp, vp, vp, vp, vp, vp, sz, vp, vp, ctypes.c_int32]),
         "ce_scale_grad": (st, [P, vp, vp, vp]),
         "ce_fused_plan": (st, [P, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32),
                                ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)]),
@@ -253,6 +254,32 @@ def ce_fwd_bwd_noalloc(logits, target, *, grad_output=None, weight=None, ignore_
                            device=logits.device)
     _check(_lib.ce_fwd_bwd_noalloc(ctypes.byref(p), _ptr(logits), _ptr(target), _ptr(loss),
                                    _ptr(grad_output), _stream(stream)), "ce_fwd_bwd_noalloc")
+    return loss
+
+
+def ce_fwd_bwd_from_host(host_logits, dev_logits, target, *, grad_output=None, weight=None, ignore_index=-100,
+                         label_smoothing=0.0, reduction="mean", loss=None, ws=None, stream=None,
+                         copy_stream=None, n_parts=8):
+    """ce_fwd_bwd for logits in (page-locked) host memory: the rows are copied
+    into ``dev_logits`` (same shape and strides) in ``n_parts`` blocks on
+    ``copy_stream`` while each block's forward + backward runs on ``stream``;
+    ``dev_logits`` holds the gradient afterwards. ``host_logits`` must stay
+    unchanged until ``stream`` has passed the call."""
+    _check_dev(dev_logits, target, grad_output, weight)
+    if host_logits.is_cuda or host_logits.shape != dev_logits.shape or host_logits.stride() != dev_logits.stride() \
+            or host_logits.dtype != dev_logits.dtype:
+        raise ValueError("host_logits must be a host tensor with the device tensor's shape, strides and dtype")
+    p = make_params(dev_logits, target, weight=weight, ignore_index=ignore_index,
+                    label_smoothing=label_smoothing, reduction=reduction)
+    if loss is None:
+        loss = torch.empty(dev_logits.shape[0] if reduction == "none" else 1, dtype=torch.float32,
+                           device=dev_logits.device)
+    ws, ws_bytes = _ws(ws, dev_logits.shape[0], dev_logits.device)
+    if copy_stream is None:
+        copy_stream = torch.cuda.Stream(device=dev_logits.device)
+    _check(_lib.ce_fwd_bwd_from_host(ctypes.byref(p), ctypes.c_void_p(host_logits.data_ptr()), _ptr(dev_logits),
+                                     _ptr(target), _ptr(loss), _ptr(grad_output), _ptr(ws), ws_bytes,
+                                     _stream(stream), _stream(copy_stream), int(n_parts)), "ce_fwd_bwd_from_host")
     return loss
 
 

@@ -356,6 +356,70 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
     return e == cudaSuccess ? CE_OK : cuda_fail(e);
 }
 
+ce_status ce_fwd_bwd_from_host(const ce_params *p, const void *logits_host, void *logits_dev, const void *target,
+                               float *loss, const float *grad_output, void *ws, size_t ws_bytes, void *stream,
+                               void *copy_stream, int32_t n_parts) {
+    ce_status st = check_params(p);
+    if (st != CE_OK) return st;
+    if ((st = check_ws(p, ws, ws_bytes)) != CE_OK) return st;
+    if (n_parts < 1 || p->variant != 0) return CE_ERR_INVALID_ARG;
+    if (has_options(p)) return CE_ERR_UNSUPPORTED;
+    if (!loss || (p->n_rows > 0 && (!logits_host || !logits_dev || !target))) return CE_ERR_INVALID_ARG;
+    const int64_t esz = elem_bytes(p->dtype);
+    if (!aligned(logits_dev, esz) || !aligned(logits_host, esz)) return CE_ERR_INVALID_ARG;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    cudaStream_t cs = reinterpret_cast<cudaStream_t>(copy_stream);
+    if (cs == s) return CE_ERR_INVALID_ARG;  // the copies must run beside the kernels
+    const int64_t R = p->n_rows;
+    cudaError_t e = run_prep(p, target, ws, s);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (R == 0) {
+        if (p->reduction != CE_RED_NONE && (e = cudaMemsetAsync(loss, 0, sizeof(float), s)) != cudaSuccess)
+            return cuda_fail(e);
+        return CE_OK;
+    }
+    const int64_t parts = n_parts < R ? n_parts : R;
+    const int64_t per = (R + parts - 1) / parts;
+    // events: one for the work already queued on `stream` (the copies must not
+    // overwrite logits_dev under an earlier call's kernels), one per part;
+    // destroyed once queued (the runtime releases them when they complete)
+    cudaEvent_t ev_start = nullptr;
+    if ((e = cudaEventCreateWithFlags(&ev_start, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
+    e = cudaEventRecord(ev_start, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(cs, ev_start, 0);
+    cudaEventDestroy(ev_start);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int tb = p->target_is_int32 ? 4 : 8;
+    for (int64_t r0 = 0; r0 < R; r0 += per) {
+        const int64_t n = (R - r0) < per ? (R - r0) : per;
+        const size_t off = static_cast<size_t>(r0 * p->ld * esz);
+        const size_t bytes = static_cast<size_t>(((n - 1) * p->ld + p->vocab) * esz);  // not past the last row
+        e = cudaMemcpyAsync(static_cast<char *>(logits_dev) + off, static_cast<const char *>(logits_host) + off, bytes,
+                            cudaMemcpyHostToDevice, cs);
+        if (e != cudaSuccess) return cuda_fail(e);
+        cudaEvent_t ev = nullptr;
+        if ((e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming)) != cudaSuccess) return cuda_fail(e);
+        e = cudaEventRecord(ev, cs);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(s, ev, 0);
+        cudaEventDestroy(ev);
+        if (e != cudaSuccess) return cuda_fail(e);
+        // this block's rows, with the batch normalisers from the kernel above
+        RowArgs a = row_args(p, static_cast<const char *>(target) + r0 * tb, ws);
+        a.n_rows = n;
+        a.grad = static_cast<char *>(logits_dev) + off;
+        a.row_loss = ws_row_loss(ws) + r0;
+        a.loss = p->reduction == CE_RED_NONE ? loss + r0 : loss;
+        a.grad_output = grad_output ? (p->reduction == CE_RED_NONE ? grad_output + r0 : grad_output) : nullptr;
+        a.no_finalize = 1;
+        if ((e = launch_stream(a, p->dtype, smoothing_mode(p), 0, 0, false, s)) != cudaSuccess) return cuda_fail(e);
+    }
+    if (p->reduction != CE_RED_NONE) {
+        e = launch_reduce_row_losses(ws_row_loss(ws), R, p->reduction, reinterpret_cast<const WsCtl *>(ws), loss, s);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    return CE_OK;
+}
+
 ce_status ce_scale_grad(const ce_params *p, void *grad_inout, const float *grad_output, void *stream) {
     ce_status st = check_params(p);
     if (st != CE_OK) return st;

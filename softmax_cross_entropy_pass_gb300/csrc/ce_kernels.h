@@ -44,6 +44,7 @@ struct RowArgs {
     float softcap;             // > 0: logits become c tanh(x / c)
     float z_loss;              // lambda of lambda LSE^2
     float *accuracy;           // token accuracy out [1] or NULL
+    int32_t no_finalize;       // stream kernel: leave the batch reduction to a later kernel
 };
 
 struct ScaleArgs {
@@ -101,6 +102,10 @@ cudaError_t launch_scale(const ScaleArgs &a, int dtype, int grid, cudaStream_t s
 cudaError_t launch_rowpass(const RowArgs &a, int dtype, int mode, int ctas_per_sm, cudaStream_t s);
 // the same two passes streamed through a shared-memory ring by bulk copies
 // (16-byte aligned rows only)
+// loss[0] = sum of row_loss[0, n) in fp64 (divided by the workspace's W_y for
+// mean), one block; for the row kernels launched with no_finalize.
+cudaError_t launch_reduce_row_losses(const float *row_loss, int64_t n, int reduction, const WsCtl *ctl, float *loss,
+                                     cudaStream_t s);
 cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm, int tune, bool after_prep,
                           cudaStream_t s);
 

@@ -551,7 +551,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             }
         }
         // ---------------------------------------------------- batch reduction (last CTA)
-        if (a.reduction != CE_RED_NONE) {
+        if (a.reduction != CE_RED_NONE && !a.no_finalize) {
             __shared__ unsigned sh_last;
             __shared__ double sh_sum[kStreamConsumerWarps];
             if (!have_norm) pdl_wait();

@@ -653,6 +653,13 @@ __global__ void __launch_bounds__(256) flce_reduce_kernel(const float *row_loss,
     }
 }
 
+cudaError_t launch_reduce_row_losses(const float *row_loss, int64_t n, int reduction, const WsCtl *ctl, float *loss,
+                                     cudaStream_t s) {
+    const int *none = nullptr;
+    void *args[] = {&row_loss, &n, &reduction, &ctl, &loss, &none};
+    return cudaLaunchKernel(reinterpret_cast<const void *>(&flce_reduce_kernel), dim3(1), dim3(256), args, 0, s);
+}
+
 // ------------------------------------------------------------------ host: tensor maps and launch
 static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;

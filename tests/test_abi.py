@@ -164,3 +164,18 @@ def test_logits_not_element_aligned_rejected_on_host(lib):
     assert L.ce_fwd_bwd(ctypes.byref(p), odd, fake, fake, None, ws, nb, None) == 1
     assert L.ce_forward(ctypes.byref(p), odd, fake, fake, fake, ws, nb, None) == 1
     assert L.ce_backward(ctypes.byref(p), odd, fake, fake, None, ws, nb, None) == 1
+
+
+def test_from_host_argument_errors_on_host(lib):
+    """ce_fwd_bwd_from_host refuses n_parts < 1, the same stream for copies and
+    kernels, a variant, and the options, before any CUDA call."""
+    L = lib._lib
+    fake, ws = ctypes.c_void_p(0x100000), ctypes.c_void_p(0x200000)
+    p = _params(lib, n_rows=4, vocab=1000, ld=1000)
+    s1, s2 = ctypes.c_void_p(0x1000), ctypes.c_void_p(0x2000)
+    assert L.ce_fwd_bwd_from_host(ctypes.byref(p), fake, fake, fake, fake, None, ws, 1 << 20, s1, s2, 0) == 1
+    assert L.ce_fwd_bwd_from_host(ctypes.byref(p), fake, fake, fake, fake, None, ws, 1 << 20, s1, s1, 4) == 1
+    p.variant = 4
+    assert L.ce_fwd_bwd_from_host(ctypes.byref(p), fake, fake, fake, fake, None, ws, 1 << 20, s1, s2, 4) == 1
+    p = _params(lib, n_rows=4, vocab=1000, ld=1000, softcap=10.0)
+    assert L.ce_fwd_bwd_from_host(ctypes.byref(p), fake, fake, fake, fake, None, ws, 1 << 20, s1, s2, 4) == 2

@@ -444,6 +444,48 @@ def test_stream_tuning_variants(ce, tune, shape):
     _check_all(x, t, w, 0.05, "sum", g, ref, loss, x_in)
 
 
+@pytest.mark.parametrize("case", ["mean", "sum_weighted", "none_ragged", "int32_ld", "one_part", "tiny"])
+def test_from_host_matches_device_call(ce, case):
+    """ce_fwd_bwd_from_host (row blocks copied from pinned host memory on a
+    second stream, each block's kernel started when its copy lands): the same
+    gradient, bit for bit, as ce_fwd_bwd on a device copy, and losses within
+    the oracle's tolerances; called twice in a row on the same buffers."""
+    R, V, ld, red, eps, weighted, t32, parts = {
+        "mean": (300, 4096, 4096, "mean", 0.1, False, False, 8),
+        "sum_weighted": (257, 3000, 3000, "sum", 0.05, True, False, 5),
+        "none_ragged": (129, 1001, 1001, "none", 0.1, False, False, 7),
+        "int32_ld": (64, 2000, 2011, "mean", 0.0, False, True, 3),
+        "one_part": (33, 5000, 5000, "mean", 0.1, True, False, 1),
+        "tiny": (3, 7, 7, "sum", 0.0, False, False, 8),
+    }[case]
+    dev = torch.device("cuda")
+    seed = zlib.crc32(case.encode()) % 10007
+    x = make_logits(R, V, "bf16", 2.0, seed, device=dev, ld=ld if ld > V else None)
+    t = make_targets(R, V, 0.2, seed, device=dev)
+    if t32:
+        t = t.to(torch.int32)
+    w = make_weights(V, seed, device=dev) if weighted else None
+    g = (torch.rand(R, generator=torch.Generator().manual_seed(seed)).to(dev) if red == "none"
+         else torch.tensor([0.37], device=dev))
+    x_in = x.cpu()
+    ref = _oracle(x, t, w, eps, red, g)
+    want = torch.empty((R, ld), dtype=x.dtype, device=dev)[:, :V]   # the same layout as the call under test
+    want.copy_(x)
+    want_loss = ce.ce_fwd_bwd(want, t, weight=w, label_smoothing=eps, reduction=red, grad_output=g)
+    host = torch.empty_strided(x.shape, x.stride(), dtype=x.dtype).pin_memory() if ld == V else \
+        torch.empty(R, ld, dtype=x.dtype).pin_memory()[:, :V]
+    host.copy_(x_in)
+    for _ in range(2):
+        got = torch.full((R, ld), float("nan"), dtype=x.dtype, device=dev)[:, :V]
+        loss = ce.ce_fwd_bwd_from_host(host, got, t, weight=w, label_smoothing=eps, reduction=red, grad_output=g,
+                                       n_parts=parts)
+        torch.cuda.synchronize()
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+        _check_all(got, t, w, eps, red, g, ref, loss, x_in)
+        if red == "none":
+            assert torch.equal(loss, want_loss)
+
+
 def test_bounded_wait_gives_up_with_status_and_context_survives(ce):
     """A device wait that nothing satisfies ends after its limit with
     CE_FLAG_WAIT_TIMEOUT, and the context keeps working."""
