@@ -91,18 +91,21 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     //  rows <= 96 KB: three CTAs per SM, one CTA per row (4096 x 32000 bf16:
     //    0.102 ms vs 0.121 ms with two CTAs per SM);
     //  rows <= 384 KB: three CTAs per SM, a pair of CTAs per row, so the
-    //    second pass is served by L2 without misses (8192 x 128256 bf16:
-    //    0.759 ms vs 0.775 ms unpaired, vs 0.827 ms paired at two per SM);
+    //    second pass is served by L2 (8192 x 128256 bf16: 0.751 ms vs 0.775
+    //    ms unpaired, vs 0.827 ms paired at two CTAs per SM);
     //  larger rows: one 16-warp CTA per SM, a pair per row: the half rows
     //    waiting in L2 for their second pass (152 x 256 KB at 16384 x 256000
-    //    bf16) fit with room to spare, where three CTAs per SM (117 MB)
-    //    sometimes run at 4.3 ms and mostly at 5.3-5.4 ms; this shape runs at
-    //    4.8-4.9 ms.
+    //    bf16) fit with room to spare (three CTAs per SM: 117 MB, bimodal
+    //    4.3 / 5.4 ms); 4.50 ms.
+    //  In every case the first pass carries no L2 evict-last hint: with the
+    //  hint the second pass missed more (8192 x 128256: 9.5% reads over the
+    //  algorithmic bytes against 5.3%; 16384 x 256000: 4.93 ms against 4.50),
+    //  while the second pass keeps its evict-first hint (without it 0.762 ms).
     if (tune == 0) {
         const int64_t row_bytes = a.vocab * (dtype == CE_DT_F32 ? 4 : 2);
-        tune = row_bytes <= 96 * 1024 ? kTuneThree
-             : row_bytes <= 384 * 1024 ? (kTuneThree | kTuneCluster2)
-                                      : (kTuneWide | kTuneCluster2);
+        tune = row_bytes <= 96 * 1024 ? (kTuneThree | kTuneNoKeep)
+             : row_bytes <= 384 * 1024 ? (kTuneThree | kTuneCluster2 | kTuneNoKeep)
+                                      : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
     }
     const bool pair = (tune & kTuneCluster2) && a.vocab >= 2 * (dtype == CE_DT_F32 ? 4 : 8);
     if (tune & kTuneWide)
