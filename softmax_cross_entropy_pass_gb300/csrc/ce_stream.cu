@@ -91,8 +91,9 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     //  rows <= 96 KB: three CTAs per SM, one CTA per row (4096 x 32000 bf16:
     //    0.102 ms vs 0.121 ms with two CTAs per SM);
     //  rows <= 384 KB: three CTAs per SM, a pair of CTAs per row, so the
-    //    second pass is served by L2 (8192 x 128256 bf16: 0.751 ms vs 0.775
-    //    ms unpaired, vs 0.827 ms paired at two CTAs per SM);
+    //    second pass is served by L2, walking each half row last chunk first
+    //    (8192 x 128256 bf16: 0.746 ms; 0.749 ms first chunk first; 0.775 ms
+    //    unpaired; 0.827 ms paired at two CTAs per SM);
     //  larger rows: one 16-warp CTA per SM, a pair per row: the half rows
     //    waiting in L2 for their second pass (152 x 256 KB at 16384 x 256000
     //    bf16) fit with room to spare (three CTAs per SM: 117 MB, bimodal
@@ -104,7 +105,7 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     if (tune == 0) {
         const int64_t row_bytes = a.vocab * (dtype == CE_DT_F32 ? 4 : 2);
         tune = row_bytes <= 96 * 1024 ? (kTuneThree | kTuneNoKeep)
-             : row_bytes <= 384 * 1024 ? (kTuneThree | kTuneCluster2 | kTuneNoKeep)
+             : row_bytes <= 384 * 1024 ? (kTuneThree | kTuneCluster2 | kTuneNoKeep | kTuneReverse)
                                       : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
     }
     const bool pair = (tune & kTuneCluster2) && a.vocab >= 2 * (dtype == CE_DT_F32 ? 4 : 8);
