@@ -53,6 +53,43 @@ __device__ inline void mma_commit(uint32_t bar) {
                  :: "r"(bar) : "memory");
 }
 
+// ---------------------------------------------------------------- CTA pairs (cta_group::2)
+// A pair of CTAs (ranks 2i, 2i+1 of a cluster) shares one MMA: the even CTA
+// issues it, A's rows are split between the two CTAs' shared memory (first
+// half in the even CTA) and so are B's columns, and each CTA's tensor memory
+// holds its half of the accumulator rows. One warp of each CTA takes part in
+// the allocation and release of the tensor memory.
+__device__ inline void tmem_alloc_pair(uint32_t dst_smem_addr, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;"
+                 :: "r"(dst_smem_addr), "r"(ncols) : "memory");
+}
+__device__ inline void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+__device__ inline void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" :: "r"(taddr), "r"(ncols) : "memory");
+}
+__device__ inline void mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accumulate) {
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "setp.ne.b32 p, %4, 0;\n\t"
+                 "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}"
+                 :: "r"(d_tmem), "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate) : "memory");
+}
+// arrive once on the mbarrier at this shared-memory offset in every CTA of
+// cta_mask when the pair's MMAs issued so far have completed
+__device__ inline void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask) {
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;"
+                 :: "r"(bar), "h"(cta_mask) : "memory");
+}
+// tiled TMA load into this CTA's shared memory, completion counted on an
+// mbarrier that may sit in the peer CTA of the pair (shared::cluster address)
+__device__ inline void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map, int x, int y, uint32_t cluster_bar) {
+    asm volatile("cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+                 " [%0], [%1, {%2, %3}], [%4];"
+                 :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(cluster_bar) : "memory");
+}
+
 // ---------------------------------------------------------------- TMEM -> registers
 // Each thread of the warp gets 32 consecutive 32-bit columns of its lane.
 __device__ inline void tmem_ld_32x32b_x32(uint32_t taddr, uint32_t (&r)[32]) {
