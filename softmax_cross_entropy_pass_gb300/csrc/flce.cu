@@ -351,6 +351,197 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
     if (threadIdx.x == 0 && *abort_flag && g.status) atomicOr(g.status, CE_FLAG_WAIT_TIMEOUT);
 }
 
+// ------------------------------------------------------------------ CTA-pair GEMM
+// The same product with a pair of CTAs (a cluster of 2, one CTA per SM) per
+// 256 x 256 tile: the even CTA issues tcgen05.mma.cta_group::2; each CTA
+// loads its 128 rows of A and its 128 columns of B per 64-deep K stage
+// (32 KB instead of 48 KB per SM), and holds its 128 accumulator rows in its
+// own tensor memory. Stage barriers: `full` in the even CTA counts both
+// CTAs' bytes (TMA loads of the odd CTA complete on it), `empty` in each CTA
+// is signalled by the MMA's multicast commit, `tfull` likewise, and `tempty`
+// in the even CTA collects the 8 epilogue warps of the pair.
+constexpr int GP_M = 256, GP_N = 256, GP_STAGES = 6;
+constexpr int GP_A_BYTES = 128 * GB_K * 2;   // 16 KB: this CTA's half of A
+constexpr int GP_B_BYTES = 128 * GB_K * 2;   // 16 KB: this CTA's half of B
+constexpr size_t GP_SMEM = 1024 + GP_STAGES * (GP_A_BYTES + GP_B_BYTES) + 256;
+
+template <int EPI>
+__global__ void __launch_bounds__(GB_THREADS, 1)
+flce_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmArgs g) {
+    if (g.dyn_count) {
+        int n = __ldg(g.dyn_count) - g.dyn_off;
+        if (g.dyn_dim == 0) {
+            g.M = n < 0 ? 0 : (n < g.M ? n : g.M);
+            g.tiles_m = (g.M + GP_M - 1) / GP_M;
+        } else {
+            g.K = n < 0 ? 0 : (n < g.K ? n : g.K);
+        }
+    }
+    const int ksplit = g.ksplit > 1 ? g.ksplit : 1;
+    const int mn_tiles = g.tiles_m * g.tiles_n;
+    const int num_tiles = mn_tiles * ksplit;
+    const int kiters = (g.K + GB_K - 1) / GB_K;
+    const int kper = (kiters + ksplit - 1) / ksplit;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const int cid = static_cast<int>(cluster_id_x()), ncl = static_cast<int>(nclusters_x());
+    // both CTAs of a pair see the same sizes, so they leave here together
+    if (num_tiles == 0) return;
+    if (kiters == 0) {
+        if (g.out_kind != OUT_F32_ACCUM && warp >= 2) {
+            const int q = warp & 3;
+            const uint32_t zero[32] = {};
+            for (int t = cid; t < num_tiles; t += ncl) {
+                int tm, tn;
+                tile_coords(g, t % mn_tiles, tm, tn);
+                const int row = tm * GP_M + static_cast<int>(rank) * 128 + q * 32 + lane;
+                const int orow = (g.row_map && row < g.M) ? __ldg(g.row_map + row) : row;
+                const int64_t base = static_cast<int64_t>(t / mn_tiles) * g.split_stride;
+                for (int c0 = 0; c0 < GP_N; c0 += 32) epilogue_store(g, row, orow, tn * GP_N + c0, zero, base);
+            }
+        }
+        return;
+    }
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t base = (raw + 1023u) & ~1023u;   // the same offsets in both CTAs of the pair
+    uint8_t *basep = smem_raw + (base - raw);
+    const uint32_t sA = base;
+    const uint32_t sB = base + GP_STAGES * GP_A_BYTES;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(basep + GP_STAGES * (GP_A_BYTES + GP_B_BYTES));
+    uint64_t *full = bars, *empty = bars + GP_STAGES, *tfull = bars + 2 * GP_STAGES, *tempty = bars + 2 * GP_STAGES + 2;
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(bars + 2 * GP_STAGES + 4);
+    int *abort_flag = reinterpret_cast<int *>(tmem_slot + 1);
+    volatile int *abort = abort_flag;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < GP_STAGES; ++st) {
+            mbar_init(smem_u32(&full[st]), 1);
+            mbar_init(smem_u32(&empty[st]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&tfull[a]), 1);
+            mbar_init(smem_u32(&tempty[a]), 8);
+        }
+        *abort_flag = 0;
+        fence_mbar_init_cluster();
+        tma_prefetch_desc(&tmA);
+        tma_prefetch_desc(&tmB);
+    }
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before any remote arrive or copy
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), GB_TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer (both CTAs)
+            uint32_t it = 0;
+            for (int t = cid; t < num_tiles; t += ncl) {
+                int tm, tn;
+                tile_coords(g, t % mn_tiles, tm, tn);
+                const int kb = (t / mn_tiles) * kper, ke = min(kiters, kb + kper);
+                const int row0 = tm * GP_M + static_cast<int>(rank) * 128, col0 = tn * GP_N + static_cast<int>(rank) * 128;
+                for (int k = kb; k < ke; ++k, ++it) {
+                    const uint32_t st = it % GP_STAGES, r = it / GP_STAGES;
+                    if (r > 0) mbar_wait_bounded<false>(smem_u32(&empty[st]), (r - 1) & 1u, abort);
+                    const uint32_t fb = mapa_shared(smem_u32(&full[st]), 0);  // the even CTA's barrier
+                    if (rank == 0) mbar_expect_tx(smem_u32(&full[st]), 2 * (GP_A_BYTES + GP_B_BYTES));
+                    const uint32_t a_dst = sA + st * GP_A_BYTES, b_dst = sB + st * GP_B_BYTES;
+                    if (!g.a_mn) tma_load_2d_pair(a_dst, &tmA, k * GB_K, row0, fb);
+                    else for (int j = 0; j < 2; ++j) tma_load_2d_pair(a_dst + j * 8192, &tmA, row0 + 64 * j, k * GB_K, fb);
+                    if (!g.b_mn) tma_load_2d_pair(b_dst, &tmB, k * GB_K, col0, fb);
+                    else for (int j = 0; j < 2; ++j) tma_load_2d_pair(b_dst + j * 8192, &tmB, col0 + 64 * j, k * GB_K, fb);
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ MMA issuer (even CTA)
+            const uint32_t idesc = idesc_bf16_f32(GP_M, GP_N, g.a_mn, g.b_mn);
+            const uint32_t a_kstep = g.a_mn ? 2048u : 32u, b_kstep = g.b_mn ? 2048u : 32u;
+            const uint32_t a_lbo = g.a_mn ? 8192u : 16u, b_lbo = g.b_mn ? 8192u : 16u;
+            uint32_t it = 0, lt = 0;
+            for (int t = cid; t < num_tiles; t += ncl, ++lt) {
+                const uint32_t acc = lt & 1u, u = lt >> 1;
+                if (u > 0) mbar_wait_bounded<false>(smem_u32(&tempty[acc]), (u - 1) & 1u, abort);
+                tc_fence_after();
+                const uint32_t d = tmem + acc * GP_N;
+                const int kb = (t / mn_tiles) * kper, ke = min(kiters, kb + kper);
+                for (int k = kb; k < ke; ++k, ++it) {
+                    const uint32_t st = it % GP_STAGES, r = it / GP_STAGES;
+                    mbar_wait_bounded<false>(smem_u32(&full[st]), r & 1u, abort);
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < GB_K / 16; ++kk) {
+                        const uint64_t ad = smem_desc_sw128(sA + st * GP_A_BYTES + kk * a_kstep, a_lbo, 1024);
+                        const uint64_t bd = smem_desc_sw128(sB + st * GP_B_BYTES + kk * b_kstep, b_lbo, 1024);
+                        mma_bf16_pair(d, ad, bd, idesc, (k > kb || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit_pair_mc(smem_u32(&empty[st]), 0x3);
+                }
+                mma_commit_pair_mc(smem_u32(&tfull[acc]), 0x3);
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue (warps 2..5, both CTAs)
+        const int q = warp & 3;
+        const uint32_t tempty0 = mapa_shared(smem_u32(&tempty[0]), 0);
+        uint32_t lt = 0;
+        for (int t = cid; t < num_tiles; t += ncl, ++lt) {
+            int tm, tn;
+            tile_coords(g, t % mn_tiles, tm, tn);
+            const int64_t obase = static_cast<int64_t>(t / mn_tiles) * g.split_stride;
+            const uint32_t acc = lt & 1u, u = lt >> 1;
+            mbar_wait_bounded<false>(smem_u32(&tfull[acc]), u & 1u, abort);
+            tc_fence_after();
+            const int row = tm * GP_M + static_cast<int>(rank) * 128 + q * 32 + lane;
+            const int orow = (g.row_map && row < g.M) ? __ldg(g.row_map + row) : row;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * GP_N;
+            RowState stt = row_state_empty();
+            int y_rel = -(1 << 30);
+            if (EPI != 0 && row < g.M) {
+                const int64_t y = load_target(g.st_target, g.st_tgt32, row);
+                if (target_valid(y, g.st_ignore, g.N)) y_rel = static_cast<int>(y - static_cast<int64_t>(tn) * GP_N);
+            }
+#pragma unroll 1
+            for (int c0 = 0; c0 < GP_N; c0 += 32) {
+                uint32_t v[32];
+                tmem_ld_32x32b_x32(taddr + c0, v);
+                tmem_ld_wait();
+                if (EPI == 0) {
+                    epilogue_store(g, row, orow, tn * GP_N + c0, v, obase);
+                } else if (row < g.M) {
+                    const int skip = (static_cast<unsigned>(y_rel - c0) < 32u) ? y_rel - c0 : -1;
+                    epilogue_stats<(EPI > 0 ? EPI - 1 : 0)>(g, row, tn * GP_N + c0, v, stt, skip);
+                }
+            }
+            if (EPI != 0 && row < g.M)
+                g.part[static_cast<int64_t>(row) * g.tiles_n + tn] = make_float4(stt.m, stt.s, stt.r, stt.n);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) {
+                if (rank == 0) mbar_arrive(smem_u32(&tempty[acc]));
+                else mbar_arrive_remote(tempty0 + acc * 8u);
+            }
+        }
+    }
+    __syncthreads();
+    cluster_sync_all();  // every MMA of the pair has completed and both CTAs have read their accumulators
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, GB_TMEM_COLS);
+    }
+    if (threadIdx.x == 0 && *abort_flag && g.status) atomicOr(g.status, CE_FLAG_WAIT_TIMEOUT);
+    cluster_sync_all();  // no CTA leaves while its peer may still signal one of its barriers
+}
+
 // ------------------------------------------------------------------ small kernels
 // Rows past a device-side count are skipped: n = clamp(*count - off, 0, n).
 __device__ inline int64_t dyn_rows(int64_t n, const int *count, int64_t off) {
@@ -711,32 +902,59 @@ int gemm_fit_ksplit(int K, int ksplit) {
     return ksplit;
 }
 
+// Resident CTA pairs of a pair kernel on a device (0 if unknown), asked once.
+static int pair_clusters(const void *fn, int dev) {
+    static const void *fns[8];
+    static int devs[8], vals[8], used = 0;
+    for (int i = 0; i < used; ++i)
+        if (fns[i] == fn && devs[i] == dev) return vals[i];
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * 128);
+    cfg.blockDim = dim3(GB_THREADS);
+    cfg.dynamicSmemBytes = GP_SMEM;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = 2;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, fn, &cfg) != cudaSuccess) n = 0;
+    (void)cudaGetLastError();
+    if (used < 8) { fns[used] = fn; devs[used] = dev; vals[used] = n; ++used; }
+    return n;
+}
+
 // D[M,N] = A[M,K] B[K,N]. A: K-major = memory [M, K] (lda >= K); MN-major =
 // memory [K, M] (lda >= M). B: K-major = memory [N, K]; MN-major = memory [K, N].
 cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B, int64_t ldb,
                       int b_mn, int out_kind, void *out, int64_t ldo, const float *bias, unsigned int *status,
                       cudaStream_t s, const GemmDyn *dyn, const GemmStats *stats, int ksplit,
-                      int64_t split_stride) {
+                      int64_t split_stride, int mode) {
     if (M <= 0 || N <= 0 || K <= 0) return cudaSuccess;
     if (stats && out_kind != OUT_F32_STORE) return cudaErrorInvalidValue;
     if (ksplit < 1) ksplit = 1;
     if (ksplit > 1 && (out_kind != OUT_F32_STORE || stats || (dyn && dyn->dim == 1) || bias ||
                        gemm_fit_ksplit(K, ksplit) != ksplit))
         return cudaErrorInvalidValue;
+    if (mode < GEMM_AUTO || mode > GEMM_PAIR) return cudaErrorInvalidValue;
+    // CTA pairs (256 x 256 tiles) when both sides span at least two pair tiles
+    const bool pair = mode == GEMM_PAIR || (mode == GEMM_AUTO && M >= 2 * GP_M && N >= 2 * GP_N);
     CUtensorMap ta, tb;
     cudaError_t e;
-    if (!a_mn) e = make_tmap(&ta, A, M, K, lda, GB_K, GB_M);
+    if (!a_mn) e = make_tmap(&ta, A, M, K, lda, GB_K, GB_M);          // 128 rows per CTA in both kernels
     else e = make_tmap(&ta, A, K, M, lda, 64, GB_K);
     if (e != cudaSuccess) return e;
-    if (!b_mn) e = make_tmap(&tb, B, N, K, ldb, GB_K, GB_N);
+    if (!b_mn) e = make_tmap(&tb, B, N, K, ldb, GB_K, pair ? 128 : GB_N);
     else e = make_tmap(&tb, B, K, N, ldb, 64, GB_K);
     if (e != cudaSuccess) return e;
     GemmArgs g{};
     g.M = M; g.N = N; g.K = K;
     g.a_mn = a_mn; g.b_mn = b_mn;
     g.out_kind = out_kind; g.out = out; g.ldo = ldo; g.bias = bias;
-    g.tiles_m = (M + GB_M - 1) / GB_M;
-    g.tiles_n = (N + GB_N - 1) / GB_N;
+    g.tiles_m = (M + (pair ? GP_M : GB_M) - 1) / (pair ? GP_M : GB_M);
+    g.tiles_n = (N + GB_N - 1) / GB_N;                                 // 256 columns in both kernels
     g.m_fastest = g.tiles_m <= g.tiles_n ? 1 : 0;  // the operand of the short side stays in L2
     g.status = status;
     g.ksplit = ksplit;
@@ -758,24 +976,48 @@ cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn,
         if (stats->smooth_mode < 0 || stats->smooth_mode > 2 || (stats->smooth_mode == 2 && !stats->weight))
             return cudaErrorInvalidValue;
     }
-    static const void *const kernels[4] = {
-        reinterpret_cast<const void *>(&flce_gemm_kernel<0>), reinterpret_cast<const void *>(&flce_gemm_kernel<1>),
-        reinterpret_cast<const void *>(&flce_gemm_kernel<2>), reinterpret_cast<const void *>(&flce_gemm_kernel<3>)};
+    static const void *const kernels[2][4] = {
+        {reinterpret_cast<const void *>(&flce_gemm_kernel<0>), reinterpret_cast<const void *>(&flce_gemm_kernel<1>),
+         reinterpret_cast<const void *>(&flce_gemm_kernel<2>), reinterpret_cast<const void *>(&flce_gemm_kernel<3>)},
+        {reinterpret_cast<const void *>(&flce_gemm_pair_kernel<0>),
+         reinterpret_cast<const void *>(&flce_gemm_pair_kernel<1>),
+         reinterpret_cast<const void *>(&flce_gemm_pair_kernel<2>),
+         reinterpret_cast<const void *>(&flce_gemm_pair_kernel<3>)}};
+    const void *fn = kernels[pair ? 1 : 0][epi];
+    const size_t smem = pair ? GP_SMEM : GB_SMEM;
     // the shared-memory limit is a per-device attribute of each kernel: set it once per device
-    static uint64_t attr_set[4] = {};
+    static uint64_t attr_set[2][4] = {};
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     const uint64_t bit = dev < 64 ? (1ull << dev) : 0ull;
-    if (!bit || !(attr_set[epi] & bit)) {
-        e = cudaFuncSetAttribute(kernels[epi], cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(GB_SMEM));
+    if (!bit || !(attr_set[pair ? 1 : 0][epi] & bit)) {
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
-        attr_set[epi] |= bit;
+        attr_set[pair ? 1 : 0][epi] |= bit;
     }
     const int tiles = g.tiles_m * g.tiles_n * ksplit;
-    const int grid = tiles < sm_count() ? tiles : sm_count();
     void *args[] = {&ta, &tb, &g};
-    return cudaLaunchKernel(kernels[epi], dim3(grid), dim3(GB_THREADS), args, GB_SMEM, s);
+    if (!pair) {
+        const int grid = tiles < sm_count() ? tiles : sm_count();
+        return cudaLaunchKernel(fn, dim3(grid), dim3(GB_THREADS), args, GB_SMEM, s);
+    }
+    // persistent pairs: no more clusters than can be resident at once
+    int clusters = pair_clusters(fn, dev);
+    if (clusters < 1) clusters = sm_count() / 2 > 0 ? sm_count() / 2 : 1;
+    if (clusters > tiles) clusters = tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * clusters));
+    cfg.blockDim = dim3(GB_THREADS);
+    cfg.dynamicSmemBytes = GP_SMEM;
+    cfg.stream = s;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = 2;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
 }  // namespace ce

@@ -39,10 +39,16 @@ struct GemmStats {
 };
 constexpr int kGemmTileN = 256;
 
+// `mode`: GEMM_AUTO (CTA pairs on 256 x 256 tiles when M and N both span at
+// least two such tiles, else one CTA per 128 x 256 tile), GEMM_ONE_CTA,
+// GEMM_PAIR.
+enum { GEMM_AUTO = 0, GEMM_ONE_CTA = 1, GEMM_PAIR = 2 };
+
 cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn, const void *B,
                       int64_t ldb, int b_mn, int out_kind, void *out, int64_t ldo, const float *bias,
                       unsigned int *status, cudaStream_t s, const GemmDyn *dyn = nullptr,
-                      const GemmStats *stats = nullptr, int ksplit = 1, int64_t split_stride = 0);
+                      const GemmStats *stats = nullptr, int ksplit = 1, int64_t split_stride = 0,
+                      int mode = GEMM_AUTO);
 
 // K steps of 64 per split-K part: ksplit parts over kiters steps, each
 // non-empty (the split count actually used, <= ksplit).

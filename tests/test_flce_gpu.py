@@ -30,8 +30,11 @@ def _rand_bf16(*shape, seed=0, scale=1.0):
 
 @pytest.mark.parametrize("a_mn", [False, True])
 @pytest.mark.parametrize("b_mn", [False, True])
-@pytest.mark.parametrize("shape", [(128, 256, 64), (200, 296, 136), (1024, 2048, 1024), (384, 512, 4096)])
+@pytest.mark.parametrize("shape", [(128, 256, 64), (200, 296, 136), (1024, 2048, 1024), (384, 512, 4096),
+                                   (520, 776, 200), (2048, 1536, 2112)])
 def test_gemm_layouts_against_float64(ce, a_mn, b_mn, shape):
+    """M and N both >= 512 take the CTA-pair kernel (256 x 256 tiles), the
+    others one CTA per 128 x 256 tile."""
     M, N, K = shape
     A = _rand_bf16(M, K, seed=1)                # logical [M, K]
     B = _rand_bf16(N, K, seed=2)                # logical [N, K] (B^T)
@@ -45,8 +48,8 @@ def test_gemm_layouts_against_float64(ce, a_mn, b_mn, shape):
     assert (err <= bound).all(), f"max err {float(err.max()):.3e}"
 
 
-def test_gemm_bias_accumulate_and_bf16_out(ce):
-    M, N, K = 256, 512, 256
+@pytest.mark.parametrize("M,N,K", [(256, 512, 256), (768, 1024, 320)])
+def test_gemm_bias_accumulate_and_bf16_out(ce, M, N, K):
     A = _rand_bf16(M, K, seed=3).cuda()
     B = _rand_bf16(N, K, seed=4).cuda()
     bias = torch.randn(N, device="cuda")
