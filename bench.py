@@ -240,7 +240,8 @@ def measure_e2e(ce, pristine, target, work, flush, loss, kw, stream, steps):
     host_loss = torch.empty(1, dtype=torch.float32).pin_memory()
     dev_t = torch.empty_like(target)
     copy_stream = torch.cuda.Stream(device=work.device)
-    piped = kw.get("variant", "auto") == "auto" and not kw.get("tune") and not kw.get("cluster")
+    piped = kw.get("variant", "auto") == "auto" and not kw.get("tune") and not kw.get("cluster") and \
+        not kw.get("softcap") and not kw.get("z_loss") and kw.get("accuracy") is None
     fkw = {k: v for k, v in kw.items() if k not in ("variant", "tune", "cluster")}
 
     def one():
@@ -409,6 +410,14 @@ def run_ours(args):
     weight = inp["weight"]
     kw = dict(label_smoothing=cfg.label_smoothing, reduction=cfg.reduction, grad_output=g, loss=loss,
               ws=ws, stream=stream, variant=args.variant, cluster=args.cluster, weight=weight, tune=args.tune)
+    options = {}
+    if args.softcap > 0:
+        options["softcap"] = args.softcap
+    if args.z_loss > 0:
+        options["z_loss"] = args.z_loss
+    if args.accuracy:
+        options["accuracy"] = torch.empty(1, dtype=torch.float32, device=device)
+    kw.update(options)
 
     def step():
         return ce.ce_fwd_bwd(work, target, **kw)
@@ -422,7 +431,7 @@ def run_ours(args):
                             weighted=weight is not None)
     n_valid = int((target >= 0).sum().item())
     esz = pristine.element_size()
-    path = args.variant if args.variant != "auto" else ce.auto_variant(pristine, target, weight=weight)
+    path = args.variant if args.variant != "auto" else ce.auto_variant(pristine, target, weight=weight, **options)
     # algorithmic bytes per step of the chosen path: the one-read paths read
     # every valid row once and write every row once (ignored rows are only
     # zeroed); the split path also reads every row in its statistics pass.
@@ -524,6 +533,7 @@ def run_ours(args):
                                f"{'class weights, ' if cfg.weighted else ''}gradient in place",
                    "global_batch": R * world, "seq_len": None, "parallelism": f"replicas x{world}",
                    "variant": args.variant, "path": path, "tune": args.tune, "fused_plan": plan,
+                   "options": {k: (v if k != "accuracy" else True) for k, v in options.items()} or None,
                    "l2": "inputs 2.1 GB > 129 MB L2; logits restored and a 256 MB buffer written "
                          "before every step, outside the timed region"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
@@ -564,6 +574,9 @@ def main():
     ap.add_argument("--flce-only", action="store_true", help="only the fused-linear measurement")
     ap.add_argument("--gemm-only", default="", help="only one GEMM: M,N,K,a_mn,b_mn")
     ap.add_argument("--rows", type=int, default=0, help="rows of a smaller case of the workload (profiling)")
+    ap.add_argument("--softcap", type=float, default=0.0, help="logit softcap c (0: off)")
+    ap.add_argument("--z-loss", type=float, default=0.0, help="z-loss weight lambda (0: off)")
+    ap.add_argument("--accuracy", action="store_true", help="also compute the token accuracy")
     ap.add_argument("--vocab", type=int, default=0,
                     help="another vocabulary size for the workload (e.g. one that leaves rows unaligned)")
     ap.add_argument("--workload", default=WORKLOAD,

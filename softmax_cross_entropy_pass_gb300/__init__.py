@@ -283,9 +283,11 @@ def ce_fwd_bwd_from_host(host_logits, dev_logits, target, *, grad_output=None, w
     return loss
 
 
-def auto_variant(logits, target, *, weight=None, label_smoothing=0.0) -> str:
+def auto_variant(logits, target, *, weight=None, label_smoothing=0.0, softcap=0.0, z_loss=0.0,
+                 accuracy=None) -> str:
     """The kernel path ce_fwd_bwd(variant="auto") takes for these tensors."""
-    p = make_params(logits, target, weight=weight, label_smoothing=label_smoothing)
+    p = make_params(logits, target, weight=weight, label_smoothing=label_smoothing, softcap=softcap,
+                    z_loss=z_loss, accuracy=accuracy)
     out = ctypes.c_int32()
     _check(_lib.ce_select_variant(ctypes.byref(p), _ptr(logits), ctypes.byref(out)), "ce_select_variant")
     return {v: k for k, v in VARIANTS.items()}[out.value]

@@ -150,13 +150,10 @@ bool fused_layout_ok(const ce_params *p, const void *x) {
 
 // The path of CE_VARIANT_AUTO: the stream kernel (HBM read once, the second
 // read served by L2 through a bulk-copy ring) is the fastest measured path
-// on GB300 for every row size and takes any row alignment (the unaligned
-// head and tail of a row go through plain accesses); the row pass carries
-// the options; the split path remains for callers that ask for it.
-int auto_path(const ce_params *p, const void *) {
-    if (has_options(p)) return CE_VARIANT_ROWPASS;  // the options live in the row-pass and split kernels
-    return CE_VARIANT_STREAM;
-}
+// on GB300 for every row size, takes any row alignment (the unaligned head
+// and tail of a row go through plain accesses) and carries the options; the
+// row pass and the split path remain for callers that ask for them.
+int auto_path(const ce_params *, const void *) { return CE_VARIANT_STREAM; }
 
 }  // namespace
 
@@ -262,7 +259,7 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
         return CE_ERR_INVALID_ARG;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
 
-    if ((path == CE_VARIANT_STREAM || path == CE_VARIANT_FUSED) && has_options(p)) return CE_ERR_UNSUPPORTED;
+    if (path == CE_VARIANT_FUSED && has_options(p)) return CE_ERR_UNSUPPORTED;
     if (path == CE_VARIANT_STREAM) {
         cudaError_t e = enqueue_prep(p, target, ws, s);
         if (e != cudaSuccess) return cuda_fail(e);

@@ -34,7 +34,9 @@ static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, i
     // rows that all start on a 16-byte boundary take the fixed-geometry instantiation
     const int64_t esz = dtype == CE_DT_F32 ? 4 : 2;
     const bool ragged = (reinterpret_cast<uintptr_t>(a.grad) & 15u) != 0 || (a.n_rows > 1 && ((a.ld * esz) & 15) != 0);
-    const void *fn = ragged ? stream_kernel_ragged(dtype, mode, SHAPE, CL) : stream_kernel_for<false>(dtype, mode, SHAPE, CL);
+    const void *fn = a.softcap > 0.f ? stream_kernel_softcap(dtype, mode, SHAPE, CL, ragged)
+                   : (a.z_loss > 0.f || a.accuracy) ? stream_kernel_options(dtype, mode, SHAPE, CL, ragged)
+                   : ragged ? stream_kernel_ragged(dtype, mode, SHAPE, CL) : stream_kernel_for<false>(dtype, mode, SHAPE, CL);
     if (!fn) return cudaErrorInvalidValue;
     cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SH::kSmem);
     if (e != cudaSuccess) return e;
@@ -109,6 +111,12 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
                                       : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
     }
     const bool pair = (tune & kTuneCluster2) && a.vocab >= 2 * (dtype == CE_DT_F32 ? 4 : 8);
+    if (a.softcap > 0.f || a.z_loss > 0.f || a.accuracy) {
+        // the options are built for the three shapes the library picks by row size
+        if ((tune & kTuneWide) && pair) return launch_stream_shape<1, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
+        return pair ? launch_stream_shape<2, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+                    : launch_stream_shape<2, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
+    }
     if (tune & kTuneWide)
         return pair ? launch_stream_shape<1, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
                     : launch_stream_shape<1, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);

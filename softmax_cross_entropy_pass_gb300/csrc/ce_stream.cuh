@@ -57,6 +57,7 @@ struct StreamSmem {
     // waits for every warp)
     RowState red[2][16];    // per-warp partial states of pass 1
     float2 defer[2][16];    // class-weighted smoothing: per-warp {sum w x, sum w} of pass 2
+    ArgMax am[2][16];       // token accuracy: per-warp first column of the row maximum
     float xy[2];            // the target logit
     int abort;
 };
@@ -140,18 +141,23 @@ __device__ inline float4 load_w4(const float *w, int64_t c, bool vec4) {
 // the first CTA of the row.
 __device__ inline void finish_deferred_loss(const RowArgs &a, uint32_t rank, int64_t row, float m, float s, float xy,
                                             float r, float n, int yg, float wy, float w_all, float eps,
-                                            float inv_v) {
+                                            float inv_v, float z_loss) {
     if (rank != 0) return;
     const float rrel = n > 0.f ? __fsub_rn(r, __fmul_rn(n, m)) : 0.f;
-    const RowScalars rl = make_row_scalars(m, s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f);
+    const RowScalars rl = make_row_scalars(m, s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f, z_loss);
     if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
     else a.row_loss[row] = rl.loss;
 }
 
 // RAG: rows may start off a 16-byte boundary (per-row head and tail);
 // without it every row of the launch is 16-byte aligned and the geometry is
-// fixed for the whole launch.
-template <int DT, int MODE, int SHAPE, int CL, bool RAG>
+// fixed for the whole launch. OPT 1: z-loss and token accuracy (the argmax
+// of the raw logits, the same column as that of the capped ones since tanh
+// is increasing); OPT 2: the same plus softcap (every logit becomes
+// c tanh(x / c), the gradient gains the factor 1 - (z / c)^2). Softcap has
+// its own instantiations: its accurate tanh, inlined into the element
+// loops, costs instruction-cache room even when it is not taken.
+template <int DT, int MODE, int SHAPE, int CL, bool RAG, int OPT = 0>
 __global__ void __launch_bounds__(StreamShape<SHAPE>::kThreads, StreamShape<SHAPE>::kCtasPerSm)
 ce_stream_kernel(RowArgs a, int tune) {
     using F = Fmt<DT>;
@@ -192,6 +198,11 @@ ce_stream_kernel(RowArgs a, int tune) {
     // weights as float4 when the base allows it (each row's interior start decides the rest)
     const bool w_base16 = (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
     const RowGeom g_aligned = row_geom_aligned<F::kBytes>(lo, L);
+    constexpr bool FEAT = OPT != 0;
+    constexpr bool CAPF = OPT == 2;
+    const float cap = CAPF ? a.softcap : 0.f;
+    const float zl = FEAT ? a.z_loss : 0.f;
+    const bool want_am = FEAT && a.accuracy != nullptr;
 
     if (tid == 0) {
         for (int s = 0; s < kStreamSlots; ++s) {
@@ -289,6 +300,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             const float wy = a.weight ? __ldg(a.weight + yg) : 1.f;
             // ------------------------------------------------ pass 1: statistics
             RowState st = row_state_empty();
+            ArgMax am{-INFINITY, 0x7fffffff};
             for (int c = 0; c < nch; ++c, ++it) {
                 const uint32_t s = it % kStreamSlots;
                 mbar_wait_bounded<false>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
@@ -298,7 +310,34 @@ ce_stream_kernel(RowArgs a, int tune) {
                 // does one of this thread's vectors hold the target column?
                 const unsigned q = static_cast<unsigned>(y / VEC - v0 - tid);
                 const bool mine = q < static_cast<unsigned>(VPT * NCT) && (q % NCT) == 0;
-                if (nv == VPC && !mine) {
+                if (CAPF && cap > 0.f) {
+                    // softcap: capped logits, first-maximum column of the raw logits
+                    for (int v = tid; v < nv; v += NCT) {
+                        const uint4 raw = ld_shared_v4(base_s + 16u * v);
+                        const int vb = (v0 + v) * VEC;
+                        float x[VEC], z[VEC];
+                        F::unpack(raw, x);
+                        float zmax = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) {
+                            z[j] = cap > 0.f ? softcap_logit(x[j], cap) : x[j];
+                            zmax = fmaxf(zmax, z[j]);
+                        }
+                        if (want_am) {
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j)
+                                am = argmax_merge(am, ArgMax{x[j], static_cast<int>(vlo + vb + j)});
+                        }
+                        const int skip = (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) ? y - vb : -1;
+                        if (skip >= 0) {
+                            float zv = 0.f;
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) zv = (j == skip) ? z[j] : zv;
+                            S.xy[rp] = zv;  // the capped target logit, for the merge
+                        }
+                        row_state_add<VEC, P1S>(st, z, zmax, skip, nullptr);
+                    }
+                } else if (nv == VPC && !mine) {
                     // full chunk, no target: one max per chunk, four independent sums
                     uint4 raw[VPT];
 #pragma unroll
@@ -306,6 +345,20 @@ ce_stream_kernel(RowArgs a, int tune) {
                     float cm = F::vmax(raw[0]);
 #pragma unroll
                     for (int k = 1; k < VPT; ++k) cm = fmaxf(cm, F::vmax(raw[k]));
+                    if (FEAT && want_am && cm > am.v) {
+                        // a new maximum: its first column among this thread's vectors of the
+                        // chunk (earlier chunks hold smaller columns, so ties keep those)
+                        int col = -1;
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) {
+                            float xk[VEC];
+                            F::unpack(raw[k], xk);
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e)
+                                if (col < 0 && xk[e] == cm) col = static_cast<int>(vlo + (v0 + tid + k * NCT) * VEC + e);
+                        }
+                        am = ArgMax{cm, col};
+                    }
                     if (cm > st.m) {
                         if (st.m != -INFINITY) st.s *= ex2_hw((st.m - cm) * kLog2e);
                         st.m = cm;
@@ -360,6 +413,10 @@ ce_stream_kernel(RowArgs a, int tune) {
                             for (int j = 0; j < VEC; ++j) xv = (j == skip) ? x[j] : xv;
                             S.xy[rp] = xv;  // the target logit, for the merge
                         }
+                        if (FEAT && want_am) {
+#pragma unroll
+                            for (int e = 0; e < VEC; ++e) am = argmax_merge(am, ArgMax{x[e], static_cast<int>(vlo + vb + e)});
+                        }
                         row_state_add<VEC, P1S>(st, x, F::vmax(raw), skip, nullptr);
                     }
                 }
@@ -368,7 +425,9 @@ ce_stream_kernel(RowArgs a, int tune) {
             }
             if (tid < nedge) {
                 const int64_t c = edge_c;
-                float x = F::load1(rowp, c);
+                const float xr = F::load1(rowp, c);
+                float x = (CAPF && cap > 0.f) ? softcap_logit(xr, cap) : xr;
+                if (want_am) am = argmax_merge(am, ArgMax{xr, static_cast<int>(c)});
                 if (c == yg) S.xy[rp] = x;
                 row_state_add<1, P1S>(st, &x, x, (c == yg) ? 0 : -1, nullptr);
             }
@@ -379,10 +438,18 @@ ce_stream_kernel(RowArgs a, int tune) {
             // scalar work.
             st = warp_merge(st);
             if (lane == 0) S.red[rp][warp] = st;
+            if (want_am) {
+                am = warp_argmax(am);
+                if (lane == 0) S.am[rp][warp] = am;
+            }
             stream_consumer_sync<NCW>();
             RowState m = lane < kStreamConsumerWarps ? S.red[rp][lane] : row_state_empty();
             m = warp_merge(m);
             float xy = S.xy[rp];
+            if (want_am) {
+                am = lane < kStreamConsumerWarps ? S.am[rp][lane] : ArgMax{-INFINITY, 0x7fffffff};
+                am = warp_argmax(am);
+            }
             if (DEFER) {
                 // r and n of this state carry the previous row's deferred sums (this CTA's
                 // part, then both CTAs' after the exchange); pass 1 left them at 0
@@ -405,17 +472,20 @@ ce_stream_kernel(RowArgs a, int tune) {
                     for (uint32_t d = 0; d < static_cast<uint32_t>(CL); ++d) {
                         const uint32_t rs_addr = mapa_shared(my_slot, d);
                         st_cluster_v4(rs_addr, m.m, m.s, m.r, m.n);
-                        st_cluster_v4(rs_addr + 16u, xy, 0.f, 0.f, 0.f);
+                        st_cluster_v4(rs_addr + 16u, xy, am.v, __int_as_float(am.i), 0.f);
                         mbar_arrive_remote(mapa_shared(my_bar, d));
                     }
                 }
                 mbar_wait_bounded<true>(my_bar, (j >> 1) & 1u, abort);
                 RowState tot = row_state_empty();
+                ArgMax amt{-INFINITY, 0x7fffffff};
                 for (int d = 0; d < CL; ++d) {
                     const StreamXSlot &xs = S.slot[par][d];
                     tot = row_state_merge(tot, RowState{xs.m, xs.s, xs.r, xs.n});
+                    if (want_am) amt = argmax_merge(amt, ArgMax{xs.pad0, __float_as_int(xs.pad1)});
                 }
                 m = tot;
+                am = amt;
                 xy = S.slot[par][yg / half].xy;
             }
             if (!have_norm) {
@@ -430,7 +500,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             if (DEFER) {
                 if (writer) {
                     if (pend) finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, m.r, m.n,
-                                                   pend_yg, pend_wy, w_all, eps, inv_v);
+                                                   pend_yg, pend_wy, w_all, eps, inv_v, zl);
                     pend_row = row; pend_m = m.m; pend_s = m.s; pend_xy = xy; pend_yg = yg; pend_wy = wy;
                 }
                 rrel = 0.f;  // the gradient does not use it; this row's loss waits for pass 2
@@ -439,11 +509,12 @@ ce_stream_kernel(RowArgs a, int tune) {
             float scale = g;
             if (a.reduction == CE_RED_MEAN) scale = w_y_sum != 0.f ? g / w_y_sum : 0.f;
             if (writer && rank == 0 && !DEFER) {
-                const RowScalars rl = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f);
+                const RowScalars rl = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f, zl);
                 if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
                 else a.row_loss[row] = rl.loss;
             }
-            const RowScalars rs = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, scale);
+            if (want_am && writer && rank == 0 && am.i == yg) atomicAdd(&a.ctl->n_correct, 1u);
+            const RowScalars rs = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, scale, zl);
             // grad_elem over packed pairs: p = 2^((x - m) log2e - log2 d), g = a p - b w
             const F2 rs_m = f2(rs.m, rs.m), rs_l2 = f2(kLog2e, kLog2e), rs_nl = f2(rs.neg_log2d, rs.neg_log2d);
             const F2 rs_a = f2(rs.a, rs.a), rs_nb = f2(-rs.b, -rs.b);
@@ -457,10 +528,30 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const int v0 = c * VPC;
                 const int nv = min(VPC, nvec - v0);
                 for (int v = tid; v < nv; v += NCT) {
-                    float x[VEC], gr[VEC];
+                    float x[VEC], gr[VEC], z[VEC];
                     F::unpack(ld_shared_v4(base_s + 16u * v), x);
                     const int vb = (v0 + v) * VEC;
-                    if (MODE == 2) {
+                    if (CAPF && cap > 0.f) {
+                        // softcap: the gradient of the capped logits, times dz/dx below
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) z[j] = cap > 0.f ? softcap_logit(x[j], cap) : x[j];
+#pragma unroll
+                        for (int h = 0; h < VEC / 4; ++h) {
+                            const float4 wv = MODE == 2 ? load_w4(a.weight, vlo + vb + 4 * h, w4)
+                                                        : make_float4(1.f, 1.f, 1.f, 1.f);
+                            gr[4 * h] = grad_elem(rs, z[4 * h], wv.x);
+                            gr[4 * h + 1] = grad_elem(rs, z[4 * h + 1], wv.y);
+                            gr[4 * h + 2] = grad_elem(rs, z[4 * h + 2], wv.z);
+                            gr[4 * h + 3] = grad_elem(rs, z[4 * h + 3], wv.w);
+                            if (DEFER) {
+                                const F2 w01 = f2(wv.x, wv.y), w23 = f2(wv.z, wv.w);
+                                dr[0] = f2_fma(w01, f2(z[4 * h], z[4 * h + 1]), dr[0]);
+                                dr[1] = f2_fma(w23, f2(z[4 * h + 2], z[4 * h + 3]), dr[1]);
+                                dn[0] = f2_add(dn[0], w01);
+                                dn[1] = f2_add(dn[1], w23);
+                            }
+                        }
+                    } else if (MODE == 2) {
 #pragma unroll
                         for (int h = 0; h < VEC / 4; ++h) {
                             const float4 wv = load_w4(a.weight, vlo + vb + 4 * h, w4);
@@ -487,6 +578,10 @@ ce_stream_kernel(RowArgs a, int tune) {
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
                     }
+                    if (CAPF && cap > 0.f) {
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) gr[j] *= softcap_deriv(z[j], cap);
+                    }
                     st_stream(vp + v0 + v, F::pack(gr));  // vp points at this CTA's slice
                 }
                 __syncwarp();
@@ -496,10 +591,13 @@ ce_stream_kernel(RowArgs a, int tune) {
             if (tid < nedge) {
                 const int64_t c = edge_c;
                 const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
-                const float xe = F::load1(rowp, c);
+                const float xr = F::load1(rowp, c);
+                const float xe = (CAPF && cap > 0.f) ? softcap_logit(xr, cap) : xr;
                 er = wc * xe;
                 en = wc;
-                F::store1(rowp, c, (c == yg) ? rs.dxy : grad_elem(rs, xe, wc));
+                float ge = (c == yg) ? rs.dxy : grad_elem(rs, xe, wc);
+                if (CAPF && cap > 0.f) ge *= softcap_deriv(xe, cap);
+                F::store1(rowp, c, ge);
             }
             if (DEFER) {
                 // this thread's, then this warp's, deferred sums (fixed order), for the next merge
@@ -547,11 +645,11 @@ ce_stream_kernel(RowArgs a, int tune) {
                     pn = tot.n;
                 }
                 finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, pr, pn, pend_yg, pend_wy, w_all,
-                                     eps, inv_v);
+                                     eps, inv_v, zl);
             }
         }
         // ---------------------------------------------------- batch reduction (last CTA)
-        if (a.reduction != CE_RED_NONE && !a.no_finalize) {
+        if ((a.reduction != CE_RED_NONE || want_am) && !a.no_finalize) {
             __shared__ unsigned sh_last;
             __shared__ double sh_sum[kStreamConsumerWarps];
             if (!have_norm) pdl_wait();
@@ -562,7 +660,13 @@ ce_stream_kernel(RowArgs a, int tune) {
                 sh_last = (prev == gridDim.x - 1) ? 1u : 0u;
             }
             stream_consumer_sync<NCW>();
-            if (sh_last) {
+            if (sh_last && want_am && tid == 0) {
+                __threadfence();
+                const float nv = a.ctl->n_valid;
+                a.accuracy[0] = nv > 0.f ? static_cast<float>(__ldcg(&a.ctl->n_correct)) / nv : 0.f;
+            }
+            if (sh_last && a.reduction == CE_RED_NONE && tid == 0) a.ctl->done = 0u;
+            if (sh_last && a.reduction != CE_RED_NONE) {
                 __threadfence();
                 double sum = 0.0;
                 for (int64_t i = tid; i < a.n_rows; i += NCT) sum += static_cast<double>(__ldcg(a.row_loss + i));
@@ -593,28 +697,39 @@ ce_stream_kernel(RowArgs a, int tune) {
 
 // Kernel entry of one instantiation (the aligned ones are compiled in
 // ce_stream.cu, the ragged ones in ce_stream_ragged.cu).
-template <int DT, int SHAPE, int CL, bool RAG>
+template <int DT, int SHAPE, int CL, bool RAG, int OPT = 0>
 const void *stream_fn(int mode) {
     switch (mode) {
-    case 0: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 0, SHAPE, CL, RAG>);
-    case 1: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 1, SHAPE, CL, RAG>);
-    default: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 2, SHAPE, CL, RAG>);
+    case 0: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 0, SHAPE, CL, RAG, OPT>);
+    case 1: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 1, SHAPE, CL, RAG, OPT>);
+    default: return reinterpret_cast<const void *>(&ce_stream_kernel<DT, 2, SHAPE, CL, RAG, OPT>);
     }
 }
 
+#define CE_STREAM_PICK(S, C, R, OP)                                                                          \
+    if (shape == S && cl == C)                                                                               \
+        return dtype == CE_DT_F32 ? stream_fn<CE_DT_F32, S, C, R, OP>(mode)                                  \
+             : dtype == CE_DT_BF16 ? stream_fn<CE_DT_BF16, S, C, R, OP>(mode) : stream_fn<CE_DT_F16, S, C, R, OP>(mode);
+
 template <bool RAG>
 const void *stream_kernel_for(int dtype, int mode, int shape, int cl) {
-#define CE_STREAM_PICK(S, C)                                                                  \
-    if (shape == S && cl == C)                                                                \
-        return dtype == CE_DT_F32 ? stream_fn<CE_DT_F32, S, C, RAG>(mode)                     \
-             : dtype == CE_DT_BF16 ? stream_fn<CE_DT_BF16, S, C, RAG>(mode) : stream_fn<CE_DT_F16, S, C, RAG>(mode);
-    CE_STREAM_PICK(0, 1) CE_STREAM_PICK(0, 2) CE_STREAM_PICK(1, 1) CE_STREAM_PICK(1, 2)
-    CE_STREAM_PICK(2, 1) CE_STREAM_PICK(2, 2)
-#undef CE_STREAM_PICK
+    CE_STREAM_PICK(0, 1, RAG, 0) CE_STREAM_PICK(0, 2, RAG, 0) CE_STREAM_PICK(1, 1, RAG, 0)
+    CE_STREAM_PICK(1, 2, RAG, 0) CE_STREAM_PICK(2, 1, RAG, 0) CE_STREAM_PICK(2, 2, RAG, 0)
     return nullptr;
 }
 
-// defined in ce_stream_ragged.cu
+// With the options: the three shapes the library picks by row size (three
+// CTAs per SM, alone or in pairs; one wide CTA per SM in pairs).
+template <bool RAG, int OPT>
+const void *stream_kernel_options_for(int dtype, int mode, int shape, int cl) {
+    CE_STREAM_PICK(2, 1, RAG, OPT) CE_STREAM_PICK(2, 2, RAG, OPT) CE_STREAM_PICK(1, 2, RAG, OPT)
+    return nullptr;
+}
+#undef CE_STREAM_PICK
+
+// defined in ce_stream_ragged.cu, ce_stream_options.cu and ce_stream_softcap.cu
 const void *stream_kernel_ragged(int dtype, int mode, int shape, int cl);
+const void *stream_kernel_options(int dtype, int mode, int shape, int cl, bool ragged);
+const void *stream_kernel_softcap(int dtype, int mode, int shape, int cl, bool ragged);
 
 }  // namespace ce

@@ -41,8 +41,9 @@ def rne(v64: torch.Tensor, dtype: torch.dtype) -> torch.Tensor:
 def magnitude_T(x: torch.Tensor, target: torch.Tensor, stats64: torch.Tensor, weight, eps: float,
                 w_all: float, scale: torch.Tensor, softcap: float = 0.0, z_loss: float = 0.0) -> torch.Tensor:
     """|s_i| * T_ic for every element, in fp64 (rows not valid: 0). With a
-    softcap the terms are those of the capped logits times dz/dx; z-loss adds
-    its |2 lambda LSE p| term."""
+    softcap the terms are those of the capped logits times dz/dx, and times
+    max(1, |z| / 8) for the fp32 rounding of z itself; z-loss adds its
+    |2 lambda LSE p| term."""
     xd = x.double()
     deriv = None
     if softcap > 0:
@@ -62,7 +63,10 @@ def magnitude_T(x: torch.Tensor, target: torch.Tensor, stats64: torch.Tensor, we
     if z_loss > 0:
         T = T + (2 * z_loss * lse).abs() * p
     if deriv is not None:
-        T = T * deriv
+        # the capped logit z = c tanh(x / c) carries ~2.5 ulp of fp32 rounding,
+        # up to 2^-21.7 |z| absolute, which moves p by that relative amount: the
+        # 2^-18 floor covers it up to |z| = 16, so scale the terms by |z| / 8 beyond
+        T = T * deriv * torch.clamp(xd.abs() / 8.0, min=1.0)
     T = T * scale.abs().reshape(-1, 1).double()
     T[~valid] = 0.0
     return T

@@ -101,9 +101,8 @@ def test_workspace_is_o_rows_and_far_below_one_logits_tensor(lib):
 
 
 def test_automatic_path_choice_is_host_logic(lib):
-    """ce_select_variant (no GPU work): every row layout takes the stream
-    kernel (aligned or ragged rows), calls with softcap / z-loss / accuracy
-    the register row-pass kernel; explicit variants are returned as asked."""
+    """ce_select_variant (no GPU work): every row layout and every option set
+    takes the stream kernel; explicit variants are returned as asked."""
     out = ctypes.c_int32()
     p = _params(lib, n_rows=4, vocab=128256, ld=128256)
     assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
@@ -117,7 +116,7 @@ def test_automatic_path_choice_is_host_logic(lib):
     p = _params(lib, n_rows=4, vocab=128256, ld=128256)
     p.softcap = 30.0
     assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
-    assert out.value == lib.VARIANTS["rowpass"]
+    assert out.value == lib.VARIANTS["stream"]
     p = _params(lib, variant=lib.VARIANTS["split"])
     assert lib._lib.ce_select_variant(ctypes.byref(p), ctypes.c_void_p(0x10000), ctypes.byref(out)) == 0
     assert out.value == lib.VARIANTS["split"]

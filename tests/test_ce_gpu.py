@@ -501,14 +501,16 @@ def test_bounded_wait_gives_up_with_status_and_context_survives(ce):
     assert ce.ce_get_status(ws) == 0
 
 
-@pytest.mark.parametrize("api", ["auto", "split", "fwd+bwd calls"])
+@pytest.mark.parametrize("api", ["auto", "stream-pair", "stream-wide", "rowpass", "split", "fwd+bwd calls"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("red", ["mean", "sum", "none"])
-@pytest.mark.parametrize("opts", [(15.0, 0.0), (0.0, 1e-4), (30.0, 1e-4)], ids=["softcap", "zloss", "both"])
+@pytest.mark.parametrize("opts", [(15.0, 0.0), (0.0, 1e-4), (30.0, 1e-4), (0.0, 0.0)],
+                         ids=["softcap", "zloss", "both", "accuracy"])
 @pytest.mark.parametrize("shape", [(17, 1000), (9, 33000), (5, 7), (6, 1001)], ids=lambda s: f"{s[0]}x{s[1]}")
 def test_softcap_zloss_accuracy(ce, api, dtype, red, opts, shape):
-    """Softcap, z-loss and token accuracy against the oracle (the row-pass
-    and split kernels carry the options)."""
+    """Softcap, z-loss and token accuracy against the oracle, in the stream
+    kernel (automatic path, CTA pairs, wide CTAs), the row pass and the split
+    kernels; the token accuracy is asked for in every case."""
     R, V = shape
     cap, zl = opts
     seed = zlib.crc32(repr((R, V, dtype, red, opts)).encode()) % 9973
@@ -528,8 +530,9 @@ def test_softcap_zloss_accuracy(ce, api, dtype, red, opts, shape):
         ce.ce_backward(x, t, stats, grad_output=g, weight=w, label_smoothing=0.1, reduction=red, softcap=cap,
                        z_loss=zl)
     else:
+        variant, tune = {"stream-pair": ("stream", 8), "stream-wide": ("stream", 9)}.get(api, (api, 0))
         loss = ce.ce_fwd_bwd(x, t, grad_output=g, weight=w, label_smoothing=0.1, reduction=red,
-                             variant=api, softcap=cap, z_loss=zl, accuracy=acc)
+                             variant=variant, tune=tune, softcap=cap, z_loss=zl, accuracy=acc)
     torch.cuda.synchronize()
     _check_all(x, t, w, 0.1, red, g, ref, loss, x_in, softcap=cap, z_loss=zl)
     assert float(acc.item()) == pytest.approx(ref["accuracy"], abs=1e-7)
@@ -538,9 +541,8 @@ def test_softcap_zloss_accuracy(ce, api, dtype, red, opts, shape):
 def test_options_refused_where_not_implemented(ce):
     x = make_logits(4, 1024, "bf16", 1.0, 1, device="cuda")
     t = make_targets(4, 1024, 0.0, 1, device="cuda")
-    for variant in ("fused", "stream"):
-        with pytest.raises(ce.CEError, match="UNSUPPORTED"):
-            ce.ce_fwd_bwd(x, t, variant=variant, softcap=10.0)
+    with pytest.raises(ce.CEError, match="UNSUPPORTED"):
+        ce.ce_fwd_bwd(x, t, variant="fused", softcap=10.0)
 
 
 @pytest.mark.parametrize("variant", ["auto", "fused", "split", "rowpass", "stream", "stream-pair"])
