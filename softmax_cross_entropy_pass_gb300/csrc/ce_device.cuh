@@ -330,6 +330,28 @@ __device__ inline float softcap_deriv(float z, float c) {
     return fmaf(-u, u, 1.f);
 }
 
+// tanh(u) for the stream kernel's softcap, cheaper than the accurate tanhf:
+// for |u| < 0.8 an odd polynomial u (1 + c1 w + ... + c6 w^6), w = u^2, with
+// the c_k from the least-squares fit in tanh_fit.py (fit error below 4e-9);
+// beyond, the identity tanh|u| = 1 - 2 / (1 + e^(2|u|)) with the hardware
+// exponential and an approximate divide (no cancellation there: the result
+// is above 0.66). About 2 units in the last place on both sides; the
+// exponent is clamped at 126 so the divide's denominator stays in range
+// (tanh is 1 in fp32 well before).
+__device__ inline float tanh_fast(float u) {
+    const float a = fabsf(u);
+    const float w = u * u;
+    float p = fmaf(w, 0.0015856500249356031f, -0.007411024998873472f);
+    p = fmaf(p, w, 0.021303808316588402f);
+    p = fmaf(p, w, -0.053852491080760956f);
+    p = fmaf(p, w, 0.13332220911979675f);
+    p = fmaf(p, w, -0.33333298563957214f);
+    p = fmaf(p, w, 1.f);
+    const float e = ex2_hw(fminf(a * (2.f * kLog2e), 126.f));
+    const float big = copysignf(1.f - __fdividef(2.f, 1.f + e), u);
+    return a < 0.8f ? u * p : big;
+}
+
 // The first column holding the maximum (ties go to the smaller column).
 struct ArgMax {
     float v;

@@ -201,6 +201,7 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr bool FEAT = OPT != 0;
     constexpr bool CAPF = OPT == 2;
     const float cap = CAPF ? a.softcap : 0.f;
+    const float inv_cap = CAPF && cap > 0.f ? 1.f / cap : 0.f;
     const float zl = FEAT ? a.z_loss : 0.f;
     const bool want_am = FEAT && a.accuracy != nullptr;
 
@@ -320,7 +321,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                         float zmax = -INFINITY;
 #pragma unroll
                         for (int j = 0; j < VEC; ++j) {
-                            z[j] = cap > 0.f ? softcap_logit(x[j], cap) : x[j];
+                            z[j] = cap > 0.f ? cap * tanh_fast(x[j] * inv_cap) : x[j];
                             zmax = fmaxf(zmax, z[j]);
                         }
                         if (want_am) {
@@ -342,22 +343,27 @@ ce_stream_kernel(RowArgs a, int tune) {
                     uint4 raw[VPT];
 #pragma unroll
                     for (int k = 0; k < VPT; ++k) raw[k] = ld_shared_v4(base_s + 16u * (tid + k * NCT));
-                    float cm = F::vmax(raw[0]);
+                    float vm[VPT];
 #pragma unroll
-                    for (int k = 1; k < VPT; ++k) cm = fmaxf(cm, F::vmax(raw[k]));
+                    for (int k = 0; k < VPT; ++k) vm[k] = F::vmax(raw[k]);
+                    float cm = vm[0];
+#pragma unroll
+                    for (int k = 1; k < VPT; ++k) cm = fmaxf(cm, vm[k]);
                     if (FEAT && want_am && cm > am.v) {
                         // a new maximum: its first column among this thread's vectors of the
                         // chunk (earlier chunks hold smaller columns, so ties keep those)
-                        int col = -1;
+                        int kk = VPT - 1;
 #pragma unroll
-                        for (int k = 0; k < VPT; ++k) {
-                            float xk[VEC];
-                            F::unpack(raw[k], xk);
+                        for (int k = VPT - 1; k >= 0; --k) kk = (vm[k] == cm) ? k : kk;
+                        uint4 rk = raw[0];
 #pragma unroll
-                            for (int e = 0; e < VEC; ++e)
-                                if (col < 0 && xk[e] == cm) col = static_cast<int>(vlo + (v0 + tid + k * NCT) * VEC + e);
-                        }
-                        am = ArgMax{cm, col};
+                        for (int k = 1; k < VPT; ++k) rk = (k == kk) ? raw[k] : rk;
+                        float xk[VEC];
+                        F::unpack(rk, xk);
+                        int e0 = VEC - 1;
+#pragma unroll
+                        for (int e = VEC - 1; e >= 0; --e) e0 = (xk[e] == cm) ? e : e0;
+                        am = ArgMax{cm, static_cast<int>(vlo + (v0 + tid + kk * NCT) * VEC + e0)};
                     }
                     if (cm > st.m) {
                         if (st.m != -INFINITY) st.s *= ex2_hw((st.m - cm) * kLog2e);
@@ -413,11 +419,15 @@ ce_stream_kernel(RowArgs a, int tune) {
                             for (int j = 0; j < VEC; ++j) xv = (j == skip) ? x[j] : xv;
                             S.xy[rp] = xv;  // the target logit, for the merge
                         }
-                        if (FEAT && want_am) {
+                        const float vmx = F::vmax(raw);
+                        if (FEAT && want_am && vmx > am.v) {
+                            // vectors come in increasing column order: ties keep the earlier one
+                            int e0 = VEC - 1;
 #pragma unroll
-                            for (int e = 0; e < VEC; ++e) am = argmax_merge(am, ArgMax{x[e], static_cast<int>(vlo + vb + e)});
+                            for (int e = VEC - 1; e >= 0; --e) e0 = (x[e] == vmx) ? e : e0;
+                            am = ArgMax{vmx, static_cast<int>(vlo + vb + e0)};
                         }
-                        row_state_add<VEC, P1S>(st, x, F::vmax(raw), skip, nullptr);
+                        row_state_add<VEC, P1S>(st, x, vmx, skip, nullptr);
                     }
                 }
                 __syncwarp();
@@ -426,7 +436,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             if (tid < nedge) {
                 const int64_t c = edge_c;
                 const float xr = F::load1(rowp, c);
-                float x = (CAPF && cap > 0.f) ? softcap_logit(xr, cap) : xr;
+                float x = (CAPF && cap > 0.f) ? cap * tanh_fast(xr * inv_cap) : xr;
                 if (want_am) am = argmax_merge(am, ArgMax{xr, static_cast<int>(c)});
                 if (c == yg) S.xy[rp] = x;
                 row_state_add<1, P1S>(st, &x, x, (c == yg) ? 0 : -1, nullptr);
@@ -534,7 +544,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                     if (CAPF && cap > 0.f) {
                         // softcap: the gradient of the capped logits, times dz/dx below
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) z[j] = cap > 0.f ? softcap_logit(x[j], cap) : x[j];
+                        for (int j = 0; j < VEC; ++j) z[j] = cap > 0.f ? cap * tanh_fast(x[j] * inv_cap) : x[j];
 #pragma unroll
                         for (int h = 0; h < VEC / 4; ++h) {
                             const float4 wv = MODE == 2 ? load_w4(a.weight, vlo + vb + 4 * h, w4)
@@ -580,7 +590,10 @@ ce_stream_kernel(RowArgs a, int tune) {
                     }
                     if (CAPF && cap > 0.f) {
 #pragma unroll
-                        for (int j = 0; j < VEC; ++j) gr[j] *= softcap_deriv(z[j], cap);
+                        for (int j = 0; j < VEC; ++j) {
+                            const float tj = z[j] * inv_cap;
+                            gr[j] *= fmaf(-tj, tj, 1.f);
+                        }
                     }
                     st_stream(vp + v0 + v, F::pack(gr));  // vp points at this CTA's slice
                 }
@@ -592,11 +605,14 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const int64_t c = edge_c;
                 const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
                 const float xr = F::load1(rowp, c);
-                const float xe = (CAPF && cap > 0.f) ? softcap_logit(xr, cap) : xr;
+                const float xe = (CAPF && cap > 0.f) ? cap * tanh_fast(xr * inv_cap) : xr;
                 er = wc * xe;
                 en = wc;
                 float ge = (c == yg) ? rs.dxy : grad_elem(rs, xe, wc);
-                if (CAPF && cap > 0.f) ge *= softcap_deriv(xe, cap);
+                if (CAPF && cap > 0.f) {
+                    const float te = xe * inv_cap;
+                    ge *= fmaf(-te, te, 1.f);
+                }
                 F::store1(rowp, c, ge);
             }
             if (DEFER) {
