@@ -201,7 +201,7 @@ def flce_logits(hidden: torch.Tensor, weight: torch.Tensor, bias=None, row_block
 def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
          label_smoothing: float = 0.0, reduction: str = "mean", sample_rows=None,
          sample_cols=None, abs_sums: bool = False, n_threads: int | None = None,
-         class_weight=None, grad_output=None) -> dict:
+         class_weight=None, grad_output=None, softcap: float = 0.0, z_loss: float = 0.0) -> dict:
     """Fused-linear cross-entropy reference (fp64).
 
     Returns the reduced loss, the per-row losses, grad_hidden on
@@ -210,8 +210,9 @@ def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
     with dZ the oracle gradient of the loss with respect to z = h W^T + b.
     With ``abs_sums`` it also returns |dZ| @ |W| and |dZ|^T @ |h| on the same
     samples (the magnitudes that bound rounding errors of dZ in the tests).
-    ``class_weight`` and ``grad_output`` (scalar, or one value per row for
-    reduction none) are handed to the row oracle unchanged."""
+    ``class_weight``, ``grad_output`` (scalar, or one value per row for
+    reduction none), ``softcap`` and ``z_loss`` are handed to the row oracle
+    unchanged; ``accuracy`` is the token accuracy of the logits' argmax."""
     BT, H = hidden.shape
     V = weight.shape[0]
     n, wy, wall, bad = normalizers(target, V, ignore_index, class_weight)
@@ -233,6 +234,7 @@ def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
     grad_b = torch.zeros(len(cols_sel), dtype=torch.float64) if bias is not None else None
     abs_h = torch.zeros(len(rows_sel), H, dtype=torch.float64) if abs_sums else None
     abs_w = torch.zeros(len(cols_sel), H, dtype=torch.float64) if abs_sums else None
+    amax = torch.zeros(BT, dtype=torch.int64)
     for r0, z in flce_logits(hidden, weight, bias):
         r1 = r0 + z.shape[0]
         g = None
@@ -240,7 +242,9 @@ def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
             g = g_all[r0:r1] if reduction == "none" else g_all
         res = rows(z, tgt[r0:r1], weight=class_weight, ignore_index=ignore_index,
                    label_smoothing=label_smoothing, reduction=reduction, grad_output=g,
-                   norm_wy=wy, w_all=wall, want_grad=True, want_stats=False, n_threads=n_threads)
+                   norm_wy=wy, w_all=wall, want_grad=True, want_stats=False, n_threads=n_threads,
+                   softcap=softcap, z_loss=z_loss)
+        amax[r0:r1] = res["argmax"]
         row_loss[r0:r1] = res["row_loss"]
         dz = res["grad"]
         grad_w += dz[:, cols_sel].T @ hd[r0:r1]
@@ -256,4 +260,5 @@ def flce(hidden, weight, target, *, bias=None, ignore_index: int = -100,
     return {"loss": reduce(row_loss, reduction, wy), "row_loss": row_loss,
             "grad_hidden": grad_h, "grad_weight": grad_w, "grad_bias": grad_b,
             "grad_hidden_abs": abs_h, "grad_weight_abs": abs_w,
-            "rows": rows_sel, "cols": cols_sel, "norm_wy": wy}
+            "rows": rows_sel, "cols": cols_sel, "norm_wy": wy,
+            "accuracy": accuracy(amax, tgt, V, ignore_index)}

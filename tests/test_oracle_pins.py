@@ -306,6 +306,31 @@ def test_flce_class_weight_grad_output_against_torch_autograd_fp64(reduction):
     assert torch.allclose(out["grad_weight"], Wr.grad, rtol=1e-10, atol=1e-15)
 
 
+def test_flce_softcap_zloss_accuracy_against_torch_autograd_fp64():
+    """The fused-linear reference with softcap and z-loss vs torch autograd of
+    linear -> c tanh(. / c) -> cross_entropy + lambda logsumexp^2 (valid rows,
+    the cross-entropy's normaliser); its token accuracy vs the argmax of the
+    linear layer's output."""
+    BT, H, V = 30, 12, 40
+    c, lam = 2.0, 1e-3
+    g = torch.Generator().manual_seed(6)
+    h = torch.randn(BT, H, generator=g, dtype=torch.float64)
+    W = torch.randn(V, H, generator=g, dtype=torch.float64)
+    t = make_targets(BT, V, 0.2, 6)
+    hr, Wr = (a.clone().requires_grad_(True) for a in (h, W))
+    z = c * torch.tanh(F.linear(hr, Wr) / c)
+    valid = t != IGNORE_INDEX
+    base = F.cross_entropy(z, t, ignore_index=IGNORE_INDEX, label_smoothing=0.1)
+    loss = base + lam * (torch.logsumexp(z, dim=1) ** 2 * valid).sum() / valid.sum()
+    loss.backward()
+    out = oracle.flce(h, W, t, label_smoothing=0.1, softcap=c, z_loss=lam)
+    assert out["loss"] == pytest.approx(loss.item(), rel=1e-12)
+    assert torch.allclose(out["grad_hidden"], hr.grad, rtol=1e-10, atol=1e-15)
+    assert torch.allclose(out["grad_weight"], Wr.grad, rtol=1e-10, atol=1e-15)
+    am = (h @ W.T).argmax(dim=1)
+    assert out["accuracy"] == pytest.approx(float((am[valid] == t[valid]).double().mean()), abs=1e-15)
+
+
 # ----------------------------------------------------------------- the pages' numbers
 def _bf16_round(v: torch.Tensor) -> torch.Tensor:
     return v.to(torch.float32).to(torch.bfloat16).to(torch.float64)
