@@ -116,9 +116,10 @@ typedef struct ce_params {
      * suite: "class weights, softcap, label smoothing, z-loss"; its dx_y
      * correction keeps the "softcap factors") without a definition there;
      * this library takes the plain ones. Supported by ce_forward /
-     * ce_backward and ce_fwd_bwd's stream, row-pass and split paths; the
-     * cluster variant, ce_fwd_bwd_from_host and flce_fwd_bwd return
-     * CE_ERR_UNSUPPORTED with an option set. */
+     * ce_backward and ce_fwd_bwd's stream, row-pass and split paths, and by
+     * flce_fwd_bwd (softcap applied to the GEMM's logits); the cluster
+     * variants (CE_VARIANT_FUSED, CE_FLCE_CE_CLUSTER) and
+     * ce_fwd_bwd_from_host return CE_ERR_UNSUPPORTED with an option set. */
     float softcap;              /* c > 0: every logit becomes c*tanh(x/c); 0 = off */
     float z_loss;               /* lambda >= 0: loss_i += lambda*LSE_i^2 on valid rows */
     float *accuracy;            /* device fp32 [1] or NULL: share of valid rows whose argmax

@@ -423,12 +423,14 @@ def flce_workspace_size(n_rows: int, hidden: int, vocab: int, chunk_rows: int, d
 def flce_fwd_bwd(hidden, weight, target, *, bias=None, class_weight=None, ignore_index=-100,
                  label_smoothing=0.0, reduction="mean", grad_output=None, chunk_rows=4096, loss=None,
                  grad_hidden=None, grad_weight=None, grad_bias=None, ws=None, stream=None, dense=False,
-                 ce_cluster=False):
+                 ce_cluster=False, softcap=0.0, z_loss=0.0, accuracy=None):
     """Fused-linear cross-entropy: returns (loss, grad_hidden [BT, H] bf16,
     grad_weight [V, H] fp32, grad_bias [V] fp32 or None). ``dense=True``
     runs every row through the GEMMs instead of skipping ignored rows;
     ``ce_cluster=True`` runs each chunk's cross-entropy with the cluster
-    kernel instead of the GEMM-epilogue statistics and the streaming map."""
+    kernel instead of the GEMM-epilogue statistics and the streaming map.
+    ``softcap`` / ``z_loss`` / ``accuracy`` (a device fp32 [1] tensor) as in
+    ce_fwd_bwd (not with ``ce_cluster``)."""
     _check_dev(hidden, weight, target, bias, class_weight, grad_output)
     BT, H = hidden.shape
     V = weight.shape[0]
@@ -441,6 +443,10 @@ def flce_fwd_bwd(hidden, weight, target, *, bias=None, class_weight=None, ignore
     p.reduction = CE_RED[reduction]
     p.target_is_int32 = 1 if target.dtype == torch.int32 else 0
     p.variant = _flce_variant(dense, ce_cluster)
+    p.softcap, p.z_loss = float(softcap), float(z_loss)
+    if accuracy is not None:
+        _check_dev(accuracy)
+        p.accuracy = accuracy.data_ptr()
     dev = hidden.device
     if loss is None:
         loss = torch.empty(BT if reduction == "none" else 1, dtype=torch.float32, device=dev)

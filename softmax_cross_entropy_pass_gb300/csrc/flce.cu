@@ -66,6 +66,8 @@ struct GemmArgs {
     // columns {max m, exp-sum s without the target column, smoothing sum r,
     // weight sum n}, stored at part[row * tiles_n + tile].
     float4 *part;
+    float2 *pam;           // token accuracy: per row and tile {raw maximum, its first column}, or NULL
+    float st_cap, st_inv_cap;  // softcap c (0: off): the stored logits are c tanh(x / c)
     const void *st_target;
     int st_tgt32;
     int64_t st_ignore;
@@ -133,13 +135,16 @@ __device__ inline void epilogue_store(const GemmArgs &g, int row, int orow, int 
     }
 }
 
-// Statistics epilogue: store 32 fp32 logits (+ bias) of one row and fold
-// them into the row's softmax state over the current column tile. `skip` is
-// the target's position among the 32 columns (-1: not among them). SMODE 0:
-// no smoothing sums; 1: sum of the logits; 2: class-weighted sum.
+// Statistics epilogue: store 32 fp32 logits (+ bias; capped to c tanh(x / c)
+// with a softcap) of one row and fold them into the row's softmax state over
+// the current column tile. `skip` is the target's position among the 32
+// columns (-1: not among them). With `pam`, `am` follows the first column
+// of the raw maximum (columns arrive in increasing order, so a strictly
+// greater value is needed to move it). SMODE 0: no smoothing sums; 1: sum of
+// the logits; 2: class-weighted sum.
 template <int SMODE>
 __device__ inline void epilogue_stats(const GemmArgs &g, int row, int col0, const uint32_t (&v)[32], RowState &st,
-                                      int skip) {
+                                      int skip, ArgMax &am) {
     const int nv = g.N - col0;
     if (nv <= 0) return;
     float x[32];
@@ -154,6 +159,21 @@ __device__ inline void epilogue_stats(const GemmArgs &g, int row, int col0, cons
                 const float4 bb = __ldg(b4 + q);
                 x[4 * q] += bb.x; x[4 * q + 1] += bb.y; x[4 * q + 2] += bb.z; x[4 * q + 3] += bb.w;
             }
+        }
+        if (g.pam) {
+            float rmax = x[0];
+#pragma unroll
+            for (int j = 1; j < 32; ++j) rmax = fmaxf(rmax, x[j]);
+            if (rmax > am.v) {
+                int e0 = 31;
+#pragma unroll
+                for (int j = 31; j >= 0; --j) e0 = (x[j] == rmax) ? j : e0;
+                am = ArgMax{rmax, col0 + e0};
+            }
+        }
+        if (g.st_cap > 0.f) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) x[j] = g.st_cap * tanh_fast(x[j] * g.st_inv_cap);
         }
         float4 *o4 = reinterpret_cast<float4 *>(o);
 #pragma unroll
@@ -176,6 +196,8 @@ __device__ inline void epilogue_stats(const GemmArgs &g, int row, int col0, cons
         for (int j = 0; j < 32; ++j) {
             if (j < nv) {
                 float xv = x[j] + (g.bias ? __ldg(g.bias + col0 + j) : 0.f);
+                if (g.pam) am = argmax_merge(am, ArgMax{xv, col0 + j});
+                if (g.st_cap > 0.f) xv = g.st_cap * tanh_fast(xv * g.st_inv_cap);
                 o[j] = xv;
                 float wj = SMODE == 2 ? __ldg(g.st_weight + col0 + j) : 1.f;
                 row_state_add<1, SMODE != 0>(st, &xv, xv, skip == j ? 0 : -1, SMODE == 2 ? &wj : nullptr);
@@ -319,6 +341,7 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
             const int orow = (g.row_map && row < g.M) ? __ldg(g.row_map + row) : row;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * GB_N;
             RowState st = row_state_empty();
+            ArgMax am{-INFINITY, 0x7fffffff};
             int y_rel = -(1 << 30);   // target column relative to the tile (none: far outside)
             if (EPI != 0 && row < g.M) {
                 const int64_t y = load_target(g.st_target, g.st_tgt32, row);
@@ -333,11 +356,13 @@ flce_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant_
                     epilogue_store(g, row, orow, tn * GB_N + c0, v, base);
                 } else if (row < g.M) {
                     const int skip = (static_cast<unsigned>(y_rel - c0) < 32u) ? y_rel - c0 : -1;
-                    epilogue_stats<(EPI > 0 ? EPI - 1 : 0)>(g, row, tn * GB_N + c0, v, st, skip);
+                    epilogue_stats<(EPI > 0 ? EPI - 1 : 0)>(g, row, tn * GB_N + c0, v, st, skip, am);
                 }
             }
-            if (EPI != 0 && row < g.M)
+            if (EPI != 0 && row < g.M) {
                 g.part[static_cast<int64_t>(row) * g.tiles_n + tn] = make_float4(st.m, st.s, st.r, st.n);
+                if (g.pam) g.pam[static_cast<int64_t>(row) * g.tiles_n + tn] = make_float2(am.v, __int_as_float(am.i));
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&tempty[acc]));
@@ -505,6 +530,7 @@ flce_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
             const int orow = (g.row_map && row < g.M) ? __ldg(g.row_map + row) : row;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + acc * GP_N;
             RowState stt = row_state_empty();
+            ArgMax am{-INFINITY, 0x7fffffff};
             int y_rel = -(1 << 30);
             if (EPI != 0 && row < g.M) {
                 const int64_t y = load_target(g.st_target, g.st_tgt32, row);
@@ -519,11 +545,13 @@ flce_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_cons
                     epilogue_store(g, row, orow, tn * GP_N + c0, v, obase);
                 } else if (row < g.M) {
                     const int skip = (static_cast<unsigned>(y_rel - c0) < 32u) ? y_rel - c0 : -1;
-                    epilogue_stats<(EPI > 0 ? EPI - 1 : 0)>(g, row, tn * GP_N + c0, v, stt, skip);
+                    epilogue_stats<(EPI > 0 ? EPI - 1 : 0)>(g, row, tn * GP_N + c0, v, stt, skip, am);
                 }
             }
-            if (EPI != 0 && row < g.M)
+            if (EPI != 0 && row < g.M) {
                 g.part[static_cast<int64_t>(row) * g.tiles_n + tn] = make_float4(stt.m, stt.s, stt.r, stt.n);
+                if (g.pam) g.pam[static_cast<int64_t>(row) * g.tiles_n + tn] = make_float2(am.v, __int_as_float(am.i));
+            }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
@@ -686,8 +714,11 @@ struct ChunkArgs {
     const float *grad_output;  // [1], or [n_rows] for none, or NULL
     float *loss;               // reduction none: [n_rows]
     float *row_loss;           // mean / sum: [n_rows]
-    const WsCtl *ctl;
+    WsCtl *ctl;
     MapRow *rows;
+    float cap, inv_cap;        // softcap (0: off); the logits chunk holds the capped logits
+    float z_loss;
+    const float2 *pam;         // token accuracy: the logits GEMM's per-tile argmax, or NULL
     __nv_bfloat16 *out;        // dZ [n_rows, ld_out] bf16
     int64_t ld_out;
     const int *row_limit;
@@ -705,6 +736,7 @@ __global__ void __launch_bounds__(256) flce_row_scalars_kernel(ChunkArgs a) {
         const int64_t t = load_target(a.target, a.tgt32, row);
         const bool valid = target_valid(t, a.ignore_index, V);
         RowState st = row_state_empty();
+        ArgMax am{-INFINITY, 0x7fffffff};
         if (valid) {
             const float4 *pp = a.part + row * a.tiles;
             for (int j = lane; j < a.tiles; j += 32) {
@@ -712,6 +744,14 @@ __global__ void __launch_bounds__(256) flce_row_scalars_kernel(ChunkArgs a) {
                 st = row_state_merge(st, RowState{q.x, q.y, q.z, q.w});
             }
             st = warp_merge(st);
+            if (a.pam) {
+                const float2 *pa = a.pam + row * a.tiles;
+                for (int j = lane; j < a.tiles; j += 32) {
+                    const float2 q = __ldg(pa + j);
+                    am = argmax_merge(am, ArgMax{q.x, __float_as_int(q.y)});
+                }
+                am = warp_argmax(am);
+            }
         }
         if (lane != 0) continue;
         MapRow mr{};
@@ -725,8 +765,10 @@ __global__ void __launch_bounds__(256) flce_row_scalars_kernel(ChunkArgs a) {
             float scale = g;
             if (a.reduction == CE_RED_MEAN) scale = (w_y_sum != 0.f) ? g / w_y_sum : 0.f;
             const float rrel = row_state_rel_sum(st);
-            const RowScalars rs = make_row_scalars(st.m, st.s, xy, rrel, true, t, wy, w_all, a.eps, inv_v, scale);
-            loss = make_row_scalars(st.m, st.s, xy, rrel, true, t, wy, w_all, a.eps, inv_v, 1.f).loss;
+            const RowScalars rs =
+                make_row_scalars(st.m, st.s, xy, rrel, true, t, wy, w_all, a.eps, inv_v, scale, a.z_loss);
+            loss = make_row_scalars(st.m, st.s, xy, rrel, true, t, wy, w_all, a.eps, inv_v, 1.f, a.z_loss).loss;
+            if (a.pam && am.i == static_cast<int>(t)) atomicAdd(&a.ctl->n_correct, 1u);
             mr.neg_log2d = rs.neg_log2d; mr.m = rs.m; mr.a = rs.a; mr.b = rs.b; mr.dxy = rs.dxy;
             mr.y = static_cast<int>(t);
         }
@@ -758,6 +800,14 @@ __device__ inline uint4 map_vec(const ChunkArgs &a, uint32_t row, uint32_t col, 
     for (int e = 0; e < 8; ++e) {
         gr[e] = grad_elem(rs, x[e], WEIGHTED ? w[e] : 1.f);
         gr[e] = (e == yr) ? mr.dxy : gr[e];
+    }
+    if (a.cap > 0.f) {
+        // softcap: the chunk holds z = c tanh(x / c); dz/dx = 1 - (z / c)^2
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+            const float te = x[e] * a.inv_cap;
+            gr[e] *= fmaf(-te, te, 1.f);
+        }
     }
     return Fmt<CE_DT_BF16>::pack(gr);
 }
@@ -791,6 +841,14 @@ __global__ void __launch_bounds__(256) flce_map_kernel(ChunkArgs a) {
             const uint4 o1 = mr1.y >= 0 ? map_vec<WEIGHTED>(a, r1, c1, mr1, u10, u11) : zero;
             st_stream(a.out + static_cast<int64_t>(r1) * a.ld_out + c1, o1);
         }
+    }
+}
+
+// token accuracy = correct rows / valid rows (counted by the row-scalars kernels)
+__global__ void flce_accuracy_kernel(const WsCtl *ctl, float *acc) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) {
+        const float n = ctl->n_valid;
+        acc[0] = n > 0.f ? static_cast<float>(__ldcg(&ctl->n_correct)) / n : 0.f;
     }
 }
 
@@ -972,6 +1030,9 @@ cudaError_t gemm_bf16(int M, int N, int K, const void *A, int64_t lda, int a_mn,
         g.st_tgt32 = stats->tgt32;
         g.st_ignore = stats->ignore_index;
         g.st_weight = stats->weight;
+        g.st_cap = stats->cap > 0.f ? stats->cap : 0.f;
+        g.st_inv_cap = stats->cap > 0.f ? 1.f / stats->cap : 0.f;
+        g.pam = stats->pam;
         epi = 1 + stats->smooth_mode;
         if (stats->smooth_mode < 0 || stats->smooth_mode > 2 || (stats->smooth_mode == 2 && !stats->weight))
             return cudaErrorInvalidValue;
@@ -1037,8 +1098,8 @@ struct FlceLayout {
     // ignored-row compaction: compacted hidden rows, the maps, the compacted
     // targets and per-row grad_output, the valid-row count
     size_t hc_off, idx_off, pos_off, tgt_off, gc_off, cnt_off;
-    // statistics path: the logits GEMM's per-tile row states and the per-row map scalars
-    size_t part_off, rows_off;
+    // statistics path: the logits GEMM's per-tile row states (and argmax), the per-row map scalars
+    size_t part_off, pam_off, rows_off;
     int tiles;
     // split-K parts of grad_hidden = dZ W (fp32, dh_splits x chunk x H)
     size_t dhp_off;
@@ -1080,7 +1141,8 @@ FlceLayout flce_layout(int64_t n_rows, int64_t vocab, int64_t chunk, int64_t hid
     if (map_ce) {
         L.tiles = static_cast<int>((vocab + kGemmTileN - 1) / kGemmTileN);
         L.part_off = L.total;
-        L.rows_off = L.part_off + round_up(chunk * L.tiles * 16, 1024);
+        L.pam_off = L.part_off + round_up(chunk * L.tiles * 16, 1024);
+        L.rows_off = L.pam_off + round_up(chunk * L.tiles * 8, 1024);
         L.total = L.rows_off + round_up(chunk * static_cast<int64_t>(sizeof(MapRow)), 1024);
     }
     return L;
@@ -1138,7 +1200,9 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
     if (!(p->label_smoothing >= 0.f && p->label_smoothing <= 1.f) || p->reserved != 0) return CE_ERR_INVALID_ARG;
     if (p->target_is_int32 != 0 && p->target_is_int32 != 1) return CE_ERR_INVALID_ARG;
     if (p->class_weight && (reinterpret_cast<uintptr_t>(p->class_weight) & 15u)) return CE_ERR_INVALID_ARG;
-    if (p->softcap != 0.f || p->z_loss != 0.f || p->accuracy) return CE_ERR_UNSUPPORTED;
+    if (!(p->softcap >= 0.f && p->softcap < INFINITY) || !(p->z_loss >= 0.f && p->z_loss < INFINITY))
+        return CE_ERR_INVALID_ARG;
+    if (p->accuracy && (reinterpret_cast<uintptr_t>(p->accuracy) & 3u)) return CE_ERR_INVALID_ARG;
     if ((p->variant & ~(CE_FLCE_DENSE | CE_FLCE_CE_CLUSTER)) != 0) return CE_ERR_INVALID_ARG;
     if (bias && !al16(bias)) return CE_ERR_INVALID_ARG;
     if (!loss || !ws || (reinterpret_cast<uintptr_t>(ws) & 255u)) return CE_ERR_INVALID_ARG;
@@ -1147,6 +1211,8 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
     const int64_t C = chunk_rows < BT ? chunk_rows : (BT > 0 ? BT : 1);
     const bool compact = flce_compacts(p);
     const bool map_ce = flce_maps(p, C);
+    const bool options = p->softcap > 0.f || p->z_loss > 0.f || p->accuracy;
+    if (options && !map_ce) return CE_ERR_UNSUPPORTED;  // the options live in the statistics path
     const FlceLayout L = flce_layout(BT, V, C, H, compact, map_ce);
     if (ws_bytes < L.total) return CE_ERR_WORKSPACE;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -1174,6 +1240,8 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
         if ((e = cudaMemsetAsync(grad_weight, 0, static_cast<size_t>(V) * H * 4, s)) != cudaSuccess)
             return flce_cuda_fail(e);
         if (grad_bias && (e = cudaMemsetAsync(grad_bias, 0, static_cast<size_t>(V) * 4, s)) != cudaSuccess)
+            return flce_cuda_fail(e);
+        if (p->accuracy && (e = cudaMemsetAsync(p->accuracy, 0, sizeof(float), s)) != cudaSuccess)
             return flce_cuda_fail(e);
         return CE_OK;
     }
@@ -1248,7 +1316,8 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
             // Z = h_c W^T (+ b), fp32, with the per-tile row states; then the
             // row scalars and the flat map to dZ (bf16) and the row losses
             float4 *part = reinterpret_cast<float4 *>(wsb + L.part_off);
-            const GemmStats gs{part, tgt_chunk, tgt32, p->ignore_index, mode, p->class_weight};
+            float2 *pam = p->accuracy ? reinterpret_cast<float2 *>(wsb + L.pam_off) : nullptr;
+            const GemmStats gs{part, tgt_chunk, tgt32, p->ignore_index, mode, p->class_weight, p->softcap, pam};
             e = gemm_bf16(static_cast<int>(c), static_cast<int>(V), static_cast<int>(H), h_c, H, 0, weight, H, 0,
                           0, Z, L.ldz, bias, &ctl->status, s, compact ? &rows_m : nullptr, &gs);
             if (e != cudaSuccess) return flce_cuda_fail(e);
@@ -1260,6 +1329,10 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
             ca.loss = none ? loss_rows + r0 : loss;
             ca.row_loss = row_loss + r0;
             ca.ctl = ctl;
+            ca.cap = p->softcap > 0.f ? p->softcap : 0.f;
+            ca.inv_cap = p->softcap > 0.f ? 1.f / p->softcap : 0.f;
+            ca.z_loss = p->z_loss;
+            ca.pam = pam;
             ca.rows = reinterpret_cast<MapRow *>(wsb + L.rows_off);
             ca.out = dZ; ca.ld_out = L.ldd;
             ca.row_limit = count; ca.row_limit_off = r0;
@@ -1339,6 +1412,13 @@ ce_status flce_fwd_bwd(const ce_params *p, int64_t H, const void *hidden, const 
                                  args, 0, s);
             if (e != cudaSuccess) return flce_cuda_fail(e);
         }
+    }
+    if (p->accuracy) {
+        const WsCtl *cc = ctl;
+        float *acc = p->accuracy;
+        void *args[] = {&cc, &acc};
+        e = cudaLaunchKernel(reinterpret_cast<const void *>(&flce_accuracy_kernel), dim3(1), dim3(32), args, 0, s);
+        if (e != cudaSuccess) return flce_cuda_fail(e);
     }
     if (!none) {
         const float *rl = row_loss;

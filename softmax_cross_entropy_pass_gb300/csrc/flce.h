@@ -36,6 +36,8 @@ struct GemmStats {
     int64_t ignore_index;
     int smooth_mode;
     const float *weight;
+    float cap;      // softcap c > 0: the stored logits and the states are those of c tanh(x / c)
+    float2 *pam;    // or NULL: per row and tile {raw maximum, its first column} (token accuracy)
 };
 constexpr int kGemmTileN = 256;
 

@@ -195,6 +195,50 @@ def test_flce_ignored_rows_against_oracle(ce, case, dense, ce_cluster):
         assert torch.count_nonzero(loss_c[skipped]) == 0
 
 
+@pytest.mark.parametrize("opts", [(15.0, 0.0), (0.0, 1e-4), (30.0, 1e-4)], ids=["softcap", "zloss", "both"])
+@pytest.mark.parametrize("red", ["mean", "none"])
+@pytest.mark.parametrize("dense", [False, True], ids=["compact", "dense"])
+def test_flce_softcap_zloss_accuracy(ce, opts, red, dense):
+    """Softcap (applied to the GEMM's logits), z-loss and token accuracy in
+    the fused-linear path against the fp64 oracle; the bound on the
+    gradients is the bf16 rounding of dZ, as for the plain path."""
+    cap, zl = opts
+    BT, H, V = 300, 128, 1000
+    h = _rand_bf16(BT, H, seed=41)
+    W = _rand_bf16(V, H, seed=42, scale=0.3)          # logits of a few units: the cap bites
+    t = make_targets(BT, V, 0.1, 43)
+    am = (h.double() @ W.double().T).argmax(dim=1)
+    t[:40] = am[:40]                                    # some correct rows
+    g = torch.rand(BT, generator=torch.Generator().manual_seed(44)) if red == "none" else None
+    acc = torch.full((1,), float("nan"), device="cuda")
+    loss, gh, gw, _ = ce.flce_fwd_bwd(h.cuda(), W.cuda(), t.cuda(), label_smoothing=0.1, reduction=red,
+                                      grad_output=None if g is None else g.cuda(), chunk_rows=128, dense=dense,
+                                      softcap=cap, z_loss=zl, accuracy=acc)
+    torch.cuda.synchronize()
+    ref = oracle.flce(h, W, t, label_smoothing=0.1, reduction=red, grad_output=g, softcap=cap, z_loss=zl,
+                      abs_sums=True)
+    if red == "none":
+        err = (loss.double().cpu() - ref["loss"]).abs()
+        assert (err <= 1e-4 * ref["loss"].abs() + 1e-6).all()
+    else:
+        assert abs(float(loss.item()) - ref["loss"]) <= 1e-4 * abs(ref["loss"])
+    err_h = (gh.double().cpu() - ref["grad_hidden"]).abs()
+    assert (err_h <= ref["grad_hidden_abs"] * 2.0 ** -8 + ref["grad_hidden"].abs() * 2.0 ** -7).all(), \
+        f"grad_hidden max err {float(err_h.max()):.3e}"
+    err_w = (gw.double().cpu() - ref["grad_weight"]).abs()
+    assert (err_w <= ref["grad_weight_abs"] * 2.0 ** -8 + ref["grad_weight"].abs() * 2.0 ** -20).all(), \
+        f"grad_weight max err {float(err_w.max()):.3e}"
+    assert float(acc.item()) == pytest.approx(ref["accuracy"], abs=1e-7)
+
+
+def test_flce_options_refused_with_the_cluster_chunk_kernel(ce):
+    h = _rand_bf16(64, 64, seed=1).cuda()
+    W = _rand_bf16(256, 64, seed=2).cuda()
+    t = make_targets(64, 256, 0.0, 3, device="cuda")
+    with pytest.raises(ce.CEError, match="UNSUPPORTED"):
+        ce.flce_fwd_bwd(h, W, t, ce_cluster=True, softcap=10.0)
+
+
 @pytest.mark.slow
 def test_flce_grad_hidden_without_split_k(ce):
     """A chunk whose grad_hidden GEMM has 2048 output tiles (16384 rows x H
