@@ -1,25 +1,27 @@
-// ce_stream.cuh -- streaming forward + backward: each CTA owns whole rows and
-// a producer warp streams every row through a ring of shared-memory chunks
-// twice, with 1-D bulk async copies:
-//   pass 1 (statistics): the row comes from HBM; its lines are marked
-//          evict-last in L2;
-//   pass 2 (gradient):   the same bytes again, now served by L2 (marked
-//          evict-first), while consumer warps write the fp32 gradient,
-//          rounded once, over the logits.
+// ce_stream.cuh -- streaming forward + backward: each CTA (or CTA pair) owns
+// whole rows and a producer warp streams every row through a ring of
+// shared-memory chunks twice, with 1-D bulk async copies:
+//   pass 1 (statistics): the row comes from HBM (no L2 hint by default; an
+//          evict-last hint is a tuning bit, measured slower);
+//   pass 2 (gradient):   the same bytes again, now served by L2 under an
+//          evict-first hint, while the consumer warps write the fp32
+//          gradient, rounded once, over the logits.
 // The ring is not tied to a row: while the consumers merge a row's
 // statistics, the producer keeps copying (the row's pass-2 chunks and the
 // next row's pass-1 chunks), so the memory system never idles between
 // phases, and the bytes in flight are set by the ring, not by registers.
-// HBM sees one read and one write per element, as the cluster kernel does,
-// without a cluster exchange; the L2 holds about one row per CTA.
+// HBM sees one read and one write per element; the L2 holds about one row
+// per CTA pair between the passes.
 //
 // With a cluster of two CTAs per row, each CTA streams half of the row and
 // the two halves' statistics are exchanged through distributed shared
 // memory (st.shared::cluster + a remote mbarrier arrive), which halves the
 // bytes each CTA keeps waiting in L2 for its second pass.
 //
-// Requires 16-byte aligned row starts (ce_fwd_bwd falls back to the
-// register row-pass kernel otherwise). Every wait is bounded.
+// Rows at any alignment: the part of a row before its first 16-byte boundary
+// and after its last goes through plain accesses (RAG instantiations). The
+// options (softcap, z-loss, token accuracy) have their own instantiations
+// (OPT). Every wait is bounded.
 #pragma once
 
 #include "ce_device.cuh"
