@@ -71,6 +71,11 @@ template <> struct Fmt<CE_DT_F32> {
         return fmaxf(fmaxf(__uint_as_float(v.x), __uint_as_float(v.y)),
                      fmaxf(__uint_as_float(v.z), __uint_as_float(v.w)));
     }
+    // max of the magnitudes (sign bits cleared)
+    __device__ static inline float vabsmax(const uint4 &v) {
+        const uint32_t m = 0x7fffffffu;
+        return vmax(make_uint4(v.x & m, v.y & m, v.z & m, v.w & m));
+    }
 };
 template <> struct Fmt<CE_DT_BF16> {
     static constexpr int kVec = 8;
@@ -109,6 +114,11 @@ template <> struct Fmt<CE_DT_BF16> {
         unpack2(m, lo, hi);
         return fmaxf(lo, hi);
     }
+    // max of the magnitudes (sign bits cleared)
+    __device__ static inline float vabsmax(const uint4 &v) {
+        const uint32_t m = 0x7fff7fffu;
+        return vmax(make_uint4(v.x & m, v.y & m, v.z & m, v.w & m));
+    }
 };
 template <> struct Fmt<CE_DT_F16> {
     static constexpr int kVec = 8;
@@ -143,6 +153,11 @@ template <> struct Fmt<CE_DT_F16> {
         float lo, hi;
         unpack2(m, lo, hi);
         return fmaxf(lo, hi);
+    }
+    // max of the magnitudes (sign bits cleared)
+    __device__ static inline float vabsmax(const uint4 &v) {
+        const uint32_t m = 0x7fff7fffu;
+        return vmax(make_uint4(v.x & m, v.y & m, v.z & m, v.w & m));
     }
 };
 
@@ -330,26 +345,125 @@ __device__ inline float softcap_deriv(float z, float c) {
     return fmaf(-u, u, 1.f);
 }
 
-// tanh(u) for the stream kernel's softcap, cheaper than the accurate tanhf:
-// for |u| < 0.8 an odd polynomial u (1 + c1 w + ... + c6 w^6), w = u^2, with
-// the c_k from the least-squares fit in tanh_fit.py (fit error below 4e-9);
-// beyond, the identity tanh|u| = 1 - 2 / (1 + e^(2|u|)) with the hardware
-// exponential and an approximate divide (no cancellation there: the result
-// is above 0.66). About 2 units in the last place on both sides; the
-// exponent is clamped at 126 so the divide's denominator stays in range
-// (tanh is 1 in fp32 well before).
-__device__ inline float tanh_fast(float u) {
-    const float a = fabsf(u);
-    const float w = u * u;
-    float p = fmaf(w, 0.0015856500249356031f, -0.007411024998873472f);
-    p = fmaf(p, w, 0.021303808316588402f);
-    p = fmaf(p, w, -0.053852491080760956f);
-    p = fmaf(p, w, 0.13332220911979675f);
-    p = fmaf(p, w, -0.33333298563957214f);
-    p = fmaf(p, w, 1.f);
-    const float e = ex2_hw(fminf(a * (2.f * kLog2e), 126.f));
-    const float big = copysignf(1.f - __fdividef(2.f, 1.f + e), u);
-    return a < 0.8f ? u * p : big;
+// The softcap z = c tanh(x / c) of the stream kernel and of the fused-linear
+// epilogue, cheaper than c * tanhf(x / c). With u = x / c and w = u^2:
+//   |u| < 0.3:  z = x (1 + n1 w + n2 w^2 + n3 w^3),
+//   |u| < 0.8:  z = x (1 + c1 w + ... + c6 w^6),
+//   otherwise:  z = c sign(u) (1 - 2 / (1 + e^(2|u|))), with the hardware
+//               exponential and an approximate divide (no cancellation: the
+//               result is above 0.66 c; the exponent is clamped at 126 so the
+//               denominator stays in range, tanh being 1 in fp32 well before).
+// The polynomials are least-squares fits (tanh_fit.py) of tanh(u) / u, within
+// about 1.2 and 2.5 units in the last place of tanh in fp32; x p(w) stands for
+// c u p(w) (the two differ by the rounding of c / c). NaN stays NaN.
+constexpr float kTanhN1 = -0.33333057165145874f;
+constexpr float kTanhN2 = 0.1331467479467392f;
+constexpr float kTanhN3 = -0.05035468563437462f;
+constexpr float kTanhC1 = -0.33333298563957214f;
+constexpr float kTanhC2 = 0.13332220911979675f;
+constexpr float kTanhC3 = -0.053852491080760956f;
+constexpr float kTanhC4 = 0.021303808316588402f;
+constexpr float kTanhC5 = -0.007411024998873472f;
+constexpr float kTanhC6 = 0.0015856500249356031f;
+constexpr float kTanhNarrowEdge = 0.3f;
+constexpr float kTanhPolyEdge = 0.8f;
+
+__device__ inline float tanh_poly_narrow(float w) {
+    float p = fmaf(w, kTanhN3, kTanhN2);
+    p = fmaf(p, w, kTanhN1);
+    return fmaf(p, w, 1.f);
+}
+__device__ inline float tanh_poly(float w) {
+    float p = fmaf(w, kTanhC6, kTanhC5);
+    p = fmaf(p, w, kTanhC4);
+    p = fmaf(p, w, kTanhC3);
+    p = fmaf(p, w, kTanhC2);
+    p = fmaf(p, w, kTanhC1);
+    return fmaf(p, w, 1.f);
+}
+__device__ inline F2 tanh_poly_narrow2(F2 w) {
+    F2 p = f2_fma(w, f2(kTanhN3, kTanhN3), f2(kTanhN2, kTanhN2));
+    p = f2_fma(p, w, f2(kTanhN1, kTanhN1));
+    return f2_fma(p, w, f2(1.f, 1.f));
+}
+__device__ inline F2 tanh_poly2(F2 w) {
+    F2 p = f2_fma(w, f2(kTanhC6, kTanhC6), f2(kTanhC5, kTanhC5));
+    p = f2_fma(p, w, f2(kTanhC4, kTanhC4));
+    p = f2_fma(p, w, f2(kTanhC3, kTanhC3));
+    p = f2_fma(p, w, f2(kTanhC2, kTanhC2));
+    p = f2_fma(p, w, f2(kTanhC1, kTanhC1));
+    return f2_fma(p, w, f2(1.f, 1.f));
+}
+__device__ inline float tanh_exp_form(float u) {
+    const float e = ex2_hw(fminf(fabsf(u) * (2.f * kLog2e), 126.f));
+    return copysignf(1.f - __fdividef(2.f, 1.f + e), u);
+}
+
+// One logit, its range chosen by its own |x| against 0.3 c and 0.8 c.
+__device__ inline float softcap_fast(float x, float cap, float inv_cap) {
+    const float a = fabsf(x);
+    if (a >= kTanhPolyEdge * cap) return cap * tanh_exp_form(x * inv_cap);
+    const float u = x * inv_cap, w = u * u;
+    return x * (a < kTanhNarrowEdge * cap ? tanh_poly_narrow(w) : tanh_poly(w));
+}
+
+// The form softcap_vec_form takes for values with |x| <= a: 0 the narrow
+// polynomial alone, 1 the general form (correct for any values).
+__device__ inline unsigned softcap_form(float a, float cap) {
+    return a < kTanhNarrowEdge * cap ? 0u : 1u;
+}
+
+// N logits (N even) in packed pairs, in the given form (one that covers every
+// value of the vector, softcap_form): the narrow polynomial alone, or the wide
+// polynomial and the exponential form for every value with a select (no
+// divergence inside the vector). The stream kernel takes one form per thread
+// and chunk and keeps it for the second pass, so logits of ordinary size never
+// pay for the wider polynomial, an exponential or a divide; two forms only keep
+// the inlined code small. The forms agree to about 2 units in the last place.
+// x and z may alias.
+template <int N>
+__device__ inline void softcap_vec_form(const float *x, float *z, float cap, float inv_cap, unsigned form) {
+    const F2 ic = f2(inv_cap, inv_cap);
+    if (form == 0u) {
+#pragma unroll
+        for (int p = 0; p < N / 2; ++p) {
+            const F2 xx = f2(x[2 * p], x[2 * p + 1]), u = f2_mul(xx, ic);
+            f2_split(f2_mul(xx, tanh_poly_narrow2(f2_mul(u, u))), z[2 * p], z[2 * p + 1]);
+        }
+    } else {
+        const float edge = kTanhPolyEdge * cap;
+#pragma unroll
+        for (int p = 0; p < N / 2; ++p) {
+            const float x0 = x[2 * p], x1 = x[2 * p + 1];
+            const F2 xx = f2(x0, x1), u = f2_mul(xx, ic);
+            float q0, q1;
+            f2_split(f2_mul(xx, tanh_poly2(f2_mul(u, u))), q0, q1);
+            const float e0 = cap * tanh_exp_form(x0 * inv_cap), e1 = cap * tanh_exp_form(x1 * inv_cap);
+            z[2 * p] = fabsf(x0) >= edge ? e0 : q0;
+            z[2 * p + 1] = fabsf(x1) >= edge ? e1 : q1;
+        }
+    }
+}
+
+// The same with the form the vector's own largest |x| needs.
+template <int N>
+__device__ inline void softcap_vec(const float *x, float *z, float cap, float inv_cap) {
+    float xmax = 0.f;
+#pragma unroll
+    for (int j = 0; j < N; ++j) xmax = fmaxf(xmax, fabsf(x[j]));
+    softcap_vec_form<N>(x, z, cap, inv_cap, softcap_form(xmax, cap));
+}
+
+// g *= dz/dx = 1 - (z / c)^2 for N values (N even), in packed pairs;
+// nic2 = -1 / c^2.
+template <int N>
+__device__ inline void softcap_deriv_vec(float *g, const float *z, float nic2) {
+    const F2 n2 = f2(nic2, nic2), one = f2(1.f, 1.f);
+#pragma unroll
+    for (int p = 0; p < N / 2; ++p) {
+        const F2 zz = f2(z[2 * p], z[2 * p + 1]);
+        f2_split(f2_mul(f2(g[2 * p], g[2 * p + 1]), f2_fma(f2_mul(zz, zz), n2, one)), g[2 * p], g[2 * p + 1]);
+    }
 }
 
 // The first column holding the maximum (ties go to the smaller column).

@@ -204,6 +204,7 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr bool CAPF = OPT == 2;
     const float cap = CAPF ? a.softcap : 0.f;
     const float inv_cap = CAPF && cap > 0.f ? 1.f / cap : 0.f;
+    const float nic2 = -(inv_cap * inv_cap);
     const float zl = FEAT ? a.z_loss : 0.f;
     const bool want_am = FEAT && a.accuracy != nullptr;
 
@@ -304,6 +305,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             // ------------------------------------------------ pass 1: statistics
             RowState st = row_state_empty();
             ArgMax am{-INFINITY, 0x7fffffff};
+            uint64_t cap_forms = 0;  // softcap: the form of chunk c (c < 32) in bits 2c, 2c+1
             for (int c = 0; c < nch; ++c, ++it) {
                 const uint32_t s = it % kStreamSlots;
                 mbar_wait_bounded<false>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
@@ -313,38 +315,21 @@ ce_stream_kernel(RowArgs a, int tune) {
                 // does one of this thread's vectors hold the target column?
                 const unsigned q = static_cast<unsigned>(y / VEC - v0 - tid);
                 const bool mine = q < static_cast<unsigned>(VPT * NCT) && (q % NCT) == 0;
-                if (CAPF && cap > 0.f) {
-                    // softcap: capped logits, first-maximum column of the raw logits
-                    for (int v = tid; v < nv; v += NCT) {
-                        const uint4 raw = ld_shared_v4(base_s + 16u * v);
-                        const int vb = (v0 + v) * VEC;
-                        float x[VEC], z[VEC];
-                        F::unpack(raw, x);
-                        float zmax = -INFINITY;
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) {
-                            z[j] = cap > 0.f ? cap * tanh_fast(x[j] * inv_cap) : x[j];
-                            zmax = fmaxf(zmax, z[j]);
-                        }
-                        if (want_am) {
-#pragma unroll
-                            for (int j = 0; j < VEC; ++j)
-                                am = argmax_merge(am, ArgMax{x[j], static_cast<int>(vlo + vb + j)});
-                        }
-                        const int skip = (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) ? y - vb : -1;
-                        if (skip >= 0) {
-                            float zv = 0.f;
-#pragma unroll
-                            for (int j = 0; j < VEC; ++j) zv = (j == skip) ? z[j] : zv;
-                            S.xy[rp] = zv;  // the capped target logit, for the merge
-                        }
-                        row_state_add<VEC, P1S>(st, z, zmax, skip, nullptr);
-                    }
-                } else if (nv == VPC && !mine) {
+                // softcap: a form (softcap_form) that covers this thread's vectors of the
+                // chunk, taken on the full-chunk path, kept for the second pass over the
+                // same vectors (the partial and target chunks take the general form here)
+                unsigned form = 0u;
+                if (nv == VPC && !mine) {
                     // full chunk, no target: one max per chunk, four independent sums
                     uint4 raw[VPT];
 #pragma unroll
                     for (int k = 0; k < VPT; ++k) raw[k] = ld_shared_v4(base_s + 16u * (tid + k * NCT));
+                    if (CAPF && cap > 0.f) {
+                        float ax = 0.f;
+#pragma unroll
+                        for (int k = 0; k < VPT; ++k) ax = fmaxf(ax, F::vabsmax(raw[k]));
+                        form = softcap_form(ax, cap);
+                    }
                     float vm[VPT];
 #pragma unroll
                     for (int k = 0; k < VPT; ++k) vm[k] = F::vmax(raw[k]);
@@ -367,9 +352,13 @@ ce_stream_kernel(RowArgs a, int tune) {
                         for (int e = VEC - 1; e >= 0; --e) e0 = (xk[e] == cm) ? e : e0;
                         am = ArgMax{cm, static_cast<int>(vlo + (v0 + tid + kk * NCT) * VEC + e0)};
                     }
-                    if (cm > st.m) {
-                        if (st.m != -INFINITY) st.s *= ex2_hw((st.m - cm) * kLog2e);
-                        st.m = cm;
+                    // softcap is increasing: the chunk's capped maximum is that of its raw
+                    // maximum (up to the rounding of the two evaluations, which the online
+                    // sum absorbs)
+                    const float zm = (CAPF && cap > 0.f) ? softcap_fast(cm, cap, inv_cap) : cm;
+                    if (zm > st.m) {
+                        if (st.m != -INFINITY) st.s *= ex2_hw((st.m - zm) * kLog2e);
+                        st.m = zm;
                     }
                     if (st.m != -INFINITY) {
                         // four accumulators, column j into sum j mod 4, held as two packed
@@ -381,6 +370,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                         for (int k = 0; k < VPT; ++k) {
                             float x[VEC];
                             F::unpack(raw[k], x);
+                            if (CAPF && cap > 0.f) softcap_vec_form<VEC>(x, x, cap, inv_cap, form);
 #pragma unroll
                             for (int p = 0; p < VEC / 2; ++p) {
                                 const F2 xx = f2(x[2 * p], x[2 * p + 1]);
@@ -403,10 +393,38 @@ ce_stream_kernel(RowArgs a, int tune) {
                         for (int k = 0; k < VPT; ++k) {
                             float x[VEC];
                             F::unpack(raw[k], x);
+                            if (CAPF && cap > 0.f) softcap_vec_form<VEC>(x, x, cap, inv_cap, form);
 #pragma unroll
                             for (int j = 0; j < VEC; ++j) st.r += x[j];
                         }
                         st.n += static_cast<float>(VPT * VEC);
+                    }
+                } else if (CAPF && cap > 0.f) {
+                    // softcap, partial chunk or the target's: capped logits, first-maximum
+                    // column of the raw logits
+                    for (int v = tid; v < nv; v += NCT) {
+                        const uint4 raw = ld_shared_v4(base_s + 16u * v);
+                        const int vb = (v0 + v) * VEC;
+                        float x[VEC], z[VEC];
+                        F::unpack(raw, x);
+                        form = max(form, softcap_form(F::vabsmax(raw), cap));
+                        softcap_vec_form<VEC>(x, z, cap, inv_cap, 1u);  // general form: a rare path
+                        float zmax = -INFINITY;
+#pragma unroll
+                        for (int j = 0; j < VEC; ++j) zmax = fmaxf(zmax, z[j]);
+                        if (want_am) {
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j)
+                                am = argmax_merge(am, ArgMax{x[j], static_cast<int>(vlo + vb + j)});
+                        }
+                        const int skip = (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) ? y - vb : -1;
+                        if (skip >= 0) {
+                            float zv = 0.f;
+#pragma unroll
+                            for (int j = 0; j < VEC; ++j) zv = (j == skip) ? z[j] : zv;
+                            S.xy[rp] = zv;  // the capped target logit, for the merge
+                        }
+                        row_state_add<VEC, P1S>(st, z, zmax, skip, nullptr);
                     }
                 } else {
                     for (int v = tid; v < nv; v += NCT) {
@@ -432,13 +450,14 @@ ce_stream_kernel(RowArgs a, int tune) {
                         row_state_add<VEC, P1S>(st, x, vmx, skip, nullptr);
                     }
                 }
+                if (CAPF && c < 32) cap_forms |= static_cast<uint64_t>(form) << (2 * c);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
             }
             if (tid < nedge) {
                 const int64_t c = edge_c;
                 const float xr = F::load1(rowp, c);
-                float x = (CAPF && cap > 0.f) ? cap * tanh_fast(xr * inv_cap) : xr;
+                float x = (CAPF && cap > 0.f) ? softcap_fast(xr, cap, inv_cap) : xr;
                 if (want_am) am = argmax_merge(am, ArgMax{xr, static_cast<int>(c)});
                 if (c == yg) S.xy[rp] = x;
                 row_state_add<1, P1S>(st, &x, x, (c == yg) ? 0 : -1, nullptr);
@@ -539,31 +558,14 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const uint32_t base_s = ring + s * kStreamChunk;
                 const int v0 = c * VPC;
                 const int nv = min(VPC, nvec - v0);
+                const unsigned form = c < 32 ? static_cast<unsigned>(cap_forms >> (2 * c)) & 3u : 2u;
                 for (int v = tid; v < nv; v += NCT) {
-                    float x[VEC], gr[VEC], z[VEC];
+                    float x[VEC], gr[VEC];
                     F::unpack(ld_shared_v4(base_s + 16u * v), x);
                     const int vb = (v0 + v) * VEC;
-                    if (CAPF && cap > 0.f) {
-                        // softcap: the gradient of the capped logits, times dz/dx below
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) z[j] = cap > 0.f ? cap * tanh_fast(x[j] * inv_cap) : x[j];
-#pragma unroll
-                        for (int h = 0; h < VEC / 4; ++h) {
-                            const float4 wv = MODE == 2 ? load_w4(a.weight, vlo + vb + 4 * h, w4)
-                                                        : make_float4(1.f, 1.f, 1.f, 1.f);
-                            gr[4 * h] = grad_elem(rs, z[4 * h], wv.x);
-                            gr[4 * h + 1] = grad_elem(rs, z[4 * h + 1], wv.y);
-                            gr[4 * h + 2] = grad_elem(rs, z[4 * h + 2], wv.z);
-                            gr[4 * h + 3] = grad_elem(rs, z[4 * h + 3], wv.w);
-                            if (DEFER) {
-                                const F2 w01 = f2(wv.x, wv.y), w23 = f2(wv.z, wv.w);
-                                dr[0] = f2_fma(w01, f2(z[4 * h], z[4 * h + 1]), dr[0]);
-                                dr[1] = f2_fma(w23, f2(z[4 * h + 2], z[4 * h + 3]), dr[1]);
-                                dn[0] = f2_add(dn[0], w01);
-                                dn[1] = f2_add(dn[1], w23);
-                            }
-                        }
-                    } else if (MODE == 2) {
+                    // softcap: the capped logits replace the raw ones; dz/dx scales below
+                    if (CAPF && cap > 0.f) softcap_vec_form<VEC>(x, x, cap, inv_cap, form);
+                    if (MODE == 2) {
 #pragma unroll
                         for (int h = 0; h < VEC / 4; ++h) {
                             const float4 wv = load_w4(a.weight, vlo + vb + 4 * h, w4);
@@ -590,13 +592,7 @@ ce_stream_kernel(RowArgs a, int tune) {
 #pragma unroll
                         for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
                     }
-                    if (CAPF && cap > 0.f) {
-#pragma unroll
-                        for (int j = 0; j < VEC; ++j) {
-                            const float tj = z[j] * inv_cap;
-                            gr[j] *= fmaf(-tj, tj, 1.f);
-                        }
-                    }
+                    if (CAPF && cap > 0.f) softcap_deriv_vec<VEC>(gr, x, nic2);
                     st_stream(vp + v0 + v, F::pack(gr));  // vp points at this CTA's slice
                 }
                 __syncwarp();
@@ -607,14 +603,11 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const int64_t c = edge_c;
                 const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
                 const float xr = F::load1(rowp, c);
-                const float xe = (CAPF && cap > 0.f) ? cap * tanh_fast(xr * inv_cap) : xr;
+                const float xe = (CAPF && cap > 0.f) ? softcap_fast(xr, cap, inv_cap) : xr;
                 er = wc * xe;
                 en = wc;
                 float ge = (c == yg) ? rs.dxy : grad_elem(rs, xe, wc);
-                if (CAPF && cap > 0.f) {
-                    const float te = xe * inv_cap;
-                    ge *= fmaf(-te, te, 1.f);
-                }
+                if (CAPF && cap > 0.f) ge *= fmaf(xe * xe, nic2, 1.f);
                 F::store1(rowp, c, ge);
             }
             if (DEFER) {

@@ -173,7 +173,7 @@ __device__ inline void epilogue_stats(const GemmArgs &g, int row, int col0, cons
         }
         if (g.st_cap > 0.f) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) x[j] = g.st_cap * tanh_fast(x[j] * g.st_inv_cap);
+            for (int q = 0; q < 4; ++q) softcap_vec<8>(x + 8 * q, x + 8 * q, g.st_cap, g.st_inv_cap);
         }
         float4 *o4 = reinterpret_cast<float4 *>(o);
 #pragma unroll
@@ -197,7 +197,7 @@ __device__ inline void epilogue_stats(const GemmArgs &g, int row, int col0, cons
             if (j < nv) {
                 float xv = x[j] + (g.bias ? __ldg(g.bias + col0 + j) : 0.f);
                 if (g.pam) am = argmax_merge(am, ArgMax{xv, col0 + j});
-                if (g.st_cap > 0.f) xv = g.st_cap * tanh_fast(xv * g.st_inv_cap);
+                if (g.st_cap > 0.f) xv = softcap_fast(xv, g.st_cap, g.st_inv_cap);
                 o[j] = xv;
                 float wj = SMODE == 2 ? __ldg(g.st_weight + col0 + j) : 1.f;
                 row_state_add<1, SMODE != 0>(st, &xv, xv, skip == j ? 0 : -1, SMODE == 2 ? &wj : nullptr);
