@@ -337,8 +337,9 @@ __device__ inline float row_state_rel_sum(const RowState &st) {
 }
 
 // ------------------------------------------------------------------ softcap and argmax
-// z = c tanh(x / c) with the accurate tanh (an approximate tanh would move
-// exp(z) by more than half a bf16 ulp), and dz/dx = 1 - (z / c)^2.
+// z = c tanh(x / c) with CUDA's accurate tanhf, for the row-pass and split
+// kernels (the hardware tanh.approx, about 2^-11 relative, would move exp(z)
+// by more than half a bf16 ulp), and dz/dx = 1 - (z / c)^2.
 __device__ inline float softcap_logit(float x, float c) { return c * tanhf(x / c); }
 __device__ inline float softcap_deriv(float z, float c) {
     const float u = z / c;

@@ -157,7 +157,7 @@ __device__ inline void finish_deferred_loss(const RowArgs &a, uint32_t rank, int
 // of the raw logits, the same column as that of the capped ones since tanh
 // is increasing); OPT 2: the same plus softcap (every logit becomes
 // c tanh(x / c), the gradient gains the factor 1 - (z / c)^2). Softcap has
-// its own instantiations: its accurate tanh, inlined into the element
+// its own instantiations: its tanh evaluation, inlined into the element
 // loops, costs instruction-cache room even when it is not taken.
 template <int DT, int MODE, int SHAPE, int CL, bool RAG, int OPT = 0>
 __global__ void __launch_bounds__(StreamShape<SHAPE>::kThreads, StreamShape<SHAPE>::kCtasPerSm)
