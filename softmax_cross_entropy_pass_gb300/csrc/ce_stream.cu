@@ -96,22 +96,36 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     //    second pass is served by L2, walking each half row last chunk first
     //    (8192 x 128256 bf16: 0.746 ms; 0.749 ms first chunk first; 0.775 ms
     //    unpaired; 0.827 ms paired at two CTAs per SM);
-    //  larger rows: one 16-warp CTA per SM, a pair per row: the half rows
-    //    waiting in L2 for their second pass (152 x 256 KB at 16384 x 256000
-    //    bf16) fit with room to spare (three CTAs per SM: 117 MB, bimodal
-    //    4.3 / 5.4 ms); 4.50 ms.
+    //  rows <= 512 KB (<= 640 KB without class-weighted smoothing): three
+    //    CTAs per SM, a cluster of four per row, each streaming a quarter,
+    //    second pass last chunk first: the 114 rows in flight keep 58 MB
+    //    waiting in L2 at 512 KB (16384 x 256000 bf16 with class weights:
+    //    4.42 ms vs 4.63 ms for 16-warp pairs; 8192 x 256000: 1.513 vs 1.675
+    //    ms; 8192 x 320000: 1.878 vs 2.013 ms; with class weights at 640 KB
+    //    4.80 vs 4.45 ms, whose pass-2 weight loads add to the L2 traffic);
+    //    not for the softcap / z-loss / accuracy kernels (pairs only);
+    //  larger rows (or with those options): one 16-warp CTA per SM, a pair
+    //    per row: the half rows waiting in L2 for their second pass fit with
+    //    room to spare (8192 x 448000: 2.708 ms vs 2.728 for quads; three
+    //    CTAs per SM in pairs at 16384 x 256000: 117 MB waiting, bimodal
+    //    4.3 / 5.4 ms).
     //  In every case the first pass carries no L2 evict-last hint: with the
     //  hint the second pass missed more (8192 x 128256: 9.5% reads over the
     //  algorithmic bytes against 5.3%; 16384 x 256000: 4.93 ms against 4.50),
     //  while the second pass keeps its evict-first hint (without it 0.762 ms).
+    const bool opts = a.softcap > 0.f || a.z_loss > 0.f || a.accuracy;
     if (tune == 0) {
         const int64_t row_bytes = a.vocab * (dtype == CE_DT_F32 ? 4 : 2);
+        const int64_t quad_max = (mode == 2 ? 512 : 640) * 1024;
         tune = row_bytes <= 96 * 1024 ? (kTuneThree | kTuneNoKeep)
              : row_bytes <= 384 * 1024 ? (kTuneThree | kTuneCluster2 | kTuneNoKeep | kTuneReverse)
-                                      : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
+             : (row_bytes <= quad_max && !opts) ? (kTuneThree | kTuneCluster4 | kTuneNoKeep | kTuneReverse)
+                                                : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
     }
-    const bool pair = (tune & kTuneCluster2) && a.vocab >= 2 * (dtype == CE_DT_F32 ? 4 : 8);
-    if (a.softcap > 0.f || a.z_loss > 0.f || a.accuracy) {
+    const int vec = dtype == CE_DT_F32 ? 4 : 8;
+    const bool pair = (tune & kTuneCluster2) && a.vocab >= 2 * vec;
+    const bool quad = (tune & kTuneCluster4) && a.vocab >= 4 * vec;
+    if (opts) {
         // the options are built for the three shapes the library picks by row size
         if ((tune & kTuneWide) && pair) return launch_stream_shape<1, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
         return pair ? launch_stream_shape<2, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
@@ -121,7 +135,8 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
         return pair ? launch_stream_shape<1, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
                     : launch_stream_shape<1, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
     if (tune & kTuneThree)
-        return pair ? launch_stream_shape<2, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+        return quad ? launch_stream_shape<2, 4>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+             : pair ? launch_stream_shape<2, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
                     : launch_stream_shape<2, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
     return pair ? launch_stream_shape<0, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
                 : launch_stream_shape<0, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);

@@ -13,10 +13,10 @@
 // HBM sees one read and one write per element; the L2 holds about one row
 // per CTA pair between the passes.
 //
-// With a cluster of two CTAs per row, each CTA streams half of the row and
-// the two halves' statistics are exchanged through distributed shared
-// memory (st.shared::cluster + a remote mbarrier arrive), which halves the
-// bytes each CTA keeps waiting in L2 for its second pass.
+// With a cluster of two (or four) CTAs per row, each CTA streams half (a
+// quarter) of the row and the parts' statistics are exchanged through
+// distributed shared memory (st.shared::cluster + a remote mbarrier arrive),
+// which divides the bytes each CTA keeps waiting in L2 for its second pass.
 //
 // Rows at any alignment: the part of a row before its first 16-byte boundary
 // and after its last goes through plain accesses (RAG instantiations). The
@@ -53,7 +53,7 @@ struct StreamSmem {
     uint64_t full[kStreamMaxSlots];
     uint64_t empty[kStreamMaxSlots];
     uint64_t xbar[2];
-    StreamXSlot slot[2][2];
+    StreamXSlot slot[2][4];  // [row parity][CTA of the cluster]
     // per row parity: a warp may write the next row's values while a slower
     // warp still reads this row's (never further ahead: the row's barrier
     // waits for every warp)
@@ -71,6 +71,7 @@ constexpr int kTuneReverse = 2;    // second pass walks the row's chunks last to
 constexpr int kTuneNoKeep = 4;     // first pass without the L2 evict-last policy
 constexpr int kTuneCluster2 = 8;   // a cluster of two CTAs per row, each streaming half
 constexpr int kTuneThree = 16;     // three CTAs per SM with a 4-slot ring
+constexpr int kTuneCluster4 = 32;  // a cluster of four CTAs per row (three CTAs per SM)
 
 template <int NCW>
 __device__ inline void stream_consumer_sync() {
@@ -179,7 +180,7 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr int VPC = kStreamChunk / 16;          // vectors per full chunk
     constexpr int VPT = VPC / NCT;                  // vectors per thread per full chunk
     static_assert(VPC % NCT == 0, "chunk must split evenly over the consumers");
-    static_assert(CL == 1 || CL == 2, "one or two CTAs per row");
+    static_assert(CL == 1 || CL == 2 || CL == 4, "one, two or four CTAs per row");
 
     extern __shared__ __align__(128) uint8_t smem[];
     StreamSmem &S = *reinterpret_cast<StreamSmem *>(smem + kStreamSlots * kStreamChunk);
@@ -726,6 +727,7 @@ template <bool RAG>
 const void *stream_kernel_for(int dtype, int mode, int shape, int cl) {
     CE_STREAM_PICK(0, 1, RAG, 0) CE_STREAM_PICK(0, 2, RAG, 0) CE_STREAM_PICK(1, 1, RAG, 0)
     CE_STREAM_PICK(1, 2, RAG, 0) CE_STREAM_PICK(2, 1, RAG, 0) CE_STREAM_PICK(2, 2, RAG, 0)
+    CE_STREAM_PICK(2, 4, RAG, 0)
     return nullptr;
 }
 

@@ -75,10 +75,10 @@ RAGGED = [
 @pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
 @pytest.mark.parametrize("shape", RAGGED, ids=lambda s: f"{s[0]}x{s[1]}ld{s[2]}@{s[3]}")
 @pytest.mark.parametrize("opt", ["plain", "weighted_smooth"])
-@pytest.mark.parametrize("tune", [0, 8, 9, 16, 24], ids=lambda t: f"tune{t}")
+@pytest.mark.parametrize("tune", [0, 8, 9, 16, 24, 54], ids=lambda t: f"tune{t}")
 def test_stream_ragged_rows(ce, dtype, shape, opt, tune):
     """The stream kernel on rows that do not start on a 16-byte boundary: the
-    head and tail of each row (and of each half row for a CTA pair) go
+    head and tail of each row (and of each part for a CTA pair or quad) go
     through plain accesses, the interior through the bulk-copy ring; the
     view starts inside a wider buffer so the base itself is misaligned."""
     R, V, ld, off = shape
@@ -426,15 +426,17 @@ def test_tiny_config(ce):
     _check_all(x, t, None, 0.0, "mean", None, ref, loss, x_in)
 
 
-@pytest.mark.parametrize("tune", [0, 1, 2, 3, 4, 8, 9, 10, 12, 15, 16, 24, 26])
-@pytest.mark.parametrize("shape", [(70, 128256), (33, 33008), (9, 256000), (5, 1000)])
+@pytest.mark.parametrize("tune", [0, 1, 2, 3, 4, 8, 9, 10, 12, 15, 16, 24, 26, 48, 52, 54])
+@pytest.mark.parametrize("shape", [(70, 128256), (33, 33008), (9, 256000), (5, 1000), (6, 40)])
 def test_stream_tuning_variants(ce, tune, shape):
     """Every stream-kernel tuning combination (wide CTA, reversed second
-    pass, no L2 evict-last) against the oracle."""
+    pass, no L2 evict-last, CTA pairs and quads) against the oracle; class
+    weights on the odd tunes and on 54 (a quad); at V = 40 the last CTA of a
+    quad has no columns (the parts are 16, 16 and 8 columns)."""
     R, V = shape
     x = make_logits(R, V, "bf16", 1.5, 300 + tune, device="cuda")
     t = make_targets(R, V, 0.1, 300 + tune, device="cuda")
-    w = make_weights(V, 300 + tune, device="cuda") if tune % 2 else None
+    w = make_weights(V, 300 + tune, device="cuda") if tune % 2 or tune == 54 else None
     x_in = x.cpu()
     g = torch.tensor([0.37], device="cuda")
     ref = _oracle(x, t, w, 0.05, "sum", g)
