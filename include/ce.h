@@ -96,8 +96,7 @@ typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
  * chunks in reverse order, 4 = first pass without the L2 evict-last policy,
  * 8 = a cluster of two CTAs per row (each streams half the row),
  * 16 = three CTAs per SM with a smaller ring, 32 = with 16: a cluster of four
- * CTAs per row (each streams a quarter; without the softcap, z-loss and
- * accuracy options) */
+ * CTAs per row (each streams a quarter) */
 #define CE_VARIANT_TUNE_SHIFT 20
 
 typedef struct ce_params {

@@ -102,9 +102,11 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     //    waiting in L2 at 512 KB (16384 x 256000 bf16 with class weights:
     //    4.42 ms vs 4.63 ms for 16-warp pairs; 8192 x 256000: 1.513 vs 1.675
     //    ms; 8192 x 320000: 1.878 vs 2.013 ms; with class weights at 640 KB
-    //    4.80 vs 4.45 ms, whose pass-2 weight loads add to the L2 traffic);
-    //    not for the softcap / z-loss / accuracy kernels (pairs only);
-    //  larger rows (or with those options): one 16-warp CTA per SM, a pair
+    //    4.80 vs 4.45 ms, whose pass-2 weight loads add to the L2 traffic;
+    //    8192 x 256000 with softcap 30: 2.673 vs 2.907 ms, with z-loss and
+    //    accuracy 1.626 vs 1.930 ms; 16384 x 256000 with class weights and
+    //    softcap 30: 7.087 vs 7.045 ms);
+    //  larger rows: one 16-warp CTA per SM, a pair
     //    per row: the half rows waiting in L2 for their second pass fit with
     //    room to spare (8192 x 448000: 2.708 ms vs 2.728 for quads; three
     //    CTAs per SM in pairs at 16384 x 256000: 117 MB waiting, bimodal
@@ -119,16 +121,17 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
         const int64_t quad_max = (mode == 2 ? 512 : 640) * 1024;
         tune = row_bytes <= 96 * 1024 ? (kTuneThree | kTuneNoKeep)
              : row_bytes <= 384 * 1024 ? (kTuneThree | kTuneCluster2 | kTuneNoKeep | kTuneReverse)
-             : (row_bytes <= quad_max && !opts) ? (kTuneThree | kTuneCluster4 | kTuneNoKeep | kTuneReverse)
-                                                : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
+             : row_bytes <= quad_max ? (kTuneThree | kTuneCluster4 | kTuneNoKeep | kTuneReverse)
+                                     : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
     }
     const int vec = dtype == CE_DT_F32 ? 4 : 8;
     const bool pair = (tune & kTuneCluster2) && a.vocab >= 2 * vec;
     const bool quad = (tune & kTuneCluster4) && a.vocab >= 4 * vec;
     if (opts) {
-        // the options are built for the three shapes the library picks by row size
+        // the options are built for the four shapes the library picks by row size
         if ((tune & kTuneWide) && pair) return launch_stream_shape<1, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
-        return pair ? launch_stream_shape<2, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+        return quad ? launch_stream_shape<2, 4>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+             : pair ? launch_stream_shape<2, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
                     : launch_stream_shape<2, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
     }
     if (tune & kTuneWide)

@@ -731,18 +731,22 @@ const void *stream_kernel_for(int dtype, int mode, int shape, int cl) {
     return nullptr;
 }
 
-// With the options: the three shapes the library picks by row size (three
-// CTAs per SM, alone or in pairs; one wide CTA per SM in pairs).
+// With the options: the four shapes the library picks by row size (three
+// CTAs per SM, alone, in pairs or in quads; one wide CTA per SM in pairs).
 template <bool RAG, int OPT>
 const void *stream_kernel_options_for(int dtype, int mode, int shape, int cl) {
-    CE_STREAM_PICK(2, 1, RAG, OPT) CE_STREAM_PICK(2, 2, RAG, OPT) CE_STREAM_PICK(1, 2, RAG, OPT)
+    CE_STREAM_PICK(2, 1, RAG, OPT) CE_STREAM_PICK(2, 2, RAG, OPT) CE_STREAM_PICK(2, 4, RAG, OPT)
+    CE_STREAM_PICK(1, 2, RAG, OPT)
     return nullptr;
 }
 #undef CE_STREAM_PICK
 
-// defined in ce_stream_ragged.cu, ce_stream_options.cu and ce_stream_softcap.cu
+// defined in ce_stream_ragged.cu, ce_stream_options.cu, ce_stream_options_ragged.cu,
+// ce_stream_softcap.cu and ce_stream_softcap_ragged.cu
 const void *stream_kernel_ragged(int dtype, int mode, int shape, int cl);
 const void *stream_kernel_options(int dtype, int mode, int shape, int cl, bool ragged);
+const void *stream_kernel_options_ragged(int dtype, int mode, int shape, int cl);
 const void *stream_kernel_softcap(int dtype, int mode, int shape, int cl, bool ragged);
+const void *stream_kernel_softcap_ragged(int dtype, int mode, int shape, int cl);
 
 }  // namespace ce
