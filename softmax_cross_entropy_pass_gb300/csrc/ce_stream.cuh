@@ -138,6 +138,13 @@ __device__ inline float4 load_w4(const float *w, int64_t c, bool vec4) {
     if (vec4) return __ldg(reinterpret_cast<const float4 *>(w + c));
     return make_float4(__ldg(w + c), __ldg(w + c + 1), __ldg(w + c + 2), __ldg(w + c + 3));
 }
+// 8 class weights at a 32-byte aligned address, one 256-bit read-only load
+// (one full sector per lane instead of two half-sector loads)
+__device__ inline void load_w8(const float *p, float4 &lo, float4 &hi) {
+    asm volatile("ld.global.nc.v8.f32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=f"(lo.x), "=f"(lo.y), "=f"(lo.z), "=f"(lo.w), "=f"(hi.x), "=f"(hi.y), "=f"(hi.z), "=f"(hi.w)
+                 : "l"(p));
+}
 
 // The loss of a row whose class-weighted smoothing sums (r = sum w x,
 // n = sum w over the whole row) arrived after its gradient pass; written by
@@ -200,6 +207,7 @@ ce_stream_kernel(RowArgs a, int tune) {
     char *const xbase = reinterpret_cast<char *>(a.grad);
     // weights as float4 when the base allows it (each row's interior start decides the rest)
     const bool w_base16 = (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
+    const bool w_base32 = (reinterpret_cast<uintptr_t>(a.weight) & 31u) == 0;
     const RowGeom g_aligned = row_geom_aligned<F::kBytes>(lo, L);
     constexpr bool FEAT = OPT != 0;
     constexpr bool CAPF = OPT == 2;
@@ -286,6 +294,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             const int64_t edge_c = tid < gm.nhead ? lo + tid : gm.tail0 + (tid - gm.nhead);
             uint4 *vp = reinterpret_cast<uint4 *>(rowp + vlo * F::kBytes);
             const bool w4 = w_base16 && (vlo & 3) == 0;
+            const bool w8 = VEC == 8 && w_base32 && (vlo & 7) == 0;  // 8 weights per vector, one load
             if (!valid) {
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 for (int v = tid; v < nvec; v += NCT) st_stream(vp + v, z);
@@ -567,9 +576,16 @@ ce_stream_kernel(RowArgs a, int tune) {
                     // softcap: the capped logits replace the raw ones; dz/dx scales below
                     if (CAPF && cap > 0.f) softcap_vec_form<VEC>(x, x, cap, inv_cap, form);
                     if (MODE == 2) {
+                        float4 wq[VEC / 4];
+                        if (VEC == 8 && w8) {
+                            load_w8(a.weight + vlo + vb, wq[0], wq[VEC / 4 - 1]);
+                        } else {
+#pragma unroll
+                            for (int h = 0; h < VEC / 4; ++h) wq[h] = load_w4(a.weight, vlo + vb + 4 * h, w4);
+                        }
 #pragma unroll
                         for (int h = 0; h < VEC / 4; ++h) {
-                            const float4 wv = load_w4(a.weight, vlo + vb + 4 * h, w4);
+                            const float4 wv = wq[h];
                             const F2 w01 = f2(wv.x, wv.y), w23 = f2(wv.z, wv.w);
                             const F2 x01 = f2(x[4 * h], x[4 * h + 1]), x23 = f2(x[4 * h + 2], x[4 * h + 3]);
                             const F2 nbw0 = f2_mul(rs_nb, w01), nbw1 = f2_mul(rs_nb, w23);
