@@ -503,7 +503,8 @@ def test_bounded_wait_gives_up_with_status_and_context_survives(ce):
     assert ce.ce_get_status(ws) == 0
 
 
-@pytest.mark.parametrize("api", ["auto", "stream-pair", "stream-wide", "rowpass", "split", "fwd+bwd calls"])
+@pytest.mark.parametrize("api", ["auto", "stream-pair", "stream-wide", "stream-quad", "rowpass", "split",
+                                 "fwd+bwd calls"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("red", ["mean", "sum", "none"])
 @pytest.mark.parametrize("opts", [(15.0, 0.0), (0.0, 1e-4), (30.0, 1e-4), (0.0, 0.0)],
@@ -511,8 +512,9 @@ def test_bounded_wait_gives_up_with_status_and_context_survives(ce):
 @pytest.mark.parametrize("shape", [(17, 1000), (9, 33000), (5, 7), (6, 1001)], ids=lambda s: f"{s[0]}x{s[1]}")
 def test_softcap_zloss_accuracy(ce, api, dtype, red, opts, shape):
     """Softcap, z-loss and token accuracy against the oracle, in the stream
-    kernel (automatic path, CTA pairs, wide CTAs), the row pass and the split
-    kernels; the token accuracy is asked for in every case."""
+    kernel (automatic path, CTA pairs, wide CTAs, clusters of four), the row
+    pass and the split kernels; the token accuracy is asked for in every
+    case."""
     R, V = shape
     cap, zl = opts
     seed = zlib.crc32(repr((R, V, dtype, red, opts)).encode()) % 9973
@@ -532,7 +534,8 @@ def test_softcap_zloss_accuracy(ce, api, dtype, red, opts, shape):
         ce.ce_backward(x, t, stats, grad_output=g, weight=w, label_smoothing=0.1, reduction=red, softcap=cap,
                        z_loss=zl)
     else:
-        variant, tune = {"stream-pair": ("stream", 8), "stream-wide": ("stream", 9)}.get(api, (api, 0))
+        variant, tune = {"stream-pair": ("stream", 8), "stream-wide": ("stream", 9),
+                         "stream-quad": ("stream", 52)}.get(api, (api, 0))
         loss = ce.ce_fwd_bwd(x, t, grad_output=g, weight=w, label_smoothing=0.1, reduction=red,
                              variant=variant, tune=tune, softcap=cap, z_loss=zl, accuracy=acc)
     torch.cuda.synchronize()
