@@ -396,9 +396,10 @@ def run_ours(args):
     import softmax_cross_entropy_pass_gb300 as ce
     from workloads import CONFIGS, make_ce_inputs
     cfg = CONFIGS[args.workload]
-    if args.rows or args.vocab:
+    if args.rows or args.vocab or args.dtype:
         import dataclasses
-        cfg = dataclasses.replace(cfg, n_rows=args.rows or cfg.n_rows, vocab=args.vocab or cfg.vocab)
+        cfg = dataclasses.replace(cfg, n_rows=args.rows or cfg.n_rows, vocab=args.vocab or cfg.vocab,
+                                  dtype=args.dtype or cfg.dtype)
     R, V = cfg.n_rows, cfg.vocab
     inp = make_ce_inputs(cfg, device=device)
     pristine, target, g = inp["logits"], inp["target"], inp["grad_output"]
@@ -526,7 +527,9 @@ def run_ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        # the arithmetic type: statistics and gradient are formed in fp32 (the
+        # logits' storage type is config.logits_dtype)
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": f"{cfg.name}: BT={R}, V={V}, {cfg.dtype} logits N(0,{cfg.sigma:g}^2), "
                                f"{R - n_valid} rows ignore_index=-100, label_smoothing={cfg.label_smoothing:g}, "
                                f"{cfg.reduction}, grad_output={cfg.grad_output}, "
@@ -534,8 +537,10 @@ def run_ours(args):
                    "global_batch": R * world, "seq_len": None, "parallelism": f"replicas x{world}",
                    "variant": args.variant, "path": path, "tune": args.tune, "fused_plan": plan,
                    "options": {k: (v if k != "accuracy" else True) for k, v in options.items()} or None,
-                   "l2": "inputs 2.1 GB > 129 MB L2; logits restored and a 256 MB buffer written "
-                         "before every step, outside the timed region"},
+                   "logits_dtype": cfg.dtype,
+                   "l2": f"inputs {R * V * esz / 1e9:.2f} GB {'>' if R * V * esz > 129e6 else '<'} 129 MB L2; "
+                         "logits restored and a 256 MB buffer written before every step, outside the timed "
+                         "region"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": kernel_name, "kernel_ms": kernel_avg_s * 1e3,
@@ -577,6 +582,8 @@ def main():
     ap.add_argument("--softcap", type=float, default=0.0, help="logit softcap c (0: off)")
     ap.add_argument("--z-loss", type=float, default=0.0, help="z-loss weight lambda (0: off)")
     ap.add_argument("--accuracy", action="store_true", help="also compute the token accuracy")
+    ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default="",
+                    help="logits storage type (default: the workload's)")
     ap.add_argument("--vocab", type=int, default=0,
                     help="another vocabulary size for the workload (e.g. one that leaves rows unaligned)")
     ap.add_argument("--workload", default=WORKLOAD,

@@ -96,21 +96,22 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     //    second pass is served by L2, walking each half row last chunk first
     //    (8192 x 128256 bf16: 0.746 ms; 0.749 ms first chunk first; 0.775 ms
     //    unpaired; 0.827 ms paired at two CTAs per SM);
-    //  rows <= 512 KB (<= 640 KB without class-weighted smoothing): three
-    //    CTAs per SM, a cluster of four per row, each streaming a quarter,
-    //    second pass last chunk first: the 114 rows in flight keep 58 MB
-    //    waiting in L2 at 512 KB (16384 x 256000 bf16 with class weights:
-    //    4.42 ms vs 4.63 ms for 16-warp pairs; 8192 x 256000: 1.513 vs 1.675
-    //    ms; 8192 x 320000: 1.878 vs 2.013 ms; with class weights at 640 KB
-    //    4.80 vs 4.45 ms, whose pass-2 weight loads add to the L2 traffic;
-    //    8192 x 256000 with softcap 30: 2.673 vs 2.907 ms, with z-loss and
-    //    accuracy 1.626 vs 1.930 ms; 16384 x 256000 with class weights and
-    //    softcap 30: 7.087 vs 7.045 ms);
-    //  larger rows: one 16-warp CTA per SM, a pair
-    //    per row: the half rows waiting in L2 for their second pass fit with
-    //    room to spare (8192 x 448000: 2.708 ms vs 2.728 for quads; three
-    //    CTAs per SM in pairs at 16384 x 256000: 117 MB waiting, bimodal
-    //    4.3 / 5.4 ms).
+    //  bf16 / f16 rows <= 512 KB (<= 640 KB without class-weighted
+    //    smoothing): three CTAs per SM, a cluster of four per row, each
+    //    streaming a quarter, second pass last chunk first: the 114 rows in
+    //    flight keep 58 MB waiting in L2 at 512 KB (16384 x 256000 bf16 with
+    //    class weights: 4.42 ms vs 4.63 ms for 16-warp pairs; 8192 x 256000:
+    //    1.513 vs 1.675 ms; 8192 x 320000: 1.878 vs 2.013 ms; with class
+    //    weights at 640 KB 4.80 vs 4.45 ms, whose pass-2 weight loads add to
+    //    the L2 traffic; 8192 x 256000 with softcap 30: 2.673 vs 2.907 ms,
+    //    with z-loss and accuracy 1.626 vs 1.930 ms; 16384 x 256000 with
+    //    class weights and softcap 30: 7.087 vs 7.045 ms);
+    //  larger rows, and fp32 rows over 384 KB: one 16-warp CTA per SM, a
+    //    pair per row: the half rows waiting in L2 for their second pass fit
+    //    with room to spare (8192 x 448000: 2.708 ms vs 2.728 for quads;
+    //    fp32 8192 x 128256: 1.408 ms vs 1.455 for quads, fewer elements per
+    //    byte needing fewer warps; three CTAs per SM in pairs at 16384 x
+    //    256000: 117 MB waiting, bimodal 4.3 / 5.4 ms).
     //  In every case the first pass carries no L2 evict-last hint: with the
     //  hint the second pass missed more (8192 x 128256: 9.5% reads over the
     //  algorithmic bytes against 5.3%; 16384 x 256000: 4.93 ms against 4.50),
@@ -121,7 +122,7 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
         const int64_t quad_max = (mode == 2 ? 512 : 640) * 1024;
         tune = row_bytes <= 96 * 1024 ? (kTuneThree | kTuneNoKeep)
              : row_bytes <= 384 * 1024 ? (kTuneThree | kTuneCluster2 | kTuneNoKeep | kTuneReverse)
-             : row_bytes <= quad_max ? (kTuneThree | kTuneCluster4 | kTuneNoKeep | kTuneReverse)
+             : (dtype != CE_DT_F32 && row_bytes <= quad_max) ? (kTuneThree | kTuneCluster4 | kTuneNoKeep | kTuneReverse)
                                      : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
     }
     const int vec = dtype == CE_DT_F32 ? 4 : 8;
