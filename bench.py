@@ -548,7 +548,9 @@ def run_ours(args):
         "e2e": None if args.no_e2e else {"value": R * world / (e2e_ms / 1e3), "unit": "tokens/s",
                 "h2d_bytes_per_step": pristine.numel() * esz + R * 8, "d2h_bytes_per_step": loss.numel() * 4,
                 "ms_per_step": e2e_ms},
-        "gpu_launches": (3 if path == "split" else 2) * args.steps,
+        # per step: the normaliser kernel (two with class weights: eight partial
+        # blocks, then the kernel combining them) and the row kernel(s)
+        "gpu_launches": ((3 if path == "split" else 2) + (1 if cfg.weighted else 0)) * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
         "flce": flce,

@@ -19,6 +19,8 @@ constexpr float kLn2 = 0.6931471805599453f;
 
 // ------------------------------------------------------------------ workspace
 // Control block at the start of the workspace (the rest holds per-row loss).
+constexpr size_t kWsCtlBytes = 256;
+constexpr int kPrepParts = 8;  // blocks of the normaliser pass with class weights
 struct WsCtl {
     unsigned int status;      // CE_FLAG_* bits of the current call
     unsigned int done;        // blocks finished (last-block reduction)
@@ -28,8 +30,12 @@ struct WsCtl {
     float w_y;                // sum of w_{t_i} over valid rows (n_valid when unweighted)
     float w_all;              // sum_c w_c (vocab when unweighted)
     float pad1;
+    // per-block partials of the class-weighted normaliser pass, combined in
+    // block order by its finishing kernel
+    unsigned int prep_bad[kPrepParts];
+    double prep_part[kPrepParts][3];  // valid rows, sum w_{t_i}, sum w_c
 };
-constexpr size_t kWsCtlBytes = 256;
+static_assert(sizeof(WsCtl) <= kWsCtlBytes, "workspace control block too large");
 
 // Workspace layout: [control block 256 B][row loss: n_rows fp32, padded to
 // 256 B][row statistics: n_rows x 4 fp32 (split ce_fwd_bwd only)].

@@ -18,8 +18,25 @@
 namespace ce {
 
 // ------------------------------------------------------------------ prep
-// One small block (it shares an SM with the next kernel's CTAs, which may
-// start before it ends): every thread keeps 8 target loads in flight.
+// The normalisers written to the control block (the status word, counters
+// reset for the call).
+__device__ inline void prep_write_ctl(const PrepArgs &a, double c, double y, double w, unsigned bad) {
+    WsCtl *ctl = a.ctl;
+    unsigned status = bad ? CE_FLAG_TARGET_OUT_OF_RANGE : 0u;
+    if (a.reduction == CE_RED_MEAN && y == 0.0) status |= CE_FLAG_NO_VALID_ROWS;
+    ctl->status = status;
+    ctl->done = 0u;
+    ctl->n_correct = 0u;
+    ctl->n_valid = static_cast<float>(c);
+    ctl->w_y = static_cast<float>(y);
+    ctl->w_all = a.weight ? static_cast<float>(w) : static_cast<float>(a.vocab);
+}
+
+// Small blocks (they share SMs with the next kernel's CTAs, which may start
+// before they end): every thread keeps 8 target loads in flight. Without
+// class weights one block writes the normalisers; with them kPrepParts
+// blocks each write a partial (the weight gathers and the sum over the
+// vocabulary spread over SMs) and ce_prep_finish_kernel combines them.
 __global__ void __launch_bounds__(kPrepThreads) ce_prep_kernel(PrepArgs a) {
     pdl_launch_dependents();
     __shared__ double sh[3][kPrepThreads / 32];
@@ -29,11 +46,13 @@ __global__ void __launch_bounds__(kPrepThreads) ce_prep_kernel(PrepArgs a) {
     __syncthreads();
     double cnt = 0.0, wy = 0.0, wall = 0.0;
     unsigned bad = 0;
-    for (int64_t i0 = threadIdx.x; i0 < a.n_rows; i0 += static_cast<int64_t>(blockDim.x) * U) {
+    const int64_t nt = static_cast<int64_t>(gridDim.x) * blockDim.x;  // threads of the grid
+    const int64_t gt = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t i0 = gt; i0 < a.n_rows; i0 += nt * U) {
         int64_t t[U];
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int64_t i = i0 + static_cast<int64_t>(u) * blockDim.x;
+            const int64_t i = i0 + static_cast<int64_t>(u) * nt;
             t[u] = i < a.n_rows ? load_target(a.target, a.tgt32, i) : a.ignore_index;
         }
         float w[U];
@@ -50,17 +69,21 @@ __global__ void __launch_bounds__(kPrepThreads) ce_prep_kernel(PrepArgs a) {
     if (a.weight && a.need_w_all) {
         const int64_t n4 = (reinterpret_cast<uintptr_t>(a.weight) & 15u) ? 0 : a.vocab / 4;
         const float4 *w4 = reinterpret_cast<const float4 *>(a.weight);
-        for (int64_t c0 = threadIdx.x; c0 < n4; c0 += static_cast<int64_t>(blockDim.x) * U) {
+        for (int64_t c0 = gt; c0 < n4; c0 += nt * U) {
             float4 v[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int64_t c = c0 + static_cast<int64_t>(u) * blockDim.x;
+                const int64_t c = c0 + static_cast<int64_t>(u) * nt;
                 v[u] = c < n4 ? __ldg(w4 + c) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
+            // 32 weights summed in fp32 (a fixed tree), then one fp64 add: the
+            // fp64 rate of this GPU is a small fraction of its fp32 rate
+            float ps = 0.f;
 #pragma unroll
-            for (int u = 0; u < U; ++u) wall += static_cast<double>(v[u].x) + v[u].y + v[u].z + v[u].w;
+            for (int u = 0; u < U; ++u) ps += (v[u].x + v[u].y) + (v[u].z + v[u].w);
+            wall += static_cast<double>(ps);
         }
-        for (int64_t c = 4 * n4 + threadIdx.x; c < a.vocab; c += blockDim.x) wall += __ldg(a.weight + c);
+        for (int64_t c = 4 * n4 + gt; c < a.vocab; c += nt) wall += __ldg(a.weight + c);
     }
     // fixed-order block reduction (deterministic)
 #pragma unroll
@@ -76,15 +99,32 @@ __global__ void __launch_bounds__(kPrepThreads) ce_prep_kernel(PrepArgs a) {
     if (threadIdx.x == 0) {
         double c = 0.0, y = 0.0, w = 0.0;
         for (int k = 0; k < static_cast<int>(blockDim.x >> 5); ++k) { c += sh[0][k]; y += sh[1][k]; w += sh[2][k]; }
-        WsCtl *ctl = a.ctl;
-        unsigned status = sh_bad ? CE_FLAG_TARGET_OUT_OF_RANGE : 0u;
-        if (a.reduction == CE_RED_MEAN && y == 0.0) status |= CE_FLAG_NO_VALID_ROWS;
-        ctl->status = status;
-        ctl->done = 0u;
-        ctl->n_correct = 0u;
-        ctl->n_valid = static_cast<float>(c);
-        ctl->w_y = static_cast<float>(y);
-        ctl->w_all = a.weight ? static_cast<float>(w) : static_cast<float>(a.vocab);
+        if (gridDim.x == 1) {
+            prep_write_ctl(a, c, y, w, sh_bad);
+        } else {
+            a.ctl->prep_part[blockIdx.x][0] = c;
+            a.ctl->prep_part[blockIdx.x][1] = y;
+            a.ctl->prep_part[blockIdx.x][2] = w;
+            a.ctl->prep_bad[blockIdx.x] = sh_bad;
+        }
+    }
+}
+
+// The partials of the kPrepParts normaliser blocks, combined in block order
+// (deterministic) once those blocks have finished.
+__global__ void __launch_bounds__(32) ce_prep_finish_kernel(PrepArgs a) {
+    pdl_launch_dependents();
+    pdl_wait();
+    if (threadIdx.x == 0) {
+        double c = 0.0, y = 0.0, w = 0.0;
+        unsigned bad = 0u;
+        for (int k = 0; k < kPrepParts; ++k) {
+            c += a.ctl->prep_part[k][0];
+            y += a.ctl->prep_part[k][1];
+            w += a.ctl->prep_part[k][2];
+            bad |= a.ctl->prep_bad[k];
+        }
+        prep_write_ctl(a, c, y, w, bad);
     }
 }
 
@@ -640,7 +680,12 @@ static const void *grad_fn_dt(int dtype, int mode) {
 }
 
 cudaError_t launch_prep(const PrepArgs &a, cudaStream_t s) {
-    return launch(reinterpret_cast<const void *>(&ce_prep_kernel), 1, kPrepThreads, a, s, false);
+    if (!a.weight) return launch(reinterpret_cast<const void *>(&ce_prep_kernel), 1, kPrepThreads, a, s, false);
+    // with class weights: kPrepParts blocks, then the finishing kernel in
+    // stream order (the next kernel is its programmatic dependent)
+    cudaError_t e = launch(reinterpret_cast<const void *>(&ce_prep_kernel), kPrepParts, kPrepThreads, a, s, false);
+    if (e != cudaSuccess) return e;
+    return launch(reinterpret_cast<const void *>(&ce_prep_finish_kernel), 1, 32, a, s, false);
 }
 
 cudaError_t launch_stats(const RowArgs &a, int dtype, int mode, int grid, cudaStream_t s) {

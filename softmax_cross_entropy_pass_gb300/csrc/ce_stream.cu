@@ -97,7 +97,9 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     //    (8192 x 128256 bf16: 0.746 ms; 0.749 ms first chunk first; 0.775 ms
     //    unpaired; 0.827 ms paired at two CTAs per SM);
     //  bf16 / f16 rows <= 512 KB (<= 640 KB without class-weighted
-    //    smoothing): three CTAs per SM, a cluster of four per row, each
+    //    smoothing; with it from 288 KB: 8192 x 150000 1.39 vs 1.48 ms for
+    //    pairs, x 180000 1.60 vs 1.81, x 196608 1.64 vs 1.98, kernel alone;
+    //    x 128256 1.25 vs 1.01): three CTAs per SM, a cluster of four per row, each
     //    streaming a quarter, second pass last chunk first: the 114 rows in
     //    flight keep 58 MB waiting in L2 at 512 KB (16384 x 256000 bf16 with
     //    class weights: 4.42 ms vs 4.63 ms for 16-warp pairs; 8192 x 256000:
@@ -120,8 +122,11 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     if (tune == 0) {
         const int64_t row_bytes = a.vocab * (dtype == CE_DT_F32 ? 4 : 2);
         const int64_t quad_max = (mode == 2 ? 512 : 640) * 1024;
+        // class-weighted smoothing leaves the pairs earlier (its pass-2 weight
+        // loads hold each row longer in L2)
+        const int64_t pair_max = (mode == 2 ? 288 : 384) * 1024;
         tune = row_bytes <= 96 * 1024 ? (kTuneThree | kTuneNoKeep)
-             : row_bytes <= 384 * 1024 ? (kTuneThree | kTuneCluster2 | kTuneNoKeep | kTuneReverse)
+             : row_bytes <= pair_max ? (kTuneThree | kTuneCluster2 | kTuneNoKeep | kTuneReverse)
              : (dtype != CE_DT_F32 && row_bytes <= quad_max) ? (kTuneThree | kTuneCluster4 | kTuneNoKeep | kTuneReverse)
                                      : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
     }
