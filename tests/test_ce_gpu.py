@@ -269,16 +269,22 @@ def test_autograd_function(ce, gscale):
 
 
 # ---------------------------------------------------------------- no host synchronisation
-def test_calls_capture_into_a_cuda_graph(ce):
-    """Stream capture fails on any synchronising call or pageable copy."""
-    R, V = 64, 32000
+@pytest.mark.parametrize("V,variants", [(32000, ("fused", "split", "stream")), (160000, ("stream",))],
+                         ids=["64KB-rows", "320KB-rows"])
+def test_calls_capture_into_a_cuda_graph(ce, V, variants):
+    """Stream capture fails on any synchronising call or pageable copy; the
+    replayed graph (class weights: the eight-block normaliser kernels, their
+    combining kernel and the row kernel with its programmatic dependency)
+    gives the eager call's bits. 320 KB rows with class weights run on
+    clusters of four."""
+    R = 64
     x0 = make_logits(R, V, "bf16", 1.0, 21, device="cuda")
     t = make_targets(R, V, 0.1, 21, device="cuda")
     g = torch.tensor([0.37], device="cuda")
     w = make_weights(V, 21, device="cuda")
     outs = {}
     for red in ("mean", "sum", "none"):
-        for variant in ("fused", "split"):
+        for variant in variants:
             x = x0.clone()
             xe = x0.clone()
             ws = ce.workspace(R)
