@@ -90,8 +90,10 @@ static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, i
 cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm, int tune, bool after_prep,
                           cudaStream_t s) {
     // Library choice by row size (GB300 measurements, CUDA events, L2 flushed):
-    //  rows <= 96 KB: three CTAs per SM, one CTA per row (4096 x 32000 bf16:
-    //    0.102 ms vs 0.121 ms with two CTAs per SM);
+    //  rows <= 176 KB: three CTAs per SM, one CTA per row (4096 x 32000 bf16:
+    //    0.102 ms vs 0.121 ms with two CTAs per SM; 8192 x 50257: 0.300 vs
+    //    0.398 ms for pairs, x 64000 0.372 vs 0.441, x 80000 0.484 vs 0.502,
+    //    x 88000 0.545 vs 0.549, x 96000 0.611 vs 0.587);
     //  rows <= 384 KB: three CTAs per SM, a pair of CTAs per row, so the
     //    second pass is served by L2, walking each half row last chunk first
     //    (8192 x 128256 bf16: 0.746 ms; 0.749 ms first chunk first; 0.775 ms
@@ -125,7 +127,7 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
         // class-weighted smoothing leaves the pairs earlier (its pass-2 weight
         // loads hold each row longer in L2)
         const int64_t pair_max = (mode == 2 ? 288 : 384) * 1024;
-        tune = row_bytes <= 96 * 1024 ? (kTuneThree | kTuneNoKeep)
+        tune = row_bytes <= 176 * 1024 ? (kTuneThree | kTuneNoKeep)
              : row_bytes <= pair_max ? (kTuneThree | kTuneCluster2 | kTuneNoKeep | kTuneReverse)
              : (dtype != CE_DT_F32 && row_bytes <= quad_max) ? (kTuneThree | kTuneCluster4 | kTuneNoKeep | kTuneReverse)
                                      : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
