@@ -168,6 +168,14 @@ def barrier(world: int):
         dist.barrier()
 
 
+def workload_text(cfg, n_rows: int, vocab: int, n_ignored: int) -> str:
+    """The workload as both arms name it in config.workload."""
+    return (f"{cfg.name}: BT={n_rows}, V={vocab}, {cfg.dtype} logits N(0,{cfg.sigma:g}^2), "
+            f"{n_ignored} rows ignore_index=-100, label_smoothing={cfg.label_smoothing:g}, "
+            f"{cfg.reduction}, grad_output={cfg.grad_output}, "
+            f"{'class weights, ' if cfg.weighted else ''}gradient in place")
+
+
 # --------------------------------------------------------------------------- CPU oracle arm
 def oracle_sample_run(cfg, n_rows: int, threads: int, block: int = 1024):
     """Oracle forward + backward (loss, statistics, fp64 gradient) on n_rows
@@ -198,8 +206,9 @@ def run_reference(args):
     if rank != 0:
         return 0
     import oracle
-    from workloads import CONFIGS
+    from workloads import CONFIGS, IGNORE_INDEX, make_targets
     cfg = CONFIGS[WORKLOAD]
+    n_ignored = int((make_targets(cfg.n_rows, cfg.vocab, cfg.ignore_frac, cfg.seed) == IGNORE_INDEX).sum())
     oracle.build()
     threads = oracle.default_threads()
     rows = args.ref_rows
@@ -213,10 +222,11 @@ def run_reference(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": per_step * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: BT=8192, V=128256, bf16 logits N(0,1), 5% ignore_index=-100, "
-                               "label_smoothing=0.1, mean, grad_output=1",
+        "config": {"workload": workload_text(cfg, cfg.n_rows, cfg.vocab, n_ignored),
+                   "global_batch": cfg.n_rows, "seq_len": None, "parallelism": "replicas x1",
+                   "logits_dtype": cfg.dtype,
                    "sample": f"{rows} rows of the batch per step (in 1024-row blocks, normalised with all "
-                             f"8192 rows' targets)"},
+                             f"{cfg.n_rows} rows' targets)"},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows} rows x 128256 per step, forward + fp64 gradient"},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -530,10 +540,7 @@ def run_ours(args):
         # the arithmetic type: statistics and gradient are formed in fp32 (the
         # logits' storage type is config.logits_dtype)
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: BT={R}, V={V}, {cfg.dtype} logits N(0,{cfg.sigma:g}^2), "
-                               f"{R - n_valid} rows ignore_index=-100, label_smoothing={cfg.label_smoothing:g}, "
-                               f"{cfg.reduction}, grad_output={cfg.grad_output}, "
-                               f"{'class weights, ' if cfg.weighted else ''}gradient in place",
+        "config": {"workload": workload_text(cfg, R, V, R - n_valid),
                    "global_batch": R * world, "seq_len": None, "parallelism": f"replicas x{world}",
                    "variant": args.variant, "path": path, "tune": args.tune, "fused_plan": plan,
                    "options": {k: (v if k != "accuracy" else True) for k, v in options.items()} or None,
