@@ -215,11 +215,16 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
  *    exits. Nothing is allocated by this call.
  *  - n_rows above CE_NOALLOC_MAX_ROWS returns CE_ERR_WORKSPACE with nothing
  *    enqueued.
+ *  - p->variant with CE_VARIANT_PREPARED returns CE_ERR_INVALID_ARG: the
+ *    normalisers must be computed by this call, since no caller can run
+ *    ce_prepare on the library's scratch.
  *  - The first call on a device looks up the array's device address (a
- *    runtime query, once per device, with that device current); make that
- *    first call before any stream capture.
+ *    runtime query with that device current), and so does the first call
+ *    after the device's context was replaced (cudaDeviceReset); make those
+ *    calls before any stream capture.
  *  - Every call on a device shares the one array, and the array keeps the
- *    last call's contents (each call resets the counters it relies on).
+ *    last call's contents (each call runs its own normaliser kernel first,
+ *    which resets every counter and sum that the later kernels read).
  *    Calls whose GPU work overlaps (different streams, or different host
  *    threads without ordering) race on it: serialise them, e.g. on one
  *    stream. Status bits are read with ce_get_status only through a

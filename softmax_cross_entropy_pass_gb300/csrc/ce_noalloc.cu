@@ -8,6 +8,8 @@
 // entry point takes its scratch from a fixed array in the library's own
 // device memory instead (the array exists on every GPU that loads the
 // library, until the process exits), and allocates nothing.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -25,23 +27,60 @@ constexpr size_t kNoallocBytes =
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocBytes];
 
+// The array's device address, looked up once per CUDA context. A context's
+// id is never reused within a process, so after cudaDeviceReset (a new
+// primary context, the module loaded again at a possibly different address)
+// the next call looks the address up again instead of using the old one.
 constexpr int kMaxDevices = 64;
+struct ScratchEntry {
+    unsigned long long ctx_id;
+    void *ptr;
+};
 std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices] = {};
+ScratchEntry g_scratch[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device. In host code
-// the array's name is only a host-side stand-in, so the address is asked
-// from the runtime, once per device, with that device current.
+PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
+PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
+
+bool driver_entry(const char *name, int version, void **fn) {
+    cudaDriverEntryPointQueryResult q;
+    return cudaGetDriverEntryPointByVersion(name, fn, version, cudaEnableDefault, &q) == cudaSuccess &&
+           q == cudaDriverEntryPointSuccess && *fn != nullptr;
+}
+
+// id of the context current on this thread, or 0 if there is none yet
+unsigned long long current_ctx_id() {
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
+    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
+
+// Device address of the scratch array in the current device's context. In
+// host code the array's name is only a host-side stand-in, so the address is
+// asked from the runtime (cudaGetSymbolAddress), with that device current.
 ce_status scratch_for_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
+    if (!g_ctx_get_current) {
+        void *a = nullptr, *b = nullptr;
+        if (!driver_entry("cuCtxGetCurrent", 4000, &a) || !driver_entry("cuCtxGetId", 12000, &b)) return CE_ERR_CUDA;
+        g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
+        g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
+    }
+    unsigned long long id = current_ctx_id();
+    if (id == 0 || g_scratch[dev].ctx_id != id || g_scratch[dev].ptr == nullptr) {
+        // also makes the device's primary context current on this thread
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return CE_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        id = current_ctx_id();
+        if (id == 0) return CE_ERR_CUDA;
+        g_scratch[dev].ctx_id = id;
+        g_scratch[dev].ptr = p;
     }
-    *out = g_scratch_ptr[dev];
+    *out = g_scratch[dev].ptr;
     return CE_OK;
 }
 
@@ -52,6 +91,9 @@ extern "C" {
 ce_status ce_fwd_bwd_noalloc(const ce_params *p, void *logits_inout, const void *target, float *loss,
                              const float *grad_output, void *stream) {
     if (!p) return CE_ERR_INVALID_ARG;
+    // The batch normalisers must come from this call's own kernel: a caller
+    // has no way to run ce_prepare on the library's scratch.
+    if (p->variant & CE_VARIANT_PREPARED) return CE_ERR_INVALID_ARG;
     if (p->n_rows > CE_NOALLOC_MAX_ROWS) return CE_ERR_WORKSPACE;  // more rows than the fixed scratch holds
     if (p->n_rows < 0) return CE_ERR_INVALID_ARG;
     size_t need = 0;
