@@ -43,23 +43,28 @@ def magnitude_T(x: torch.Tensor, target: torch.Tensor, stats64: torch.Tensor, we
     """|s_i| * T_ic for every element, in fp64 (rows not valid: 0). With a
     softcap the terms are those of the capped logits times dz/dx, and times
     max(1, |z| / 8) for the fp32 rounding of z itself; z-loss adds its
-    |2 lambda LSE p| term."""
+    |2 lambda LSE p| term. Runs on the device of ``x`` (every other tensor
+    is moved there)."""
+    dev = x.device
     xd = x.double()
     deriv = None
     if softcap > 0:
         xd = softcap * torch.tanh(xd / softcap)
         deriv = 1.0 - (xd / softcap) ** 2
     R, V = xd.shape
-    m, s, xy = stats64[:, 0:1], stats64[:, 1:2], stats64[:, 2:3]
+    st = stats64.to(dev, torch.float64)
+    m, s, xy = st[:, 0:1], st[:, 1:2], st[:, 2:3]
     lse = m + torch.log(s + torch.exp(xy - m))
     p = torch.exp(xd - lse)
+    target = target.to(dev)
     valid = (target >= 0) & (target < V)
     tt = target.clamp(0, V - 1)
-    w = weight.double() if weight is not None else torch.ones(V, dtype=torch.float64)
+    w = weight.to(dev, torch.float64) if weight is not None else torch.ones(V, dtype=torch.float64, device=dev)
     wy = w[tt][:, None]
-    onehot = torch.zeros(R, V, dtype=torch.float64)
-    onehot[torch.arange(R), tt] = 1.0
-    T = (1 - eps) * wy * (p + onehot) + (eps / V) * (p * w_all + w[None, :])
+    # (1-eps) w_y p + (eps/V)(p W_all + w_c), then (1-eps) w_y at the target column
+    T = (1 - eps) * wy * p + (eps / V) * (p * w_all + w[None, :])
+    rows = torch.arange(R, device=dev)
+    T[rows, tt] += (1 - eps) * wy[:, 0]
     if z_loss > 0:
         T = T + (2 * z_loss * lse).abs() * p
     if deriv is not None:
@@ -67,20 +72,31 @@ def magnitude_T(x: torch.Tensor, target: torch.Tensor, stats64: torch.Tensor, we
         # up to 2^-21.7 |z| absolute, which moves p by that relative amount: the
         # 2^-18 floor covers it up to |z| = 16, so scale the terms by |z| / 8 beyond
         T = T * deriv * torch.clamp(xd.abs() / 8.0, min=1.0)
-    T = T * scale.abs().reshape(-1, 1).double()
+    T = T * scale.to(dev).abs().reshape(-1, 1).double()
     T[~valid] = 0.0
     return T
 
 
-def grad_mismatch(got: torch.Tensor, want64: torch.Tensor, T: torch.Tensor):
-    """(n_bad, n_floor, max_err_over_ulp) for a gradient block on the CPU."""
+def grad_mismatch_detail(got: torch.Tensor, want64: torch.Tensor, T: torch.Tensor) -> dict:
+    """Per-element acceptance of a gradient block, computed on the device of
+    ``got``: n_bad elements outside the tolerance; n_floor elements that pass
+    only through the 2^-18 T floor, not within one ulp of the rounded oracle
+    value; worst_ulp the largest error in ulps of the rounded oracle value
+    (large only where that value is near 0); worst_tol the largest error as a
+    share of the element's tolerance (<= 1 when every element passes)."""
     dtype = got.dtype
+    want64 = want64.to(got.device)
+    T = T.to(got.device)
     g = got.double()
+    if g.numel() == 0:
+        return {"n_bad": 0, "n_floor": 0, "worst_ulp": 0.0, "worst_tol": 0.0}
     if dtype == torch.float32:
-        tol = FLOOR * T + 2.0 * ulp_of(want64.to(torch.float32), torch.float32)
+        u = ulp_of(want64.to(torch.float32), torch.float32)
+        tol = FLOOR * T + 2.0 * u
         err = (g - want64).abs()
-        bad = err > tol
-        return int(bad.sum()), 0, float((err / tol.clamp_min(1e-300)).max()) if g.numel() else 0.0
+        return {"n_bad": int((err > tol).sum()), "n_floor": 0,
+                "worst_ulp": float((err / u.clamp_min(1e-300)).max()),
+                "worst_tol": float((err / tol.clamp_min(1e-300)).max())}
     ref = rne(want64, dtype)
     u = ulp_of(ref, dtype)
     err = (g - ref.double()).abs()
@@ -88,8 +104,15 @@ def grad_mismatch(got: torch.Tensor, want64: torch.Tensor, T: torch.Tensor):
     ok_ulp = err <= u
     ok_floor = err <= floor
     bad = ~(ok_ulp | ok_floor)
-    n_floor = int((~ok_ulp & ok_floor).sum())
-    return int(bad.sum()), n_floor, float((err / u).max()) if g.numel() else 0.0
+    return {"n_bad": int(bad.sum()), "n_floor": int((~ok_ulp & ok_floor).sum()),
+            "worst_ulp": float((err / u).max()),
+            "worst_tol": float((err / torch.maximum(u, floor).clamp_min(1e-300)).max())}
+
+
+def grad_mismatch(got: torch.Tensor, want64: torch.Tensor, T: torch.Tensor):
+    """(n_bad, n_floor, worst error in ulps) of grad_mismatch_detail."""
+    d = grad_mismatch_detail(got, want64, T)
+    return d["n_bad"], d["n_floor"], d["worst_ulp"]
 
 
 def check_loss_rows(got: torch.Tensor, want64: torch.Tensor):

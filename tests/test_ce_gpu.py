@@ -3,7 +3,7 @@
 Small cases cover every dtype, reduction, smoothing / weight combination,
 ragged vocabularies, padded and misaligned row strides and every fused
 cluster size; the full-size workloads are checked on every row's loss and
-on sampled rows' gradients, plus properties that hold at any size."""
+every element of every row's gradient."""
 import time
 import zlib
 
@@ -11,8 +11,8 @@ import pytest
 import torch
 
 import oracle
-from ce_check import (DXY_RTOL, check_loss_reduced, check_loss_rows, grad_mismatch, magnitude_T,
-                      row_scale)
+from ce_check import (DXY_RTOL, check_loss_reduced, check_loss_rows, grad_mismatch, grad_mismatch_detail,
+                      magnitude_T, row_scale)
 from workloads import (CONFIGS, IGNORE_INDEX, make_ce_inputs, make_grad_output, make_logits,
                        make_targets, make_weights)
 
@@ -346,69 +346,110 @@ def test_library_allocates_no_device_memory(ce):
 
 
 # ---------------------------------------------------------------- full-size workloads
-def _full_size_check(ce, cfg, variant, sample_rows=48, check_dxy_thirds=False):
+# Share of gradient elements allowed to pass through the 2^-18 T floor
+# instead of one ulp. The floor is for elements whose exact value is near 0
+# (p_ic close to eps/V, or a softcap / weighted cancellation). With N(0,1)
+# bf16 logits and eps/V smoothing, the fp32 p of an element carries about
+# 2^-20 relative error, so the floor is needed when |G| < 2^-12 p, i.e. for
+# logits within ~2^-12 of the row's crossing point x0 = log(eps/V) + LSE: a
+# density of ~0.08 per unit times 2 * 2^-12, about 4e-5 of the elements at
+# most (measured on the full workloads: 7e-6 headline, 1.3e-5 large
+# vocabulary, 0 on the confident rows, which have no smoothing).
+FLOOR_SHARE_MAX = 5e-5
+
+
+def _record(entry: dict):
+    """Appends a JSON line to the file named by CE_PARITY_RECORD (if set)."""
+    import json
+    import os
+    path = os.environ.get("CE_PARITY_RECORD")
+    if path:
+        with open(path, "a") as f:
+            f.write(json.dumps(entry) + "\n")
+
+
+def _full_size_check(ce, cfg, variant, block_elems=1 << 27):
+    """One call of the hot path on the whole workload, then every row of it
+    against the oracle: the reduced (or per-row) loss, and the gradient
+    element by element. The oracle runs on the CPU over blocks of rows
+    (about 128 M elements each, so host memory stays bounded); each block's
+    fp64 gradient is compared with the library's output on the GPU."""
     dev = torch.device("cuda")
     inp = make_ce_inputs(cfg, device=dev)
     x, t, w, g = inp["logits"], inp["target"], inp["weight"], inp["grad_output"]
     R, V = x.shape
+    x0 = x.clone()                       # the logits, kept on the device for the tolerance terms
     x_host = x.cpu()
     w_host = None if w is None else w.cpu()
     t_host = t.cpu()
+    g_host = g.cpu()
     n, wy, wall, _ = oracle.normalizers(t_host, V, IGNORE_INDEX, w_host)
-    full = oracle.rows(x_host, t_host, weight=w_host, label_smoothing=cfg.label_smoothing,
-                       reduction=cfg.reduction, norm_wy=wy, w_all=wall, want_grad=False)
     variant, tune = (variant, 0) if variant != "stream-pair" else ("stream", 8)
     loss = ce.ce_fwd_bwd(x, t, weight=w, label_smoothing=cfg.label_smoothing, reduction=cfg.reduction,
                          grad_output=g, variant=variant, tune=tune)
     torch.cuda.synchronize()
+    block = max(1, block_elems // V)
+    row_loss = torch.empty(R, dtype=torch.float64)
+    dxy_want = torch.zeros(R, dtype=torch.float64)
+    n_bad = n_floor = 0
+    worst = worst_tol = 0.0
+    for r0 in range(0, R, block):
+        r1 = min(R, r0 + block)
+        g_rows = g_host[r0:r1] if cfg.reduction == "none" else g_host
+        ref = oracle.rows(x_host[r0:r1], t_host[r0:r1], weight=w_host, label_smoothing=cfg.label_smoothing,
+                          reduction=cfg.reduction, grad_output=g_rows, norm_wy=wy, w_all=wall)
+        row_loss[r0:r1] = ref["row_loss"]
+        tb = t_host[r0:r1]
+        ok = (tb >= 0) & (tb < V)
+        rr = ok.nonzero().flatten()
+        dxy_want[r0 + rr] = ref["grad"][rr, tb[rr]]
+        scale = row_scale(cfg.reduction, g_rows, r1 - r0, wy)
+        want = ref["grad"].to(dev)
+        T = magnitude_T(x0[r0:r1], tb, ref["stats"], w_host, cfg.label_smoothing, wall, scale)
+        d = grad_mismatch_detail(x[r0:r1], want, T)
+        n_bad, n_floor = n_bad + d["n_bad"], n_floor + d["n_floor"]
+        worst, worst_tol = max(worst, d["worst_ulp"]), max(worst_tol, d["worst_tol"])
+        del want, T, ref
     if cfg.reduction == "none":
-        check_loss_rows(loss.cpu(), full["row_loss"])
+        check_loss_rows(loss.cpu(), row_loss)
     else:
-        want = oracle.reduce(full["row_loss"], cfg.reduction, wy)
-        check_loss_reduced(float(loss.item()), want)
-    # gradient: sampled rows, element by element
-    gen = torch.Generator().manual_seed(1234)
-    rows = torch.unique(torch.cat([torch.tensor([0, R - 1]), torch.randint(0, R, (sample_rows,), generator=gen)]))
-    if check_dxy_thirds:
-        rows = torch.arange(R)
-    g_host = g.cpu()
-    g_rows = g_host[rows] if cfg.reduction == "none" else g_host
-    ref = oracle.rows(x_host[rows], t_host[rows], weight=w_host, label_smoothing=cfg.label_smoothing,
-                      reduction=cfg.reduction, grad_output=g_rows, norm_wy=wy, w_all=wall)
-    got = x[rows.to(dev)].cpu()
-    scale = row_scale(cfg.reduction, g_rows, len(rows), wy)
-    T = magnitude_T(x_host[rows], t_host[rows], ref["stats"], w_host, cfg.label_smoothing, wall, scale)
-    bad, n_floor, worst = grad_mismatch(got, ref["grad"], T)
-    assert bad == 0, f"{bad} gradient elements outside tolerance (worst {worst:.2f} ulp)"
-    # properties over every row: ignored rows are zero, rows sum to ~0
+        check_loss_reduced(float(loss.item()), oracle.reduce(row_loss, cfg.reduction, wy))
+    share = n_floor / float(R * V)
+    _record({"test": "full_size", "workload": cfg.name, "variant": variant, "tune": tune, "rows": R, "vocab": V,
+             "elements": R * V, "bad": n_bad, "n_floor": n_floor, "floor_share": share,
+             "worst_err_over_ulp": worst, "worst_err_over_tolerance": worst_tol})
+    assert n_bad == 0, f"{n_bad} gradient elements outside tolerance (worst {worst_tol:.2f} of the tolerance)"
+    assert share <= FLOOR_SHARE_MAX, f"{n_floor} elements ({share:.2e}) needed the cancellation floor"
+    # ignored rows are exactly zero
     ign = (t_host < 0) | (t_host >= V)
     if ign.any():
         assert torch.count_nonzero(x[ign.to(dev)]) == 0
-    rs = x.float().sum(dim=1).abs()
-    mag = x.float().abs().sum(dim=1)
-    assert (rs <= mag * 2.0 ** -7 + 1e-30).all()
-    out = {"rows": rows, "got": got, "ref": ref, "t": t_host[rows], "T": T, "n_floor": n_floor}
-    return out
+    valid = ~ign
+    got_dxy = torch.zeros(R, dtype=torch.float64)
+    vr = valid.nonzero().flatten()
+    got_dxy[vr] = x[vr.to(dev), t[vr.to(dev)]].double().cpu()
+    return {"valid": valid, "dxy_want": dxy_want, "dxy_got": got_dxy, "n_floor": n_floor, "share": share}
 
 
 @pytest.mark.parametrize("variant", ["fused", "split", "rowpass", "stream"])
 def test_confident_full_size_dxy(ce, variant):
-    """4096 x 32000 bf16, softmax(x_y) near 0.9 / 0.99 / 0.999: dx_y within
-    0.4% of the oracle in every third (the #1329 accuracy table's workload)."""
+    """4096 x 32000 bf16, softmax(x_y) near 0.9 / 0.99 / 0.999: every element
+    of every row against the oracle, and dx_y within 0.4% of the oracle in
+    every third (the #1329 accuracy table's workload)."""
     cfg = CONFIGS["confident"]
-    res = _full_size_check(ce, cfg, variant, check_dxy_thirds=True)
-    t = res["t"]
-    valid = t >= 0
-    rows = valid.nonzero().flatten()
-    want = res["ref"]["grad"][rows, t[rows]]
-    got = res["got"][rows, t[rows]].double()
+    res = _full_size_check(ce, cfg, variant)
+    rows = res["valid"].nonzero().flatten()
+    want, got = res["dxy_want"][rows], res["dxy_got"][rows]
     rel = (got - want).abs() / want.abs()
     R = cfg.n_rows
     third = (R + 2) // 3
-    idx = res["rows"][rows]
+    worst = []
     for k in range(3):
-        sel = (idx >= k * third) & (idx < (k + 1) * third)
-        assert rel[sel].max() <= DXY_RTOL, f"third {k}: dx_y max rel err {float(rel[sel].max()):.4%}"
+        sel = (rows >= k * third) & (rows < (k + 1) * third)
+        worst.append(float(rel[sel].max()))
+    _record({"test": "confident_dxy", "variant": variant, "dxy_max_rel_err_per_third": worst})
+    for k in range(3):
+        assert worst[k] <= DXY_RTOL, f"third {k}: dx_y max rel err {worst[k]:.4%}"
 
 
 @pytest.mark.parametrize("variant", ["fused", "split", "rowpass", "stream", "stream-pair"])
@@ -418,7 +459,7 @@ def test_headline_full_size(ce, variant):
 
 @pytest.mark.parametrize("name", ["large_vocab", "large_vocab_none"])
 def test_large_vocab_full_size(ce, name):
-    _full_size_check(ce, CONFIGS[name], "auto", sample_rows=24)
+    _full_size_check(ce, CONFIGS[name], "auto")
 
 
 def test_tiny_config(ce):
