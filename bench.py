@@ -378,6 +378,243 @@ def measure_gemm(ce, device, spec: str, steps: int, warmup: int):
             "peak_tflops": peak, "frac": tflops / peak}
 
 
+# --------------------------------------------------------------------------- workload timing
+class Workload:
+    """One CE workload resident on the device: the pristine logits, a working
+    copy the call overwrites with the gradient, targets, weights,
+    grad_output, workspace and loss, and the keyword arguments of the call."""
+
+    def __init__(self, ce, cfg, device, variant="auto", tune=0, cluster=0, options=None, stream=None):
+        import torch
+        from workloads import make_ce_inputs
+        inp = make_ce_inputs(cfg, device=device)
+        self.cfg = cfg
+        self.pristine, self.target, self.g = inp["logits"], inp["target"], inp["grad_output"]
+        self.weight = inp["weight"]
+        self.work = torch.empty_like(self.pristine)
+        self.R, self.V = cfg.n_rows, cfg.vocab
+        self.ws = ce.workspace(self.R, device)
+        self.loss = torch.empty(self.R if cfg.reduction == "none" else 1, dtype=torch.float32, device=device)
+        self.stream = stream if stream is not None else torch.cuda.current_stream(device)
+        self.options = dict(options or {})
+        self.kw = dict(label_smoothing=cfg.label_smoothing, reduction=cfg.reduction, grad_output=self.g,
+                       loss=self.loss, ws=self.ws, stream=self.stream, variant=variant, cluster=cluster,
+                       weight=self.weight, tune=tune, **self.options)
+        self.n_valid = int((self.target >= 0).sum().item())
+        self.esz = self.pristine.element_size()
+        self.path = variant if variant != "auto" else ce.auto_variant(self.pristine, self.target,
+                                                                      weight=self.weight, **self.options)
+
+    def algo_bytes(self) -> int:
+        """Algorithmic bytes of one forward + backward: every valid row read
+        once (twice on the split path, whose statistics pass reads every row),
+        every row written once (ignored rows are only zeroed), the targets
+        twice (normaliser kernel and row kernel); with reduction none the
+        per-row grad_output and losses; with class weights the weights twice
+        (normaliser sum and gradient terms)."""
+        cfg, R, V = self.cfg, self.R, self.V
+        reads = self.n_valid + (R if self.path == "split" else 0)
+        b = (reads + R) * V * self.esz + 2 * R * self.target.element_size()
+        if cfg.reduction == "none":
+            b += 2 * R * 4
+        if self.weight is not None:
+            b += 2 * V * 4
+        return b
+
+    def launches_per_step(self) -> int:
+        # the normaliser kernel (plus its combining kernel with class weights)
+        # and the row kernel(s)
+        return (3 if self.path == "split" else 2) + (1 if self.weight is not None else 0)
+
+    def step(self, ce):
+        return ce.ce_fwd_bwd(self.work, self.target, **self.kw)
+
+    def free(self):
+        for k in ("pristine", "work", "target", "g", "weight", "ws", "loss"):
+            setattr(self, k, None)
+
+
+def time_workload(ce, W: Workload, steps: int, warmup: int, flush, clock_gpu=None) -> dict:
+    """CUDA-event timing of W's step (normalisers + row kernel) and of the
+    row kernel alone (normalisers prepared before its first event), each
+    step with the logits restored from the pristine copy and a buffer larger
+    than the L2 written beforehand, outside the timed region."""
+    import torch
+    for _ in range(warmup):
+        W.work.copy_(W.pristine)
+        W.step(ce)
+    torch.cuda.synchronize()
+    sampler = ClockSampler(clock_gpu) if clock_gpu is not None else None
+    if sampler:
+        sampler.start()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for k in range(steps):
+        W.work.copy_(W.pristine)
+        flush.zero_()
+        ev[k][0].record(W.stream)
+        W.step(ce)
+        ev[k][1].record(W.stream)
+    torch.cuda.synchronize()
+    kev = []
+    for _ in range(steps):
+        W.work.copy_(W.pristine)
+        ce.ce_prepare(W.work, W.target, label_smoothing=W.cfg.label_smoothing, reduction=W.cfg.reduction,
+                      ws=W.ws, stream=W.stream, weight=W.weight)
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(W.stream)
+        ce.ce_fwd_bwd(W.work, W.target, prepared=True, **W.kw)
+        e1.record(W.stream)
+        kev.append((e0, e1))
+    torch.cuda.synchronize()
+    clocks = sampler.stop() if sampler else None
+    return {"step_ms": [a.elapsed_time(b) for a, b in ev], "kernel_ms": [a.elapsed_time(b) for a, b in kev],
+            "clocks": clocks}
+
+
+def workload_entry(W: Workload, t: dict, peak: float) -> dict:
+    """The bench-line record of one timed workload."""
+    step_ms = statistics.mean(t["step_ms"])
+    kern_ms = statistics.mean(t["kernel_ms"])
+    ab = W.algo_bytes()
+    achieved = ab / (kern_ms / 1e3) / 1e9
+    return {"workload": workload_text(W.cfg, W.R, W.V, W.R - W.n_valid), "path": W.path,
+            "ms_per_step": step_ms, "tokens_per_s": W.R / (step_ms / 1e3),
+            "step_ms_min_median_max": [min(t["step_ms"]), statistics.median(t["step_ms"]), max(t["step_ms"])],
+            "kernel_ms": kern_ms, "algorithmic_bytes": ab, "achieved_gbs": achieved, "peak_gbs": peak,
+            "frac": achieved / peak, "gpu_launches_per_step": W.launches_per_step(), "clocks": t["clocks"]}
+
+
+def measure_tiny(ce, device, flush, steps: int = 200) -> dict:
+    """The 64 x 1024 fp32 workload: device microseconds per step (CUDA
+    events around each call, inputs restored outside), and the host cost of
+    one call from API entry to return, taken while a sleep kernel keeps the
+    GPU busy so no call waits for the device: through the Python binding
+    (argument marshalling included) and through the C ABI alone (ctypes
+    with a prepared parameter block)."""
+    import ctypes
+
+    import torch
+    from workloads import CONFIGS
+    cfg = CONFIGS["tiny"]
+    W = Workload(ce, cfg, device)
+    t = time_workload(ce, W, steps, 20, flush)
+    dev_us = [1e3 * v for v in t["step_ms"]]
+    # host cost per call
+    p = ce.make_params(W.work, W.target, label_smoothing=cfg.label_smoothing, reduction=cfg.reduction)
+    st = ce._stream(W.stream)
+    args = (ctypes.byref(p), ctypes.c_void_p(W.work.data_ptr()), ctypes.c_void_p(W.target.data_ptr()),
+            ctypes.c_void_p(W.loss.data_ptr()), None, ctypes.c_void_p(W.ws.data_ptr()),
+            W.ws.numel(), st)
+    n = 100
+    torch.cuda.synchronize()
+    torch.cuda._sleep(100_000_000)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        rc = ce._lib.ce_fwd_bwd(*args)
+    c_us = (time.perf_counter() - t0) / n * 1e6
+    if rc != 0:
+        raise RuntimeError(f"ce_fwd_bwd returned {rc}")
+    torch.cuda.synchronize()
+    torch.cuda._sleep(100_000_000)
+    kw = dict(W.kw)
+    t0 = time.perf_counter()
+    for _ in range(n):
+        ce.ce_fwd_bwd(W.work, W.target, **kw)
+    py_us = (time.perf_counter() - t0) / n * 1e6
+    torch.cuda.synchronize()
+    W.free()
+    return {"workload": workload_text(cfg, cfg.n_rows, cfg.vocab, 0), "path": "stream",
+            "device_us_per_step_min_median_max": [min(dev_us), statistics.median(dev_us), max(dev_us)],
+            "kernel_us_median": 1e3 * statistics.median(t["kernel_ms"]),
+            "host_us_per_call_c_abi": c_us, "host_us_per_call_python": py_us,
+            "gpu_launches_per_step": 2, "bound": "launch (report microseconds)"}
+
+
+def pages_dxy_table() -> dict:
+    """The pages' dx_y error table (H100, bf16, V = 32000), from its cited
+    golden file, as context beside the measured errors."""
+    with open(os.path.join(ROOT, "tests", "golden", "dxy_error_table_v32000_bf16.json")) as f:
+        d = json.load(f)
+    cols = d["columns"]
+    return {"source": d["source"],
+            "softmax_xy": [r[cols.index("softmax_xy")] for r in d["rows"]],
+            "before_1268_pct": [r[cols.index("before_1268_pct")] for r in d["rows"]],
+            "at_1268_pct": [r[cols.index("at_1268_pct")] for r in d["rows"]],
+            "torch_pct": [r[cols.index("torch_pct")] for r in d["rows"]]}
+
+
+def confident_dxy_report(ce, device, threads: int) -> dict:
+    """dx_y accuracy on the confident workload (4096 x 32000 bf16, target
+    softmax near 0.9 / 0.99 / 0.999 in thirds, 10% ignored): the max
+    relative error of dx_y per third against the fp64 oracle, for this
+    library and for torch.nn.functional.cross_entropy's bf16 autograd on the
+    same GPU (a comparison column, like the pages' "torch" column), with the
+    realised softmax(x_y) range per third. Part of the CPU-baseline leg: the
+    oracle run here is also timed as that config's baseline."""
+    import torch
+    import torch.nn.functional as F
+
+    import oracle
+    from workloads import CONFIGS, IGNORE_INDEX, make_ce_inputs
+    cfg = CONFIGS["confident"]
+    inp = make_ce_inputs(cfg, device=device)
+    x, t = inp["logits"], inp["target"]
+    R, V = x.shape
+    x_host, t_host = x.cpu(), t.cpu()
+    n, wy, wall, _ = oracle.normalizers(t_host, V, IGNORE_INDEX, None)
+    t0 = time.perf_counter()
+    ref = oracle.rows(x_host, t_host, reduction="mean", norm_wy=wy, w_all=wall, want_grad=True, n_threads=threads)
+    secs = time.perf_counter() - t0
+    valid = (t_host >= 0) & (t_host < V)
+    rows = valid.nonzero().flatten()
+    want = ref["grad"][rows, t_host[rows]]
+    st = ref["stats"][rows]
+    e = torch.exp(st[:, 2] - st[:, 0])
+    p_y = e / (st[:, 1] + e)
+    del ref
+    xg = x.clone()
+    ce.ce_fwd_bwd(xg, t)
+    xt = x.clone().requires_grad_(True)
+    F.cross_entropy(xt, t, ignore_index=IGNORE_INDEX, reduction="mean").backward()
+    torch.cuda.synchronize()
+    ours = xg[rows.to(device), t[rows.to(device)]].double().cpu()
+    theirs = xt.grad[rows.to(device), t[rows.to(device)]].double().cpu()
+    third = (R + 2) // 3
+    out = {"ours_pct": [], "torch_gpu_pct": [], "p_realised_min_max": [], "rows_per_third": []}
+    for k in range(3):
+        sel = (rows >= k * third) & (rows < (k + 1) * third)
+        out["ours_pct"].append(100 * float(((ours[sel] - want[sel]).abs() / want[sel].abs()).max()))
+        out["torch_gpu_pct"].append(100 * float(((theirs[sel] - want[sel]).abs() / want[sel].abs()).max()))
+        out["p_realised_min_max"].append([float(p_y[sel].min()), float(p_y[sel].max())])
+        out["rows_per_third"].append(int(sel.sum()))
+    out["nominal_p"] = [0.9, 0.99, 0.999]
+    out["pages_h100"] = pages_dxy_table()
+    del xg, xt
+    return {"dxy": out, "oracle_secs": secs, "oracle_rows": R}
+
+
+def oracle_config_baseline(cfg, n_rows: int, threads: int) -> dict:
+    """The oracle on n_rows rows of a workload (its distribution, weights,
+    smoothing, reduction and grad_output), timed on the host cores."""
+    import oracle
+    from workloads import IGNORE_INDEX, make_grad_output, make_logits, make_targets, make_weights
+    r = min(n_rows, cfg.n_rows)
+    x = make_logits(r, cfg.vocab, cfg.dtype, cfg.sigma, cfg.seed + 1000)
+    t_all = make_targets(cfg.n_rows, cfg.vocab, cfg.ignore_frac, cfg.seed)
+    w = make_weights(cfg.vocab, cfg.seed) if cfg.weighted else None
+    g = make_grad_output(cfg)
+    n, wy, wall, _ = oracle.normalizers(t_all, cfg.vocab, IGNORE_INDEX, w)
+    t0 = time.perf_counter()
+    oracle.rows(x, t_all[:r], weight=w, label_smoothing=cfg.label_smoothing, reduction=cfg.reduction,
+                grad_output=g[:r] if cfg.reduction == "none" else g, norm_wy=wy, w_all=wall, want_grad=True,
+                n_threads=threads)
+    secs = time.perf_counter() - t0
+    return {"value": r / secs, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+            "sample": f"{r} rows x {cfg.vocab} of the workload, forward + fp64 gradient, {secs:.2f} s"}
+
+
 # --------------------------------------------------------------------------- GPU arm
 def run_ours(args):
     import torch
@@ -404,23 +641,12 @@ def run_ours(args):
         dist.init_process_group("nccl", device_id=device)
 
     import softmax_cross_entropy_pass_gb300 as ce
-    from workloads import CONFIGS, make_ce_inputs
+    from workloads import CONFIGS
     cfg = CONFIGS[args.workload]
     if args.rows or args.vocab or args.dtype:
         import dataclasses
         cfg = dataclasses.replace(cfg, n_rows=args.rows or cfg.n_rows, vocab=args.vocab or cfg.vocab,
                                   dtype=args.dtype or cfg.dtype)
-    R, V = cfg.n_rows, cfg.vocab
-    inp = make_ce_inputs(cfg, device=device)
-    pristine, target, g = inp["logits"], inp["target"], inp["grad_output"]
-    work = torch.empty_like(pristine)
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
-    ws = ce.workspace(R, device)
-    loss = torch.empty(R if cfg.reduction == "none" else 1, dtype=torch.float32, device=device)
-    stream = torch.cuda.current_stream(device)
-    weight = inp["weight"]
-    kw = dict(label_smoothing=cfg.label_smoothing, reduction=cfg.reduction, grad_output=g, loss=loss,
-              ws=ws, stream=stream, variant=args.variant, cluster=args.cluster, weight=weight, tune=args.tune)
     options = {}
     if args.softcap > 0:
         options["softcap"] = args.softcap
@@ -428,72 +654,29 @@ def run_ours(args):
         options["z_loss"] = args.z_loss
     if args.accuracy:
         options["accuracy"] = torch.empty(1, dtype=torch.float32, device=device)
-    kw.update(options)
-
-    def step():
-        return ce.ce_fwd_bwd(work, target, **kw)
-
-    for _ in range(args.warmup):
-        work.copy_(pristine)
-        step()
-    torch.cuda.synchronize()
-
-    plan = ce.ce_fused_plan(R, V, pristine.dtype, label_smoothing=cfg.label_smoothing, cluster=args.cluster,
-                            weighted=weight is not None)
-    n_valid = int((target >= 0).sum().item())
-    esz = pristine.element_size()
-    path = args.variant if args.variant != "auto" else ce.auto_variant(pristine, target, weight=weight, **options)
-    # algorithmic bytes per step of the chosen path: the one-read paths read
-    # every valid row once and write every row once (ignored rows are only
-    # zeroed); the split path also reads every row in its statistics pass.
-    # Plus the targets, read by the normaliser kernel and the row kernel.
-    reads = n_valid + (R if path == "split" else 0)
-    algo_bytes = (reads + R) * V * esz + 2 * R * 8
+    W = Workload(ce, cfg, device, variant=args.variant, tune=args.tune, cluster=args.cluster, options=options)
+    R, V = W.R, W.V
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=device)
+    plan = ce.ce_fused_plan(R, V, W.pristine.dtype, label_smoothing=cfg.label_smoothing, cluster=args.cluster,
+                            weighted=W.weight is not None)
+    path, esz = W.path, W.esz
     kernel_name = {"fused": f"ce_fused_kernel<{cfg.dtype}>", "rowpass": f"ce_rowpass_kernel<{cfg.dtype}>",
                    "stream": f"ce_stream_kernel<{cfg.dtype}>",
                    "split": f"ce_stats_kernel + ce_grad_kernel <{cfg.dtype}>"}[path]
 
-    sampler = ClockSampler(local)
-    if rank == 0:
-        sampler.start()
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier(world)
-    torch.cuda.synchronize()
-    for k in range(args.steps):
-        work.copy_(pristine)
-        flush.zero_()
-        ev[k][0].record(stream)
-        step()  # normaliser kernel + cross-entropy kernel(s)
-        ev[k][1].record(stream)
-    torch.cuda.synchronize()
+    t = time_workload(ce, W, args.steps, args.warmup, flush, clock_gpu=local if rank == 0 else None)
     barrier(world)
-    clocks = sampler.stop() if rank == 0 else None
-    step_ms = [a.elapsed_time(c) for a, c in ev]
+    clocks = t["clocks"]
+    step_ms = t["step_ms"]
     total_ms = sum(step_ms)
-
-    # the fused kernel alone (for the roofline): same steps, events around
-    # the fused launch only (normalisers prepared before the first event)
-    kern_ms = []
-    for k in range(args.steps):
-        work.copy_(pristine)
-        ce.ce_prepare(work, target, label_smoothing=cfg.label_smoothing, reduction=cfg.reduction,
-                      ws=ws, stream=stream, weight=weight)
-        flush.zero_()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        ce.ce_fwd_bwd(work, target, prepared=True, **kw)
-        e1.record(stream)
-        kern_ms.append((e0, e1))
-    torch.cuda.synchronize()
-    kern_ms = [a.elapsed_time(b) for a, b in kern_ms]
-    kernel_avg_s = sum(kern_ms) / len(kern_ms) / 1e3
+    kernel_avg_s = statistics.mean(t["kernel_ms"]) / 1e3
 
     # end to end through the public API with host buffers: H2D of the logits
     # and targets from pinned memory, the call, D2H of the loss
     e2e_ms = float("nan")
     if not args.no_e2e:
-        e2e_ms = measure_e2e(ce, pristine, target, work, flush, loss, kw, stream, args.steps)
+        e2e_ms = measure_e2e(ce, W.pristine, W.target, W.work, flush, W.loss, W.kw, W.stream, args.steps)
 
     value, ms_per_step = aggregate_throughput(R, args.steps, total_ms, world, device)
     e2e_ms = reduce_max(e2e_ms, world, device)
@@ -505,12 +688,30 @@ def run_ours(args):
         return 0
 
     peak, peak_kind = read_peaks()
+    algo_bytes = W.algo_bytes()
     achieved = algo_bytes / kernel_avg_s / 1e9
     traffic = read_traffic(path, cfg.name)
+    n_valid, h2d = W.n_valid, W.pristine.numel() * esz + R * 8
+    loss_numel, launches = W.loss.numel(), W.launches_per_step()
+    W.free()
+    del W
+    torch.cuda.empty_cache()
+
+    # the other workloads, one at a time, timed the same way (one GPU only)
+    configs = None
+    if world == 1 and not args.no_configs and not (args.rows or args.vocab or args.dtype) and \
+            args.workload == WORKLOAD and not options and args.variant == "auto" and not args.tune:
+        configs = {"tiny": measure_tiny(ce, device, flush)}
+        for name in ("confident", "large_vocab", "large_vocab_none"):
+            Wc = Workload(ce, CONFIGS[name], device)
+            tc = time_workload(ce, Wc, min(args.steps, 20), 3, flush, clock_gpu=local)
+            configs[name] = workload_entry(Wc, tc, peak)
+            Wc.free()
+            del Wc
+            torch.cuda.empty_cache()
 
     flce = None
     if not args.no_flce:
-        del work
         flce = measure_flce(ce, device, max(3, min(args.steps, 5)), args.flce_chunk)
         peak_tf = read_bf16_peak()
         flce["peak_tflops"] = peak_tf
@@ -533,6 +734,18 @@ def run_ours(args):
                          f"blocks), forward + fp64 gradient, {secs:.2f} s on {threads} threads",
                "single_core": {"value": one_rows / secs1, "unit": "tokens/s", "cores": 1,
                                "sample": f"{one_rows} rows, {secs1:.2f} s"}}
+        if configs is not None:
+            # the oracle on each other workload; on the confident one its
+            # gradient also gives the dx_y accuracy report
+            rep = confident_dxy_report(ce, device, threads)
+            configs["confident"]["dxy_max_rel_err"] = rep["dxy"]
+            configs["confident"]["cpu_baseline"] = {
+                "value": rep["oracle_rows"] / rep["oracle_secs"], "unit": "tokens/s", "cores": threads,
+                "kind": "oracle", "sample": f"the whole batch ({rep['oracle_rows']} rows), forward + fp64 "
+                                            f"gradient, {rep['oracle_secs']:.2f} s"}
+            configs["tiny"]["cpu_baseline"] = oracle_config_baseline(CONFIGS["tiny"], 64, threads)
+            for name in ("large_vocab", "large_vocab_none"):
+                configs[name]["cpu_baseline"] = oracle_config_baseline(CONFIGS[name], 256, threads)
 
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
@@ -553,13 +766,14 @@ def run_ours(args):
                      "kernel": kernel_name, "kernel_ms": kernel_avg_s * 1e3,
                      "algorithmic_bytes": algo_bytes, "peak_source": peak_kind},
         "e2e": None if args.no_e2e else {"value": R * world / (e2e_ms / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": pristine.numel() * esz + R * 8, "d2h_bytes_per_step": loss.numel() * 4,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": loss_numel * 4,
                 "ms_per_step": e2e_ms},
         # per step: the normaliser kernel (two with class weights: eight partial
         # blocks, then the kernel combining them) and the row kernel(s)
-        "gpu_launches": ((3 if path == "split" else 2) + (1 if cfg.weighted else 0)) * args.steps,
+        "gpu_launches": launches * args.steps,
         "clocks": clocks,
         "cpu_baseline": cpu,
+        "configs": configs,
         "flce": flce,
         "step_ms_min_median_max": [min(step_ms), statistics.median(step_ms), max(step_ms)],
     }
@@ -584,6 +798,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-flce", action="store_true", help="skip the fused-linear measurement")
+    ap.add_argument("--no-configs", action="store_true",
+                    help="skip the other workloads (tiny, confident, large vocabulary sum and none)")
     ap.add_argument("--flce-chunk", type=int, default=4096)
     ap.add_argument("--flce-only", action="store_true", help="only the fused-linear measurement")
     ap.add_argument("--gemm-only", default="", help="only one GEMM: M,N,K,a_mn,b_mn")

@@ -91,12 +91,14 @@ typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
  * target, weights, n_rows and reduction): ce_forward / ce_backward /
  * ce_fwd_bwd skip their own normaliser kernel */
 #define CE_VARIANT_PREPARED 0x10000
-/* bits 20..25 of variant: stream-kernel tuning (0 = the library's choice):
+/* bits 20..26 of variant: stream-kernel tuning (0 = the library's choice):
  * 1 = 16 consumer warps and one CTA per SM, 2 = second pass over each row's
  * chunks in reverse order, 4 = first pass without the L2 evict-last policy,
  * 8 = a cluster of two CTAs per row (each streams half the row),
  * 16 = three CTAs per SM with a smaller ring, 32 = with 16: a cluster of four
- * CTAs per row (each streams a quarter) */
+ * CTAs per row (each streams a quarter), 64 = with 16, for class-weighted
+ * label smoothing on bf16 / f16 rows: the class weights of the second pass
+ * bulk-copied into a shared-memory ring (other rows ignore the bit) */
 #define CE_VARIANT_TUNE_SHIFT 20
 
 typedef struct ce_params {
@@ -219,9 +221,11 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
  *    normalisers must be computed by this call, since no caller can run
  *    ce_prepare on the library's scratch.
  *  - The first call on a device looks up the array's device address (a
- *    runtime query with that device current), and so does the first call
- *    after the device's context was replaced (cudaDeviceReset); make those
- *    calls before any stream capture.
+ *    runtime query with that device current; with lazy module loading the
+ *    driver places the array in device memory at that moment), and so does
+ *    the first call after the device's context was replaced
+ *    (cudaDeviceReset); make those calls before any stream capture. Later
+ *    calls change no device memory in use.
  *  - Every call on a device shares the one array, and the array keeps the
  *    last call's contents (each call runs its own normaliser kernel first,
  *    which resets every counter and sum that the later kernels read).

@@ -13,9 +13,13 @@ Entry points (same names as the C ABI):
   ce_fwd_bwd(logits, target, ...)            -> loss; gradient over logits
   ce_scale_grad(grad, grad_output, ...)      in-place grad_output scaling
   ce_workspace_size / ce_fused_plan / ce_get_status
-and ``CrossEntropyFunction`` / ``cross_entropy``: a torch.autograd wrapper
-that computes the gradient in the forward (in place) and scales it by
-grad_output in the backward, with a device-side skip when grad_output is 1.
+and ``cross_entropy``: a torch.autograd entry with two modes.
+``CrossEntropyFunction`` computes the gradient in the forward (in place) and
+scales it by grad_output in the backward, with a device-side skip when
+grad_output is 1 (one logits read and write; a second rounding when
+grad_output is not 1). ``CrossEntropyExactFunction`` saves the row
+statistics in the forward and forms the gradient in the backward with
+grad_output applied before the one rounding (the logits read twice).
 """
 from __future__ import annotations
 
@@ -348,11 +352,14 @@ def ce_get_status(ws, stream=None) -> int:
 
 
 class CrossEntropyFunction(torch.autograd.Function):
-    """loss = CE(logits, target); the forward runs the fused pass with
-    grad_output = 1 and leaves the gradient in the logits buffer (one
-    logits tensor of peak memory); the backward scales it by grad_output in
-    place (device-side skip when grad_output == 1). The logits tensor is
-    consumed: its contents after the forward are the gradient."""
+    """loss = CE(logits, target), gradient formed in the forward pass: the
+    fused pass runs with grad_output = 1 and leaves the gradient in the
+    logits buffer (one read and one write of the logits, one logits tensor
+    of peak memory); the backward multiplies it by grad_output in place,
+    skipped on the device when grad_output == 1. With grad_output == 1 every
+    element is rounded once; otherwise the product is rounded a second time
+    (within 2 ulps). The logits tensor is consumed: its contents after the
+    forward are the gradient."""
 
     @staticmethod
     def forward(ctx, logits, target, weight, ignore_index, label_smoothing, reduction):
@@ -371,9 +378,45 @@ class CrossEntropyFunction(torch.autograd.Function):
         return grad, None, None, None, None, None
 
 
-def cross_entropy(logits, target, weight=None, ignore_index=-100, label_smoothing=0.0, reduction="mean"):
-    """torch.nn.functional.cross_entropy-like entry; ``logits`` is overwritten by its gradient."""
-    return CrossEntropyFunction.apply(logits, target, weight, ignore_index, label_smoothing, reduction)
+class CrossEntropyExactFunction(torch.autograd.Function):
+    """loss = CE(logits, target) with the gradient formed in the backward
+    pass: the forward reads the logits once and keeps the per-row statistics
+    (16 bytes a row); the backward reads them again and writes the gradient,
+    grad_output applied inside the one fp32 computation and rounded once, for
+    any grad_output (TransformerEngine #2325's forward/backward split). It
+    moves 1.5 times the bytes of CrossEntropyFunction. The logits must stay
+    unchanged until the backward, which overwrites them with the gradient."""
+
+    @staticmethod
+    def forward(ctx, logits, target, weight, ignore_index, label_smoothing, reduction):
+        x = logits.detach()
+        loss, stats = ce_forward(x, target, weight=weight, ignore_index=ignore_index,
+                                 label_smoothing=label_smoothing, reduction=reduction)
+        ctx.save_for_backward(x, target, stats, weight)
+        ctx.ignore_index, ctx.label_smoothing, ctx.reduction = ignore_index, label_smoothing, reduction
+        return loss if reduction == "none" else loss.reshape(())
+
+    @staticmethod
+    def backward(ctx, grad_out):
+        x, target, stats, weight = ctx.saved_tensors
+        g = grad_out.detach().to(torch.float32).reshape(-1).contiguous()
+        ce_backward(x, target, stats, grad_output=g, weight=weight, ignore_index=ctx.ignore_index,
+                    label_smoothing=ctx.label_smoothing, reduction=ctx.reduction)
+        return x, None, None, None, None, None
+
+
+def cross_entropy(logits, target, weight=None, ignore_index=-100, label_smoothing=0.0, reduction="mean",
+                  grad_mode="inplace"):
+    """torch.nn.functional.cross_entropy-like entry; ``logits`` is overwritten
+    by its gradient. ``grad_mode``: "inplace" (CrossEntropyFunction: one read
+    and one write of the logits, one rounding when grad_output is 1, two
+    otherwise) or "exact" (CrossEntropyExactFunction: one rounding for any
+    grad_output, the logits read twice)."""
+    if grad_mode == "inplace":
+        return CrossEntropyFunction.apply(logits, target, weight, ignore_index, label_smoothing, reduction)
+    if grad_mode == "exact":
+        return CrossEntropyExactFunction.apply(logits, target, weight, ignore_index, label_smoothing, reduction)
+    raise ValueError(f"unknown grad_mode {grad_mode!r}")
 
 
 # ---------------------------------------------------------------------- fused linear

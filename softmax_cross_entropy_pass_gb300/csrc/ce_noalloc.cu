@@ -8,14 +8,13 @@
 // entry point takes its scratch from a fixed array in the library's own
 // device memory instead (the array exists on every GPU that loads the
 // library, until the process exits), and allocates nothing.
-#include <cuda.h>
-#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "ce.h"
 #include "ce_device.cuh"
+#include "ce_host.h"
 
 namespace {
 
@@ -39,24 +38,6 @@ struct ScratchEntry {
 std::mutex g_mu;
 ScratchEntry g_scratch[kMaxDevices] = {};
 
-PFN_cuCtxGetCurrent_v4000 g_ctx_get_current = nullptr;
-PFN_cuCtxGetId_v12000 g_ctx_get_id = nullptr;
-
-bool driver_entry(const char *name, int version, void **fn) {
-    cudaDriverEntryPointQueryResult q;
-    return cudaGetDriverEntryPointByVersion(name, fn, version, cudaEnableDefault, &q) == cudaSuccess &&
-           q == cudaDriverEntryPointSuccess && *fn != nullptr;
-}
-
-// id of the context current on this thread, or 0 if there is none yet
-unsigned long long current_ctx_id() {
-    CUcontext ctx = nullptr;
-    unsigned long long id = 0;
-    if (g_ctx_get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return 0;
-    if (g_ctx_get_id(ctx, &id) != CUDA_SUCCESS) return 0;
-    return id;
-}
-
 // Device address of the scratch array in the current device's context. In
 // host code the array's name is only a host-side stand-in, so the address is
 // asked from the runtime (cudaGetSymbolAddress), with that device current.
@@ -64,18 +45,12 @@ ce_status scratch_for_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return CE_ERR_CUDA;
     std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_ctx_get_current) {
-        void *a = nullptr, *b = nullptr;
-        if (!driver_entry("cuCtxGetCurrent", 4000, &a) || !driver_entry("cuCtxGetId", 12000, &b)) return CE_ERR_CUDA;
-        g_ctx_get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(a);
-        g_ctx_get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(b);
-    }
-    unsigned long long id = current_ctx_id();
+    unsigned long long id = ce::current_context_id();
     if (id == 0 || g_scratch[dev].ctx_id != id || g_scratch[dev].ptr == nullptr) {
         // also makes the device's primary context current on this thread
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return CE_ERR_CUDA;
-        id = current_ctx_id();
+        id = ce::current_context_id();
         if (id == 0) return CE_ERR_CUDA;
         g_scratch[dev].ctx_id = id;
         g_scratch[dev].ptr = p;

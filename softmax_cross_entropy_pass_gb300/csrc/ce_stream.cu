@@ -2,9 +2,48 @@
 // (ce_stream.cuh) and its instantiations for 16-byte aligned rows.
 #include <mutex>
 
+#include "ce_host.h"
 #include "ce_stream.cuh"
 
 namespace ce {
+
+// Per (kernel, context): the dynamic shared memory attribute has been set
+// and the SM count read, so a launch makes neither call again (they were a
+// few microseconds of host time per call, which dominates at small batches).
+static cudaError_t stream_fn_ready(const void *fn, int smem, int *dev_out, int *sms_out) {
+    struct Entry {
+        const void *fn;
+        unsigned long long ctx;
+        int dev, sms;
+    };
+    static Entry cache[256];
+    static int used = 0;
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const unsigned long long ctx = current_context_id();
+    if (ctx != 0) {
+        std::lock_guard<std::mutex> lk(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].fn == fn && cache[i].ctx == ctx && cache[i].dev == dev) {
+                *dev_out = dev;
+                *sms_out = cache[i].sms;
+                return cudaSuccess;
+            }
+    }
+    if ((e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess) return e;
+    int sms = 0;
+    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    const unsigned long long ctx2 = current_context_id();  // current now, if it was not before
+    if (ctx2 != 0) {
+        std::lock_guard<std::mutex> lk(mu);
+        if (used < 256) cache[used++] = Entry{fn, ctx2, dev, sms};
+    }
+    *dev_out = dev;
+    *sms_out = sms;
+    return cudaSuccess;
+}
 
 // Resident clusters of a kernel on a device (0 if unknown), asked once per
 // kernel and device.
@@ -26,6 +65,15 @@ static int max_active_clusters(const void *fn, int dev, const cudaLaunchConfig_t
     return n;
 }
 
+// The class-weight ring shape (SHAPE 3): aligned bf16 / f16 rows with
+// class-weighted smoothing and no options.
+template <int CL>
+static const void *stream_kernel_wring(int dtype) {
+    return dtype == CE_DT_BF16 ? reinterpret_cast<const void *>(&ce_stream_kernel<CE_DT_BF16, 2, 3, CL, false, 0>)
+         : dtype == CE_DT_F16  ? reinterpret_cast<const void *>(&ce_stream_kernel<CE_DT_F16, 2, 3, CL, false, 0>)
+                               : nullptr;
+}
+
 template <int SHAPE, int CL>
 static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, int ctas_per_sm, int tune,
                                        bool after_prep, cudaStream_t s) {
@@ -34,15 +82,23 @@ static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, i
     // rows that all start on a 16-byte boundary take the fixed-geometry instantiation
     const int64_t esz = dtype == CE_DT_F32 ? 4 : 2;
     const bool ragged = (reinterpret_cast<uintptr_t>(a.grad) & 15u) != 0 || (a.n_rows > 1 && ((a.ld * esz) & 15) != 0);
-    const void *fn = a.softcap > 0.f ? stream_kernel_softcap(dtype, mode, SHAPE, CL, ragged)
-                   : (a.z_loss > 0.f || a.accuracy) ? stream_kernel_options(dtype, mode, SHAPE, CL, ragged)
-                   : ragged ? stream_kernel_ragged(dtype, mode, SHAPE, CL) : stream_kernel_for<false>(dtype, mode, SHAPE, CL);
+    const bool opts = a.softcap > 0.f || a.z_loss > 0.f || a.accuracy;
+    const void *fn = nullptr;
+    if constexpr (SHAPE == 3) {
+        // the weight ring copies whole 32-byte weight vectors from 16-byte aligned weights
+        const bool ok = mode == 2 && !ragged && !opts && dtype != CE_DT_F32 && a.weight &&
+                        (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
+        if (!ok) return launch_stream_shape<2, CL>(a0, dtype, mode, ctas_per_sm, tune, after_prep, s);
+        fn = stream_kernel_wring<CL>(dtype);
+    } else {
+        fn = a.softcap > 0.f ? stream_kernel_softcap(dtype, mode, SHAPE, CL, ragged)
+           : opts ? stream_kernel_options(dtype, mode, SHAPE, CL, ragged)
+           : ragged ? stream_kernel_ragged(dtype, mode, SHAPE, CL) : stream_kernel_for<false>(dtype, mode, SHAPE, CL);
+    }
     if (!fn) return cudaErrorInvalidValue;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, SH::kSmem);
-    if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+    cudaError_t e = stream_fn_ready(fn, SH::kSmem, &dev, &sms);
+    if (e != cudaSuccess) return e;
     int64_t grid = static_cast<int64_t>(sms) * (ctas_per_sm > 0 ? ctas_per_sm : SH::kCtasPerSm);
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(SH::kThreads);
@@ -145,6 +201,10 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     if (tune & kTuneWide)
         return pair ? launch_stream_shape<1, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
                     : launch_stream_shape<1, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
+    if ((tune & kTuneThree) && (tune & kTuneWRing))
+        return quad ? launch_stream_shape<3, 4>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+             : pair ? launch_stream_shape<3, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+                    : launch_stream_shape<3, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
     if (tune & kTuneThree)
         return quad ? launch_stream_shape<2, 4>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
              : pair ? launch_stream_shape<2, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)

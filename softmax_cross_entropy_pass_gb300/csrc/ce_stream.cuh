@@ -29,19 +29,27 @@
 
 namespace ce {
 
-// Three shapes: 8 consumer warps and a 6-slot ring (two CTAs per SM);
+// Four shapes: 8 consumer warps and a 6-slot ring (two CTAs per SM);
 // 16 consumer warps and a 12-slot ring (one CTA per SM, half the rows
 // waiting in L2 for their second pass); 8 consumer warps and a 4-slot ring
-// (three CTAs per SM, more warps to cover a cluster exchange).
+// (three CTAs per SM, more warps to cover a cluster exchange); and, for
+// bf16 / f16 rows with class-weighted smoothing, three CTAs per SM with a
+// 3-slot ring plus a 3-slot ring of class weights: a second producer lane
+// bulk-copies the fp32 weights of each second-pass chunk into shared memory
+// (8 KB per slot, one weight vector per consumer thread), so the gradient
+// loop reads them from shared memory instead of waiting on per-lane loads.
 constexpr int kStreamChunk = 16384;  // bytes per ring slot
 constexpr int kStreamMaxSlots = 12;
-constexpr int kStreamCtlBytes = 2048;  // control block after the ring
+constexpr int kStreamCtlBytes = 2048;  // control block after the rings
+constexpr int kStreamWSlotBytes = 8192;  // bytes per class-weight slot
+constexpr int kStreamWSlots = 3;
 template <int SHAPE> struct StreamShape {
     static constexpr int kWarps = SHAPE == 1 ? 16 : 8;
     static constexpr int kThreads = (kWarps + 1) * 32;
-    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : 4);
+    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : (SHAPE == 2 ? 4 : 3));
     static constexpr int kCtasPerSm = SHAPE == 0 ? 2 : (SHAPE == 1 ? 1 : 3);
-    static constexpr int kSmem = kSlots * kStreamChunk + kStreamCtlBytes;
+    static constexpr int kWSlots = SHAPE == 3 ? kStreamWSlots : 0;  // class-weight ring
+    static constexpr int kSmem = kSlots * kStreamChunk + kWSlots * kStreamWSlotBytes + kStreamCtlBytes;
 };
 
 struct StreamXSlot {      // one CTA's partial of one row (32 bytes)
@@ -52,6 +60,8 @@ struct StreamXSlot {      // one CTA's partial of one row (32 bytes)
 struct StreamSmem {
     uint64_t full[kStreamMaxSlots];
     uint64_t empty[kStreamMaxSlots];
+    uint64_t wfull[kStreamWSlots];   // class-weight ring (SHAPE 3)
+    uint64_t wempty[kStreamWSlots];
     uint64_t xbar[2];
     StreamXSlot slot[2][4];  // [row parity][CTA of the cluster]
     // per row parity: a warp may write the next row's values while a slower
@@ -72,6 +82,7 @@ constexpr int kTuneNoKeep = 4;     // first pass without the L2 evict-last polic
 constexpr int kTuneCluster2 = 8;   // a cluster of two CTAs per row, each streaming half
 constexpr int kTuneThree = 16;     // three CTAs per SM with a 4-slot ring
 constexpr int kTuneCluster4 = 32;  // a cluster of four CTAs per row (three CTAs per SM)
+constexpr int kTuneWRing = 64;     // with 16, class-weighted smoothing: weights through a shared-memory ring
 
 template <int NCW>
 __device__ inline void stream_consumer_sync() {
@@ -183,6 +194,10 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr bool P1S = SMOOTH && !DEFER;   // smoothing sums in pass 1
     constexpr int kStreamConsumerWarps = NCW;
     constexpr int kStreamSlots = SH::kSlots;
+    constexpr int kWS = SH::kWSlots;
+    constexpr bool WR = kWS > 0;  // class weights of pass 2 through the weight ring
+    static_assert(!WR || (MODE == 2 && !RAG && VEC == 8 && OPT == 0),
+                  "the class-weight ring serves aligned bf16 / f16 rows with class-weighted smoothing");
     constexpr int NCT = NCW * 32;
     constexpr int VPC = kStreamChunk / 16;          // vectors per full chunk
     constexpr int VPT = VPC / NCT;                  // vectors per thread per full chunk
@@ -190,8 +205,9 @@ ce_stream_kernel(RowArgs a, int tune) {
     static_assert(CL == 1 || CL == 2 || CL == 4, "one, two or four CTAs per row");
 
     extern __shared__ __align__(128) uint8_t smem[];
-    StreamSmem &S = *reinterpret_cast<StreamSmem *>(smem + kStreamSlots * kStreamChunk);
+    StreamSmem &S = *reinterpret_cast<StreamSmem *>(smem + kStreamSlots * kStreamChunk + kWS * kStreamWSlotBytes);
     const uint32_t ring = smem_u32(smem);
+    const uint32_t wring = ring + kStreamSlots * kStreamChunk;  // class-weight slots (SHAPE 3)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int64_t V = a.vocab;
     // this CTA's columns [lo, hi) of every row: all of it, or one half
@@ -216,11 +232,18 @@ ce_stream_kernel(RowArgs a, int tune) {
     const float nic2 = -(inv_cap * inv_cap);
     const float zl = FEAT ? a.z_loss : 0.f;
     const bool want_am = FEAT && a.accuracy != nullptr;
+    // weight pieces are bulk-copied from the weights' 16-byte aligned start
+    // plus whole 32-byte vectors of the (aligned) part
+    const bool wr = WR && w_base16;
 
     if (tid == 0) {
         for (int s = 0; s < kStreamSlots; ++s) {
             mbar_init(smem_u32(&S.full[s]), 1);
             mbar_init(smem_u32(&S.empty[s]), kStreamConsumerWarps);
+        }
+        for (int s = 0; s < kWS; ++s) {
+            mbar_init(smem_u32(&S.wfull[s]), 1);
+            mbar_init(smem_u32(&S.wempty[s]), kStreamConsumerWarps);
         }
         mbar_init(smem_u32(&S.xbar[0]), CL);
         mbar_init(smem_u32(&S.xbar[1]), CL);
@@ -267,6 +290,38 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const uint32_t i = it - 1 - k;
                 mbar_wait_bounded<false>(smem_u32(&S.full[i % kStreamSlots]), (i / kStreamSlots) & 1u, abort);
             }
+        } else if (WR && lane == 1 && wr) {
+            // class-weight producer: for every second-pass chunk, in the consumers'
+            // order, the weights of its vectors in pieces of one vector per consumer
+            // thread (NCT vectors, 8 KB), kept in L2 (every row reads them again)
+            const uint64_t wpol = policy_keep();
+            uint32_t wi = 0;
+            int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;
+            const int nch = g_aligned.nch, nvec = g_aligned.nvec;
+            const float *wsrc = a.weight + g_aligned.vlo;
+            for (int64_t row = q0; row < a.n_rows; row += nq) {
+                const int64_t t = t_next;
+                if (row + nq < a.n_rows) t_next = load_target(a.target, a.tgt32, row + nq);
+                if (!target_valid(t, a.ignore_index, V)) continue;
+                for (int k = 0; k < nch; ++k) {
+                    const int c = reverse ? nch - 1 - k : k;
+                    const int v0 = c * VPC;
+                    const int nv = min(VPC, nvec - v0);
+                    for (int q = 0; q * NCT < nv; ++q, ++wi) {
+                        const uint32_t s = wi % kWS, r = wi / kWS;
+                        if (r > 0) mbar_wait_bounded<false>(smem_u32(&S.wempty[s]), (r - 1) & 1u, abort);
+                        const int nvq = min(NCT, nv - q * NCT);
+                        const uint32_t bytes = static_cast<uint32_t>(nvq * VEC * 4);
+                        mbar_expect_tx(smem_u32(&S.wfull[s]), bytes);
+                        bulk_g2s_hint(wring + s * kStreamWSlotBytes, wsrc + static_cast<int64_t>(v0 + q * NCT) * VEC,
+                                      bytes, smem_u32(&S.wfull[s]), wpol);
+                    }
+                }
+            }
+            for (uint32_t k = 0; k < static_cast<uint32_t>(kWS) && k < wi; ++k) {
+                const uint32_t i = wi - 1 - k;
+                mbar_wait_bounded<false>(smem_u32(&S.wfull[i % kWS]), (i / kWS) & 1u, abort);
+            }
         }
         __syncwarp();
     } else {
@@ -281,6 +336,7 @@ ce_stream_kernel(RowArgs a, int tune) {
         float pend_m = 0.f, pend_s = 0.f, pend_xy = 0.f, pend_wy = 0.f;
         int pend_yg = 0;
         uint32_t it = 0, j = 0;  // ring position; valid rows done (exchange parity)
+        uint32_t wi = 0;         // class-weight ring position (SHAPE 3)
         int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;  // one row ahead
         for (int64_t row = q0; row < a.n_rows; row += nq) {
             const int64_t t = t_next;
@@ -569,6 +625,55 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const int v0 = c * VPC;
                 const int nv = min(VPC, nvec - v0);
                 const unsigned form = c < 32 ? static_cast<unsigned>(cap_forms >> (2 * c)) & 3u : 2u;
+                // class-weighted element math of one vector: p, the gradient a p - b w,
+                // and the deferred smoothing sums (the same operations whichever way
+                // the weights arrive)
+                auto weighted_vec = [&](const float *x, const float4 *wq, float *gr) {
+#pragma unroll
+                    for (int h = 0; h < VEC / 4; ++h) {
+                        const float4 wv = wq[h];
+                        const F2 w01 = f2(wv.x, wv.y), w23 = f2(wv.z, wv.w);
+                        const F2 x01 = f2(x[4 * h], x[4 * h + 1]), x23 = f2(x[4 * h + 2], x[4 * h + 3]);
+                        const F2 nbw0 = f2_mul(rs_nb, w01), nbw1 = f2_mul(rs_nb, w23);
+                        const F2 p0 = f2_ex2(f2_fma(f2_sub(x01, rs_m), rs_l2, rs_nl));
+                        const F2 p1 = f2_ex2(f2_fma(f2_sub(x23, rs_m), rs_l2, rs_nl));
+                        dr[0] = f2_fma(w01, x01, dr[0]);
+                        dr[1] = f2_fma(w23, x23, dr[1]);
+                        dn[0] = f2_add(dn[0], w01);
+                        dn[1] = f2_add(dn[1], w23);
+                        f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
+                        f2_split(f2_fma(p1, rs_a, nbw1), gr[4 * h + 2], gr[4 * h + 3]);
+                    }
+                };
+                if (WR && wr) {
+                    // weights from the weight ring: piece q holds the weights of vectors
+                    // [q NCT, (q + 1) NCT) of the chunk, thread tid's at 32 tid bytes
+                    for (int q = 0; q * NCT < nv; ++q, ++wi) {
+                        const uint32_t wsl = wi % kWS;
+                        mbar_wait_bounded<false>(smem_u32(&S.wfull[wsl]), (wi / kWS) & 1u, abort);
+                        const int v = q * NCT + tid;
+                        if (v < nv) {
+                            float x[VEC], gr[VEC];
+                            F::unpack(ld_shared_v4(base_s + 16u * v), x);
+                            const int vb = (v0 + v) * VEC;
+                            const uint32_t wa = wring + wsl * kStreamWSlotBytes + 32u * tid;
+                            const uint4 wlo = ld_shared_v4(wa), whi = ld_shared_v4(wa + 16u);
+                            const float4 wq[2] = {
+                                make_float4(__uint_as_float(wlo.x), __uint_as_float(wlo.y), __uint_as_float(wlo.z),
+                                            __uint_as_float(wlo.w)),
+                                make_float4(__uint_as_float(whi.x), __uint_as_float(whi.y), __uint_as_float(whi.z),
+                                            __uint_as_float(whi.w))};
+                            weighted_vec(x, wq, gr);
+                            if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
+#pragma unroll
+                                for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
+                            }
+                            st_stream(vp + v0 + v, F::pack(gr));
+                        }
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(smem_u32(&S.wempty[wsl]));
+                    }
+                } else {
                 for (int v = tid; v < nv; v += NCT) {
                     float x[VEC], gr[VEC];
                     F::unpack(ld_shared_v4(base_s + 16u * v), x);
@@ -583,21 +688,7 @@ ce_stream_kernel(RowArgs a, int tune) {
 #pragma unroll
                             for (int h = 0; h < VEC / 4; ++h) wq[h] = load_w4(a.weight, vlo + vb + 4 * h, w4);
                         }
-#pragma unroll
-                        for (int h = 0; h < VEC / 4; ++h) {
-                            const float4 wv = wq[h];
-                            const F2 w01 = f2(wv.x, wv.y), w23 = f2(wv.z, wv.w);
-                            const F2 x01 = f2(x[4 * h], x[4 * h + 1]), x23 = f2(x[4 * h + 2], x[4 * h + 3]);
-                            const F2 nbw0 = f2_mul(rs_nb, w01), nbw1 = f2_mul(rs_nb, w23);
-                            const F2 p0 = f2_ex2(f2_fma(f2_sub(x01, rs_m), rs_l2, rs_nl));
-                            const F2 p1 = f2_ex2(f2_fma(f2_sub(x23, rs_m), rs_l2, rs_nl));
-                            dr[0] = f2_fma(w01, x01, dr[0]);
-                            dr[1] = f2_fma(w23, x23, dr[1]);
-                            dn[0] = f2_add(dn[0], w01);
-                            dn[1] = f2_add(dn[1], w23);
-                            f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
-                            f2_split(f2_fma(p1, rs_a, nbw1), gr[4 * h + 2], gr[4 * h + 3]);
-                        }
+                        weighted_vec(x, wq, gr);
                     } else {
 #pragma unroll
                         for (int p = 0; p < VEC / 2; ++p) {
@@ -611,6 +702,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                     }
                     if (CAPF && cap > 0.f) softcap_deriv_vec<VEC>(gr, x, nic2);
                     st_stream(vp + v0 + v, F::pack(gr));  // vp points at this CTA's slice
+                }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));

@@ -11,8 +11,8 @@ import pytest
 import torch
 
 import oracle
-from ce_check import (DXY_RTOL, check_loss_reduced, check_loss_rows, grad_mismatch, grad_mismatch_detail,
-                      magnitude_T, row_scale)
+from ce_check import (DXY_RTOL, FLOOR, check_loss_reduced, check_loss_rows, grad_mismatch,
+                      grad_mismatch_detail, magnitude_T, row_scale, ulp_of)
 from workloads import (CONFIGS, IGNORE_INDEX, make_ce_inputs, make_grad_output, make_logits,
                        make_targets, make_weights)
 
@@ -243,29 +243,50 @@ def test_scale_grad_skips_at_one_and_scales(ce):
     assert torch.equal(y, (before.float() * g[:, None]).to(torch.bfloat16))
 
 
+@pytest.mark.parametrize("grad_mode", ["inplace", "exact"])
+@pytest.mark.parametrize("reduction", ["mean", "none"])
 @pytest.mark.parametrize("gscale", [1.0, 0.37])
-def test_autograd_function(ce, gscale):
+def test_autograd_function(ce, gscale, reduction, grad_mode):
+    """cross_entropy's autograd path against the oracle element by element.
+    The exact mode, and the in-place mode at grad_output 1, round each
+    element once (1 ulp, or the cancellation floor); the in-place mode at
+    grad_output != 1 rounds the g = 1 gradient, then its product with g:
+    within 2 ulps of the once-rounded oracle value (the first rounding errs
+    by half an ulp of the unscaled value, which g maps to at most one ulp of
+    the result; the second adds half an ulp), or the floor scaled the same
+    way."""
     R, V = 32, 5000
     x = make_logits(R, V, "bf16", 1.0, 12, device="cuda")
     t = make_targets(R, V, 0.1, 12, device="cuda")
+    w = make_weights(V, 12, device="cuda")
     x_in = x.cpu()
-    ref = _oracle(x, t, None, 0.1, "mean", torch.tensor([gscale]))
+    gvec = (torch.rand(R, generator=torch.Generator().manual_seed(5)) * gscale if reduction == "none"
+            else torch.tensor([gscale]))
+    ref = _oracle(x, t, w, 0.1, reduction, gvec)
     xr = x.clone().requires_grad_(True)
     buf = xr.detach()
-    loss = ce.cross_entropy(xr, t, label_smoothing=0.1)
-    (loss * gscale).backward()
+    loss = ce.cross_entropy(xr, t, weight=w, label_smoothing=0.1, reduction=reduction, grad_mode=grad_mode)
+    if reduction == "none":
+        (loss * gvec.to("cuda")).sum().backward()
+        check_loss_rows(loss.detach().cpu(), ref["row_loss"])
+    else:
+        (loss * gscale).backward()
+        check_loss_reduced(float(loss.item()), ref["loss"])
     torch.cuda.synchronize()
-    check_loss_reduced(float(loss.item()), ref["loss"])
     assert xr.grad.data_ptr() == buf.data_ptr()  # gradient lives in the logits buffer
     got = xr.grad.cpu()
-    if gscale == 1.0:
-        scale = row_scale("mean", torch.tensor([1.0]), R, ref["norm_wy"])
-        T = magnitude_T(x_in, t.cpu(), ref["stats"], None, 0.1, ref["w_all"], scale)
+    scale = row_scale(reduction, gvec, R, ref["norm_wy"])
+    T = magnitude_T(x_in, t.cpu(), ref["stats"], w.cpu(), 0.1, ref["w_all"], scale)
+    twice = grad_mode == "inplace" and not (gscale == 1.0 and reduction != "none")
+    if not twice:
         bad, _, worst = grad_mismatch(got, ref["grad"], T)
         assert bad == 0, worst
-    else:  # scaled after rounding: two roundings, within 2 ulp
-        want = ref["grad"]
-        assert ((got.double() - want).abs() <= want.abs() * 2.0 ** -6 + 1e-12).all()
+    else:
+        want = ref["grad"].to(torch.float32).to(torch.bfloat16)
+        u = ulp_of(want, torch.bfloat16)
+        err = (got.double() - want.double()).abs()
+        bad = err > torch.maximum(2 * u, FLOOR * T)
+        assert int(bad.sum()) == 0, float((err / u).max())
 
 
 # ---------------------------------------------------------------- no host synchronisation
@@ -473,17 +494,20 @@ def test_tiny_config(ce):
     _check_all(x, t, None, 0.0, "mean", None, ref, loss, x_in)
 
 
-@pytest.mark.parametrize("tune", [0, 1, 2, 3, 4, 8, 9, 10, 12, 15, 16, 24, 26, 48, 52, 54])
-@pytest.mark.parametrize("shape", [(70, 128256), (33, 33008), (9, 256000), (5, 1000), (6, 40)])
+@pytest.mark.parametrize("tune", [0, 1, 2, 3, 4, 8, 9, 10, 12, 15, 16, 24, 26, 48, 52, 54, 80, 86, 88, 94, 112,
+                                  118, 119])
+@pytest.mark.parametrize("shape", [(70, 128256), (33, 33008), (9, 256000), (5, 1000), (6, 40), (4, 24)])
 def test_stream_tuning_variants(ce, tune, shape):
     """Every stream-kernel tuning combination (wide CTA, reversed second
-    pass, no L2 evict-last, CTA pairs and quads) against the oracle; class
-    weights on the odd tunes and on 54 (a quad); at V = 40 the last CTA of a
-    quad has no columns (the parts are 16, 16 and 8 columns)."""
+    pass, no L2 evict-last, CTA pairs and quads, class weights through the
+    shared-memory weight ring) against the oracle; class weights on the odd
+    tunes, on 54 (a quad) and on every weight-ring tune (64 set); at V = 40
+    the last CTA of a quad has no columns (the parts are 16, 16 and 8
+    columns), at V = 24 the last two."""
     R, V = shape
     x = make_logits(R, V, "bf16", 1.5, 300 + tune, device="cuda")
     t = make_targets(R, V, 0.1, 300 + tune, device="cuda")
-    w = make_weights(V, 300 + tune, device="cuda") if tune % 2 or tune == 54 else None
+    w = make_weights(V, 300 + tune, device="cuda") if tune % 2 or tune == 54 or tune & 64 else None
     x_in = x.cpu()
     g = torch.tensor([0.37], device="cuda")
     ref = _oracle(x, t, w, 0.05, "sum", g)
@@ -491,6 +515,39 @@ def test_stream_tuning_variants(ce, tune, shape):
                          variant="stream", tune=tune)
     torch.cuda.synchronize()
     _check_all(x, t, w, 0.05, "sum", g, ref, loss, x_in)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("w_offset", [0, 1, 2, 4])
+@pytest.mark.parametrize("shape", [(40, 64000), (24, 128256), (12, 250000), (9, 8200)])
+def test_class_weight_ring_and_its_fallbacks(ce, dtype, w_offset, shape):
+    """Class-weighted smoothing on the automatic path: weights starting on a
+    16-byte boundary go through the shared-memory weight ring (single rows,
+    pairs and quads by row size); weights at a 4- or 8-byte offset take the
+    per-lane loads instead. Both against the oracle, and bit-identical to each
+    other."""
+    R, V = shape
+    seed = zlib.crc32(repr((dtype, w_offset, shape)).encode()) % 9973
+    x = make_logits(R, V, dtype, 1.5, seed, device="cuda")
+    t = make_targets(R, V, 0.1, seed, device="cuda")
+    wbuf = torch.empty(V + 8, dtype=torch.float32, device="cuda")
+    wbuf[w_offset:w_offset + V] = make_weights(V, seed, device="cuda")
+    w = wbuf[w_offset:w_offset + V]
+    g = torch.tensor([0.37], device="cuda")
+    x_in = x.cpu()
+    ref = _oracle(x, t, w, 0.05, "sum", g)
+    x2 = x.clone()
+    loss = ce.ce_fwd_bwd(x, t, weight=w, label_smoothing=0.05, reduction="sum", grad_output=g)
+    torch.cuda.synchronize()
+    _check_all(x, t, w, 0.05, "sum", g, ref, loss, x_in)
+    # the per-lane-load path on the same inputs (three CTAs per SM, pairs or quads as chosen by row size)
+    row_kb = V * 2 / 1024
+    tune = 16 | 4 | (2 if row_kb > 176 else 0) | (8 if 176 < row_kb <= 288 else 0) | (32 if row_kb > 288 else 0)
+    loss2 = ce.ce_fwd_bwd(x2, t, weight=w, label_smoothing=0.05, reduction="sum", grad_output=g, variant="stream",
+                          tune=tune)
+    torch.cuda.synchronize()
+    assert torch.equal(x.view(torch.int16), x2.view(torch.int16))
+    assert torch.equal(loss, loss2)
 
 
 @pytest.mark.parametrize("case", ["mean", "sum_weighted", "none_ragged", "int32_ld", "one_part", "tiny"])

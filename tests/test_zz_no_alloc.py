@@ -31,9 +31,20 @@ def _pair(ce, R, V, reduction, eps, seed, variant, weighted):
     return la, lb, xa, xb, free0 - free1
 
 
+def _first_call_setup(ce):
+    """The first call in a process looks up the scratch array's device
+    address; the driver may place the array (its module) in device memory
+    then. Later calls must not change device memory in use."""
+    x = make_logits(4, 64, "bf16", 1.0, 1, device="cuda")
+    t = make_targets(4, 64, 0.0, 1, device="cuda")
+    ce.ce_fwd_bwd_noalloc(x, t)
+    torch.cuda.synchronize()
+
+
 @pytest.mark.parametrize("variant", ["auto", "split", "rowpass"])
 def test_noalloc_matches_workspace_entry_bitwise(variant):
     import softmax_cross_entropy_pass_gb300 as ce
+    _first_call_setup(ce)
     cases = [(3000, 32000, "mean", 0.1, 11, False), (700, 50000, "sum", 0.0, 12, False),
              (257, 4096, "none", 0.05, 13, False),
              # class-weighted and smoothed, after batches of other sizes: the
