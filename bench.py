@@ -643,10 +643,11 @@ def run_ours(args):
     import softmax_cross_entropy_pass_gb300 as ce
     from workloads import CONFIGS
     cfg = CONFIGS[args.workload]
-    if args.rows or args.vocab or args.dtype:
+    if args.rows or args.vocab or args.dtype or args.ignore_frac >= 0:
         import dataclasses
         cfg = dataclasses.replace(cfg, n_rows=args.rows or cfg.n_rows, vocab=args.vocab or cfg.vocab,
-                                  dtype=args.dtype or cfg.dtype)
+                                  dtype=args.dtype or cfg.dtype,
+                                  ignore_frac=args.ignore_frac if args.ignore_frac >= 0 else cfg.ignore_frac)
     options = {}
     if args.softcap > 0:
         options["softcap"] = args.softcap
@@ -700,6 +701,7 @@ def run_ours(args):
     # the other workloads, one at a time, timed the same way (one GPU only)
     configs = None
     if world == 1 and not args.no_configs and not (args.rows or args.vocab or args.dtype) and \
+            args.ignore_frac < 0 and \
             args.workload == WORKLOAD and not options and args.variant == "auto" and not args.tune:
         configs = {"tiny": measure_tiny(ce, device, flush)}
         for name in ("confident", "large_vocab", "large_vocab_none"):
@@ -811,6 +813,8 @@ def main():
                     help="logits storage type (default: the workload's)")
     ap.add_argument("--vocab", type=int, default=0,
                     help="another vocabulary size for the workload (e.g. one that leaves rows unaligned)")
+    ap.add_argument("--ignore-frac", type=float, default=-1.0,
+                    help="share of ignored rows for the workload (default: the workload's own)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="CE workload of workloads.CONFIGS (the default is the headline metric's)")
     ap.add_argument("--print-kernel-hash", action="store_true")

@@ -585,6 +585,26 @@ __device__ inline bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
                  : "=r"(ok) : "r"(bar), "r"(parity) : "memory");
     return ok != 0;
 }
+// The same with a suspend-time hint: a thread whose phase is not complete
+// sleeps in hardware until the phase completes or about hint_ns have passed,
+// instead of returning at once and spinning (spinning warps take issue slots
+// from the working warps of their scheduler).
+__device__ inline bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
+__device__ inline bool mbar_try_wait_cluster_sleep(uint32_t bar, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile("{\n\t.reg .pred p;\n\t"
+                 "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n\t"
+                 "selp.u32 %0, 1, 0, p;\n\t}"
+                 : "=r"(ok) : "r"(bar), "r"(parity), "r"(hint_ns) : "memory");
+    return ok != 0;
+}
 __device__ inline uint64_t globaltimer_ns() {
     uint64_t t;
     asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
@@ -593,9 +613,23 @@ __device__ inline uint64_t globaltimer_ns() {
 
 // Bounded wait: gives up after ~`limit_ns` and returns false. A wait that
 // gives up marks `*abort` so that later waits of the CTA return at once.
-template <bool CLUSTER_SCOPE>
+// SLEEP_NS > 0: each try sleeps up to that long while the phase is not
+// complete (mbar_try_wait_sleep), and the limit is checked after every try.
+template <bool CLUSTER_SCOPE, uint32_t SLEEP_NS = 0>
 __device__ inline bool mbar_wait_bounded(uint32_t bar, uint32_t parity, volatile int *abort,
                                          uint64_t limit_ns = 2000000000ull) {
+    if (SLEEP_NS > 0) {
+        if (CLUSTER_SCOPE ? mbar_try_wait_cluster_sleep(bar, parity, SLEEP_NS) : mbar_try_wait_sleep(bar, parity, SLEEP_NS))
+            return true;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+            if (CLUSTER_SCOPE ? mbar_try_wait_cluster_sleep(bar, parity, SLEEP_NS)
+                              : mbar_try_wait_sleep(bar, parity, SLEEP_NS))
+                return true;
+            if (*abort) return false;
+            if (globaltimer_ns() - t0 > limit_ns) { *abort = 1; return false; }
+        }
+    }
     if (CLUSTER_SCOPE ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
     uint64_t t0 = globaltimer_ns();
     for (uint32_t it = 0;; ++it) {

@@ -43,6 +43,26 @@ constexpr int kStreamMaxSlots = 12;
 constexpr int kStreamCtlBytes = 2048;  // control block after the rings
 constexpr int kStreamWSlotBytes = 8192;  // bytes per class-weight slot
 constexpr int kStreamWSlots = 3;
+// Suspend-time hints of the kernel's mbarrier waits (0: spin). The
+// producer sleeps while it waits for a free slot: a spinning producer takes
+// issue slots from the consumer warps of its scheduler (GB300, CUDA events:
+// 8192 x 128256 bf16 0.749 -> 0.745 ms, 4096 x 32000 0.102 -> 0.100 ms).
+// The consumers spin on data and on the cluster exchange (sleeping there
+// cost 8192 x 128256 2%: a sleeping warp wakes late), except with the
+// class-weight ring, whose consumers wait on it once per weight vector and
+// gain from sleeping (16384 x 256000 weighted pairs 3.92 -> 3.87 ms).
+#ifndef CE_STREAM_PRODUCER_WAIT_NS
+#define CE_STREAM_PRODUCER_WAIT_NS 5000
+#endif
+#ifndef CE_STREAM_CONSUMER_WAIT_NS
+#define CE_STREAM_CONSUMER_WAIT_NS 0
+#endif
+#ifndef CE_STREAM_WRING_CONSUMER_WAIT_NS
+#define CE_STREAM_WRING_CONSUMER_WAIT_NS 5000
+#endif
+constexpr uint32_t kStreamSleepP = CE_STREAM_PRODUCER_WAIT_NS;
+constexpr uint32_t kStreamSleepConsumer = CE_STREAM_CONSUMER_WAIT_NS;
+constexpr uint32_t kStreamSleepConsumerW = CE_STREAM_WRING_CONSUMER_WAIT_NS;
 template <int SHAPE> struct StreamShape {
     static constexpr int kWarps = SHAPE == 1 ? 16 : 8;
     static constexpr int kThreads = (kWarps + 1) * 32;
@@ -196,6 +216,7 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr int kStreamSlots = SH::kSlots;
     constexpr int kWS = SH::kWSlots;
     constexpr bool WR = kWS > 0;  // class weights of pass 2 through the weight ring
+    constexpr uint32_t kStreamSleepC = WR ? kStreamSleepConsumerW : kStreamSleepConsumer;
     static_assert(!WR || (MODE == 2 && !RAG && VEC == 8 && OPT == 0),
                   "the class-weight ring serves aligned bf16 / f16 rows with class-weighted smoothing");
     constexpr int NCT = NCW * 32;
@@ -276,7 +297,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                     for (int k = 0; k < nch; ++k, ++it) {
                         const int c = (pass == 1 && reverse) ? nch - 1 - k : k;
                         const uint32_t s = it % kStreamSlots, r = it / kStreamSlots;
-                        if (r > 0) mbar_wait_bounded<false>(smem_u32(&S.empty[s]), (r - 1) & 1u, abort);
+                        if (r > 0) mbar_wait_bounded<false, kStreamSleepP>(smem_u32(&S.empty[s]), (r - 1) & 1u, abort);
                         const int64_t off = static_cast<int64_t>(c) * kStreamChunk;
                         const uint32_t bytes =
                             static_cast<uint32_t>(gm.bytes - off < kStreamChunk ? gm.bytes - off : kStreamChunk);
@@ -288,7 +309,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             // drain: every issued copy has landed before the CTA may exit
             for (uint32_t k = 0; k < kStreamSlots && k < it; ++k) {
                 const uint32_t i = it - 1 - k;
-                mbar_wait_bounded<false>(smem_u32(&S.full[i % kStreamSlots]), (i / kStreamSlots) & 1u, abort);
+                mbar_wait_bounded<false, kStreamSleepP>(smem_u32(&S.full[i % kStreamSlots]), (i / kStreamSlots) & 1u, abort);
             }
         } else if (WR && lane == 1 && wr) {
             // class-weight producer: for every second-pass chunk, in the consumers'
@@ -309,7 +330,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                     const int nv = min(VPC, nvec - v0);
                     for (int q = 0; q * NCT < nv; ++q, ++wi) {
                         const uint32_t s = wi % kWS, r = wi / kWS;
-                        if (r > 0) mbar_wait_bounded<false>(smem_u32(&S.wempty[s]), (r - 1) & 1u, abort);
+                        if (r > 0) mbar_wait_bounded<false, kStreamSleepP>(smem_u32(&S.wempty[s]), (r - 1) & 1u, abort);
                         const int nvq = min(NCT, nv - q * NCT);
                         const uint32_t bytes = static_cast<uint32_t>(nvq * VEC * 4);
                         mbar_expect_tx(smem_u32(&S.wfull[s]), bytes);
@@ -320,7 +341,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             }
             for (uint32_t k = 0; k < static_cast<uint32_t>(kWS) && k < wi; ++k) {
                 const uint32_t i = wi - 1 - k;
-                mbar_wait_bounded<false>(smem_u32(&S.wfull[i % kWS]), (i / kWS) & 1u, abort);
+                mbar_wait_bounded<false, kStreamSleepP>(smem_u32(&S.wfull[i % kWS]), (i / kWS) & 1u, abort);
             }
         }
         __syncwarp();
@@ -374,7 +395,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             uint64_t cap_forms = 0;  // softcap: the form of chunk c (c < 32) in bits 2c, 2c+1
             for (int c = 0; c < nch; ++c, ++it) {
                 const uint32_t s = it % kStreamSlots;
-                mbar_wait_bounded<false>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
+                mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
                 const uint32_t base_s = ring + s * kStreamChunk;
                 const int v0 = c * VPC;
                 const int nv = min(VPC, nvec - v0);
@@ -573,7 +594,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                         mbar_arrive_remote(mapa_shared(my_bar, d));
                     }
                 }
-                mbar_wait_bounded<true>(my_bar, (j >> 1) & 1u, abort);
+                mbar_wait_bounded<true, kStreamSleepC>(my_bar, (j >> 1) & 1u, abort);
                 RowState tot = row_state_empty();
                 ArgMax amt{-INFINITY, 0x7fffffff};
                 for (int d = 0; d < CL; ++d) {
@@ -620,7 +641,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             for (int k = 0; k < nch; ++k, ++it) {
                 const int c = reverse ? nch - 1 - k : k;
                 const uint32_t s = it % kStreamSlots;
-                mbar_wait_bounded<false>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
+                mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
                 const uint32_t base_s = ring + s * kStreamChunk;
                 const int v0 = c * VPC;
                 const int nv = min(VPC, nvec - v0);
@@ -650,7 +671,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                     // [q NCT, (q + 1) NCT) of the chunk, thread tid's at 32 tid bytes
                     for (int q = 0; q * NCT < nv; ++q, ++wi) {
                         const uint32_t wsl = wi % kWS;
-                        mbar_wait_bounded<false>(smem_u32(&S.wfull[wsl]), (wi / kWS) & 1u, abort);
+                        mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.wfull[wsl]), (wi / kWS) & 1u, abort);
                         const int v = q * NCT + tid;
                         if (v < nv) {
                             float x[VEC], gr[VEC];
@@ -755,7 +776,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                         st_cluster_v4(rs_addr + 16u, 0.f, 0.f, 0.f, 0.f);
                         mbar_arrive_remote(mapa_shared(my_bar, d));
                     }
-                    mbar_wait_bounded<true>(my_bar, (j >> 1) & 1u, abort);
+                    mbar_wait_bounded<true, kStreamSleepC>(my_bar, (j >> 1) & 1u, abort);
                     RowState tot = row_state_empty();
                     for (int d = 0; d < CL; ++d) {
                         const StreamXSlot &xs = S.slot[par][d];

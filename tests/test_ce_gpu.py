@@ -522,10 +522,10 @@ def test_stream_tuning_variants(ce, tune, shape):
 @pytest.mark.parametrize("shape", [(40, 64000), (24, 128256), (12, 250000), (9, 8200)])
 def test_class_weight_ring_and_its_fallbacks(ce, dtype, w_offset, shape):
     """Class-weighted smoothing on the automatic path: weights starting on a
-    16-byte boundary go through the shared-memory weight ring (single rows,
-    pairs and quads by row size); weights at a 4- or 8-byte offset take the
-    per-lane loads instead. Both against the oracle, and bit-identical to each
-    other."""
+    16-byte boundary go through the shared-memory weight ring (one CTA per row
+    or a pair, by row size) and give the same bits as the per-lane loads with
+    the same row split; weights at a 4- or 8-byte offset take the per-lane
+    loads. All against the oracle."""
     R, V = shape
     seed = zlib.crc32(repr((dtype, w_offset, shape)).encode()) % 9973
     x = make_logits(R, V, dtype, 1.5, seed, device="cuda")
@@ -540,9 +540,12 @@ def test_class_weight_ring_and_its_fallbacks(ce, dtype, w_offset, shape):
     loss = ce.ce_fwd_bwd(x, t, weight=w, label_smoothing=0.05, reduction="sum", grad_output=g)
     torch.cuda.synchronize()
     _check_all(x, t, w, 0.05, "sum", g, ref, loss, x_in)
-    # the per-lane-load path on the same inputs (three CTAs per SM, pairs or quads as chosen by row size)
+    if w_offset != 0:
+        return
+    # the per-lane-load path on the same inputs with the same row split (one CTA
+    # per row up to 288 KB rows, a pair beyond): bit-identical
     row_kb = V * 2 / 1024
-    tune = 16 | 4 | (2 if row_kb > 176 else 0) | (8 if 176 < row_kb <= 288 else 0) | (32 if row_kb > 288 else 0)
+    tune = 16 | 4 if row_kb <= 288 else 16 | 8 | 4 | 2
     loss2 = ce.ce_fwd_bwd(x2, t, weight=w, label_smoothing=0.05, reduction="sum", grad_output=g, variant="stream",
                           tune=tune)
     torch.cuda.synchronize()
