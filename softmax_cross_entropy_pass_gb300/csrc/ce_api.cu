@@ -108,6 +108,20 @@ RowArgs row_args(const ce_params *p, const void *target, void *ws) {
     return a;
 }
 
+// The forward (row statistics and losses) of ce_forward and the split path:
+// the stream kernel's first pass (bulk-copy ring: the bytes in flight are
+// not limited by registers) where it applies, the register row kernel for
+// class-weighted smoothing and the options.
+cudaError_t launch_forward(const RowArgs &a0, const ce_params *p, cudaStream_t s) {
+    const int mode = smoothing_mode(p);
+    if (mode != 2 && !has_options(p)) {
+        RowArgs a = a0;
+        a.grad = const_cast<void *>(a0.logits);  // read only in this kernel
+        return launch_stream_forward(a, p->dtype, mode, (p->variant & CE_VARIANT_PREPARED) == 0, s);
+    }
+    return launch_stats(a0, p->dtype, mode, row_grid(p->n_rows), s);
+}
+
 // ---------------------------------------------------------------- fused plan cache
 std::mutex g_plan_mu;
 std::map<std::tuple<int, int, int, int64_t, int64_t, int>, std::pair<bool, FusedPlan>> g_plans;
@@ -220,7 +234,7 @@ ce_status ce_forward(const ce_params *p, const void *logits, const void *target,
     a.logits = logits;
     a.loss = loss;
     a.stats = stats;
-    e = launch_stats(a, p->dtype, smoothing_mode(p), row_grid(p->n_rows), s);
+    e = launch_forward(a, p, s);
     return e == cudaSuccess ? CE_OK : cuda_fail(e);
 }
 
@@ -321,7 +335,7 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
         a.logits = logits_inout;
         a.loss = loss;
         a.stats = ws_stats(ws, p->n_rows);
-        e = launch_stats(a, p->dtype, smoothing_mode(p), row_grid(p->n_rows), s);
+        e = launch_forward(a, p, s);
         if (e != cudaSuccess) return cuda_fail(e);
         a.grad = logits_inout;
         a.grad_output = grad_output;

@@ -108,6 +108,11 @@ cudaError_t launch_reduce_row_losses(const float *row_loss, int64_t n, int reduc
                                      cudaStream_t s);
 cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm, int tune, bool after_prep,
                           cudaStream_t s);
+// The forward only (row statistics and losses) by the stream kernel's first
+// pass: every row read once through the bulk-copy ring, one CTA per row.
+// a.grad holds the logits (read only), a.stats the [n_rows][4] output or
+// NULL. `mode` 0 or 1 (no class-weighted smoothing), no options.
+cudaError_t launch_stream_forward(const RowArgs &a, int dtype, int mode, bool after_prep, cudaStream_t s);
 
 // Fused kernel plan / launch. `mode`: 0 no smoothing, 1 smoothing, 2 weighted smoothing.
 struct FusedPlan {

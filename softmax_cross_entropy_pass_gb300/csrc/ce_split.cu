@@ -260,7 +260,9 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
     const bool want_am = FEAT && a.accuracy != nullptr;
     WsCtl *ctl = a.ctl;
     const float inv_v = 1.f / static_cast<float>(a.vocab);
-    pdl_wait();
+    // the normalisers (and the zeroed counters) of the normaliser kernel are
+    // waited for where they are first read, so the logits stream starts at once
+    bool have_norm = false;
 
     for (int64_t row = blockIdx.x; row < a.n_rows; row += gridDim.x) {
         const char *rowp = reinterpret_cast<const char *>(a.logits) + row * a.ld * F::kBytes;
@@ -287,10 +289,58 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
         const uint4 *vp = reinterpret_cast<const uint4 *>(rowp + head * F::kBytes);
         for (int64_t v0 = threadIdx.x; v0 < nvec; v0 += static_cast<int64_t>(blockDim.x) * UNROLL) {
             uint4 raw[UNROLL];
+            bool ok[UNROLL];
+            bool has_y = false;  // does one of these vectors hold the target column?
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u) {
-                int64_t v = v0 + static_cast<int64_t>(u) * blockDim.x;
-                if (v < nvec) raw[u] = ld_stream_ro(vp + v);
+                const int64_t v = v0 + static_cast<int64_t>(u) * blockDim.x;
+                ok[u] = v < nvec;
+                if (ok[u]) raw[u] = ld_stream_ro(vp + v);
+                has_y |= ok[u] && static_cast<uint64_t>(y - (head + v * VEC)) < static_cast<uint64_t>(VEC);
+            }
+            if (MODE != 2 && !FEAT && !has_y) {
+                // one maximum for the group, then the exp-sum over packed fp32 pairs in
+                // two independent accumulators (and the smoothing sum likewise)
+                float gm = -INFINITY;
+                int nok = 0;
+#pragma unroll
+                for (int u = 0; u < UNROLL; ++u) {
+                    if (!ok[u]) continue;
+                    gm = fmaxf(gm, F::vmax(raw[u]));
+                    ++nok;
+                }
+                if (gm > st.m) {
+                    if (st.m != -INFINITY) st.s *= ex2_hw((st.m - gm) * kLog2e);
+                    st.m = gm;
+                }
+                const float mL = st.m * kLog2e;
+                const F2 l2 = f2(kLog2e, kLog2e), nm = f2(-mL, -mL);
+                F2 acc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)}, racc[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};
+#pragma unroll
+                for (int u = 0; u < UNROLL; ++u) {
+                    if (!ok[u]) continue;
+                    float x[VEC];
+                    F::unpack(raw[u], x);
+#pragma unroll
+                    for (int p = 0; p < VEC / 2; ++p) {
+                        const F2 xx = f2(x[2 * p], x[2 * p + 1]);
+                        if (SMOOTH) racc[p & 1] = f2_add(racc[p & 1], xx);
+                        acc[p & 1] = f2_add(acc[p & 1], f2_ex2(f2_fma(xx, l2, nm)));
+                    }
+                }
+                float a0, a1, a2, a3;
+                if (SMOOTH) {
+                    f2_split(racc[0], a0, a1);
+                    f2_split(racc[1], a2, a3);
+                    st.r += (a0 + a1) + (a2 + a3);
+                    st.n += static_cast<float>(nok * VEC);
+                }
+                if (st.m != -INFINITY) {  // every value so far -inf: nothing to add
+                    f2_split(acc[0], a0, a1);
+                    f2_split(acc[1], a2, a3);
+                    st.s += (a0 + a1) + (a2 + a3);
+                }
+                continue;
             }
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u) {
@@ -314,6 +364,10 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
         }
         st = block_merge(st, sh);
         if (threadIdx.x == 0) {
+            if (!have_norm) {
+                pdl_wait();
+                have_norm = true;
+            }
             float xy = valid ? F::load1(rowp, y) : 0.f;
             if (FEAT && cap > 0.f) xy = softcap_logit(xy, cap);
             const float wy = valid ? (a.weight ? __ldg(a.weight + y) : 1.f) : 0.f;
@@ -331,7 +385,10 @@ __global__ void __launch_bounds__(kRowThreads, 3) ce_stats_kernel(RowArgs a) {
         }
         __syncthreads();
     }
-    if (a.reduction != CE_RED_NONE || (FEAT && a.accuracy)) finish_loss(a, ctl, gridDim.x);
+    if (a.reduction != CE_RED_NONE || (FEAT && a.accuracy)) {
+        pdl_wait();
+        finish_loss(a, ctl, gridDim.x);
+    }
 }
 
 // ------------------------------------------------------------------ backward: gradient in place

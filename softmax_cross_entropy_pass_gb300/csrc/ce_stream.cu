@@ -76,7 +76,7 @@ static const void *stream_kernel_wring(int dtype) {
 
 template <int SHAPE, int CL>
 static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, int ctas_per_sm, int tune,
-                                       bool after_prep, cudaStream_t s) {
+                                       bool after_prep, cudaStream_t s, bool fwd = false) {
     using SH = StreamShape<SHAPE>;
     RowArgs a = a0;
     // rows that all start on a 16-byte boundary take the fixed-geometry instantiation
@@ -84,7 +84,10 @@ static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, i
     const bool ragged = (reinterpret_cast<uintptr_t>(a.grad) & 15u) != 0 || (a.n_rows > 1 && ((a.ld * esz) & 15) != 0);
     const bool opts = a.softcap > 0.f || a.z_loss > 0.f || a.accuracy;
     const void *fn = nullptr;
-    if constexpr (SHAPE == 3) {
+    if (fwd) {
+        if (SHAPE != 2 || CL != 1 || mode == 2 || opts) return cudaErrorInvalidValue;
+        fn = stream_kernel_forward(dtype, mode, ragged);
+    } else if constexpr (SHAPE == 3) {
         // the weight ring copies whole 32-byte weight vectors from 16-byte aligned weights
         const bool ok = mode == 2 && !ragged && !opts && dtype != CE_DT_F32 && a.weight &&
                         (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
@@ -143,6 +146,12 @@ static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, i
     return cudaLaunchKernelExC(&cfg, fn, args);
 }
 
+// The forward only: one CTA per row and three CTAs per SM (rows are read
+// once, so nothing waits in L2 and a pair's exchange would only add work).
+cudaError_t launch_stream_forward(const RowArgs &a, int dtype, int mode, bool after_prep, cudaStream_t s) {
+    return launch_stream_shape<2, 1>(a, dtype, mode, 0, kTuneThree | kTuneNoKeep, after_prep, s, true);
+}
+
 cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm, int tune, bool after_prep,
                           cudaStream_t s) {
     // Library choice by row size (GB300 measurements, CUDA events, L2 flushed):
@@ -179,17 +188,19 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     const bool opts = a.softcap > 0.f || a.z_loss > 0.f || a.accuracy;
     // Class-weighted smoothing on aligned bf16 / f16 rows: the class weights of
     // the second pass go through the shared-memory weight ring, with one CTA
-    // per row up to 288 KB rows and a pair per row up to 640 KB (GB300, CUDA
-    // events: 8192 x 64000 0.525 ms against 0.538 for the per-lane loads;
-    // 8192 x 128256 1.004 against 1.020 ms (pairs) and 1.053 for ring pairs;
-    // 16384 x 256000 3.92 ms against 4.14 (quads) and 4.33 for ring quads).
+    // per row up to 288 KB rows and a pair per row up to 640 KB, the second
+    // pass last chunk first (GB300, CUDA events: 8192 x 64000 0.525 ms
+    // against 0.538 for the per-lane loads; 8192 x 128256 1.004 against
+    // 1.020 ms (pairs) and 1.053 for ring pairs, 0.995 with the reversed
+    // second pass; 16384 x 256000 3.92 ms against 4.14 (quads) and 4.33 for
+    // ring quads, 4.47 with two CTAs per SM).
     const int64_t esz = dtype == CE_DT_F32 ? 4 : 2;
     const bool ragged = (reinterpret_cast<uintptr_t>(a.grad) & 15u) != 0 || (a.n_rows > 1 && ((a.ld * esz) & 15) != 0);
     const bool wring_ok = mode == 2 && !opts && dtype != CE_DT_F32 && !ragged && a.weight &&
                           (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
     if (tune == 0 && wring_ok) {
         const int64_t row_bytes = a.vocab * esz;
-        tune = row_bytes <= 288 * 1024 ? (kTuneThree | kTuneNoKeep | kTuneWRing)
+        tune = row_bytes <= 288 * 1024 ? (kTuneThree | kTuneNoKeep | kTuneReverse | kTuneWRing)
              : row_bytes <= 640 * 1024 ? (kTuneThree | kTuneCluster2 | kTuneNoKeep | kTuneReverse | kTuneWRing)
                                        : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
     }

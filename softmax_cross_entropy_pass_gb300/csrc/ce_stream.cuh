@@ -38,7 +38,13 @@ namespace ce {
 // bulk-copies the fp32 weights of each second-pass chunk into shared memory
 // (8 KB per slot, one weight vector per consumer thread), so the gradient
 // loop reads them from shared memory instead of waiting on per-lane loads.
-constexpr int kStreamChunk = 16384;  // bytes per ring slot
+#ifndef CE_STREAM_CHUNK_BYTES
+#define CE_STREAM_CHUNK_BYTES 16384
+#endif
+#ifndef CE_STREAM_SLOTS_3CTA
+#define CE_STREAM_SLOTS_3CTA 4
+#endif
+constexpr int kStreamChunk = CE_STREAM_CHUNK_BYTES;  // bytes per ring slot
 constexpr int kStreamMaxSlots = 12;
 constexpr int kStreamCtlBytes = 2048;  // control block after the rings
 constexpr int kStreamWSlotBytes = 8192;  // bytes per class-weight slot
@@ -66,7 +72,7 @@ constexpr uint32_t kStreamSleepConsumerW = CE_STREAM_WRING_CONSUMER_WAIT_NS;
 template <int SHAPE> struct StreamShape {
     static constexpr int kWarps = SHAPE == 1 ? 16 : 8;
     static constexpr int kThreads = (kWarps + 1) * 32;
-    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : (SHAPE == 2 ? 4 : 3));
+    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : (SHAPE == 2 ? CE_STREAM_SLOTS_3CTA : 3));
     static constexpr int kCtasPerSm = SHAPE == 0 ? 2 : (SHAPE == 1 ? 1 : 3);
     static constexpr int kWSlots = SHAPE == 3 ? kStreamWSlots : 0;  // class-weight ring
     static constexpr int kSmem = kSlots * kStreamChunk + kWSlots * kStreamWSlotBytes + kStreamCtlBytes;
@@ -246,8 +252,12 @@ ce_stream_kernel(RowArgs a, int tune) {
     const bool w_base16 = (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
     const bool w_base32 = (reinterpret_cast<uintptr_t>(a.weight) & 31u) == 0;
     const RowGeom g_aligned = row_geom_aligned<F::kBytes>(lo, L);
-    constexpr bool FEAT = OPT != 0;
+    // OPT 3: the forward only (ce_forward): one pass over every row, ignored
+    // rows included, writing the row statistics and losses; no options
+    constexpr bool FWD = OPT == 3;
+    constexpr bool FEAT = OPT == 1 || OPT == 2;
     constexpr bool CAPF = OPT == 2;
+    static_assert(!FWD || (MODE != 2 && CL == 1), "the forward-only kernel: one CTA per row, no class-weighted smoothing");
     const float cap = CAPF ? a.softcap : 0.f;
     const float inv_cap = CAPF && cap > 0.f ? 1.f / cap : 0.f;
     const float nic2 = -(inv_cap * inv_cap);
@@ -287,12 +297,12 @@ ce_stream_kernel(RowArgs a, int tune) {
             for (int64_t row = q0; row < a.n_rows; row += nq) {
                 const int64_t t = t_next;
                 if (row + nq < a.n_rows) t_next = load_target(a.target, a.tgt32, row + nq);
-                if (!target_valid(t, a.ignore_index, V)) continue;
+                if (!FWD && !target_valid(t, a.ignore_index, V)) continue;
                 const char *slice = xbase + row * row_bytes + lo * F::kBytes;
                 const RowGeom gm = RAG ? row_geom<F::kBytes>(slice, lo, L) : g_aligned;
                 const char *src = slice + static_cast<int64_t>(gm.nhead) * F::kBytes;
                 const int nch = gm.nch;
-                for (int pass = 0; pass < 2; ++pass) {
+                for (int pass = 0; pass < (FWD ? 1 : 2); ++pass) {
                     const uint64_t pol = pass == 0 ? keep : drop;
                     for (int k = 0; k < nch; ++k, ++it) {
                         const int c = (pass == 1 && reverse) ? nch - 1 - k : k;
@@ -372,7 +382,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             uint4 *vp = reinterpret_cast<uint4 *>(rowp + vlo * F::kBytes);
             const bool w4 = w_base16 && (vlo & 3) == 0;
             const bool w8 = VEC == 8 && w_base32 && (vlo & 7) == 0;  // 8 weights per vector, one load
-            if (!valid) {
+            if (!valid && !FWD) {
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 for (int v = tid; v < nvec; v += NCT) st_stream(vp + v, z);
                 if (tid < nedge) F::store1(rowp, edge_c, 0.f);
@@ -382,13 +392,14 @@ ce_stream_kernel(RowArgs a, int tune) {
                 }
                 continue;
             }
-            const int yg = static_cast<int>(t);                 // target column in the row
-            const uint32_t rp = j & 1u;                         // parity of this valid row
+            // (the forward-only kernel reads ignored rows too: no target column there)
+            const int yg = valid ? static_cast<int>(t) : 0;     // target column in the row
+            const uint32_t rp = j & 1u;                         // parity of this row
             // target column relative to the interior (far outside when it is not in it)
-            const int y = (t >= vlo && t < gm.tail0) ? static_cast<int>(t - vlo) : -(1 << 30);
+            const int y = (valid && t >= vlo && t < gm.tail0) ? static_cast<int>(t - vlo) : -(1 << 30);
             // per-row values the merge needs, fetched now so their latency hides under pass 1
             const float g_row = (a.grad_output && a.reduction == CE_RED_NONE) ? __ldg(a.grad_output + row) : 0.f;
-            const float wy = a.weight ? __ldg(a.weight + yg) : 1.f;
+            const float wy = (valid && a.weight) ? __ldg(a.weight + yg) : 1.f;
             // ------------------------------------------------ pass 1: statistics
             RowState st = row_state_empty();
             ArgMax am{-INFINITY, 0x7fffffff};
@@ -546,8 +557,8 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const float xr = F::load1(rowp, c);
                 float x = (CAPF && cap > 0.f) ? softcap_fast(xr, cap, inv_cap) : xr;
                 if (want_am) am = argmax_merge(am, ArgMax{xr, static_cast<int>(c)});
-                if (c == yg) S.xy[rp] = x;
-                row_state_add<1, P1S>(st, &x, x, (c == yg) ? 0 : -1, nullptr);
+                if (valid && c == yg) S.xy[rp] = x;
+                row_state_add<1, P1S>(st, &x, x, (valid && c == yg) ? 0 : -1, nullptr);
             }
             // ------------------------------------------------ merge and row scalars
             // Every warp merges the CTA's partials and forms the row scalars itself
@@ -563,7 +574,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             stream_consumer_sync<NCW>();
             RowState m = lane < kStreamConsumerWarps ? S.red[rp][lane] : row_state_empty();
             m = warp_merge(m);
-            float xy = S.xy[rp];
+            float xy = valid ? S.xy[rp] : 0.f;
             if (want_am) {
                 am = lane < kStreamConsumerWarps ? S.am[rp][lane] : ArgMax{-INFINITY, 0x7fffffff};
                 am = warp_argmax(am);
@@ -627,9 +638,15 @@ ce_stream_kernel(RowArgs a, int tune) {
             float scale = g;
             if (a.reduction == CE_RED_MEAN) scale = w_y_sum != 0.f ? g / w_y_sum : 0.f;
             if (writer && rank == 0 && !DEFER) {
-                const RowScalars rl = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f, zl);
+                const RowScalars rl = make_row_scalars(m.m, m.s, xy, rrel, valid, yg, wy, w_all, eps, inv_v, 1.f, zl);
                 if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
                 else a.row_loss[row] = rl.loss;
+                // the row statistics {m, s without the target column, x_y, sum w (x - m)}
+                if (FWD && a.stats) reinterpret_cast<float4 *>(a.stats)[row] = make_float4(m.m, m.s, xy, rrel);
+            }
+            if (FWD) {
+                ++j;
+                continue;  // no second pass
             }
             if (want_am && writer && rank == 0 && am.i == yg) atomicAdd(&a.ctl->n_correct, 1u);
             const RowScalars rs = make_row_scalars(m.m, m.s, xy, rrel, true, yg, wy, w_all, eps, inv_v, scale, zl);
@@ -871,11 +888,12 @@ const void *stream_kernel_options_for(int dtype, int mode, int shape, int cl) {
 #undef CE_STREAM_PICK
 
 // defined in ce_stream_ragged.cu, ce_stream_options.cu, ce_stream_options_ragged.cu,
-// ce_stream_softcap.cu and ce_stream_softcap_ragged.cu
+// ce_stream_softcap.cu, ce_stream_softcap_ragged.cu and ce_stream_forward.cu
 const void *stream_kernel_ragged(int dtype, int mode, int shape, int cl);
 const void *stream_kernel_options(int dtype, int mode, int shape, int cl, bool ragged);
 const void *stream_kernel_options_ragged(int dtype, int mode, int shape, int cl);
 const void *stream_kernel_softcap(int dtype, int mode, int shape, int cl, bool ragged);
 const void *stream_kernel_softcap_ragged(int dtype, int mode, int shape, int cl);
+const void *stream_kernel_forward(int dtype, int mode, bool ragged);
 
 }  // namespace ce
