@@ -38,13 +38,7 @@ namespace ce {
 // bulk-copies the fp32 weights of each second-pass chunk into shared memory
 // (8 KB per slot, one weight vector per consumer thread), so the gradient
 // loop reads them from shared memory instead of waiting on per-lane loads.
-#ifndef CE_STREAM_CHUNK_BYTES
-#define CE_STREAM_CHUNK_BYTES 16384
-#endif
-#ifndef CE_STREAM_SLOTS_3CTA
-#define CE_STREAM_SLOTS_3CTA 4
-#endif
-constexpr int kStreamChunk = CE_STREAM_CHUNK_BYTES;  // bytes per ring slot
+constexpr int kStreamChunk = 16384;  // bytes per ring slot
 constexpr int kStreamMaxSlots = 12;
 constexpr int kStreamCtlBytes = 2048;  // control block after the rings
 constexpr int kStreamWSlotBytes = 8192;  // bytes per class-weight slot
@@ -72,7 +66,7 @@ constexpr uint32_t kStreamSleepConsumerW = CE_STREAM_WRING_CONSUMER_WAIT_NS;
 template <int SHAPE> struct StreamShape {
     static constexpr int kWarps = SHAPE == 1 ? 16 : 8;
     static constexpr int kThreads = (kWarps + 1) * 32;
-    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : (SHAPE == 2 ? CE_STREAM_SLOTS_3CTA : 3));
+    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : (SHAPE == 2 ? 4 : 3));
     static constexpr int kCtasPerSm = SHAPE == 0 ? 2 : (SHAPE == 1 ? 1 : 3);
     static constexpr int kWSlots = SHAPE == 3 ? kStreamWSlots : 0;  // class-weight ring
     static constexpr int kSmem = kSlots * kStreamChunk + kWSlots * kStreamWSlotBytes + kStreamCtlBytes;
