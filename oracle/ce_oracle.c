@@ -338,14 +338,6 @@ int ce_oracle_rows_ex(const void *logits, int dtype, int64_t n_rows, int64_t voc
     return rc == 3 ? 0 : rc;
 }
 
-/* ce_oracle_rows with the options (softcap, z-loss, argmax output). */
-int ce_oracle_rows_ex(const void *logits, int dtype, int64_t n_rows, int64_t vocab, int64_t ld,
-                      const void *target, int target_is_int32, int64_t ignore_index,
-                      const double *class_weight, double label_smoothing, int reduction,
-                      const double *grad_output, int grad_output_per_row, double norm_wy,
-                      double w_all, double *row_loss, double *stats, double *grad, int n_threads,
-                      double softcap, double z_loss, int64_t *argmax);
-
 /* mean: sum / norm_wy (0 when norm_wy is 0), sum: sum, none: not reduced. */
 double ce_oracle_reduce(const double *row_loss, int64_t n_rows, int reduction, double norm_wy)
 {

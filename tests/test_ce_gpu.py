@@ -494,6 +494,43 @@ def test_tiny_config(ce):
     _check_all(x, t, None, 0.0, "mean", None, ref, loss, x_in)
 
 
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "f16"])
+@pytest.mark.parametrize("shape", RAGGED + [(33, 32000, 32000, 0), (6, 128256, 128256, 0), (5, 24, 24, 0)],
+                         ids=lambda s: f"{s[0]}x{s[1]}ld{s[2]}@{s[3]}")
+@pytest.mark.parametrize("opt", ["plain", "smooth"])
+@pytest.mark.parametrize("red", ["mean", "none"])
+def test_forward_statistics_every_row(ce, dtype, shape, opt, red):
+    """ce_forward by the stream kernel's first pass: the statistics of every
+    row, ignored ones included (max and off-target exp-sum over all columns,
+    x_y = 0), and the losses, against the oracle; rows that start off a
+    16-byte boundary, and ignored rows whose placeholder column 0 sits in a
+    row's unaligned head."""
+    R, V, ld, off = shape
+    seed = zlib.crc32(repr((dtype, shape, opt, red)).encode()) % 9973
+    base = make_logits(R, ld + off, dtype, 2.0, seed, device="cuda")
+    x = base[:, off:off + V]
+    t = make_targets(R, V, 0.3, seed, device="cuda")
+    t[0] = -100                                   # an ignored first row
+    if R > 2:
+        t[2] = 0                                  # a valid row whose target is column 0
+    eps = 0.1 if opt == "smooth" else 0.0
+    ref = oracle.ce(x.cpu(), t.cpu(), label_smoothing=eps, reduction=red, want_grad=False)
+    loss, stats = ce.ce_forward(x, t, label_smoothing=eps, reduction=red)
+    torch.cuda.synchronize()
+    if red == "none":
+        check_loss_rows(loss.cpu(), ref["row_loss"])
+    else:
+        check_loss_reduced(float(loss.item()), ref["loss"])
+    st = stats.cpu().double()
+    valid = t.cpu() >= 0
+    assert torch.equal(st[:, 0], ref["stats"][:, 0].float().double())          # the max is exact
+    assert torch.equal(st[valid, 2], ref["stats"][valid, 2].float().double())  # x_y is exact
+    assert torch.all(st[~valid, 2] == 0)
+    assert torch.allclose(st[:, 1], ref["stats"][:, 1], rtol=2e-5, atol=0)    # exp-sum, all columns when ignored
+    # the logits are read only
+    assert torch.equal(x.cpu(), make_logits(R, ld + off, dtype, 2.0, seed, device="cuda")[:, off:off + V].cpu())
+
+
 @pytest.mark.parametrize("tune", [0, 1, 2, 3, 4, 8, 9, 10, 12, 15, 16, 24, 26, 48, 52, 54, 80, 86, 88, 94, 112,
                                   118, 119])
 @pytest.mark.parametrize("shape", [(70, 128256), (33, 33008), (9, 256000), (5, 1000), (6, 40), (4, 24)])
