@@ -177,14 +177,15 @@ __device__ inline void load_w8(const float *p, float4 &lo, float4 &hi) {
                  : "l"(p));
 }
 
-// The loss of a row whose class-weighted smoothing sums (r = sum w x,
-// n = sum w over the whole row) arrived after its gradient pass; written by
+// The loss of a row whose class-weighted smoothing sum (r = sum w x over the
+// whole row) arrived after its gradient pass; the weight sum over the row is
+// W_all, the normaliser kernel's (fp64) sum of the class weights; written by
 // the first CTA of the row.
 __device__ inline void finish_deferred_loss(const RowArgs &a, uint32_t rank, int64_t row, float m, float s, float xy,
-                                            float r, float n, int yg, float wy, float w_all, float eps,
+                                            float r, int yg, float wy, float w_all, float eps,
                                             float inv_v, float z_loss) {
     if (rank != 0) return;
-    const float rrel = n > 0.f ? __fsub_rn(r, __fmul_rn(n, m)) : 0.f;
+    const float rrel = w_all > 0.f ? __fsub_rn(r, __fmul_rn(w_all, m)) : 0.f;
     const RowScalars rl = make_row_scalars(m, s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f, z_loss);
     if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
     else a.row_loss[row] = rl.loss;
@@ -622,7 +623,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             const bool writer = warp == 0 && lane == 0;
             if (DEFER) {
                 if (writer) {
-                    if (pend) finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, m.r, m.n,
+                    if (pend) finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, m.r,
                                                    pend_yg, pend_wy, w_all, eps, inv_v, zl);
                     pend_row = row; pend_m = m.m; pend_s = m.s; pend_xy = xy; pend_yg = yg; pend_wy = wy;
                 }
@@ -647,7 +648,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             // grad_elem over packed pairs: p = 2^((x - m) log2e - log2 d), g = a p - b w
             const F2 rs_m = f2(rs.m, rs.m), rs_l2 = f2(kLog2e, kLog2e), rs_nl = f2(rs.neg_log2d, rs.neg_log2d);
             const F2 rs_a = f2(rs.a, rs.a), rs_nb = f2(-rs.b, -rs.b);
-            F2 dr[2] = {f2(0.f, 0.f), f2(0.f, 0.f)}, dn[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // deferred sums
+            F2 dr[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // deferred smoothing sum of w x
             // ------------------------------------------------ pass 2: gradient in place
             for (int k = 0; k < nch; ++k, ++it) {
                 const int c = reverse ? nch - 1 - k : k;
@@ -671,8 +672,6 @@ ce_stream_kernel(RowArgs a, int tune) {
                         const F2 p1 = f2_ex2(f2_fma(f2_sub(x23, rs_m), rs_l2, rs_nl));
                         dr[0] = f2_fma(w01, x01, dr[0]);
                         dr[1] = f2_fma(w23, x23, dr[1]);
-                        dn[0] = f2_add(dn[0], w01);
-                        dn[1] = f2_add(dn[1], w23);
                         f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
                         f2_split(f2_fma(p1, rs_a, nbw1), gr[4 * h + 2], gr[4 * h + 3]);
                     }
@@ -739,32 +738,26 @@ ce_stream_kernel(RowArgs a, int tune) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
             }
-            float er = 0.f, en = 0.f;
+            float er = 0.f;
             if (tid < nedge) {
                 const int64_t c = edge_c;
                 const float wc = (MODE == 2) ? __ldg(a.weight + c) : 1.f;
                 const float xr = F::load1(rowp, c);
                 const float xe = (CAPF && cap > 0.f) ? softcap_fast(xr, cap, inv_cap) : xr;
                 er = wc * xe;
-                en = wc;
                 float ge = (c == yg) ? rs.dxy : grad_elem(rs, xe, wc);
                 if (CAPF && cap > 0.f) ge *= fmaf(xe * xe, nic2, 1.f);
                 F::store1(rowp, c, ge);
             }
             if (DEFER) {
-                // this thread's, then this warp's, deferred sums (fixed order), for the next merge
-                float r0, r1, r2, r3, n0, n1, n2, n3;
+                // this thread's, then this warp's, deferred sum (fixed order), for the next merge
+                float r0, r1, r2, r3;
                 f2_split(dr[0], r0, r1);
                 f2_split(dr[1], r2, r3);
-                f2_split(dn[0], n0, n1);
-                f2_split(dn[1], n2, n3);
-                float rr = ((r0 + r1) + (r2 + r3)) + er, nn = ((n0 + n1) + (n2 + n3)) + en;
+                float rr = ((r0 + r1) + (r2 + r3)) + er;
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    rr += __shfl_xor_sync(0xffffffffu, rr, off);
-                    nn += __shfl_xor_sync(0xffffffffu, nn, off);
-                }
-                if (lane == 0) S.defer[rp][warp] = make_float2(rr, nn);
+                for (int off = 16; off > 0; off >>= 1) rr += __shfl_xor_sync(0xffffffffu, rr, off);
+                if (lane == 0) S.defer[rp][warp] = make_float2(rr, 0.f);
             }
             pend = true;
             ++j;
@@ -796,7 +789,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                     pr = tot.r;
                     pn = tot.n;
                 }
-                finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, pr, pn, pend_yg, pend_wy, w_all,
+                finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, pr, pend_yg, pend_wy, w_all,
                                      eps, inv_v, zl);
             }
         }
