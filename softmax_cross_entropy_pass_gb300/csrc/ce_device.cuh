@@ -58,6 +58,7 @@ template <int DT> struct Fmt;
 template <> struct Fmt<CE_DT_F32> {
     static constexpr int kVec = 4;
     static constexpr int kBytes = 4;
+    static constexpr uint32_t kNegInfWord = 0xff800000u;  // one -inf
     __device__ static inline void unpack(const uint4 &v, float *x) {
         x[0] = __uint_as_float(v.x); x[1] = __uint_as_float(v.y);
         x[2] = __uint_as_float(v.z); x[3] = __uint_as_float(v.w);
@@ -86,6 +87,7 @@ template <> struct Fmt<CE_DT_F32> {
 template <> struct Fmt<CE_DT_BF16> {
     static constexpr int kVec = 8;
     static constexpr int kBytes = 2;
+    static constexpr uint32_t kNegInfWord = 0xff80ff80u;  // two -inf (bf16)
     __device__ static inline void unpack2(uint32_t u, float &lo, float &hi) {
         lo = __uint_as_float(u << 16);
         hi = __uint_as_float(u & 0xffff0000u);
@@ -129,6 +131,7 @@ template <> struct Fmt<CE_DT_BF16> {
 template <> struct Fmt<CE_DT_F16> {
     static constexpr int kVec = 8;
     static constexpr int kBytes = 2;
+    static constexpr uint32_t kNegInfWord = 0xfc00fc00u;  // two -inf (f16)
     __device__ static inline void unpack2(uint32_t u, float &lo, float &hi) {
         float2 f = __half22float2(*reinterpret_cast<__half2 *>(&u));
         lo = f.x; hi = f.y;

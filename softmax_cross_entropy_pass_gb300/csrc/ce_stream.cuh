@@ -412,11 +412,26 @@ ce_stream_kernel(RowArgs a, int tune) {
                 // chunk, taken on the full-chunk path, kept for the second pass over the
                 // same vectors (the partial and target chunks take the general form here)
                 unsigned form = 0u;
-                if (nv == VPC && !mine) {
-                    // full chunk, no target: one max per chunk, four independent sums
+                // the unrolled path takes the full chunks of a thread without the
+                // target column and, with one CTA per row and no class-weighted
+                // smoothing or softcap, its partial chunk too: vectors past the end
+                // read as -inf, which adds exactly 0 to the exp-sum, and are left out
+                // of the smoothing sums (4096 x 32000: 0.1009 -> 0.0989 ms; in the pair
+                // and ring shapes the extra registers cost more than it saves)
+                const bool fullc = nv == VPC;
+                constexpr bool PARTIAL = CL == 1 && MODE != 2 && !CAPF;
+                if (!mine && (fullc || PARTIAL)) {
+                    // no target: one max per chunk, four independent sums
                     uint4 raw[VPT];
+                    bool okv[VPT];
+                    int nok = 0;  // this thread's vectors in the chunk
 #pragma unroll
-                    for (int k = 0; k < VPT; ++k) raw[k] = ld_shared_v4(base_s + 16u * (tid + k * NCT));
+                    for (int k = 0; k < VPT; ++k) {
+                        okv[k] = !PARTIAL || fullc || tid + k * NCT < nv;
+                        const uint32_t ninf = F::kNegInfWord;
+                        raw[k] = okv[k] ? ld_shared_v4(base_s + 16u * (tid + k * NCT)) : make_uint4(ninf, ninf, ninf, ninf);
+                        nok += okv[k] ? 1 : 0;
+                    }
                     if (CAPF && cap > 0.f) {
                         float ax = 0.f;
 #pragma unroll
@@ -468,7 +483,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                             for (int p = 0; p < VEC / 2; ++p) {
                                 const F2 xx = f2(x[2 * p], x[2 * p + 1]);
                                 acc[p & 1] = f2_add(acc[p & 1], f2_ex2(f2_fma(xx, l2, nm)));
-                                if (P1S) racc[p & 1] = f2_add(racc[p & 1], xx);
+                                if (P1S && okv[k]) racc[p & 1] = f2_add(racc[p & 1], xx);
                             }
                         }
                         float a0, a1, a2, a3;
@@ -479,18 +494,19 @@ ce_stream_kernel(RowArgs a, int tune) {
                             f2_split(racc[0], a0, a1);
                             f2_split(racc[1], a2, a3);
                             st.r += (a0 + a1) + (a2 + a3);
-                            st.n += static_cast<float>(VPT * VEC);
+                            st.n += static_cast<float>(nok * VEC);
                         }
                     } else if (P1S) {
 #pragma unroll
                         for (int k = 0; k < VPT; ++k) {
+                            if (!okv[k]) continue;
                             float x[VEC];
                             F::unpack(raw[k], x);
                             if (CAPF && cap > 0.f) softcap_vec_form<VEC>(x, x, cap, inv_cap, form);
 #pragma unroll
                             for (int j = 0; j < VEC; ++j) st.r += x[j];
                         }
-                        st.n += static_cast<float>(VPT * VEC);
+                        st.n += static_cast<float>(nok * VEC);
                     }
                 } else if (CAPF && cap > 0.f) {
                     // softcap, partial chunk or the target's: capped logits, first-maximum
