@@ -556,7 +556,7 @@ def test_stream_tuning_variants(ce, tune, shape):
 
 @pytest.mark.parametrize("dtype", ["bf16", "f16"])
 @pytest.mark.parametrize("w_offset", [0, 1, 2, 4])
-@pytest.mark.parametrize("shape", [(40, 64000), (24, 128256), (12, 250000), (9, 8200)])
+@pytest.mark.parametrize("shape", [(40, 64000), (24, 128256), (12, 250000), (8, 300000), (9, 8200)])
 def test_class_weight_ring_and_its_fallbacks(ce, dtype, w_offset, shape):
     """Class-weighted smoothing on the automatic path: weights starting on a
     16-byte boundary go through the shared-memory weight ring (one CTA per row
@@ -580,9 +580,9 @@ def test_class_weight_ring_and_its_fallbacks(ce, dtype, w_offset, shape):
     if w_offset != 0:
         return
     # the per-lane-load path on the same inputs with the same row split (one CTA
-    # per row up to 288 KB rows, a pair beyond): bit-identical
+    # per row up to 512 KB rows, a pair beyond): bit-identical
     row_kb = V * 2 / 1024
-    tune = 16 | 4 if row_kb <= 288 else 16 | 8 | 4 | 2
+    tune = 16 | 4 if row_kb <= 512 else 16 | 8 | 4 | 2
     loss2 = ce.ce_fwd_bwd(x2, t, weight=w, label_smoothing=0.05, reduction="sum", grad_output=g, variant="stream",
                           tune=tune)
     torch.cuda.synchronize()
