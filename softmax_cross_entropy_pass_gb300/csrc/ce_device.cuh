@@ -288,9 +288,12 @@ __device__ inline RowState row_state_merge(const RowState &a, const RowState &b)
     return o;
 }
 
+// Merge over groups of W lanes (W a power of two, at most 32): every lane
+// ends with the merge of its group, in the same order in every group.
+template <int W = 32>
 __device__ inline RowState warp_merge(RowState st) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
+    for (int off = W / 2; off > 0; off >>= 1) {
         RowState o;
         o.m = __shfl_xor_sync(0xffffffffu, st.m, off);
         o.s = __shfl_xor_sync(0xffffffffu, st.s, off);
@@ -485,9 +488,10 @@ __device__ inline ArgMax argmax_merge(const ArgMax &a, const ArgMax &b) {
     if (b.v > a.v || (b.v == a.v && b.i < a.i)) return b;
     return a;
 }
+template <int W = 32>
 __device__ inline ArgMax warp_argmax(ArgMax a) {
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
+    for (int off = W / 2; off > 0; off >>= 1) {
         ArgMax o;
         o.v = __shfl_xor_sync(0xffffffffu, a.v, off);
         o.i = __shfl_xor_sync(0xffffffffu, a.i, off);

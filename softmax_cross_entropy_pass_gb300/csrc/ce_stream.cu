@@ -186,25 +186,24 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     //  algorithmic bytes against 5.3%; 16384 x 256000: 4.93 ms against 4.50),
     //  while the second pass keeps its evict-first hint (without it 0.762 ms).
     const bool opts = a.softcap > 0.f || a.z_loss > 0.f || a.accuracy;
-    // Class-weighted smoothing on aligned bf16 / f16 rows up to 512 KB: the
-    // class weights of the second pass go through the shared-memory weight
-    // ring, one CTA per row, the second pass last chunk first (GB300, CUDA
-    // events, kernel alone: 8192 x 64000 0.525 ms against 0.538 for the
+    // Class-weighted smoothing on aligned bf16 / f16 rows: the class weights
+    // of the second pass go through the shared-memory weight ring, one CTA
+    // per row, the second pass last chunk first, at every row size (GB300,
+    // CUDA events, kernel alone: 8192 x 64000 0.525 ms against 0.538 for the
     // per-lane loads; 8192 x 128256 0.995 against 1.020 (per-lane pairs);
     // 8192 x 163840 1.195 against 1.246 for ring pairs, x 196608 1.439
     // against 1.479, x 229376 1.672 against 1.713; 16384 x 256000 3.695
     // against 3.819 for ring pairs, 4.25 for ring quads, 4.14 for per-lane
-    // quads). Its second pass misses L2 more (456 rows wait there), but a row
-    // needs no exchange between CTAs.
+    // quads; 8192 x 320000 2.371 against 2.414 for ring pairs; 4096 x 400000
+    // 1.501 against 1.513 for ring pairs and 2.183 for 16-warp per-lane
+    // pairs, x 524288 1.941 against 1.953 and 3.094). Its second pass misses
+    // L2 more (456 rows wait there), but a row needs no exchange between CTAs.
     const int64_t esz = dtype == CE_DT_F32 ? 4 : 2;
     const bool ragged = (reinterpret_cast<uintptr_t>(a.grad) & 15u) != 0 || (a.n_rows > 1 && ((a.ld * esz) & 15) != 0);
     const bool wring_ok = mode == 2 && !opts && dtype != CE_DT_F32 && !ragged && a.weight &&
                           (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
     if (tune == 0 && wring_ok) {
-        const int64_t row_bytes = a.vocab * esz;
-        tune = row_bytes <= 512 * 1024 ? (kTuneThree | kTuneNoKeep | kTuneReverse | kTuneWRing)
-             : row_bytes <= 640 * 1024 ? (kTuneThree | kTuneCluster2 | kTuneNoKeep | kTuneReverse | kTuneWRing)
-                                       : (kTuneWide | kTuneCluster2 | kTuneNoKeep);
+        tune = kTuneThree | kTuneNoKeep | kTuneReverse | kTuneWRing;
     }
     if (tune == 0) {
         const int64_t row_bytes = a.vocab * (dtype == CE_DT_F32 ? 4 : 2);

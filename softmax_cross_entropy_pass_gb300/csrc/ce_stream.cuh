@@ -24,6 +24,8 @@
 // (OPT). Every wait is bounded.
 #pragma once
 
+#include <type_traits>
+
 #include "ce_device.cuh"
 #include "ce_kernels.h"
 
@@ -43,6 +45,7 @@ constexpr int kStreamMaxSlots = 12;
 constexpr int kStreamCtlBytes = 2048;  // control block after the rings
 constexpr int kStreamWSlotBytes = 8192;  // bytes per class-weight slot
 constexpr int kStreamWSlots = 3;
+constexpr float kFoldMax = 32.f;  // |c| below which the gradient's exponent folds m into one FMA (below)
 // Suspend-time hints of the kernel's mbarrier waits (0: spin). The
 // producer sleeps while it waits for a free slot: a spinning producer takes
 // issue slots from the consumer warps of its scheduler (GB300, CUDA events:
@@ -225,6 +228,7 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr int VPT = VPC / NCT;                  // vectors per thread per full chunk
     static_assert(VPC % NCT == 0, "chunk must split evenly over the consumers");
     static_assert(CL == 1 || CL == 2 || CL == 4, "one, two or four CTAs per row");
+    static_assert((NCW & (NCW - 1)) == 0 && NCW <= 32, "the warp partials merge in groups of NCW lanes");
 
     extern __shared__ __align__(128) uint8_t smem[];
     StreamSmem &S = *reinterpret_cast<StreamSmem *>(smem + kStreamSlots * kStreamChunk + kWS * kStreamWSlotBytes);
@@ -583,12 +587,14 @@ ce_stream_kernel(RowArgs a, int tune) {
                 if (lane == 0) S.am[rp][warp] = am;
             }
             stream_consumer_sync<NCW>();
-            RowState m = lane < kStreamConsumerWarps ? S.red[rp][lane] : row_state_empty();
-            m = warp_merge(m);
+            // each group of NCW lanes holds the NCW warp partials and merges them
+            // (the same operations in every group)
+            RowState m = S.red[rp][lane & (NCW - 1)];
+            m = warp_merge<NCW>(m);
             float xy = valid ? S.xy[rp] : 0.f;
             if (want_am) {
-                am = lane < kStreamConsumerWarps ? S.am[rp][lane] : ArgMax{-INFINITY, 0x7fffffff};
-                am = warp_argmax(am);
+                am = S.am[rp][lane & (NCW - 1)];
+                am = warp_argmax<NCW>(am);
             }
             if (DEFER) {
                 // r and n of this state carry the previous row's deferred sums (this CTA's
@@ -664,96 +670,115 @@ ce_stream_kernel(RowArgs a, int tune) {
             // grad_elem over packed pairs: p = 2^((x - m) log2e - log2 d), g = a p - b w
             const F2 rs_m = f2(rs.m, rs.m), rs_l2 = f2(kLog2e, kLog2e), rs_nl = f2(rs.neg_log2d, rs.neg_log2d);
             const F2 rs_a = f2(rs.a, rs.a), rs_nb = f2(-rs.b, -rs.b);
+            // On 16-bit rows the exponent takes one packed FMA a pair, x log2e + c
+            // with c = -m log2e - log2 d (= -log2e LSE) rounded once, instead of the
+            // exact difference x - m and an FMA, while |c| < kFoldMax: rounding c then
+            // moves the exponent by at most 2^-20, no more than the rounding of the
+            // exponent itself already does where p is near the smoothing term (p ~
+            // eps / V, exponent in [-32, -16)). Other rows, fp32 gradients and softcap
+            // (whose instantiations have no registers to spare for a second loop) keep
+            // the exact form.
+            const float fold_c = fmaf(-rs.m, kLog2e, rs.neg_log2d);
+            const F2 rs_c = f2(fold_c, fold_c);
             F2 dr[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // deferred smoothing sum of w x
             // ------------------------------------------------ pass 2: gradient in place
-            for (int k = 0; k < nch; ++k, ++it) {
-                const int c = reverse ? nch - 1 - k : k;
-                const uint32_t s = it % kStreamSlots;
-                mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
-                const uint32_t base_s = ring + s * kStreamChunk;
-                const int v0 = c * VPC;
-                const int nv = min(VPC, nvec - v0);
-                const unsigned form = c < 32 ? static_cast<unsigned>(cap_forms >> (2 * c)) & 3u : 2u;
-                // class-weighted element math of one vector: p, the gradient a p - b w,
-                // and the deferred smoothing sums (the same operations whichever way
-                // the weights arrive)
-                auto weighted_vec = [&](const float *x, const float4 *wq, float *gr) {
-#pragma unroll
-                    for (int h = 0; h < VEC / 4; ++h) {
-                        const float4 wv = wq[h];
-                        const F2 w01 = f2(wv.x, wv.y), w23 = f2(wv.z, wv.w);
-                        const F2 x01 = f2(x[4 * h], x[4 * h + 1]), x23 = f2(x[4 * h + 2], x[4 * h + 3]);
-                        const F2 nbw0 = f2_mul(rs_nb, w01), nbw1 = f2_mul(rs_nb, w23);
-                        const F2 p0 = f2_ex2(f2_fma(f2_sub(x01, rs_m), rs_l2, rs_nl));
-                        const F2 p1 = f2_ex2(f2_fma(f2_sub(x23, rs_m), rs_l2, rs_nl));
-                        dr[0] = f2_fma(w01, x01, dr[0]);
-                        dr[1] = f2_fma(w23, x23, dr[1]);
-                        f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
-                        f2_split(f2_fma(p1, rs_a, nbw1), gr[4 * h + 2], gr[4 * h + 3]);
-                    }
+            auto pass2 = [&](auto fold_tag) {
+                constexpr bool FOLD = decltype(fold_tag)::value;
+                auto exp_arg = [&](F2 xx) {
+                    if constexpr (FOLD) return f2_fma(xx, rs_l2, rs_c);
+                    else return f2_fma(f2_sub(xx, rs_m), rs_l2, rs_nl);
                 };
-                if (WR && wr) {
-                    // weights from the weight ring: piece q holds the weights of vectors
-                    // [q NCT, (q + 1) NCT) of the chunk, thread tid's at 32 tid bytes
-                    for (int q = 0; q * NCT < nv; ++q, ++wi) {
-                        const uint32_t wsl = wi % kWS;
-                        mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.wfull[wsl]), (wi / kWS) & 1u, abort);
-                        const int v = q * NCT + tid;
-                        if (v < nv) {
-                            float x[VEC], gr[VEC];
-                            F::unpack(ld_shared_v4(base_s + 16u * v), x);
-                            const int vb = (v0 + v) * VEC;
-                            const uint32_t wa = wring + wsl * kStreamWSlotBytes + 32u * tid;
-                            const uint4 wlo = ld_shared_v4(wa), whi = ld_shared_v4(wa + 16u);
-                            const float4 wq[2] = {
-                                make_float4(__uint_as_float(wlo.x), __uint_as_float(wlo.y), __uint_as_float(wlo.z),
-                                            __uint_as_float(wlo.w)),
-                                make_float4(__uint_as_float(whi.x), __uint_as_float(whi.y), __uint_as_float(whi.z),
-                                            __uint_as_float(whi.w))};
-                            weighted_vec(x, wq, gr);
-                            if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
+                for (int k = 0; k < nch; ++k, ++it) {
+                    const int c = reverse ? nch - 1 - k : k;
+                    const uint32_t s = it % kStreamSlots;
+                    mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
+                    const uint32_t base_s = ring + s * kStreamChunk;
+                    const int v0 = c * VPC;
+                    const int nv = min(VPC, nvec - v0);
+                    const unsigned form = c < 32 ? static_cast<unsigned>(cap_forms >> (2 * c)) & 3u : 2u;
+                    // class-weighted element math of one vector: p, the gradient a p - b w,
+                    // and the deferred smoothing sums (the same operations whichever way
+                    // the weights arrive)
+                    auto weighted_vec = [&](const float *x, const float4 *wq, float *gr) {
 #pragma unroll
-                                for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
-                            }
-                            st_stream(vp + v0 + v, F::pack(gr));
+                        for (int h = 0; h < VEC / 4; ++h) {
+                            const float4 wv = wq[h];
+                            const F2 w01 = f2(wv.x, wv.y), w23 = f2(wv.z, wv.w);
+                            const F2 x01 = f2(x[4 * h], x[4 * h + 1]), x23 = f2(x[4 * h + 2], x[4 * h + 3]);
+                            const F2 nbw0 = f2_mul(rs_nb, w01), nbw1 = f2_mul(rs_nb, w23);
+                            const F2 p0 = f2_ex2(exp_arg(x01));
+                            const F2 p1 = f2_ex2(exp_arg(x23));
+                            dr[0] = f2_fma(w01, x01, dr[0]);
+                            dr[1] = f2_fma(w23, x23, dr[1]);
+                            f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
+                            f2_split(f2_fma(p1, rs_a, nbw1), gr[4 * h + 2], gr[4 * h + 3]);
                         }
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(smem_u32(&S.wempty[wsl]));
-                    }
-                } else {
-                for (int v = tid; v < nv; v += NCT) {
-                    float x[VEC], gr[VEC];
-                    F::unpack(ld_shared_v4(base_s + 16u * v), x);
-                    const int vb = (v0 + v) * VEC;
-                    // softcap: the capped logits replace the raw ones; dz/dx scales below
-                    if (CAPF && cap > 0.f) softcap_vec_form<VEC>(x, x, cap, inv_cap, form);
-                    if (MODE == 2) {
-                        float4 wq[VEC / 4];
-                        if (VEC == 8 && w8) {
-                            load_w8(a.weight + vlo + vb, wq[0], wq[VEC / 4 - 1]);
+                    };
+                    if (WR && wr) {
+                        // weights from the weight ring: piece q holds the weights of vectors
+                        // [q NCT, (q + 1) NCT) of the chunk, thread tid's at 32 tid bytes
+                        for (int q = 0; q * NCT < nv; ++q, ++wi) {
+                            const uint32_t wsl = wi % kWS;
+                            mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.wfull[wsl]), (wi / kWS) & 1u, abort);
+                            const int v = q * NCT + tid;
+                            if (v < nv) {
+                                float x[VEC], gr[VEC];
+                                F::unpack(ld_shared_v4(base_s + 16u * v), x);
+                                const int vb = (v0 + v) * VEC;
+                                const uint32_t wa = wring + wsl * kStreamWSlotBytes + 32u * tid;
+                                const uint4 wlo = ld_shared_v4(wa), whi = ld_shared_v4(wa + 16u);
+                                const float4 wq[2] = {
+                                    make_float4(__uint_as_float(wlo.x), __uint_as_float(wlo.y), __uint_as_float(wlo.z),
+                                                __uint_as_float(wlo.w)),
+                                    make_float4(__uint_as_float(whi.x), __uint_as_float(whi.y), __uint_as_float(whi.z),
+                                                __uint_as_float(whi.w))};
+                                weighted_vec(x, wq, gr);
+                                if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
+#pragma unroll
+                                    for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
+                                }
+                                st_stream(vp + v0 + v, F::pack(gr));
+                            }
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(smem_u32(&S.wempty[wsl]));
+                        }
+                    } else {
+                    for (int v = tid; v < nv; v += NCT) {
+                        float x[VEC], gr[VEC];
+                        F::unpack(ld_shared_v4(base_s + 16u * v), x);
+                        const int vb = (v0 + v) * VEC;
+                        // softcap: the capped logits replace the raw ones; dz/dx scales below
+                        if (CAPF && cap > 0.f) softcap_vec_form<VEC>(x, x, cap, inv_cap, form);
+                        if (MODE == 2) {
+                            float4 wq[VEC / 4];
+                            if (VEC == 8 && w8) {
+                                load_w8(a.weight + vlo + vb, wq[0], wq[VEC / 4 - 1]);
+                            } else {
+#pragma unroll
+                                for (int h = 0; h < VEC / 4; ++h) wq[h] = load_w4(a.weight, vlo + vb + 4 * h, w4);
+                            }
+                            weighted_vec(x, wq, gr);
                         } else {
 #pragma unroll
-                            for (int h = 0; h < VEC / 4; ++h) wq[h] = load_w4(a.weight, vlo + vb + 4 * h, w4);
+                            for (int p = 0; p < VEC / 2; ++p) {
+                                const F2 pp = f2_ex2(exp_arg(f2(x[2 * p], x[2 * p + 1])));
+                                f2_split(f2_fma(pp, rs_a, rs_nb), gr[2 * p], gr[2 * p + 1]);
+                            }
                         }
-                        weighted_vec(x, wq, gr);
-                    } else {
+                        if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
 #pragma unroll
-                        for (int p = 0; p < VEC / 2; ++p) {
-                            const F2 pp = f2_ex2(f2_fma(f2_sub(f2(x[2 * p], x[2 * p + 1]), rs_m), rs_l2, rs_nl));
-                            f2_split(f2_fma(pp, rs_a, rs_nb), gr[2 * p], gr[2 * p + 1]);
+                            for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
                         }
+                        if (CAPF && cap > 0.f) softcap_deriv_vec<VEC>(gr, x, nic2);
+                        st_stream(vp + v0 + v, F::pack(gr));  // vp points at this CTA's slice
                     }
-                    if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
-#pragma unroll
-                        for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
                     }
-                    if (CAPF && cap > 0.f) softcap_deriv_vec<VEC>(gr, x, nic2);
-                    st_stream(vp + v0 + v, F::pack(gr));  // vp points at this CTA's slice
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
                 }
-                }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
-            }
+            };
+            if (F::kBytes == 2 && !CAPF && fabsf(fold_c) < kFoldMax) pass2(std::true_type{});
+            else pass2(std::false_type{});
             float er = 0.f;
             if (tid < nedge) {
                 const int64_t c = edge_c;

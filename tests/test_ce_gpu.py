@@ -559,8 +559,8 @@ def test_stream_tuning_variants(ce, tune, shape):
 @pytest.mark.parametrize("shape", [(40, 64000), (24, 128256), (12, 250000), (8, 300000), (9, 8200)])
 def test_class_weight_ring_and_its_fallbacks(ce, dtype, w_offset, shape):
     """Class-weighted smoothing on the automatic path: weights starting on a
-    16-byte boundary go through the shared-memory weight ring (one CTA per row
-    or a pair, by row size) and give the same bits as the per-lane loads with
+    16-byte boundary go through the shared-memory weight ring (one CTA per
+    row) and give the same bits as the per-lane loads with
     the same row split; weights at a 4- or 8-byte offset take the per-lane
     loads. All against the oracle."""
     R, V = shape
@@ -580,14 +580,43 @@ def test_class_weight_ring_and_its_fallbacks(ce, dtype, w_offset, shape):
     if w_offset != 0:
         return
     # the per-lane-load path on the same inputs with the same row split (one CTA
-    # per row up to 512 KB rows, a pair beyond): bit-identical
-    row_kb = V * 2 / 1024
-    tune = 16 | 4 if row_kb <= 512 else 16 | 8 | 4 | 2
+    # per row): bit-identical
+    tune = 16 | 4
     loss2 = ce.ce_fwd_bwd(x2, t, weight=w, label_smoothing=0.05, reduction="sum", grad_output=g, variant="stream",
                           tune=tune)
     torch.cuda.synchronize()
     assert torch.equal(x.view(torch.int16), x2.view(torch.int16))
     assert torch.equal(loss, loss2)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("opt", ["plain", "smooth", "weighted_smooth"])
+@pytest.mark.parametrize("tune", [0, 30, 86], ids=lambda t: f"tune{t}")
+def test_exponent_forms_by_row_maximum(ce, dtype, opt, tune):
+    """On 16-bit rows the gradient's exponent is one FMA, x log2e + c with
+    c = -log2e LSE, while |c| < 32, and subtracts the row maximum exactly
+    otherwise: rows on both sides of that bound (and far beyond, either
+    sign), one CTA per row, pairs and the class-weight ring, against the
+    oracle."""
+    if tune == 86 and opt != "weighted_smooth":
+        pytest.skip("the class-weight ring serves class-weighted smoothing")
+    R, V = 12, 9000
+    seed = zlib.crc32(repr((dtype, opt, tune)).encode()) % 9973
+    base = make_logits(R, V, "f32", 1.5, seed, device="cuda")
+    offs = torch.tensor([0., 8., 10., 11., 12., 14., 20., -20., -25., -35., 300., -300.], device="cuda")
+    x = (base + offs[:, None]).to(DT[dtype])
+    t = make_targets(R, V, 0.1, seed, device="cuda")
+    w = make_weights(V, seed, device="cuda") if opt == "weighted_smooth" else None
+    eps = 0.0 if opt == "plain" else 0.1
+    g = torch.tensor([0.37], device="cuda")
+    c = (torch.logsumexp(x.double(), dim=1) * 1.4426950408889634).abs().cpu()
+    assert bool((c < 31).any()) and bool((c > 33).any())
+    x_in = x.cpu()
+    ref = _oracle(x, t, w, eps, "sum", g)
+    loss = ce.ce_fwd_bwd(x, t, weight=w, label_smoothing=eps, reduction="sum", grad_output=g, variant="stream",
+                         tune=tune)
+    torch.cuda.synchronize()
+    _check_all(x, t, w, eps, "sum", g, ref, loss, x_in)
 
 
 @pytest.mark.parametrize("case", ["mean", "sum_weighted", "none_ragged", "int32_ld", "one_part", "tiny"])
