@@ -643,11 +643,12 @@ def run_ours(args):
     import softmax_cross_entropy_pass_gb300 as ce
     from workloads import CONFIGS
     cfg = CONFIGS[args.workload]
-    if args.rows or args.vocab or args.dtype or args.ignore_frac >= 0:
+    if args.rows or args.vocab or args.dtype or args.ignore_frac >= 0 or args.reduction:
         import dataclasses
         cfg = dataclasses.replace(cfg, n_rows=args.rows or cfg.n_rows, vocab=args.vocab or cfg.vocab,
                                   dtype=args.dtype or cfg.dtype,
-                                  ignore_frac=args.ignore_frac if args.ignore_frac >= 0 else cfg.ignore_frac)
+                                  ignore_frac=args.ignore_frac if args.ignore_frac >= 0 else cfg.ignore_frac,
+                                  reduction=args.reduction or cfg.reduction)
     options = {}
     if args.softcap > 0:
         options["softcap"] = args.softcap
@@ -700,7 +701,7 @@ def run_ours(args):
 
     # the other workloads, one at a time, timed the same way (one GPU only)
     configs = None
-    if world == 1 and not args.no_configs and not (args.rows or args.vocab or args.dtype) and \
+    if world == 1 and not args.no_configs and not (args.rows or args.vocab or args.dtype or args.reduction) and \
             args.ignore_frac < 0 and \
             args.workload == WORKLOAD and not options and args.variant == "auto" and not args.tune:
         configs = {"tiny": measure_tiny(ce, device, flush)}
@@ -811,6 +812,8 @@ def main():
     ap.add_argument("--accuracy", action="store_true", help="also compute the token accuracy")
     ap.add_argument("--dtype", choices=["bf16", "f16", "f32"], default="",
                     help="logits storage type (default: the workload's)")
+    ap.add_argument("--reduction", choices=["mean", "sum", "none"], default="",
+                    help="another reduction for the workload (profiling)")
     ap.add_argument("--vocab", type=int, default=0,
                     help="another vocabulary size for the workload (e.g. one that leaves rows unaligned)")
     ap.add_argument("--ignore-frac", type=float, default=-1.0,

@@ -91,14 +91,17 @@ typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
  * target, weights, n_rows and reduction): ce_forward / ce_backward /
  * ce_fwd_bwd skip their own normaliser kernel */
 #define CE_VARIANT_PREPARED 0x10000
-/* bits 20..26 of variant: stream-kernel tuning (0 = the library's choice):
+/* bits 20..30 of variant: stream-kernel tuning (0 = the library's choice):
  * 1 = 16 consumer warps and one CTA per SM, 2 = second pass over each row's
  * chunks in reverse order, 4 = first pass without the L2 evict-last policy,
  * 8 = a cluster of two CTAs per row (each streams half the row),
  * 16 = three CTAs per SM with a smaller ring, 32 = with 16: a cluster of four
  * CTAs per row (each streams a quarter), 64 = with 16, for class-weighted
  * label smoothing on bf16 / f16 rows: the class weights of the second pass
- * bulk-copied into a shared-memory ring (other rows ignore the bit) */
+ * bulk-copied into a shared-memory ring (other rows ignore the bit);
+ * bits 7..10 of the tuning value (128 x k, k = 0..15): the first k/16 of the
+ * first-pass chunks of each row part carry an L2 evict-first hint (useful
+ * with 2, where the rows waiting for their second pass exceed the L2) */
 #define CE_VARIANT_TUNE_SHIFT 20
 
 typedef struct ce_params {

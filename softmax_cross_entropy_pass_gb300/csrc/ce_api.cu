@@ -266,7 +266,7 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
     if (!loss || (p->n_rows > 0 && (!logits_inout || !target))) return CE_ERR_INVALID_ARG;
     if (!aligned(logits_inout, elem_bytes(p->dtype))) return CE_ERR_INVALID_ARG;
     int path = p->variant & 0xff;
-    if (p->variant & ~(0xffff | CE_VARIANT_PREPARED | (0x7f << CE_VARIANT_TUNE_SHIFT))) return CE_ERR_INVALID_ARG;
+    if (p->variant & ~(0xffff | CE_VARIANT_PREPARED | (0x7ff << CE_VARIANT_TUNE_SHIFT))) return CE_ERR_INVALID_ARG;
     if (path == CE_VARIANT_AUTO) path = auto_path(p, logits_inout);
     if (path != CE_VARIANT_AUTO && path != CE_VARIANT_SPLIT && path != CE_VARIANT_FUSED &&
         path != CE_VARIANT_ROWPASS && path != CE_VARIANT_STREAM)
@@ -287,7 +287,7 @@ ce_status ce_fwd_bwd(const ce_params *p, void *logits_inout, const void *target,
         a.loss = loss;
         a.grad_output = grad_output;
         e = launch_stream(a, p->dtype, smoothing_mode(p), (p->variant >> CE_VARIANT_CLUSTER_SHIFT) & 0xff,
-                          (p->variant >> CE_VARIANT_TUNE_SHIFT) & 0x7f, (p->variant & CE_VARIANT_PREPARED) == 0, s);
+                          (p->variant >> CE_VARIANT_TUNE_SHIFT) & 0x7ff, (p->variant & CE_VARIANT_PREPARED) == 0, s);
         return e == cudaSuccess ? CE_OK : cuda_fail(e);
     }
 

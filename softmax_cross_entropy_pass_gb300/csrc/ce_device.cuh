@@ -685,6 +685,18 @@ __device__ inline uint32_t cluster_id_x() {
     asm volatile("mov.u32 %0, %clusterid.x;" : "=r"(r));
     return r;
 }
+// the CTA's index and the grid's size along x read afresh (asm volatile: not
+// merged with earlier reads, so no register holds them through a long loop)
+__device__ inline uint32_t ctaid_x_fresh() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %ctaid.x;" : "=r"(r));
+    return r;
+}
+__device__ inline uint32_t nctaid_x_fresh() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %nctaid.x;" : "=r"(r));
+    return r;
+}
 __device__ inline uint32_t nclusters_x() {
     uint32_t r;
     asm volatile("mov.u32 %0, %nclusterid.x;" : "=r"(r));

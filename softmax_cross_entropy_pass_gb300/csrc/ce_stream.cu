@@ -45,6 +45,53 @@ static cudaError_t stream_fn_ready(const void *fn, int smem, int *dev_out, int *
     return cudaSuccess;
 }
 
+// SM count and L2 size of the current device, asked once per device.
+static cudaError_t device_sms_l2(int *sms_out, int64_t *l2_out) {
+    struct Entry {
+        int sms, l2;
+    };
+    constexpr int kMaxDev = 64;
+    static Entry cache[kMaxDev] = {};
+    static std::mutex mu;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(mu);
+    Entry *c = dev >= 0 && dev < kMaxDev ? &cache[dev] : nullptr;
+    if (!c || c->sms == 0) {
+        Entry n{};
+        if ((e = cudaDeviceGetAttribute(&n.sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return e;
+        if ((e = cudaDeviceGetAttribute(&n.l2, cudaDevAttrL2CacheSize, dev)) != cudaSuccess) return e;
+        if (!c) {
+            *sms_out = n.sms;
+            *l2_out = n.l2;
+            return cudaSuccess;
+        }
+        *c = n;
+    }
+    *sms_out = c->sms;
+    *l2_out = c->l2;
+    return cudaSuccess;
+}
+
+// The first-pass evict-first share (in sixteenths) of a launch whose second
+// pass walks each row part last chunk first: the bytes waiting in L2 for
+// their second pass are F = (CTAs in flight) x (bytes of a row part), and
+// when F exceeds the L2 (size C) the first 1 - C / F of each part -- the
+// chunks read again last -- are loaded under evict-first, so the L2 keeps
+// the parts' later chunks, which the second pass reads first. GB300 (L2 135.5
+// MB), class-weight ring, kernel alone, CUDA events, best share against the
+// rule: 456 x 500 KB waiting (16384 x 256000) 6-8 against 7 (3.492 ms
+// against 3.547 with none), 456 x 1 MB (4096 x 524288) 10-12 against 11
+// (1.864 against 1.891), 456 x 320 KB 0-5 (flat) against 1, 456 x 250 KB 0-2
+// against 0.
+static int first_pass_drop16(int64_t ctas, int64_t part_bytes, int64_t l2) {
+    const double f = static_cast<double>(ctas) * static_cast<double>(part_bytes);
+    if (l2 <= 0 || f <= static_cast<double>(l2)) return 0;
+    const int k = static_cast<int>(16.0 * (1.0 - static_cast<double>(l2) / f) + 0.5);
+    return k < 0 ? 0 : (k > 15 ? 15 : k);
+}
+
 // Resident clusters of a kernel on a device (0 if unknown), asked once per
 // kernel and device.
 static int max_active_clusters(const void *fn, int dev, const cudaLaunchConfig_t &cfg) {
@@ -202,6 +249,7 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     const bool ragged = (reinterpret_cast<uintptr_t>(a.grad) & 15u) != 0 || (a.n_rows > 1 && ((a.ld * esz) & 15) != 0);
     const bool wring_ok = mode == 2 && !opts && dtype != CE_DT_F32 && !ragged && a.weight &&
                           (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
+    const bool auto_tune = tune == 0;
     if (tune == 0 && wring_ok) {
         tune = kTuneThree | kTuneNoKeep | kTuneReverse | kTuneWRing;
     }
@@ -219,6 +267,18 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     const int vec = dtype == CE_DT_F32 ? 4 : 8;
     const bool pair = (tune & kTuneCluster2) && a.vocab >= 2 * vec;
     const bool quad = (tune & kTuneCluster4) && a.vocab >= 4 * vec;
+    if (auto_tune && (tune & kTuneReverse)) {
+        int sms = 0;
+        int64_t l2 = 0;
+        if (device_sms_l2(&sms, &l2) == cudaSuccess) {
+            const int cl = quad ? 4 : (pair ? 2 : 1);
+            const int per_sm = ctas_per_sm > 0 ? ctas_per_sm : ((tune & kTuneWide) ? 1 : ((tune & kTuneThree) ? 3 : 2));
+            int64_t ctas = static_cast<int64_t>(sms) * per_sm;
+            if (ctas > a.n_rows * cl) ctas = a.n_rows * cl;
+            const int64_t part = ((a.vocab + cl - 1) / cl) * esz;
+            tune |= first_pass_drop16(ctas, part, l2) << kTuneDropShift;
+        }
+    }
     if (opts) {
         // the options are built for the four shapes the library picks by row size
         if ((tune & kTuneWide) && pair) return launch_stream_shape<1, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);

@@ -95,6 +95,7 @@ struct StreamSmem {
     ArgMax am[2][16];       // token accuracy: per-warp first column of the row maximum
     float xy[2];            // the target logit
     int abort;
+    double cta_sum;         // this CTA's row losses (first CTA of a cluster; thread 0 only)
 };
 static_assert(sizeof(StreamSmem) <= kStreamCtlBytes, "stream control block too large");
 
@@ -106,6 +107,11 @@ constexpr int kTuneCluster2 = 8;   // a cluster of two CTAs per row, each stream
 constexpr int kTuneThree = 16;     // three CTAs per SM with a 4-slot ring
 constexpr int kTuneCluster4 = 32;  // a cluster of four CTAs per row (three CTAs per SM)
 constexpr int kTuneWRing = 64;     // with 16, class-weighted smoothing: weights through a shared-memory ring
+// bits 7..10: how many sixteenths of each row part's first-pass chunks (the
+// first ones, which a reversed second pass reads last) carry an L2
+// evict-first hint, so that where the rows waiting for their second pass
+// exceed the L2 the lines given up are those least likely to be read again
+constexpr int kTuneDropShift = 7;
 
 template <int NCW>
 __device__ inline void stream_consumer_sync() {
@@ -180,18 +186,23 @@ __device__ inline void load_w8(const float *p, float4 &lo, float4 &hi) {
                  : "l"(p));
 }
 
+// A row's loss: stored per row for reduction none (and, for a batch
+// reduction left to a later kernel, in the workspace), else added in fp64 to
+// the CTA's sum, in row order; the CTA's sum goes to the workspace at the end
+// and the last CTA adds those up. Called by the first CTA of the row only.
+__device__ inline void put_row_loss(const RowArgs &a, int64_t row, float loss, double &cta_sum) {
+    if (a.reduction == CE_RED_NONE) a.loss[row] = loss;
+    else if (a.no_finalize) a.row_loss[row] = loss;
+    else cta_sum += static_cast<double>(loss);
+}
+
 // The loss of a row whose class-weighted smoothing sum (r = sum w x over the
 // whole row) arrived after its gradient pass; the weight sum over the row is
-// W_all, the normaliser kernel's (fp64) sum of the class weights; written by
-// the first CTA of the row.
-__device__ inline void finish_deferred_loss(const RowArgs &a, uint32_t rank, int64_t row, float m, float s, float xy,
-                                            float r, int yg, float wy, float w_all, float eps,
-                                            float inv_v, float z_loss) {
-    if (rank != 0) return;
+// W_all, the normaliser kernel's (fp64) sum of the class weights.
+__device__ inline float deferred_loss(float m, float s, float xy, float r, int yg, float wy, float w_all, float eps,
+                                      float inv_v, float z_loss) {
     const float rrel = w_all > 0.f ? __fsub_rn(r, __fmul_rn(w_all, m)) : 0.f;
-    const RowScalars rl = make_row_scalars(m, s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f, z_loss);
-    if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
-    else a.row_loss[row] = rl.loss;
+    return make_row_scalars(m, s, xy, rrel, true, yg, wy, w_all, eps, inv_v, 1.f, z_loss).loss;
 }
 
 // RAG: rows may start off a 16-byte boundary (per-row head and tail);
@@ -278,6 +289,7 @@ ce_stream_kernel(RowArgs a, int tune) {
         mbar_init(smem_u32(&S.xbar[0]), CL);
         mbar_init(smem_u32(&S.xbar[1]), CL);
         S.abort = 0;
+        S.cta_sum = 0.0;
         fence_mbar_init_cluster();
     }
     __syncthreads();
@@ -290,6 +302,7 @@ ce_stream_kernel(RowArgs a, int tune) {
         if (lane == 0) {
             const uint64_t drop = policy_evict_first();
             const uint64_t keep = (tune & kTuneNoKeep) ? createpolicy_normal() : policy_keep();
+            const int drop16 = (tune >> kTuneDropShift) & 15;
             uint32_t it = 0;
             // each row's target is loaded one row ahead, so its latency hides under the previous row
             int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;
@@ -301,10 +314,11 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const RowGeom gm = RAG ? row_geom<F::kBytes>(slice, lo, L) : g_aligned;
                 const char *src = slice + static_cast<int64_t>(gm.nhead) * F::kBytes;
                 const int nch = gm.nch;
+                const int ndrop = (nch * drop16) >> 4;
                 for (int pass = 0; pass < (FWD ? 1 : 2); ++pass) {
-                    const uint64_t pol = pass == 0 ? keep : drop;
                     for (int k = 0; k < nch; ++k, ++it) {
                         const int c = (pass == 1 && reverse) ? nch - 1 - k : k;
+                        const uint64_t pol = pass == 1 || c < ndrop ? drop : keep;
                         const uint32_t s = it % kStreamSlots, r = it / kStreamSlots;
                         if (r > 0) mbar_wait_bounded<false, kStreamSleepP>(smem_u32(&S.empty[s]), (r - 1) & 1u, abort);
                         const int64_t off = static_cast<int64_t>(c) * kStreamChunk;
@@ -366,7 +380,8 @@ ce_stream_kernel(RowArgs a, int tune) {
         float pend_m = 0.f, pend_s = 0.f, pend_xy = 0.f, pend_wy = 0.f;
         int pend_yg = 0;
         uint32_t it = 0, j = 0;  // ring position; valid rows done (exchange parity)
-        uint32_t wi = 0;         // class-weight ring position (SHAPE 3)
+        uint32_t wsl = 0, wph = 0;  // class-weight ring slot and phase (SHAPE 3)
+        double &cta_sum = S.cta_sum;  // kept in shared memory: no registers to spare
         int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;  // one row ahead
         for (int64_t row = q0; row < a.n_rows; row += nq) {
             const int64_t t = t_next;
@@ -385,10 +400,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const uint4 z = make_uint4(0u, 0u, 0u, 0u);
                 for (int v = tid; v < nvec; v += NCT) st_stream(vp + v, z);
                 if (tid < nedge) F::store1(rowp, edge_c, 0.f);
-                if (tid == 0 && rank == 0) {
-                    if (a.reduction == CE_RED_NONE) a.loss[row] = 0.f;
-                    else a.row_loss[row] = 0.f;
-                }
+                if (tid == 0 && rank == 0) put_row_loss(a, row, 0.f, cta_sum);
                 continue;
             }
             // (the forward-only kernel reads ignored rows too: no target column there)
@@ -645,8 +657,10 @@ ce_stream_kernel(RowArgs a, int tune) {
             const bool writer = warp == 0 && lane == 0;
             if (DEFER) {
                 if (writer) {
-                    if (pend) finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, m.r,
-                                                   pend_yg, pend_wy, w_all, eps, inv_v, zl);
+                    if (pend && rank == 0)
+                        put_row_loss(a, pend_row,
+                                     deferred_loss(pend_m, pend_s, pend_xy, m.r, pend_yg, pend_wy, w_all, eps, inv_v, zl),
+                                     cta_sum);
                     pend_row = row; pend_m = m.m; pend_s = m.s; pend_xy = xy; pend_yg = yg; pend_wy = wy;
                 }
                 rrel = 0.f;  // the gradient does not use it; this row's loss waits for pass 2
@@ -656,8 +670,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             if (a.reduction == CE_RED_MEAN) scale = w_y_sum != 0.f ? g / w_y_sum : 0.f;
             if (writer && rank == 0 && !DEFER) {
                 const RowScalars rl = make_row_scalars(m.m, m.s, xy, rrel, valid, yg, wy, w_all, eps, inv_v, 1.f, zl);
-                if (a.reduction == CE_RED_NONE) a.loss[row] = rl.loss;
-                else a.row_loss[row] = rl.loss;
+                put_row_loss(a, row, rl.loss, cta_sum);
                 // the row statistics {m, s without the target column, x_y, sum w (x - m)}
                 if (FWD && a.stats) reinterpret_cast<float4 *>(a.stats)[row] = make_float4(m.m, m.s, xy, rrel);
             }
@@ -678,14 +691,23 @@ ce_stream_kernel(RowArgs a, int tune) {
             // eps / V, exponent in [-32, -16)). Other rows, fp32 gradients and softcap
             // (whose instantiations have no registers to spare for a second loop) keep
             // the exact form.
+            // With class-weighted smoothing on aligned rows and a > 0, log2 a joins c
+            // as well (form 2): a p = 2^(x log2e + c + log2 a) and the gradient is one FMA,
+            // w (-b) + a p. Its two further roundings (of log2 d - log2 a, then of
+            // the sum with -m log2e) keep the exponent within about 2^-18 in all;
+            // the smoothing term b w then dominates every element whose a p
+            // leaves fp32's normal range and flushes to 0.
             const float fold_c = fmaf(-rs.m, kLog2e, rs.neg_log2d);
-            const F2 rs_c = f2(fold_c, fold_c);
+            const float fold_ca = MODE == 2 && rs.a > 0.f ? fmaf(-rs.m, kLog2e, rs.neg_log2d + log2f(rs.a)) : INFINITY;
+            const F2 rs_c = f2(fold_c, fold_c), rs_ca = f2(fold_ca, fold_ca);
             F2 dr[2] = {f2(0.f, 0.f), f2(0.f, 0.f)};  // deferred smoothing sum of w x
             // ------------------------------------------------ pass 2: gradient in place
-            auto pass2 = [&](auto fold_tag) {
-                constexpr bool FOLD = decltype(fold_tag)::value;
+            // form 0: exact x - m; 1: m folded into c; 2: m and a folded (class weights)
+            auto pass2 = [&](auto form_tag) {
+                constexpr int FORM = decltype(form_tag)::value;
                 auto exp_arg = [&](F2 xx) {
-                    if constexpr (FOLD) return f2_fma(xx, rs_l2, rs_c);
+                    if constexpr (FORM == 2) return f2_fma(xx, rs_l2, rs_ca);
+                    else if constexpr (FORM == 1) return f2_fma(xx, rs_l2, rs_c);
                     else return f2_fma(f2_sub(xx, rs_m), rs_l2, rs_nl);
                 };
                 for (int k = 0; k < nch; ++k, ++it) {
@@ -705,21 +727,29 @@ ce_stream_kernel(RowArgs a, int tune) {
                             const float4 wv = wq[h];
                             const F2 w01 = f2(wv.x, wv.y), w23 = f2(wv.z, wv.w);
                             const F2 x01 = f2(x[4 * h], x[4 * h + 1]), x23 = f2(x[4 * h + 2], x[4 * h + 3]);
-                            const F2 nbw0 = f2_mul(rs_nb, w01), nbw1 = f2_mul(rs_nb, w23);
-                            const F2 p0 = f2_ex2(exp_arg(x01));
-                            const F2 p1 = f2_ex2(exp_arg(x23));
-                            dr[0] = f2_fma(w01, x01, dr[0]);
-                            dr[1] = f2_fma(w23, x23, dr[1]);
-                            f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
-                            f2_split(f2_fma(p1, rs_a, nbw1), gr[4 * h + 2], gr[4 * h + 3]);
+                            if constexpr (FORM == 2) {  // a p directly
+                                const F2 ap0 = f2_ex2(exp_arg(x01));
+                                const F2 ap1 = f2_ex2(exp_arg(x23));
+                                dr[0] = f2_fma(w01, x01, dr[0]);
+                                dr[1] = f2_fma(w23, x23, dr[1]);
+                                f2_split(f2_fma(w01, rs_nb, ap0), gr[4 * h], gr[4 * h + 1]);
+                                f2_split(f2_fma(w23, rs_nb, ap1), gr[4 * h + 2], gr[4 * h + 3]);
+                            } else {
+                                const F2 nbw0 = f2_mul(rs_nb, w01), nbw1 = f2_mul(rs_nb, w23);
+                                const F2 p0 = f2_ex2(exp_arg(x01));
+                                const F2 p1 = f2_ex2(exp_arg(x23));
+                                dr[0] = f2_fma(w01, x01, dr[0]);
+                                dr[1] = f2_fma(w23, x23, dr[1]);
+                                f2_split(f2_fma(p0, rs_a, nbw0), gr[4 * h], gr[4 * h + 1]);
+                                f2_split(f2_fma(p1, rs_a, nbw1), gr[4 * h + 2], gr[4 * h + 3]);
+                            }
                         }
                     };
                     if (WR && wr) {
                         // weights from the weight ring: piece q holds the weights of vectors
                         // [q NCT, (q + 1) NCT) of the chunk, thread tid's at 32 tid bytes
-                        for (int q = 0; q * NCT < nv; ++q, ++wi) {
-                            const uint32_t wsl = wi % kWS;
-                            mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.wfull[wsl]), (wi / kWS) & 1u, abort);
+                        for (int q = 0; q * NCT < nv; ++q) {
+                            mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.wfull[wsl]), wph, abort);
                             const int v = q * NCT + tid;
                             if (v < nv) {
                                 float x[VEC], gr[VEC];
@@ -741,6 +771,10 @@ ce_stream_kernel(RowArgs a, int tune) {
                             }
                             __syncwarp();
                             if (lane == 0) mbar_arrive(smem_u32(&S.wempty[wsl]));
+                            if (++wsl == static_cast<uint32_t>(kWS)) {
+                                wsl = 0;
+                                wph ^= 1u;
+                            }
                         }
                     } else {
                     for (int v = tid; v < nv; v += NCT) {
@@ -777,8 +811,12 @@ ce_stream_kernel(RowArgs a, int tune) {
                     if (lane == 0) mbar_arrive(smem_u32(&S.empty[s]));
                 }
             };
-            if (F::kBytes == 2 && !CAPF && fabsf(fold_c) < kFoldMax) pass2(std::true_type{});
-            else pass2(std::false_type{});
+            if (F::kBytes == 2 && !CAPF && !RAG && MODE == 2 && fabsf(fold_ca) < kFoldMax)
+                pass2(std::integral_constant<int, 2>{});
+            else if (F::kBytes == 2 && !CAPF && MODE != 2 && fabsf(fold_c) < kFoldMax)
+                pass2(std::integral_constant<int, 1>{});
+            else
+                pass2(std::integral_constant<int, 0>{});
             float er = 0.f;
             if (tid < nedge) {
                 const int64_t c = edge_c;
@@ -830,8 +868,10 @@ ce_stream_kernel(RowArgs a, int tune) {
                     pr = tot.r;
                     pn = tot.n;
                 }
-                finish_deferred_loss(a, rank, pend_row, pend_m, pend_s, pend_xy, pr, pend_yg, pend_wy, w_all,
-                                     eps, inv_v, zl);
+                if (rank == 0)
+                    put_row_loss(a, pend_row, deferred_loss(pend_m, pend_s, pend_xy, pr, pend_yg, pend_wy, w_all, eps,
+                                                            inv_v, zl),
+                                 cta_sum);
             }
         }
         // ---------------------------------------------------- batch reduction (last CTA)
@@ -841,6 +881,10 @@ ce_stream_kernel(RowArgs a, int tune) {
             if (!have_norm) pdl_wait();
             stream_consumer_sync<NCW>();
             if (tid == 0) {
+                // this CTA's (cluster's) sum of its rows' losses, in the slot of its first row
+                // (the index read again here rather than kept in a register through the rows)
+                if (a.reduction != CE_RED_NONE && (CL == 1 || cluster_ctarank() == 0))
+                    a.row_loss[CL == 1 ? ctaid_x_fresh() : cluster_id_x()] = static_cast<float>(cta_sum);
                 __threadfence();
                 const unsigned prev = atomicAdd(&a.ctl->done, 1u);
                 sh_last = (prev == gridDim.x - 1) ? 1u : 0u;
@@ -855,7 +899,9 @@ ce_stream_kernel(RowArgs a, int tune) {
             if (sh_last && a.reduction != CE_RED_NONE) {
                 __threadfence();
                 double sum = 0.0;
-                for (int64_t i = tid; i < a.n_rows; i += NCT) sum += static_cast<double>(__ldcg(a.row_loss + i));
+                // the CTAs' (clusters') sums in CTA order, then a fixed tree
+                const int n_part = static_cast<int>(CL == 1 ? nctaid_x_fresh() : nclusters_x());
+                for (int i = tid; i < n_part; i += NCT) sum += static_cast<double>(__ldcg(a.row_loss + i));
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
                 if (lane == 0) sh_sum[warp] = sum;
