@@ -99,9 +99,11 @@ typedef enum { CE_DT_F32 = 0, CE_DT_BF16 = 1, CE_DT_F16 = 2 } ce_dtype;
  * CTAs per row (each streams a quarter), 64 = with 16, for class-weighted
  * label smoothing on bf16 / f16 rows: the class weights of the second pass
  * bulk-copied into a shared-memory ring (other rows ignore the bit);
- * bits 7..10 of the tuning value (128 x k, k = 0..15): the first k/16 of the
+ * bits 7..9 of the tuning value (128 x k, k = 0..7): the first k/8 of the
  * first-pass chunks of each row part carry an L2 evict-first hint (useful
- * with 2, where the rows waiting for their second pass exceed the L2) */
+ * with 2, where the rows waiting for their second pass exceed the L2);
+ * 1024 = with 64 and one CTA per row: the weight ring at two CTAs per SM
+ * with a deeper logits ring */
 #define CE_VARIANT_TUNE_SHIFT 20
 
 typedef struct ce_params {

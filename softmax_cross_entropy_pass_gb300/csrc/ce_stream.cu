@@ -77,19 +77,23 @@ static cudaError_t device_sms_l2(int *sms_out, int64_t *l2_out) {
 // The first-pass evict-first share (in sixteenths) of a launch whose second
 // pass walks each row part last chunk first: the bytes waiting in L2 for
 // their second pass are F = (CTAs in flight) x (bytes of a row part), and
-// when F exceeds the L2 (size C) the first 1 - C / F of each part -- the
-// chunks read again last -- are loaded under evict-first, so the L2 keeps
-// the parts' later chunks, which the second pass reads first. GB300 (L2 135.5
-// MB), class-weight ring, kernel alone, CUDA events, best share against the
-// rule: 456 x 500 KB waiting (16384 x 256000) 6-8 against 7 (3.492 ms
-// against 3.547 with none), 456 x 1 MB (4096 x 524288) 10-12 against 11
-// (1.864 against 1.891), 456 x 320 KB 0-5 (flat) against 1, 456 x 250 KB 0-2
-// against 0.
-static int first_pass_drop16(int64_t ctas, int64_t part_bytes, int64_t l2) {
+// when F exceeds what the L2 keeps of them (about 0.8 of its size C; the
+// rest holds the written gradient lines) the first 1 - 0.8 C / F of each
+// part -- the chunks read again last -- are loaded under evict-first, so the
+// L2 keeps the parts' later chunks, which the second pass reads first.
+// GB300 (L2 135.5 MB), class-weight ring, kernel alone, CUDA events, best
+// share in sixteenths against the rule's: three CTAs per SM, 456 x 500 KB
+// waiting (16384 x 256000) 6-8 (flat to 10) against 9 (3.492 ms against
+// 3.547 with none), 456 x 1 MB (4096 x 524288) 10-12 against 12 (1.864
+// against 1.891), 456 x 320 KB 0-5 (flat) against 4, 456 x 250 KB 0-2
+// against 1; two CTAs per SM, 304 x 500 KB 4-5 (flat 3-6) against 5 (3.436
+// against 3.486 with none). The share is applied in eighths.
+static int first_pass_drop8(int64_t ctas, int64_t part_bytes, int64_t l2) {
     const double f = static_cast<double>(ctas) * static_cast<double>(part_bytes);
-    if (l2 <= 0 || f <= static_cast<double>(l2)) return 0;
-    const int k = static_cast<int>(16.0 * (1.0 - static_cast<double>(l2) / f) + 0.5);
-    return k < 0 ? 0 : (k > 15 ? 15 : k);
+    const double kept = 0.8 * static_cast<double>(l2);
+    if (l2 <= 0 || f <= kept) return 0;
+    const int k = static_cast<int>(8.0 * (1.0 - kept / f) + 0.5);
+    return k < 0 ? 0 : (k > 7 ? 7 : k);
 }
 
 // Resident clusters of a kernel on a device (0 if unknown), asked once per
@@ -112,12 +116,12 @@ static int max_active_clusters(const void *fn, int dev, const cudaLaunchConfig_t
     return n;
 }
 
-// The class-weight ring shape (SHAPE 3): aligned bf16 / f16 rows with
-// class-weighted smoothing and no options.
-template <int CL>
+// The class-weight ring shapes (SHAPE 3 and 4): aligned bf16 / f16 rows
+// with class-weighted smoothing and no options.
+template <int SHAPE, int CL>
 static const void *stream_kernel_wring(int dtype) {
-    return dtype == CE_DT_BF16 ? reinterpret_cast<const void *>(&ce_stream_kernel<CE_DT_BF16, 2, 3, CL, false, 0>)
-         : dtype == CE_DT_F16  ? reinterpret_cast<const void *>(&ce_stream_kernel<CE_DT_F16, 2, 3, CL, false, 0>)
+    return dtype == CE_DT_BF16 ? reinterpret_cast<const void *>(&ce_stream_kernel<CE_DT_BF16, 2, SHAPE, CL, false, 0>)
+         : dtype == CE_DT_F16  ? reinterpret_cast<const void *>(&ce_stream_kernel<CE_DT_F16, 2, SHAPE, CL, false, 0>)
                                : nullptr;
 }
 
@@ -134,12 +138,12 @@ static cudaError_t launch_stream_shape(const RowArgs &a0, int dtype, int mode, i
     if (fwd) {
         if (SHAPE != 2 || CL != 1 || mode == 2 || opts) return cudaErrorInvalidValue;
         fn = stream_kernel_forward(dtype, mode, ragged);
-    } else if constexpr (SHAPE == 3) {
+    } else if constexpr (SHAPE == 3 || SHAPE == 4) {
         // the weight ring copies whole 32-byte weight vectors from 16-byte aligned weights
         const bool ok = mode == 2 && !ragged && !opts && dtype != CE_DT_F32 && a.weight &&
                         (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
         if (!ok) return launch_stream_shape<2, CL>(a0, dtype, mode, ctas_per_sm, tune, after_prep, s);
-        fn = stream_kernel_wring<CL>(dtype);
+        fn = stream_kernel_wring<SHAPE, CL>(dtype);
     } else {
         fn = a.softcap > 0.f ? stream_kernel_softcap(dtype, mode, SHAPE, CL, ragged)
            : opts ? stream_kernel_options(dtype, mode, SHAPE, CL, ragged)
@@ -245,13 +249,21 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     // 1.501 against 1.513 for ring pairs and 2.183 for 16-warp per-lane
     // pairs, x 524288 1.941 against 1.953 and 3.094). Its second pass misses
     // L2 more (456 rows wait there), but a row needs no exchange between CTAs.
+    // Rows of 160-640 KB take the ring at two CTAs per SM with a 5-slot ring
+    // (304 rows waiting; kernel alone, with the evict-first share: 8192 x
+    // 128256 0.879 ms against 0.899 at three per SM, x 163840 1.103 against
+    // 1.132, 16384 x 256000 3.396 against 3.476, 8192 x 320000 2.202 against
+    // 2.224), the others at three (8192 x 64000 0.466 against 0.475 at two,
+    // 4096 x 393216 1.390 against 1.423, x 524288 1.866 against 1.908).
     const int64_t esz = dtype == CE_DT_F32 ? 4 : 2;
     const bool ragged = (reinterpret_cast<uintptr_t>(a.grad) & 15u) != 0 || (a.n_rows > 1 && ((a.ld * esz) & 15) != 0);
     const bool wring_ok = mode == 2 && !opts && dtype != CE_DT_F32 && !ragged && a.weight &&
                           (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
     const bool auto_tune = tune == 0;
     if (tune == 0 && wring_ok) {
+        const int64_t row_bytes = a.vocab * esz;
         tune = kTuneThree | kTuneNoKeep | kTuneReverse | kTuneWRing;
+        if (row_bytes > 160 * 1024 && row_bytes <= 640 * 1024) tune |= kTuneWRing2;
     }
     if (tune == 0) {
         const int64_t row_bytes = a.vocab * (dtype == CE_DT_F32 ? 4 : 2);
@@ -272,11 +284,16 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
         int64_t l2 = 0;
         if (device_sms_l2(&sms, &l2) == cudaSuccess) {
             const int cl = quad ? 4 : (pair ? 2 : 1);
-            const int per_sm = ctas_per_sm > 0 ? ctas_per_sm : ((tune & kTuneWide) ? 1 : ((tune & kTuneThree) ? 3 : 2));
+            const bool ring = (tune & kTuneThree) && (tune & kTuneWRing) && wring_ok;
+            const int per_sm = ctas_per_sm > 0 ? ctas_per_sm
+                             : (tune & kTuneWide) ? StreamShape<1>::kCtasPerSm
+                             : (ring && (tune & kTuneWRing2) && cl == 1) ? StreamShape<4>::kCtasPerSm
+                             : ring ? StreamShape<3>::kCtasPerSm
+                             : (tune & kTuneThree) ? StreamShape<2>::kCtasPerSm : StreamShape<0>::kCtasPerSm;
             int64_t ctas = static_cast<int64_t>(sms) * per_sm;
             if (ctas > a.n_rows * cl) ctas = a.n_rows * cl;
             const int64_t part = ((a.vocab + cl - 1) / cl) * esz;
-            tune |= first_pass_drop16(ctas, part, l2) << kTuneDropShift;
+            tune |= first_pass_drop8(ctas, part, l2) << kTuneDropShift;
         }
     }
     if (opts) {
@@ -291,6 +308,7 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
                     : launch_stream_shape<1, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
     if ((tune & kTuneThree) && (tune & kTuneWRing))
         return quad ? launch_stream_shape<3, 4>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
+             : (!pair && (tune & kTuneWRing2)) ? launch_stream_shape<4, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
              : pair ? launch_stream_shape<3, 2>(a, dtype, mode, ctas_per_sm, tune, after_prep, s)
                     : launch_stream_shape<3, 1>(a, dtype, mode, ctas_per_sm, tune, after_prep, s);
     if (tune & kTuneThree)

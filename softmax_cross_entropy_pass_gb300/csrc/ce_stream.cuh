@@ -31,15 +31,18 @@
 
 namespace ce {
 
-// Four shapes: 8 consumer warps and a 6-slot ring (two CTAs per SM);
+// Five shapes: 8 consumer warps and a 6-slot ring (two CTAs per SM);
 // 16 consumer warps and a 12-slot ring (one CTA per SM, half the rows
 // waiting in L2 for their second pass); 8 consumer warps and a 4-slot ring
 // (three CTAs per SM, more warps to cover a cluster exchange); and, for
-// bf16 / f16 rows with class-weighted smoothing, three CTAs per SM with a
-// 3-slot ring plus a 3-slot ring of class weights: a second producer lane
-// bulk-copies the fp32 weights of each second-pass chunk into shared memory
-// (8 KB per slot, one weight vector per consumer thread), so the gradient
-// loop reads them from shared memory instead of waiting on per-lane loads.
+// bf16 / f16 rows with class-weighted smoothing, a 3-slot ring plus a 3-slot
+// ring of class weights at three CTAs per SM (SHAPE 3), or a 5-slot ring
+// plus the same weight ring at two CTAs per SM (SHAPE 4: a third fewer rows
+// waiting in L2 for their second pass, which pays for 250-500 KB rows). A
+// second producer lane bulk-copies the fp32 weights of each second-pass
+// chunk into shared memory (8 KB per slot, one weight vector per consumer
+// thread), so the gradient loop reads them from shared memory instead of
+// waiting on per-lane loads.
 constexpr int kStreamChunk = 16384;  // bytes per ring slot
 constexpr int kStreamMaxSlots = 12;
 constexpr int kStreamCtlBytes = 2048;  // control block after the rings
@@ -69,9 +72,9 @@ constexpr uint32_t kStreamSleepConsumerW = CE_STREAM_WRING_CONSUMER_WAIT_NS;
 template <int SHAPE> struct StreamShape {
     static constexpr int kWarps = SHAPE == 1 ? 16 : 8;
     static constexpr int kThreads = (kWarps + 1) * 32;
-    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : (SHAPE == 2 ? 4 : 3));
-    static constexpr int kCtasPerSm = SHAPE == 0 ? 2 : (SHAPE == 1 ? 1 : 3);
-    static constexpr int kWSlots = SHAPE == 3 ? kStreamWSlots : 0;  // class-weight ring
+    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : (SHAPE == 2 ? 4 : (SHAPE == 3 ? 3 : 5)));
+    static constexpr int kCtasPerSm = SHAPE == 0 ? 2 : (SHAPE == 1 ? 1 : (SHAPE == 4 ? 2 : 3));
+    static constexpr int kWSlots = SHAPE >= 3 ? kStreamWSlots : 0;  // class-weight ring
     static constexpr int kSmem = kSlots * kStreamChunk + kWSlots * kStreamWSlotBytes + kStreamCtlBytes;
 };
 
@@ -107,11 +110,12 @@ constexpr int kTuneCluster2 = 8;   // a cluster of two CTAs per row, each stream
 constexpr int kTuneThree = 16;     // three CTAs per SM with a 4-slot ring
 constexpr int kTuneCluster4 = 32;  // a cluster of four CTAs per row (three CTAs per SM)
 constexpr int kTuneWRing = 64;     // with 16, class-weighted smoothing: weights through a shared-memory ring
-// bits 7..10: how many sixteenths of each row part's first-pass chunks (the
+// bits 7..9: how many eighths of each row part's first-pass chunks (the
 // first ones, which a reversed second pass reads last) carry an L2
 // evict-first hint, so that where the rows waiting for their second pass
 // exceed the L2 the lines given up are those least likely to be read again
 constexpr int kTuneDropShift = 7;
+constexpr int kTuneWRing2 = 1024;  // with 64 and one CTA per row: the weight ring at two CTAs per SM
 
 template <int NCW>
 __device__ inline void stream_consumer_sync() {
@@ -267,6 +271,7 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr bool FWD = OPT == 3;
     constexpr bool FEAT = OPT == 1 || OPT == 2;
     constexpr bool CAPF = OPT == 2;
+    constexpr bool TGT_AFTER = !CAPF && CL == 1;  // the target element stored after the gradient loop
     static_assert(!FWD || (MODE != 2 && CL == 1), "the forward-only kernel: one CTA per row, no class-weighted smoothing");
     const float cap = CAPF ? a.softcap : 0.f;
     const float inv_cap = CAPF && cap > 0.f ? 1.f / cap : 0.f;
@@ -302,7 +307,7 @@ ce_stream_kernel(RowArgs a, int tune) {
         if (lane == 0) {
             const uint64_t drop = policy_evict_first();
             const uint64_t keep = (tune & kTuneNoKeep) ? createpolicy_normal() : policy_keep();
-            const int drop16 = (tune >> kTuneDropShift) & 15;
+            const int drop8 = (tune >> kTuneDropShift) & 7;
             uint32_t it = 0;
             // each row's target is loaded one row ahead, so its latency hides under the previous row
             int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;
@@ -314,7 +319,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const RowGeom gm = RAG ? row_geom<F::kBytes>(slice, lo, L) : g_aligned;
                 const char *src = slice + static_cast<int64_t>(gm.nhead) * F::kBytes;
                 const int nch = gm.nch;
-                const int ndrop = (nch * drop16) >> 4;
+                const int ndrop = (nch * drop8) >> 3;
                 for (int pass = 0; pass < (FWD ? 1 : 2); ++pass) {
                     for (int k = 0; k < nch; ++k, ++it) {
                         const int c = (pass == 1 && reverse) ? nch - 1 - k : k;
@@ -763,7 +768,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                                     make_float4(__uint_as_float(whi.x), __uint_as_float(whi.y), __uint_as_float(whi.z),
                                                 __uint_as_float(whi.w))};
                                 weighted_vec(x, wq, gr);
-                                if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
+                                if (!TGT_AFTER && static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
 #pragma unroll
                                     for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
                                 }
@@ -799,7 +804,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                                 f2_split(f2_fma(pp, rs_a, rs_nb), gr[2 * p], gr[2 * p + 1]);
                             }
                         }
-                        if (static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
+                        if (!TGT_AFTER && static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
 #pragma unroll
                             for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
                         }
@@ -817,6 +822,14 @@ ce_stream_kernel(RowArgs a, int tune) {
                 pass2(std::integral_constant<int, 1>{});
             else
                 pass2(std::integral_constant<int, 0>{});
+            // With one CTA per row and no softcap the target column of the interior
+            // is written after the row's loop, not tested for in every vector: the
+            // thread that stored its vector (vector y / VEC of a chunk belongs to
+            // thread (y / VEC) mod NCT, VPC being a multiple of NCT) overwrites that
+            // element, after its vector store in program order (4096 x 32000: fewer
+            // instructions; in the pair shapes the compiler then took two more
+            // registers and the loop ran slower).
+            if (TGT_AFTER && y >= 0 && (y / VEC) % NCT == tid) F::store1(rowp, vlo + y, rs.dxy);
             float er = 0.f;
             if (tid < nedge) {
                 const int64_t c = edge_c;

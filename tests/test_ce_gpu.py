@@ -532,13 +532,14 @@ def test_forward_statistics_every_row(ce, dtype, shape, opt, red):
 
 
 @pytest.mark.parametrize("tune", [0, 1, 2, 3, 4, 8, 9, 10, 12, 15, 16, 24, 26, 48, 52, 54, 80, 86, 88, 94, 112,
-                                  118, 119, 30 + 4 * 128, 86 + 8 * 128, 118 + 15 * 128])
+                                  118, 119, 30 + 2 * 128, 86 + 4 * 128, 118 + 7 * 128, 86 + 1024,
+                                  86 + 1024 + 3 * 128, 94 + 1024])
 @pytest.mark.parametrize("shape", [(70, 128256), (33, 33008), (9, 256000), (5, 1000), (6, 40), (4, 24)])
 def test_stream_tuning_variants(ce, tune, shape):
     """Every stream-kernel tuning combination (wide CTA, reversed second
     pass, no L2 evict-last, CTA pairs and quads, class weights through the
-    shared-memory weight ring, a share of the first pass under evict-first)
-    against the oracle; class weights on the odd
+    shared-memory weight ring at three or two CTAs per SM, a share of the
+    first pass under evict-first) against the oracle; class weights on the odd
     tunes, on 54 (a quad) and on every weight-ring tune (64 set); at V = 40
     the last CTA of a quad has no columns (the parts are 16, 16 and 8
     columns), at V = 24 the last two."""
