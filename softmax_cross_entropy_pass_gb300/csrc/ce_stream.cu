@@ -249,21 +249,19 @@ cudaError_t launch_stream(const RowArgs &a, int dtype, int mode, int ctas_per_sm
     // 1.501 against 1.513 for ring pairs and 2.183 for 16-warp per-lane
     // pairs, x 524288 1.941 against 1.953 and 3.094). Its second pass misses
     // L2 more (456 rows wait there), but a row needs no exchange between CTAs.
-    // Rows of 160-640 KB take the ring at two CTAs per SM with a 5-slot ring
-    // (304 rows waiting; kernel alone, with the evict-first share: 8192 x
-    // 128256 0.879 ms against 0.899 at three per SM, x 163840 1.103 against
-    // 1.132, 16384 x 256000 3.396 against 3.476, 8192 x 320000 2.202 against
-    // 2.224), the others at three (8192 x 64000 0.466 against 0.475 at two,
-    // 4096 x 393216 1.390 against 1.423, x 524288 1.866 against 1.908).
+    // The ring runs at two CTAs per SM with two weight vectors per thread in a
+    // weight slot (304 rows waiting, half the weight-slot hand-overs; kernel
+    // alone, with the evict-first share, against three CTAs per SM with one:
+    // 8192 x 64000 0.440 ms against 0.457, x 128256 0.839 against 0.899,
+    // 16384 x 256000 3.339 against 3.476, 4096 x 393216 1.347 against 1.386,
+    // x 524288 1.810 against 1.852).
     const int64_t esz = dtype == CE_DT_F32 ? 4 : 2;
     const bool ragged = (reinterpret_cast<uintptr_t>(a.grad) & 15u) != 0 || (a.n_rows > 1 && ((a.ld * esz) & 15) != 0);
     const bool wring_ok = mode == 2 && !opts && dtype != CE_DT_F32 && !ragged && a.weight &&
                           (reinterpret_cast<uintptr_t>(a.weight) & 15u) == 0;
     const bool auto_tune = tune == 0;
     if (tune == 0 && wring_ok) {
-        const int64_t row_bytes = a.vocab * esz;
-        tune = kTuneThree | kTuneNoKeep | kTuneReverse | kTuneWRing;
-        if (row_bytes > 160 * 1024 && row_bytes <= 640 * 1024) tune |= kTuneWRing2;
+        tune = kTuneThree | kTuneNoKeep | kTuneReverse | kTuneWRing | kTuneWRing2;
     }
     if (tune == 0) {
         const int64_t row_bytes = a.vocab * (dtype == CE_DT_F32 ? 4 : 2);

@@ -36,18 +36,17 @@ namespace ce {
 // waiting in L2 for their second pass); 8 consumer warps and a 4-slot ring
 // (three CTAs per SM, more warps to cover a cluster exchange); and, for
 // bf16 / f16 rows with class-weighted smoothing, a 3-slot ring plus a 3-slot
-// ring of class weights at three CTAs per SM (SHAPE 3), or a 5-slot ring
-// plus the same weight ring at two CTAs per SM (SHAPE 4: a third fewer rows
-// waiting in L2 for their second pass, which pays for 250-500 KB rows). A
-// second producer lane bulk-copies the fp32 weights of each second-pass
-// chunk into shared memory (8 KB per slot, one weight vector per consumer
-// thread), so the gradient loop reads them from shared memory instead of
-// waiting on per-lane loads.
+// ring of class weights, at three CTAs per SM with one weight vector per
+// consumer thread in a weight slot (SHAPE 3, 8 KB slots) or at two CTAs per
+// SM with two (SHAPE 4, 16 KB slots: a third fewer rows waiting in L2 for
+// their second pass and half the weight-slot hand-overs, which pays for
+// 160-640 KB rows). A second producer lane bulk-copies the fp32 weights of
+// each second-pass chunk into shared memory, so the gradient loop reads them
+// from shared memory instead of waiting on per-lane loads.
 constexpr int kStreamChunk = 16384;  // bytes per ring slot
 constexpr int kStreamMaxSlots = 12;
 constexpr int kStreamCtlBytes = 2048;  // control block after the rings
-constexpr int kStreamWSlotBytes = 8192;  // bytes per class-weight slot
-constexpr int kStreamWSlots = 3;
+constexpr int kStreamWSlots = 3;  // class-weight slots (at most)
 constexpr float kFoldMax = 32.f;  // |c| below which the gradient's exponent folds m into one FMA (below)
 // Suspend-time hints of the kernel's mbarrier waits (0: spin). The
 // producer sleeps while it waits for a free slot: a spinning producer takes
@@ -72,10 +71,13 @@ constexpr uint32_t kStreamSleepConsumerW = CE_STREAM_WRING_CONSUMER_WAIT_NS;
 template <int SHAPE> struct StreamShape {
     static constexpr int kWarps = SHAPE == 1 ? 16 : 8;
     static constexpr int kThreads = (kWarps + 1) * 32;
-    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : (SHAPE == 2 ? 4 : (SHAPE == 3 ? 3 : 5)));
+    static constexpr int kSlots = SHAPE == 0 ? 6 : (SHAPE == 1 ? 12 : (SHAPE == 2 ? 4 : 3));
     static constexpr int kCtasPerSm = SHAPE == 0 ? 2 : (SHAPE == 1 ? 1 : (SHAPE == 4 ? 2 : 3));
     static constexpr int kWSlots = SHAPE >= 3 ? kStreamWSlots : 0;  // class-weight ring
-    static constexpr int kSmem = kSlots * kStreamChunk + kWSlots * kStreamWSlotBytes + kStreamCtlBytes;
+    // weight vectors per consumer thread in one class-weight slot (a piece)
+    static constexpr int kWVecs = SHAPE == 4 ? 2 : 1;
+    static constexpr int kWSlotBytes = kWVecs * kWarps * 32 * 32;  // one 32-byte weight vector per thread
+    static constexpr int kSmem = kSlots * kStreamChunk + kWSlots * kWSlotBytes + kStreamCtlBytes;
 };
 
 struct StreamXSlot {      // one CTA's partial of one row (32 bytes)
@@ -234,6 +236,7 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr int kStreamConsumerWarps = NCW;
     constexpr int kStreamSlots = SH::kSlots;
     constexpr int kWS = SH::kWSlots;
+    constexpr int kWV = SH::kWVecs;
     constexpr bool WR = kWS > 0;  // class weights of pass 2 through the weight ring
     constexpr uint32_t kStreamSleepC = WR ? kStreamSleepConsumerW : kStreamSleepConsumer;
     static_assert(!WR || (MODE == 2 && !RAG && VEC == 8 && OPT == 0),
@@ -246,7 +249,7 @@ ce_stream_kernel(RowArgs a, int tune) {
     static_assert((NCW & (NCW - 1)) == 0 && NCW <= 32, "the warp partials merge in groups of NCW lanes");
 
     extern __shared__ __align__(128) uint8_t smem[];
-    StreamSmem &S = *reinterpret_cast<StreamSmem *>(smem + kStreamSlots * kStreamChunk + kWS * kStreamWSlotBytes);
+    StreamSmem &S = *reinterpret_cast<StreamSmem *>(smem + kStreamSlots * kStreamChunk + kWS * SH::kWSlotBytes);
     const uint32_t ring = smem_u32(smem);
     const uint32_t wring = ring + kStreamSlots * kStreamChunk;  // class-weight slots (SHAPE 3)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -341,8 +344,8 @@ ce_stream_kernel(RowArgs a, int tune) {
             }
         } else if (WR && lane == 1 && wr) {
             // class-weight producer: for every second-pass chunk, in the consumers'
-            // order, the weights of its vectors in pieces of one vector per consumer
-            // thread (NCT vectors, 8 KB), kept in L2 (every row reads them again)
+            // order, the weights of its vectors in pieces of kWV vectors per consumer
+            // thread (8 KB each), kept in L2 (every row reads them again)
             const uint64_t wpol = policy_keep();
             uint32_t wi = 0;
             int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;
@@ -356,13 +359,13 @@ ce_stream_kernel(RowArgs a, int tune) {
                     const int c = reverse ? nch - 1 - k : k;
                     const int v0 = c * VPC;
                     const int nv = min(VPC, nvec - v0);
-                    for (int q = 0; q * NCT < nv; ++q, ++wi) {
+                    for (int q = 0; q * NCT * kWV < nv; ++q, ++wi) {
                         const uint32_t s = wi % kWS, r = wi / kWS;
                         if (r > 0) mbar_wait_bounded<false, kStreamSleepP>(smem_u32(&S.wempty[s]), (r - 1) & 1u, abort);
-                        const int nvq = min(NCT, nv - q * NCT);
+                        const int nvq = min(NCT * kWV, nv - q * NCT * kWV);
                         const uint32_t bytes = static_cast<uint32_t>(nvq * VEC * 4);
                         mbar_expect_tx(smem_u32(&S.wfull[s]), bytes);
-                        bulk_g2s_hint(wring + s * kStreamWSlotBytes, wsrc + static_cast<int64_t>(v0 + q * NCT) * VEC,
+                        bulk_g2s_hint(wring + s * SH::kWSlotBytes, wsrc + static_cast<int64_t>(v0 + q * NCT * kWV) * VEC,
                                       bytes, smem_u32(&S.wfull[s]), wpol);
                     }
                 }
@@ -752,15 +755,18 @@ ce_stream_kernel(RowArgs a, int tune) {
                     };
                     if (WR && wr) {
                         // weights from the weight ring: piece q holds the weights of vectors
-                        // [q NCT, (q + 1) NCT) of the chunk, thread tid's at 32 tid bytes
-                        for (int q = 0; q * NCT < nv; ++q) {
+                        // [q kWV NCT, (q + 1) kWV NCT) of the chunk, those of vector
+                        // (q kWV + u) NCT + tid at 32 (u NCT + tid) bytes
+                        for (int q = 0; q * NCT * kWV < nv; ++q) {
                             mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.wfull[wsl]), wph, abort);
-                            const int v = q * NCT + tid;
+#pragma unroll
+                            for (int u = 0; u < kWV; ++u) {
+                            const int v = (q * kWV + u) * NCT + tid;
                             if (v < nv) {
                                 float x[VEC], gr[VEC];
                                 F::unpack(ld_shared_v4(base_s + 16u * v), x);
                                 const int vb = (v0 + v) * VEC;
-                                const uint32_t wa = wring + wsl * kStreamWSlotBytes + 32u * tid;
+                                const uint32_t wa = wring + wsl * SH::kWSlotBytes + 32u * (u * NCT + tid);
                                 const uint4 wlo = ld_shared_v4(wa), whi = ld_shared_v4(wa + 16u);
                                 const float4 wq[2] = {
                                     make_float4(__uint_as_float(wlo.x), __uint_as_float(wlo.y), __uint_as_float(wlo.z),
@@ -773,6 +779,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                                     for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
                                 }
                                 st_stream(vp + v0 + v, F::pack(gr));
+                            }
                             }
                             __syncwarp();
                             if (lane == 0) mbar_arrive(smem_u32(&S.wempty[wsl]));
