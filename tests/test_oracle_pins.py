@@ -60,7 +60,7 @@ def test_uniform_logits_closed_form(V, eps):
         assert torch.allclose(row, torch.full((V,), off, dtype=torch.float64), rtol=1e-12, atol=1e-16)
 
 
-def test_uniform_eps0_north_star_dxy():
+def test_uniform_logits_eps0_dxy():
     """At eps = 0: dx_y = (1/V - 1)/N."""
     V, N = 1000, 4
     x = torch.zeros(N, V, dtype=torch.float64)
