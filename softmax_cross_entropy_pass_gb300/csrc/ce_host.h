@@ -15,7 +15,7 @@ namespace ce {
 
 // Id of the context current on this thread; 0 if there is none (the runtime
 // makes the device's primary context current at its first call that needs
-// one) or the driver entry points are unavailable.
+// one) or the CUDA driver entry points are unavailable.
 inline unsigned long long current_context_id() {
     static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
     static PFN_cuCtxGetId_v12000 get_id = nullptr;

@@ -33,7 +33,7 @@ def _pair(ce, R, V, reduction, eps, seed, variant, weighted):
 
 def _first_call_setup(ce):
     """The first call in a process looks up the scratch array's device
-    address; the driver may place the array (its module) in device memory
+    address; the CUDA driver may place the array (its module) in device memory
     then. Later calls must not change device memory in use."""
     x = make_logits(4, 64, "bf16", 1.0, 1, device="cuda")
     t = make_targets(4, 64, 0.0, 1, device="cuda")
