@@ -39,8 +39,8 @@ namespace ce {
 // ring of class weights, at three CTAs per SM with one weight vector per
 // consumer thread in a weight slot (SHAPE 3, 8 KB slots) or at two CTAs per
 // SM with two (SHAPE 4, 16 KB slots: a third fewer rows waiting in L2 for
-// their second pass and half the weight-slot hand-overs, which pays for
-// 160-640 KB rows). A second producer lane bulk-copies the fp32 weights of
+// their second pass and half the weight-slot hand-overs; the library's
+// choice at every row size). A second producer lane bulk-copies the fp32 weights of
 // each second-pass chunk into shared memory, so the gradient loop reads them
 // from shared memory instead of waiting on per-lane loads.
 constexpr int kStreamChunk = 16384;  // bytes per ring slot
@@ -345,7 +345,7 @@ ce_stream_kernel(RowArgs a, int tune) {
         } else if (WR && lane == 1 && wr) {
             // class-weight producer: for every second-pass chunk, in the consumers'
             // order, the weights of its vectors in pieces of kWV vectors per consumer
-            // thread (8 KB each), kept in L2 (every row reads them again)
+            // thread (kWV x 8 KB), kept in L2 (every row reads them again)
             const uint64_t wpol = policy_keep();
             uint32_t wi = 0;
             int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;
@@ -388,7 +388,7 @@ ce_stream_kernel(RowArgs a, int tune) {
         float pend_m = 0.f, pend_s = 0.f, pend_xy = 0.f, pend_wy = 0.f;
         int pend_yg = 0;
         uint32_t it = 0, j = 0;  // ring position; valid rows done (exchange parity)
-        uint32_t wsl = 0, wph = 0;  // class-weight ring slot and phase (SHAPE 3)
+        uint32_t wsl = 0, wph = 0;  // class-weight ring slot and phase (SHAPE 3 and 4)
         double &cta_sum = S.cta_sum;  // kept in shared memory: no registers to spare
         int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;  // one row ahead
         for (int64_t row = q0; row < a.n_rows; row += nq) {
@@ -761,25 +761,25 @@ ce_stream_kernel(RowArgs a, int tune) {
                             mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.wfull[wsl]), wph, abort);
 #pragma unroll
                             for (int u = 0; u < kWV; ++u) {
-                            const int v = (q * kWV + u) * NCT + tid;
-                            if (v < nv) {
-                                float x[VEC], gr[VEC];
-                                F::unpack(ld_shared_v4(base_s + 16u * v), x);
-                                const int vb = (v0 + v) * VEC;
-                                const uint32_t wa = wring + wsl * SH::kWSlotBytes + 32u * (u * NCT + tid);
-                                const uint4 wlo = ld_shared_v4(wa), whi = ld_shared_v4(wa + 16u);
-                                const float4 wq[2] = {
-                                    make_float4(__uint_as_float(wlo.x), __uint_as_float(wlo.y), __uint_as_float(wlo.z),
-                                                __uint_as_float(wlo.w)),
-                                    make_float4(__uint_as_float(whi.x), __uint_as_float(whi.y), __uint_as_float(whi.z),
-                                                __uint_as_float(whi.w))};
-                                weighted_vec(x, wq, gr);
-                                if (!TGT_AFTER && static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
+                                const int v = (q * kWV + u) * NCT + tid;
+                                if (v < nv) {
+                                    float x[VEC], gr[VEC];
+                                    F::unpack(ld_shared_v4(base_s + 16u * v), x);
+                                    const int vb = (v0 + v) * VEC;
+                                    const uint32_t wa = wring + wsl * SH::kWSlotBytes + 32u * (u * NCT + tid);
+                                    const uint4 wlo = ld_shared_v4(wa), whi = ld_shared_v4(wa + 16u);
+                                    const float4 wq[2] = {
+                                        make_float4(__uint_as_float(wlo.x), __uint_as_float(wlo.y), __uint_as_float(wlo.z),
+                                                    __uint_as_float(wlo.w)),
+                                        make_float4(__uint_as_float(whi.x), __uint_as_float(whi.y), __uint_as_float(whi.z),
+                                                    __uint_as_float(whi.w))};
+                                    weighted_vec(x, wq, gr);
+                                    if (!TGT_AFTER && static_cast<unsigned>(y - vb) < static_cast<unsigned>(VEC)) {
 #pragma unroll
-                                    for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
+                                        for (int e = 0; e < VEC; ++e) gr[e] = (vb + e == y) ? rs.dxy : gr[e];
+                                    }
+                                    st_stream(vp + v0 + v, F::pack(gr));
                                 }
-                                st_stream(vp + v0 + v, F::pack(gr));
-                            }
                             }
                             __syncwarp();
                             if (lane == 0) mbar_arrive(smem_u32(&S.wempty[wsl]));
