@@ -275,8 +275,10 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr bool FEAT = OPT == 1 || OPT == 2;
     constexpr bool CAPF = OPT == 2;
     constexpr bool TGT_AFTER = !CAPF && CL == 1;  // the target element stored after the gradient loop
-    // one CTA per row in the three-per-SM shape: a row of at most kStreamSlots
-    // chunks stays in the ring between the passes (no second copy from L2)
+    // one CTA per row in the three-per-SM shape: the last kStreamSlots chunks
+    // of a row (all of a row of at most that many) stay in the ring between
+    // the passes; the second pass reads them there first, then the earlier
+    // chunks copied again from L2
     constexpr bool KEEPABLE = CL == 1 && SHAPE == 2 && OPT == 0;
     static_assert(!FWD || (MODE != 2 && CL == 1), "the forward-only kernel: one CTA per row, no class-weighted smoothing");
     const float cap = CAPF ? a.softcap : 0.f;
@@ -326,10 +328,10 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const char *src = slice + static_cast<int64_t>(gm.nhead) * F::kBytes;
                 const int nch = gm.nch;
                 const int ndrop = (nch * drop8) >> 3;
-                const bool kept = KEEPABLE && nch <= kStreamSlots;  // the second pass reads the ring again
-                for (int pass = 0; pass < ((FWD || kept) ? 1 : 2); ++pass) {
-                    for (int k = 0; k < nch; ++k, ++it) {
-                        const int c = (pass == 1 && reverse) ? nch - 1 - k : k;
+                const int nkeep = KEEPABLE ? min(nch, kStreamSlots) : 0;  // chunks the second pass reads in the ring
+                for (int pass = 0; pass < (FWD ? 1 : 2); ++pass) {
+                    for (int k = 0; k < (pass == 0 ? nch : nch - nkeep); ++k, ++it) {
+                        const int c = (pass == 1 && reverse && !KEEPABLE) ? nch - 1 - k : k;
                         const uint64_t pol = pass == 1 || c < ndrop ? drop : keep;
                         const uint32_t s = it % kStreamSlots, r = it / kStreamSlots;
                         if (r > 0) mbar_wait_bounded<false, kStreamSleepP>(smem_u32(&S.empty[s]), (r - 1) & 1u, abort);
@@ -427,8 +429,8 @@ ce_stream_kernel(RowArgs a, int tune) {
             RowState st = row_state_empty();
             ArgMax am{-INFINITY, 0x7fffffff};
             uint64_t cap_forms = 0;  // softcap: the form of chunk c (c < 32) in bits 2c, 2c+1
-            const bool kept = KEEPABLE && nch <= kStreamSlots;  // the row stays in the ring for pass 2
-            const uint32_t it_row = it;                         // the row's first ring position
+            const int nkeep = KEEPABLE ? min(nch, kStreamSlots) : 0;  // last chunks kept in the ring
+            const uint32_t it_row = it;                               // the row's first ring position
             for (int c = 0; c < nch; ++c, ++it) {
                 const uint32_t s = it % kStreamSlots;
                 mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
@@ -591,7 +593,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                 }
                 if (CAPF && c < 32) cap_forms |= static_cast<uint64_t>(form) << (2 * c);
                 __syncwarp();
-                if (lane == 0 && !kept) mbar_arrive(smem_u32(&S.empty[s]));
+                if (lane == 0 && c < nch - nkeep) mbar_arrive(smem_u32(&S.empty[s]));
             }
             if (tid < nedge) {
                 const int64_t c = edge_c;
@@ -724,13 +726,16 @@ ce_stream_kernel(RowArgs a, int tune) {
                     else if constexpr (FORM == 1) return f2_fma(xx, rs_l2, rs_c);
                     else return f2_fma(f2_sub(xx, rs_m), rs_l2, rs_nl);
                 };
-                // a kept row is read again from the slots its first pass filled, first
-                // chunk first (its slots go back to the producer in ring order)
-                for (int k = 0; k < nch; ++k, it += kept ? 0u : 1u) {
-                    const int c = (reverse && !kept) ? nch - 1 - k : k;
-                    const uint32_t s = (kept ? it_row + static_cast<uint32_t>(c) : it) % kStreamSlots;
-                    if (!kept)
+                // the kept chunks first, from the slots the first pass filled (they go
+                // back to the producer in ring order), then the earlier ones copied again
+                for (int k = 0; k < nch; ++k) {
+                    const bool in_ring = k < nkeep;
+                    const int c = in_ring ? nch - nkeep + k : (KEEPABLE ? k - nkeep : (reverse ? nch - 1 - k : k));
+                    const uint32_t s = (in_ring ? it_row + static_cast<uint32_t>(c) : it) % kStreamSlots;
+                    if (!in_ring) {
                         mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
+                        ++it;
+                    }
                     const uint32_t base_s = ring + s * kStreamChunk;
                     const int v0 = c * VPC;
                     const int nv = min(VPC, nvec - v0);
