@@ -275,11 +275,11 @@ ce_stream_kernel(RowArgs a, int tune) {
     constexpr bool FEAT = OPT == 1 || OPT == 2;
     constexpr bool CAPF = OPT == 2;
     constexpr bool TGT_AFTER = !CAPF && CL == 1;  // the target element stored after the gradient loop
-    // one CTA per row in the three-per-SM shape: the last kStreamSlots chunks
-    // of a row (all of a row of at most that many) stay in the ring between
-    // the passes; the second pass reads them there first, then the earlier
-    // chunks copied again from L2
-    constexpr bool KEEPABLE = CL == 1 && SHAPE == 2 && OPT == 0;
+    // one CTA or a pair per row in the three-per-SM shape: the last
+    // kStreamSlots chunks of a row part (all of a part of at most that many)
+    // stay in the ring between the passes; the second pass reads them there
+    // first, then the earlier chunks copied again from L2
+    constexpr bool KEEPABLE = CL <= 2 && SHAPE == 2 && OPT == 0;
     static_assert(!FWD || (MODE != 2 && CL == 1), "the forward-only kernel: one CTA per row, no class-weighted smoothing");
     const float cap = CAPF ? a.softcap : 0.f;
     const float inv_cap = CAPF && cap > 0.f ? 1.f / cap : 0.f;
@@ -331,7 +331,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                 const int nkeep = KEEPABLE ? min(nch, kStreamSlots) : 0;  // chunks the second pass reads in the ring
                 for (int pass = 0; pass < (FWD ? 1 : 2); ++pass) {
                     for (int k = 0; k < (pass == 0 ? nch : nch - nkeep); ++k, ++it) {
-                        const int c = (pass == 1 && reverse && !KEEPABLE) ? nch - 1 - k : k;
+                        const int c = (pass == 1 && reverse) ? nch - nkeep - 1 - k : k;
                         const uint64_t pol = pass == 1 || c < ndrop ? drop : keep;
                         const uint32_t s = it % kStreamSlots, r = it / kStreamSlots;
                         if (r > 0) mbar_wait_bounded<false, kStreamSleepP>(smem_u32(&S.empty[s]), (r - 1) & 1u, abort);
@@ -730,7 +730,7 @@ ce_stream_kernel(RowArgs a, int tune) {
                 // back to the producer in ring order), then the earlier ones copied again
                 for (int k = 0; k < nch; ++k) {
                     const bool in_ring = k < nkeep;
-                    const int c = in_ring ? nch - nkeep + k : (KEEPABLE ? k - nkeep : (reverse ? nch - 1 - k : k));
+                    const int c = in_ring ? nch - nkeep + k : (reverse ? nch - 1 - k : k - nkeep);
                     const uint32_t s = (in_ring ? it_row + static_cast<uint32_t>(c) : it) % kStreamSlots;
                     if (!in_ring) {
                         mbar_wait_bounded<false, kStreamSleepC>(smem_u32(&S.full[s]), (it / kStreamSlots) & 1u, abort);
