@@ -4,8 +4,10 @@
 //   pass 1 (statistics): the row comes from HBM (no L2 hint by default; an
 //          evict-last hint is a tuning bit, measured slower);
 //   pass 2 (gradient):   the same bytes again, now served by L2 under an
-//          evict-first hint, while the consumer warps write the fp32
-//          gradient, rounded once, over the logits.
+//          evict-first hint (in the one-CTA and pair shapes the last four
+//          chunks of a row part stay in the ring and are read there), while
+//          the consumer warps write the fp32 gradient, rounded once, over
+//          the logits.
 // The ring is not tied to a row: while the consumers merge a row's
 // statistics, the producer keeps copying (the row's pass-2 chunks and the
 // next row's pass-1 chunks), so the memory system never idles between
