@@ -318,6 +318,7 @@ ce_stream_kernel(RowArgs a, int tune) {
             const uint64_t drop = policy_evict_first();
             const uint64_t keep = (tune & kTuneNoKeep) ? createpolicy_normal() : policy_keep();
             const int drop8 = (tune >> kTuneDropShift) & 7;
+            const uint64_t hold = policy_keep();  // evict-last
             uint32_t it = 0;
             // each row's target is loaded one row ahead, so its latency hides under the previous row
             int64_t t_next = q0 < a.n_rows ? load_target(a.target, a.tgt32, q0) : 0;
@@ -334,7 +335,10 @@ ce_stream_kernel(RowArgs a, int tune) {
                 for (int pass = 0; pass < (FWD ? 1 : 2); ++pass) {
                     for (int k = 0; k < (pass == 0 ? nch : nch - nkeep); ++k, ++it) {
                         const int c = (pass == 1 && reverse) ? nch - nkeep - 1 - k : k;
-                        const uint64_t pol = pass == 1 || c < ndrop ? drop : keep;
+                        // evict-first for the second pass and the evict-first share; with
+                        // chunks kept in the ring, evict-last for the earlier ones, which
+                        // the second pass copies again from L2
+                        const uint64_t pol = pass == 1 || c < ndrop ? drop : (nkeep > 0 && c < nch - nkeep ? hold : keep);
                         const uint32_t s = it % kStreamSlots, r = it / kStreamSlots;
                         if (r > 0) mbar_wait_bounded<false, kStreamSleepP>(smem_u32(&S.empty[s]), (r - 1) & 1u, abort);
                         const int64_t off = static_cast<int64_t>(c) * kStreamChunk;
